@@ -1,0 +1,458 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself:
+values the pages print, format definitions, closed forms, invariants, library
+routines (torch's float8 cast, scipy's Hadamard matrix, torch SDPA) and brute
+force on tiny inputs.  CPU only."""
+import math
+import os
+from decimal import Decimal, getcontext
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _kv(path):
+    out = {}
+    for line in open(os.path.join(GOLDEN, path)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        for tok in line.split():
+            if "=" in tok:
+                k, v = tok.split("=")
+                out[k] = float(v)
+    return out
+
+
+# --------------------------------------------------------------------------- E2M1
+def test_e2m1_value_set_matches_page():
+    vals = [float(x) for line in open(os.path.join(GOLDEN, "e2m1_values.txt"))
+            if not line.startswith("#") for x in line.split()]
+    dec = [oracle.e2m1_decode(c) for c in range(16)]
+    assert dec[:8] == vals
+    assert dec[8:] == [-v for v in vals]
+    assert math.copysign(1.0, dec[8]) == -1.0  # 0x8 is negative zero
+
+
+def test_e2m1_encoder_ties_and_saturation():
+    # round-to-nearest-even on the E2M1 grid: a tie picks the even-mantissa code
+    cases = {0.25: 0.0, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0, 5.0: 4.0,
+             6.0: 6.0, 7.0: 6.0, 1e9: 6.0, 0.2: 0.0, 0.3: 0.5, 4.9: 4.0, 5.1: 6.0}
+    for x, want in cases.items():
+        assert oracle.e2m1_decode(oracle.e2m1_encode(x)) == want, x
+        assert oracle.e2m1_decode(oracle.e2m1_encode(-x)) == -want, x
+    assert oracle.e2m1_encode(-0.0) == 0x8
+    assert oracle.e2m1_encode(-0.1) == 0x8
+
+
+def test_e2m1_encoder_is_nearest_on_dense_sweep():
+    grid = np.array([oracle.e2m1_decode(c) for c in range(8)])
+    xs = np.concatenate([np.arange(-8 * 64, 8 * 64 + 1) / 64.0,
+                         np.random.default_rng(7).uniform(-7, 7, 3000)]).astype(np.float32)
+    for x in xs:
+        c = oracle.e2m1_encode(float(x))
+        got = oracle.e2m1_decode(c)
+        a = min(abs(float(x)), 6.0)
+        dist = np.abs(grid - a)
+        assert abs(abs(got) - a) == dist.min(), x
+        ties = np.flatnonzero(dist == dist.min())
+        if len(ties) == 2:           # exact midpoint: even code
+            assert (c & 7) % 2 == 0, x
+        if x != 0:
+            assert (c >> 3) == (1 if x < 0 else 0)
+
+
+# --------------------------------------------------------------------------- E4M3
+def test_e4m3_decode_matches_torch_float8():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    same = (ref == got) | (np.isnan(ref) & np.isnan(got))
+    assert same.all()
+    assert oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_float8_in_range():
+    rng = np.random.default_rng(11)
+    pos = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+    mids = ((pos[1:] + pos[:-1]) / 2).astype(np.float32)     # every tie
+    xs = np.concatenate([mids, -mids, rng.uniform(-448, 448, 20000),
+                         rng.standard_normal(20000) * 1e-2, rng.standard_normal(2000) * 1e-4]
+                        ).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(x)) for x in xs], dtype=np.uint8)
+    assert (ref == got).all()
+
+
+def test_e4m3_saturation_and_sign_of_zero():
+    for x in (448.0, 460.0, 464.0, 500.0, 1e30):
+        assert oracle.e4m3_encode(x) == 0x7E
+        assert oracle.e4m3_encode(-x) == 0xFE
+    assert oracle.e4m3_encode(-0.0) == 0x80
+    assert oracle.e4m3_encode(-2.0 ** -12) == 0x80
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00      # tie between 0 and 2^-9: even (zero)
+    assert oracle.e4m3_encode(3 * 2.0 ** -10) == 0x02   # 1.5 x 2^-9 ties to 2 x 2^-9
+    assert oracle.e4m3_encode(3 * 2.0 ** -11) == 0x01   # 0.75 x 2^-9 is nearest to 2^-9
+
+
+# --------------------------------------------------------------------------- INT8
+def test_int8_encoder_half_even_and_clip():
+    assert [oracle.int8_encode(x) for x in (0.5, 1.5, 2.5, -0.5, -1.5, 126.5, 127.4, 200.0, -200.0)] \
+        == [0, 2, 2, 0, -2, 126, 127, 127, -127]
+
+
+def test_int8_pth_row_properties():
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        x = (rng.standard_normal(32) * rng.uniform(1e-3, 50)).astype(np.float32)
+        q, sb = oracle.quant_row("int8_per_token_head", x)
+        s = float(sb.view(np.float32)[0])
+        q = q.view(np.int8).astype(np.float64)
+        amax = np.abs(x).max()
+        assert s == np.float32(np.float32(amax) / np.float32(127.0))
+        assert np.abs(q).max() == 127 and np.abs(q).max() <= 127
+        err = np.abs(q * s - x)
+        assert err.max() <= s / 2 * (1 + 1e-6) + 1e-12
+    q, sb = oracle.quant_row("int8_per_token_head", np.zeros(32, np.float32))
+    assert (q == 0).all() and sb.view(np.float32)[0] == np.float32(np.float32(1e-8) / np.float32(127))
+
+
+def test_fake_quant_bytes_and_ratio():
+    """The page's printed byte counts and ratio, from the oracle's page layout."""
+    g = _kv("fake_quant_int8.txt")
+    B, H, T, D = int(g["B"]), int(g["H"]), int(g["T"]), int(g["D"])
+    P = 16
+    blk = oracle.block_bytes("int8_per_token_head", P, D)
+    n_blocks = B * H * (T // P)
+    payload = 2 * P * D * n_blocks
+    scales = (blk - 2 * P * D) * n_blocks
+    assert payload == g["int8_payload_bytes"]
+    assert scales == g["scale_metadata_bytes"]
+    fp16 = 2 * (B * H * T * D) * 2
+    assert fp16 == g["fp16_payload_bytes"]
+    assert round(fp16 / (blk * n_blocks), 3) == g["effective_compression_ratio"]
+
+
+def test_fake_quant_replay_bounds():
+    """Replay of the page's experiment (torch CPU RNG, seed 137, draw order q, k, v).
+    The printed errors are not reproduced by the CPU generator (the page's device is
+    unstated), so the pin is the listing's own tolerance and the s/2 bound."""
+    g = _kv("fake_quant_int8.txt")
+    torch.manual_seed(137)
+    b, h, t, d = 2, 4, 16, 32
+    q = torch.randn(b, h, 1, d, dtype=torch.float32)
+    k = torch.randn(b, h, t, d, dtype=torch.float32)
+    v = torch.randn_like(k)
+
+    def fq(x):
+        rows = x.reshape(-1, d).numpy()
+        out = np.zeros_like(rows, dtype=np.float64)
+        for i, r in enumerate(rows):
+            qq, sb = oracle.quant_row("int8_per_token_head", r)
+            out[i] = qq.view(np.int8) * float(sb.view(np.float32)[0])
+        return torch.from_numpy(out.reshape(x.shape))
+
+    kh, vh = fq(k), fq(v)
+    assert (kh - k.double()).abs().max() <= g["listing_atol"]
+    assert (vh - v.double()).abs().max() <= g["listing_atol"]
+    ref = torch.softmax(q.double() @ k.double().transpose(-2, -1) / math.sqrt(d), -1) @ v.double()
+    qa = torch.softmax(q.double() @ kh.transpose(-2, -1) / math.sqrt(d), -1) @ vh
+    err = (qa - ref).abs().max().item()
+    assert err <= g["listing_atol"]
+    assert 0.1 * g["attention_max_abs_error"] < err < 10 * g["attention_max_abs_error"]
+
+
+# --------------------------------------------------------------------------- FP8 PT / PTH
+def test_fp8_pth_row_against_torch_cast():
+    rng = np.random.default_rng(5)
+    for _ in range(100):
+        x = (rng.standard_normal(128) * rng.uniform(1e-2, 30)).astype(np.float32)
+        q, sb = oracle.quant_row("fp8_per_token_head", x)
+        s = sb.view(np.float32)[0]
+        assert s == np.float32(np.float32(np.abs(x).max()) / np.float32(448.0))
+        y = torch.from_numpy((x / s).astype(np.float32))   # |x/s| <= 448 (+ rounding)
+        ref = y.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert (ref == q).all()
+        assert np.abs(q & 0x7F).max() == 0x7E   # the row max maps to 448
+
+
+def test_fp8_per_tensor_scale_and_row():
+    assert oracle.fp8_tensor_scale(448.0) == 1.0
+    assert oracle.fp8_tensor_scale(0.0) == 1.0          # all-zero tensor keeps the default 1.0
+    x = np.array([0.0, -0.0, 1.0, -3.5, 100.0, 104.0, 896.0, 1e6], np.float32)
+    q, _ = oracle.quant_row("fp8_per_tensor", x, 2.0)
+    ref = torch.from_numpy(np.clip(x / np.float32(2.0), -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert list(q) == ref.tolist()
+    assert oracle.e4m3_decode(q[4]) == 48.0             # 50 ties between 48 and 52: even mantissa
+    assert q[6] == 0x7E and q[7] == 0x7E                # 448 and saturation
+
+
+# --------------------------------------------------------------------------- NVFP4
+def test_nvfp4_format_arithmetic():
+    g = _kv("nvfp4_format.txt")
+    P, D = 16, 128
+    blk = oracle.block_bytes("nvfp4", P, D)
+    bits = blk * 8 / (2 * P * D)
+    assert bits == g["bits_per_value"]
+    assert blk // (2 * P) == 72                     # bytes per token-head per side
+    assert round(16 / bits, 2) == g["ratio_vs_bf16"]
+    assert round(8 / bits, 2) == g["ratio_vs_fp8"]
+    assert round(bits / 16, 2) == g["fraction_of_fp16"]
+
+
+def test_per_token_head_scale_counts():
+    g = _kv("nvfp4_format.txt")
+    P, D, Hkv = 16, 128, 8
+    per_token_head = (oracle.block_bytes("int8_per_token_head", P, D) - 2 * P * D) // (4 * P)
+    assert per_token_head == 2                   # one K scale and one V scale
+    assert 32768 * Hkv * per_token_head == g["scales_32k"]
+    assert 131072 * Hkv * per_token_head == g["scales_128k"]
+    # FP16 -> FP8 halves the bytes per token per layer: GQA 8 x 128 is 4 KB in FP16
+    assert oracle.block_bytes("fp8_per_tensor", P, D) // P * Hkv == 4096 // 2
+
+
+def test_nvfp4_two_block_worked_example():
+    """Two blocks, one in [-0.7, 0.7], one in [-5.5, 5.5], each get their own scale
+    and both map their max to (about) 6 and use many grid points."""
+    x = np.concatenate([np.linspace(-0.7, 0.7, 16), np.linspace(-5.5, 5.5, 16)]).astype(np.float32)
+    st = oracle.nvfp4_tensor_scale(oracle.amax(x))
+    q, bs = oracle.quant_row("nvfp4", x, st)
+    codes = np.stack([q & 15, q >> 4], 1).reshape(-1)
+    for blk in range(2):
+        c = codes[16 * blk:16 * blk + 16]
+        mags = c & 7
+        assert mags.max() == 7                    # block max maps to 6
+        assert len(set(mags.tolist())) >= 6       # the block uses the grid
+        sb = oracle.e4m3_decode(bs[blk])
+        den = np.float32(np.float32(st) * np.float32(sb))
+        xh = np.array([oracle.e2m1_decode(int(cc)) for cc in c]) * float(den)
+        err = np.abs(xh - x[16 * blk:16 * blk + 16])
+        assert err.max() <= float(den) * 1.0 + max(0.0, np.abs(x[16 * blk:16 * blk + 16]).max() - 6 * float(den)) + 1e-6
+    assert bs[0] != bs[1]
+
+
+def test_nvfp4_error_bound_random():
+    rng = np.random.default_rng(9)
+    for _ in range(50):
+        x = (rng.standard_normal(128) * rng.uniform(0.1, 20)).astype(np.float32)
+        st = oracle.nvfp4_tensor_scale(oracle.amax(x) * rng.uniform(1.0, 3.0))
+        q, bs = oracle.quant_row("nvfp4", x, st)
+        codes = np.stack([q & 15, q >> 4], 1).reshape(-1)
+        for b in range(8):
+            sb = oracle.e4m3_decode(bs[b])
+            den = float(np.float32(np.float32(st) * np.float32(sb)))
+            seg = x[16 * b:16 * b + 16].astype(np.float64)
+            xh = np.array([oracle.e2m1_decode(int(c)) for c in codes[16 * b:16 * b + 16]]) * den
+            # half the widest E2M1 gap (4 -> 6) times the block denominator, plus clipping
+            assert np.abs(xh - seg).max() <= den + max(0.0, np.abs(seg).max() - 6 * den) + 1e-7
+
+
+# --------------------------------------------------------------------------- KVarN
+def test_inv_sqrt128_is_correctly_rounded():
+    getcontext().prec = 60
+    exact = Decimal(1) / Decimal(128).sqrt()
+    f = np.float32(float(exact))
+    lo = np.nextafter(f, np.float32(0))
+    hi = np.nextafter(f, np.float32(1))
+    assert abs(Decimal(float(f)) - exact) <= abs(Decimal(float(lo)) - exact)
+    assert abs(Decimal(float(f)) - exact) <= abs(Decimal(float(hi)) - exact)
+    assert np.float32(oracle.inv_sqrt128()) == f
+
+
+def test_fwht_matches_sylvester_matrix_and_is_orthogonal():
+    from scipy.linalg import hadamard
+    H = hadamard(128).astype(np.float64) / math.sqrt(128)
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(128)
+    assert np.allclose(oracle.hadamard_f64(x), H @ x, atol=1e-12)
+    assert np.allclose(oracle.hadamard_f64(oracle.hadamard_f64(x)), x, atol=1e-12)
+    xf = x.astype(np.float32)
+    yf = oracle.fwht128_f32(xf)
+    assert np.allclose(yf, H @ xf.astype(np.float64), rtol=0, atol=2e-6 * np.abs(xf).max() * 4)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    assert abs(oracle.hadamard_f64(q) @ oracle.hadamard_f64(k) - q @ k) < 1e-12
+    qf, kf = q.astype(np.float32), k.astype(np.float32)
+    assert abs(float(oracle.fwht128_f32(qf).astype(np.float64) @ oracle.fwht128_f32(kf))
+               - float(qf.astype(np.float64) @ kf)) < 1e-4
+
+
+def test_sum128_tree_order():
+    v = np.arange(128, dtype=np.float32)
+    assert oracle.sum128(v) == 127 * 128 / 2
+    v = np.zeros(128, np.float32)
+    v[0], v[64], v[32] = 2.0 ** 24, 1.0, 1.0
+    # pairwise tree: (2^24 + 1) rounds to 2^24 twice; a running sum would give 2^24 + 2
+    assert oracle.sum128(v) == 2.0 ** 24
+
+
+def test_normalization_invariants():
+    rng = np.random.default_rng(2)
+    X = rng.standard_normal((128, 128)).astype(np.float32)
+    X[:, [3, 77]] *= 15
+    Y, r, c = oracle.kvarn_normalize(X, 8)
+    assert (r > 0).all() and (c > 0).all()
+    col_std = Y.astype(np.float64).std(axis=0)
+    assert np.allclose(col_std, 1.0, atol=1e-5)     # last step is per channel
+    recon = r[:, None].astype(np.float64) * c[None, :] * Y
+    assert np.allclose(recon, X, rtol=1e-5, atol=1e-5)
+    Y7, r7, c7 = oracle.kvarn_normalize(X, 7)
+    assert np.allclose(Y7.astype(np.float64).std(axis=1), 1.0, atol=1e-5)   # last step per token
+    Y1, r1, c1 = oracle.kvarn_normalize(X, 1)
+    assert np.all(c1 == 1.0)
+    assert np.allclose(r1, X.astype(np.float64).std(axis=1), rtol=1e-5)      # first step is per token
+    # a constant token (std 0) is left as is
+    Z = X.copy()
+    Z[5] = 0.25
+    Yz, rz, cz = oracle.kvarn_normalize(Z, 1)
+    assert rz[5] == 1.0 and np.all(Yz[5] == 0.25)
+
+
+@pytest.mark.parametrize("is_value", [False, True])
+def test_kvarn_tile_rtn(is_value):
+    from scipy.linalg import hadamard
+    rng = np.random.default_rng(4 + is_value)
+    X = rng.standard_normal((128, 128)).astype(np.float32)
+    X[:, [1, 50, 90, 127]] *= 15
+    codes, scale, zero, r, c = oracle.kvarn_tile(X, is_value)
+    steps = 3 if is_value else 15
+    assert codes.max() <= steps
+    # rebuild the normalised tile from its definition and check each code
+    Yrot = np.stack([oracle.fwht128_f32(row) for row in X])
+    Y, r2, c2 = oracle.kvarn_normalize(Yrot, 8)
+    assert np.array_equal(r, r2) and np.array_equal(c, c2)
+    axis = 1 if is_value else 0      # V: per token over channels; K: per channel over tokens
+    assert np.array_equal(zero, Y.min(axis=axis))
+    amin = Y.argmin(axis=axis)
+    amax = Y.argmax(axis=axis)
+    idx = np.arange(128)
+    if is_value:
+        assert (codes[idx, amin] == 0).all() and (codes[idx, amax] == steps).all()
+        sc = scale[:, None]; z = zero[:, None]
+    else:
+        assert (codes[amin, idx] == 0).all() and (codes[amax, idx] == steps).all()
+        sc = scale[None, :]; z = zero[None, :]
+    yhat = sc.astype(np.float64) * codes + z
+    assert np.all(np.abs(yhat - Y) <= sc / 2 * (1 + 1e-5) + 1e-6)
+    # back to the original domain: x^ = H (r c y^) is close to x
+    H = hadamard(128).astype(np.float64) / math.sqrt(128)
+    xhat = (r[:, None].astype(np.float64) * c[None, :] * yhat) @ H
+    rel = np.linalg.norm(xhat - X) / np.linalg.norm(X)
+    assert rel < (0.15 if not is_value else 0.5)
+
+
+# --------------------------------------------------------------------------- pool + attention
+def _fill(mode, w, lay, k, v, slots, ks=1.0, vs=1.0):
+    pool = np.zeros(oracle.pool_bytes(mode, lay.num_pages, w.page_size, w.num_kv_heads, w.head_dim), np.uint8)
+    bad = oracle.write(mode, pool, lay.num_pages, w.page_size, w.num_kv_heads, w.head_dim, k, v, slots, ks, vs)
+    assert bad == 0
+    return pool
+
+
+def _dequant_seq(mode, w, lay, pool, b, ks=1.0, vs=1.0):
+    n = int(lay.seq_lens[b])
+    K = np.zeros((w.num_kv_heads, n, w.head_dim))
+    V = np.zeros_like(K)
+    for t in range(n):
+        slot = int(lay.block_table[b, t // w.page_size]) * w.page_size + t % w.page_size
+        for h in range(w.num_kv_heads):
+            K[h, t] = oracle.dequant_row(mode, pool, lay.num_pages, w.page_size, w.num_kv_heads, w.head_dim, ks, vs, slot, h, 0)
+            V[h, t] = oracle.dequant_row(mode, pool, lay.num_pages, w.page_size, w.num_kv_heads, w.head_dim, ks, vs, slot, h, 1)
+    return K, V
+
+
+MODES_SMALL = ["fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nvfp4"]
+
+
+@pytest.mark.parametrize("mode", MODES_SMALL + ["kvarn_k4v2_g128"])
+def test_decode_matches_torch_sdpa(mode):
+    from scipy.linalg import hadamard
+    P = 128 if mode == "kvarn_k4v2_g128" else 16
+    lens = [256, 128] if P == 128 else [37, 16, 1, 50]
+    w = wl.Workload(name="t", mode=mode, num_seqs=len(lens), num_q_heads=8, num_kv_heads=2,
+                    head_dim=128, page_size=P, io_dtype="f16", seed=42, seq_len_range=(1, 1))
+    lay = wl.paged_layout(w, np.array(lens, np.int32), slack_pages=2)
+    ks_, vs_, ss_ = [], [], []
+    for b in range(len(lens)):
+        k, v = wl.gen_kv_seq(w, b, lens[b])
+        ks_.append(k); vs_.append(v); ss_.append(wl.slots_for_seq(w, lay, b))
+    k, v, slots = np.concatenate(ks_), np.concatenate(vs_), np.concatenate(ss_)
+    kscale = oracle.tensor_scale(mode, oracle.amax(k.astype(np.float32)))
+    vscale = oracle.tensor_scale(mode, oracle.amax(v.astype(np.float32)))
+    pool = _fill(mode, w, lay, k, v, slots, kscale, vscale)
+    q = wl.gen_q(w).astype(np.float32)
+    sm = 1 / math.sqrt(w.head_dim)
+    out = oracle.decode(mode, pool, lay.num_pages, P, w.num_kv_heads, w.head_dim, q, lay.block_table,
+                        lay.seq_lens, sm, kscale, vscale)
+    H = hadamard(128).astype(np.float64) / math.sqrt(128)
+    G = w.group
+    for b in range(len(lens)):
+        K, V = _dequant_seq(mode, w, lay, pool, b, kscale, vscale)
+        if mode == "kvarn_k4v2_g128":          # stored in the rotated domain: rotate back
+            K, V = K @ H, V @ H
+        for hq in range(w.num_q_heads):
+            qq = torch.from_numpy(q[b, hq].astype(np.float64))[None, None, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qq, torch.from_numpy(K[hq // G])[None, None], torch.from_numpy(V[hq // G])[None, None],
+                scale=sm)[0, 0, 0].numpy()
+            assert np.allclose(out[b, hq], ref, rtol=1e-9, atol=1e-9), (b, hq)
+        # dequantised values stay close to the inputs (sanity of the round trip)
+        if mode != "kvarn_k4v2_g128":
+            x = k[wl.paged_layout(w, np.array(lens)).token_offset[b]:][:lens[b]].astype(np.float64)
+            assert np.abs(K.transpose(1, 0, 2) - x).max() <= 0.5 * np.abs(x).max()
+
+
+def test_decode_special_cases():
+    w = wl.Workload(name="t", mode="int8_per_token_head", num_seqs=3, num_q_heads=4, num_kv_heads=2,
+                    head_dim=32, page_size=16, io_dtype="f32", seed=5, seq_len_range=(1, 1))
+    lens = np.array([20, 1, 0], np.int32)
+    lay = wl.paged_layout(w, lens, slack_pages=1)
+    n = int(lens.sum())
+    rng = np.random.default_rng(0)
+    k = np.tile(rng.standard_normal((1, 2, 32)).astype(np.float32), (n, 1, 1))  # all keys equal
+    v = rng.standard_normal((n, 2, 32)).astype(np.float32)
+    slots = wl.slot_mapping(w, lay)
+    pool = _fill("int8_per_token_head", w, lay, k, v, slots)
+    q = rng.standard_normal((3, 4, 32)).astype(np.float32)
+    out = oracle.decode("int8_per_token_head", pool, lay.num_pages, 16, 2, 32, q, lay.block_table,
+                        lay.seq_lens, 1 / math.sqrt(32))
+    K, V = _dequant_seq("int8_per_token_head", w, lay, pool, 0)
+    for hq in range(4):
+        assert np.allclose(out[0, hq], V[hq // 2].mean(0), atol=1e-12)    # uniform attention
+    K1, V1 = _dequant_seq("int8_per_token_head", w, lay, pool, 1)
+    for hq in range(4):
+        assert np.allclose(out[1, hq], V1[hq // 2, 0], atol=1e-12)        # one token: o = v
+    assert (out[2] == 0).all()                                            # empty sequence
+    # a page id out of range drops that page's tokens only
+    bt = lay.block_table.copy()
+    bt[0, 1] = 10 ** 6
+    out2 = oracle.decode("int8_per_token_head", pool, lay.num_pages, 16, 2, 32, q, bt, lay.seq_lens,
+                         1 / math.sqrt(32))
+    assert np.allclose(out2[0, 0], V[0, :16].mean(0), atol=1e-12)
+
+
+def test_write_skips_negative_and_counts_out_of_range_slots():
+    pool = np.zeros(oracle.pool_bytes("int8_per_token_head", 2, 16, 1, 32), np.uint8)
+    k = np.ones((3, 1, 32), np.float32)
+    bad = oracle.write("int8_per_token_head", pool, 2, 16, 1, 32, k, k, np.array([-1, 40, 5], np.int32))
+    assert bad == 1
+    blk = oracle.block_bytes("int8_per_token_head", 16, 32)
+    body = pool[oracle.header_bytes():].reshape(2, blk)
+    assert (body[0, 5 * 32:6 * 32].view(np.int8) == 127).all()
+    assert body[1].sum() == 0 and body[0, :5 * 32].sum() == 0
+
+
+def test_kvarn_write_requires_whole_tiles():
+    pool = np.zeros(oracle.pool_bytes("kvarn_k4v2_g128", 2, 128, 1, 128), np.uint8)
+    x = np.random.default_rng(0).standard_normal((128, 1, 128)).astype(np.float32)
+    good = np.arange(128, 256, dtype=np.int32)
+    assert oracle.write("kvarn_k4v2_g128", pool, 2, 128, 1, 128, x, x, good) == 0
+    shifted = np.arange(1, 129, dtype=np.int32)
+    assert oracle.write("kvarn_k4v2_g128", pool, 2, 128, 1, 128, x, x, shifted) == 128
+    with pytest.raises(ValueError):
+        oracle.write("kvarn_k4v2_g128", pool, 2, 128, 1, 128, x[:64], x[:64], good[:64])
