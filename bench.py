@@ -1,0 +1,496 @@
+"""Benchmark of the quantized paged KV-cache hot path on GB300.
+
+One step = one decode step of the workload: quantize-on-write of each
+sequence's newest token into its page, then paged decode attention of every
+sequence over its whole packed history (the split-KV combine included).  The
+bulk fill of the cache (per-tensor scale calibration + quantize-write of every
+token) runs once before the timed steps and is timed on its own (``write``).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+of the workload (the path has no data exchange; weak scaling).  Inputs are
+seeded synthetic tensors from workloads.py; the decode working set (the
+packed cache) is larger than L2 for the default workload, and for smaller ones
+L2 is flushed between timed steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "decode-attn HBM GB/s (packed KV+scales) & % of peak; quantize-write GB/s"
+DEFAULT_WORKLOAD = "nvfp4_b32_s32768"
+L2_BYTES = 129 * 2 ** 20
+BYTES_PER_TOKEN_HEAD = {"fp8_per_tensor": 256, "int8_per_token_head": 264, "fp8_per_token_head": 264,
+                        "nvfp4": 144, "kvarn_k4v2_g128": 128}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def bytes_per_token_head(w: wl.Workload) -> float:
+    return BYTES_PER_TOKEN_HEAD[w.mode] * w.head_dim / 128.0
+
+
+def decode_bytes(w: wl.Workload, lens: np.ndarray) -> int:
+    scale_bytes = 8 if w.mode in ("fp8_per_tensor", "nvfp4") else 0
+    return wl.decode_bytes(w, lens, bytes_per_token_head(w), scale_bytes)
+
+
+def write_bytes(w: wl.Workload, ntok: int) -> int:
+    esz = 2 if w.io_dtype == "f16" else 4
+    return int(ntok * w.num_kv_heads * (2 * w.head_dim * esz + bytes_per_token_head(w)) + 4 * ntok)
+
+
+# --------------------------------------------------------------------------- GPU side
+class GpuWorkload:
+    """The workload resident on one GPU: full K/V, the packed cache, q, tables."""
+
+    def __init__(self, w: wl.Workload, device="cuda", keep_host: bool = False):
+        import torch
+        from quantized_paged_kv_quantize_gb300 import kvq
+        self.kvq = kvq
+        self.w = w
+        self.dev = device
+        self.lay = wl.paged_layout(w)
+        lens = self.lay.seq_lens
+        N = self.lay.num_tokens
+        tdt = torch.float16 if w.io_dtype == "f16" else torch.float32
+        self.tdt = tdt
+        self.K = torch.empty((N, w.num_kv_heads, w.head_dim), dtype=tdt, device=device)
+        self.V = torch.empty_like(self.K)
+        self.slots = torch.from_numpy(wl.slot_mapping(w, self.lay)).to(device)
+        self.host = [] if keep_host else None
+        off = 0
+        pin_k = torch.empty((int(lens.max()), w.num_kv_heads, w.head_dim), dtype=tdt).pin_memory()
+        pin_v = torch.empty_like(pin_k)
+        for b in range(len(lens)):
+            k, v = wl.gen_kv_seq(w, b, int(lens[b]))
+            n = len(k)
+            pin_k[:n].copy_(torch.from_numpy(k))
+            pin_v[:n].copy_(torch.from_numpy(v))
+            self.K[off:off + n].copy_(pin_k[:n], non_blocking=True)
+            self.V[off:off + n].copy_(pin_v[:n], non_blocking=True)
+            torch.cuda.synchronize()
+            if keep_host:
+                self.host.append((k, v))
+            off += n
+        self.q = torch.from_numpy(wl.gen_q(w)).to(device)
+        self.block_table = torch.from_numpy(self.lay.block_table).to(device)
+        self.seq_lens = torch.from_numpy(lens).to(device)
+        self.max_seq_len = int(lens.max())
+        self.cfg = kvq.make_config(self.lay.num_pages, w.page_size, w.num_kv_heads, w.head_dim, w.mode, tdt)
+        self.pool = torch.zeros(kvq.kvq_cache_bytes(self.cfg), dtype=torch.uint8, device=device)
+        self.cache = kvq.kvq_cache_alloc(self.cfg, self.pool)
+        ns, tps, wsb = kvq.kvq_decode_plan(self.cache, w.num_seqs, w.num_q_heads, self.max_seq_len)
+        self.plan = (ns, tps, wsb)
+        self.ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device=device)
+        self.out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=tdt, device=device)
+        self.amax = torch.zeros(2, dtype=torch.float32, device=device)
+        # the decode step's append: the newest token of every sequence
+        last = (self.lay.token_offset[1:] - 1).astype(np.int64)
+        last = last[lens > 0]
+        idx = torch.from_numpy(last).to(device)
+        self.step_k = self.K.index_select(0, idx).contiguous()
+        self.step_v = self.V.index_select(0, idx).contiguous()
+        self.step_slots = self.slots.index_select(0, idx).contiguous()
+        if w.mode == "kvarn_k4v2_g128":  # whole tiles only: the step re-writes each sequence's last tile
+            tiles = []
+            for b in range(len(lens)):
+                e = int(self.lay.token_offset[b + 1])
+                tiles.append(np.arange(e - 128, e))
+            tidx = torch.from_numpy(np.concatenate(tiles)).to(device)
+            self.step_k = self.K.index_select(0, tidx).contiguous()
+            self.step_v = self.V.index_select(0, tidx).contiguous()
+            self.step_slots = self.slots.index_select(0, tidx).contiguous()
+
+    def calibrate(self):
+        if self.w.mode in ("fp8_per_tensor", "nvfp4"):
+            self.kvq.kvq_tensor_amax(self.K, self.amax[0:1])
+            self.kvq.kvq_tensor_amax(self.V, self.amax[1:2])
+            self.kvq.kvq_cache_set_tensor_scales_from_amax(self.cache, self.amax[0:1], self.amax[1:2])
+
+    def fill(self):
+        self.kvq.kvq_quantize_write(self.cache, self.K, self.V, self.slots)
+
+    def write_step(self):
+        self.kvq.kvq_quantize_write(self.cache, self.step_k, self.step_v, self.step_slots)
+
+    def decode(self, out=None):
+        self.kvq.kvq_decode_attention(self.cache, self.q, self.block_table, self.seq_lens,
+                                      self.out if out is None else out, max_seq_len=self.max_seq_len,
+                                      workspace=self.ws)
+
+    def launches_per_step(self) -> int:
+        return 1 + 1 + (1 if self.plan[0] > 1 else 0)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, ws: int, device=None) -> float:
+    """Max over ranks (the slowest rank sets the time)."""
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def flush_l2(buf):
+    buf.zero_()
+
+
+def run_ours(args, w: wl.Workload):
+    import torch
+    import torch.distributed as dist
+    ws, rank, local = _dist()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    gw = GpuWorkload(w, dev)
+    lens = gw.lay.seq_lens
+    dbytes = decode_bytes(w, lens)
+    n_step_tok = int(gw.step_slots.numel())
+    sbytes = write_bytes(w, n_step_tok)
+    step_bytes = dbytes + sbytes
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- bulk fill (timed once): a0 calibration, then quantize-write of every token
+    torch.cuda.synchronize()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    e0.record(stream)
+    gw.calibrate()
+    e1.record(stream)
+    gw.fill()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    calib_ms, fill_ms = e0.elapsed_time(e1), e1.elapsed_time(e2)
+    # repeat the fill a few times for a steadier write number (idempotent)
+    reps = 3
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(reps):
+        gw.fill()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fill_ms = min(fill_ms, f0.elapsed_time(f1) / reps)
+    flags = gw.kvq.kvq_cache_read_errors(gw.cache)
+    if flags:
+        raise RuntimeError(f"device error word after fill: {flags:#x}")
+    wbytes = write_bytes(w, gw.lay.num_tokens)
+
+    flush = None
+    cache_bytes = gw.pool.numel()
+    if cache_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        gw.write_step()
+        gw.decode()
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if flush is not None:
+            flush_l2(flush)
+        starts[i].record(stream)
+        gw.write_step()
+        mids[i].record(stream)
+        gw.decode()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dec_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+    total_ms = float(np.sum(step_ms))
+    total_ms = reduce_max(total_ms, ws, dev)
+    if ws > 1:
+        dist.barrier()
+    ms_per_step = total_ms / args.steps
+    value = ws * step_bytes / (ms_per_step * 1e-3) / 1e9
+    dec_avg = float(np.mean(dec_ms))
+    peak, peak_kind = measured_peaks()
+    dec_gbs = dbytes / (dec_avg * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region)
+    q_h = gw.q.cpu().pin_memory()
+    k_h = gw.step_k.cpu().pin_memory()
+    v_h = gw.step_v.cpu().pin_memory()
+    s_h = gw.step_slots.cpu().pin_memory()
+    out_h = torch.empty(gw.out.shape, dtype=gw.out.dtype).pin_memory()
+    q_d, k_d, v_d, s_d = (torch.empty_like(t, device=dev) for t in (q_h, k_h, v_h, s_h))
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        if flush is not None:
+            flush_l2(flush)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        s_d.copy_(s_h, non_blocking=True)
+        gw.kvq.kvq_quantize_write(gw.cache, k_d, v_d, s_d)
+        gw.kvq.kvq_decode_attention(gw.cache, q_d, gw.block_table, gw.seq_lens, gw.out,
+                                    max_seq_len=gw.max_seq_len, workspace=gw.ws)
+        out_h.copy_(gw.out, non_blocking=True)
+        t1.record(stream)
+        t1.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(t0.elapsed_time(t1))
+    e2e_tot = reduce_max(float(np.sum(e2e_ms)), ws, dev)
+    e2e_val = ws * step_bytes / (e2e_tot / args.steps * 1e-3) / 1e9
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, s_h))
+    d2h = out_h.numel() * out_h.element_size()
+
+    flags = gw.kvq.kvq_cache_read_errors(gw.cache)
+    if flags:
+        raise RuntimeError(f"device error word after the timed steps: {flags:#x}")
+
+    result = None
+    if rank == 0:
+        cpu = cpu_baseline(w, args.cpu_seconds) if not args.no_cpu_baseline else None
+        tokens_heads = float(np.sum(lens.astype(np.int64))) * w.num_q_heads
+        result = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16 x f16 -> f32 tensor-core math on dequantized codes (u8 storage)",
+            "data": "synthetic",
+            "config": {
+                "workload": w.name, "mode": w.mode, "B": w.num_seqs, "Hq": w.num_q_heads,
+                "Hkv": w.num_kv_heads, "D": w.head_dim, "page_size": w.page_size,
+                "seq_len": w.seq_len if w.seq_len else list(w.seq_len_range),
+                "io_dtype": w.io_dtype, "step": "quantize-write of 1 new token/seq + decode attention",
+                "l2": ("inputs larger than L2 (%.2f GB packed cache)" % (cache_bytes / 1e9)) if flush is None
+                else "L2 flushed (256 MiB write) before each timed step",
+                "decode_splits": gw.plan[0], "tokens_per_split": gw.plan[1],
+            },
+            "decode": {"gbs": round(dec_gbs, 2), "us": round(dec_avg * 1e3, 2),
+                       "frac_of_peak": round(dec_gbs / peak, 4), "algorithmic_bytes": dbytes,
+                       "tokens_heads_per_s": tokens_heads / (dec_avg * 1e-3)},
+            "write": {"bulk_gbs": round(wbytes / (fill_ms * 1e-3) / 1e9, 2), "bulk_ms": round(fill_ms, 4),
+                      "bulk_bytes": wbytes, "tokens_heads_per_s": gw.lay.num_tokens * w.num_kv_heads / (fill_ms * 1e-3),
+                      "calibrate_ms": round(calib_ms, 4) if w.mode in ("fp8_per_tensor", "nvfp4") else None},
+            "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(dec_gbs / peak, 4), "traffic": None,
+                         "kernel": "decode_kernel + combine_kernel", "peak_kind": peak_kind},
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": gw.launches_per_step() * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+# --------------------------------------------------------------------------- oracle side
+_ORACLE_POOLS = {}
+
+
+def _oracle_seq_pool(w: wl.Workload, b: int):
+    """The oracle's own packed pages of sequence b (built once, not timed)."""
+    import oracle
+    key = (w.name, b)
+    if key not in _ORACLE_POOLS:
+        n = int(wl.seq_lens(w)[b])
+        k, v = wl.gen_kv_seq(w, b, n)
+        P = w.page_size
+        npg = (n + P - 1) // P
+        ks = vs = 1.0
+        if w.mode in ("fp8_per_tensor", "nvfp4"):
+            ks = oracle.tensor_scale(w.mode, oracle.amax(k.astype(np.float32)))
+            vs = oracle.tensor_scale(w.mode, oracle.amax(v.astype(np.float32)))
+        pool = np.zeros(oracle.pool_bytes(w.mode, npg, P, w.num_kv_heads, w.head_dim), np.uint8)
+        idx = np.arange(n)
+        oracle.write(w.mode, pool, npg, P, w.num_kv_heads, w.head_dim, k.astype(np.float32),
+                     v.astype(np.float32), (idx // P * P + idx % P).astype(np.int32), ks, vs)
+        _ORACLE_POOLS[key] = (pool, npg, n, ks, vs)
+    return _ORACLE_POOLS[key]
+
+
+def oracle_sample(w: wl.Workload, seconds: float, start: int = 0):
+    """Time the oracle (as it stands, one thread) on decode work units of the
+    workload: one unit = one (sequence, kv head) group, i.e. the G query heads
+    that share those pages.  Runs units until `seconds` are spent.
+    Returns (algorithmic bytes, seconds, units, next start)."""
+    import oracle
+    G = w.group
+    esz = 2 if w.io_dtype == "f16" else 4
+    q_all = wl.gen_q(w).astype(np.float32)
+    done_bytes, spent, units, u = 0, 0.0, 0, start
+    while True:
+        b, kvh = (u // w.num_kv_heads) % w.num_seqs, u % w.num_kv_heads
+        pool, npg, n, ks, vs = _oracle_seq_pool(w, b)
+        rows = np.arange(G, dtype=np.int32) + kvh * G
+        t0 = time.perf_counter()
+        oracle.decode(w.mode, pool, npg, w.page_size, w.num_kv_heads, w.head_dim, q_all[b:b + 1],
+                      np.arange(npg, dtype=np.int32)[None], np.array([n], np.int32),
+                      1.0 / math.sqrt(w.head_dim), ks, vs, rows=rows)
+        spent += time.perf_counter() - t0
+        done_bytes += int(n * bytes_per_token_head(w)) + 2 * G * w.head_dim * esz
+        units += 1
+        u += 1
+        if spent >= seconds:
+            return done_bytes, spent, units, u
+
+
+def cpu_baseline(w: wl.Workload, seconds: float):
+    import oracle
+    oracle.build()
+    nb, sec, units, _ = oracle_sample(w, seconds)
+    return {"value": round(nb / sec / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{units} (sequence, kv head) groups of {w.name} decoded by the single-threaded C oracle "
+                      f"(each: all {w.group} query heads over the full sequence), {sec:.1f} s"}
+
+
+def run_reference(args, w: wl.Workload):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    u = 0
+    for _ in range(args.warmup):
+        _, _, _, u = oracle_sample(w, 0.0, u)
+    tot_b, tot_s = 0, 0.0
+    for _ in range(args.steps):
+        b, s, _, u = oracle_sample(w, 0.0, u)
+        tot_b += b
+        tot_s += s
+    val = tot_b / tot_s / 1e9
+    return {
+        "metric": METRIC, "value": round(val, 6), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention from stored codes (oracle)",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "mode": w.mode, "B": w.num_seqs, "Hq": w.num_q_heads,
+                   "Hkv": w.num_kv_heads, "D": w.head_dim, "page_size": w.page_size},
+        "cpu_baseline": {"value": round(val, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: one (sequence, kv head) group of {w.name} decoded by the "
+                                   f"single-threaded C oracle"},
+        "e2e": {"value": round(val, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS) + ["pth_b64_u1k_32k:fp8"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.workload == "pth_b64_u1k_32k:fp8":
+        w = wl.WORKLOADS["pth_b64_u1k_32k"].with_mode("fp8_per_token_head")
+    else:
+        w = wl.WORKLOADS[args.workload]
+    res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

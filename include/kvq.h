@@ -1,0 +1,190 @@
+/*
+ * kvq.h -- C ABI of libkvq: quantize-on-write into a paged KV cache and paged
+ * decode attention that reads the packed low-bit cache and folds
+ * dequantization into its load path.  One process, one NVIDIA GB300 GPU
+ * (sm_103a).
+ *
+ * Sources of the operations (web pages, by title and section):
+ *  [P1] "KV Cache 量化深度解析：Per-Tensor、Per-Token-Head 与 NVFP4":
+ *       sec. 二 (the KVQuantMode enum: NONE, FP8_PER_TENSOR, INT8/FP8
+ *       PER_TOKEN_HEAD, NVFP4), sec. 2.1, 2.2, 2.3.
+ *  [P2] "KVarN：华为推出的原生 vLLM KV-cache 量化后端，打破性能与精度的权衡":
+ *       技术原理 (tile, Hadamard rotation, variance normalisation, asymmetric
+ *       RTN), 配置与部署 (preset kvarn_k4v2_g128), 注意事项 (tile = page = 128).
+ *  [P3] "KV Cache 量化 · LLM Glossary": s = max|x|/127, q = clip(round(x/s)),
+ *       dequantize while loading inside the attention kernel.
+ *  [P4] "KV 量化" (rustineverything.app): 写和读 (the write call takes the
+ *       cache dtype and the k/v scales, the read multiplies by the descale;
+ *       FP8 stored as uint8 bit patterns), per-token-head and NVFP4 scales
+ *       stored inside the page next to the data.
+ *  [P5] "NVFP4 KV Cache：Blackwell 上的 4-bit 缓存量化": two-level scaling,
+ *       KV write/read paths, attention A = softmax(QK^T/sqrt(d)), O = AV;
+ *       "unsupported combinations fail fast, never fall back silently".
+ *
+ * Conventions
+ *  - Every call returns a kvq_status; KVQ_OK is 0.  On error,
+ *    kvq_last_error() returns a message (thread-local, valid until the next
+ *    call on the same thread).  Argument errors are detected on the host
+ *    before anything is launched.
+ *  - Pointers named dev_* or documented as device pointers are CUDA device
+ *    memory owned by the caller.  The library never allocates device memory:
+ *    the cache pool and the decode workspace are caller buffers.  A kvq_cache
+ *    handle owns only a small host-side descriptor.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All device
+ *    work is enqueued on it asynchronously, unless a call says otherwise.
+ *  - There is no fallback path: an unsupported combination of mode, head_dim,
+ *    page_size or dtype returns KVQ_ERR_UNSUPPORTED.
+ *  - Errors that only the device can see (a slot or page id out of range, a
+ *    KVarN write that is not whole tiles, a seq_len above its bound) never
+ *    fault: the offending token or tile is skipped and a bit is set in the
+ *    cache's device error word; kvq_cache_read_errors() fetches it.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int kvq_status;
+#define KVQ_OK 0
+#define KVQ_ERR_INVALID_ARG 1   /* null pointer, negative size, misaligned buffer, ... */
+#define KVQ_ERR_UNSUPPORTED 2   /* mode / head_dim / page_size / dtype combination */
+#define KVQ_ERR_MODE_MISMATCH 3 /* call mode differs from the cache's mode */
+#define KVQ_ERR_CAPACITY 4      /* buffer too small for the layout or the plan */
+#define KVQ_ERR_CUDA 5          /* a CUDA runtime/driver call failed */
+#define KVQ_ERR_DEVICE_CHECK 6  /* the device error word is non-zero */
+
+/* Quantization modes ([P1] sec. 二 enum values, plus the KVarN preset of [P2]). */
+typedef enum {
+  KVQ_FP8_PER_TENSOR = 1,      /* E4M3 payload, one fp32 scale per side (K, V) */
+  KVQ_INT8_PER_TOKEN_HEAD = 2, /* int8 payload, fp32 scale per token x kv head, s = max|x|/127 */
+  KVQ_FP8_PER_TOKEN_HEAD = 3,  /* E4M3 payload, fp32 scale per token x kv head, s = max|x|/448 */
+  KVQ_NVFP4 = 4,               /* E2M1 payload, E4M3 scale per 16 values, fp32 global scale */
+  KVQ_KVARN_K4V2_G128 = 16     /* 4-bit keys, 2-bit values, 128-token tiles */
+} kvq_mode;
+
+typedef enum { KVQ_F16 = 0, KVQ_F32 = 1 } kvq_dtype;
+
+/* Device error bits (kvq_cache_read_errors). */
+#define KVQ_DEVERR_SLOT_RANGE 0x1u   /* a write slot >= num_pages * page_size */
+#define KVQ_DEVERR_PAGE_RANGE 0x2u   /* a block_table entry outside [0, num_pages) */
+#define KVQ_DEVERR_PARTIAL_TILE 0x4u /* KVarN: a write or a sequence that is not whole tiles */
+#define KVQ_DEVERR_SEQ_LEN 0x8u      /* a seq_len above max_seq_len or max_pages * page_size */
+#define KVQ_DEVERR_TIMEOUT 0x10u     /* a bounded wait on a copy ran out (work skipped) */
+
+typedef struct {
+  int32_t num_pages;    /* pages in the pool */
+  int32_t page_size;    /* tokens per page: 16 (modes 1-4) or 128 (KVarN) */
+  int32_t num_kv_heads; /* Hkv */
+  int32_t head_dim;     /* D: 32 or 128 (modes 1-4), 128 (KVarN) */
+  int32_t mode;         /* kvq_mode */
+  int32_t io_dtype;     /* kvq_dtype of the K/V written and of the decode query */
+} kvq_cache_config;
+
+typedef struct kvq_cache kvq_cache;
+
+/* Pool layout (little-endian, version 1).  The pool is a 256-byte header
+ * followed by one block per (page, kv head), page-major:
+ *   block(p, h) at byte 256 + (p * num_kv_heads + h) * block_bytes.
+ * Token t of page p is row t of that block.  Per mode (P = page_size, D = head_dim):
+ *   FP8 per-tensor : K[P][D] e4m3 | V[P][D] e4m3                    (2PD bytes)
+ *   INT8 / FP8 PTH : K[P][D] | V[P][D] | K scale[P] f32 | V scale[P] f32
+ *   NVFP4          : K[P][D/2] | V[P][D/2] | K s_b[P][D/16] e4m3 | V s_b[P][D/16] e4m3
+ *   KVarN (P=D=128): K[128][64] u4 | V[128][32] u2 |
+ *                    K scale[D] zero[D] c[D] r[P] f32 | V scale[P] zero[P] r[P] c[D] f32
+ * 4-bit codes: the even head_dim index in the low nibble.  2-bit codes:
+ * element 4i+j in bits 2j..2j+1 of byte i.  The header holds, at byte 16 and
+ * 20, the per-tensor K and V scales (FP8 per-tensor s; NVFP4 s_t), and at
+ * byte 12 the device error word.  This is the same content as the in-page
+ * layouts of [P4] (data plus one fp32 scale per token-head; head_size/2 bytes
+ * of FP4 then head_size/16 bytes of E4M3 block scales), with each kind of
+ * field gathered into its own 16-byte-aligned sub-array. */
+
+const char* kvq_last_error(void);
+int kvq_version(void); /* layout/ABI version, currently 1 */
+
+/* Bytes of the pool for `cfg` (header included), and of one (page, kv head)
+ * block.  No device work. */
+kvq_status kvq_cache_bytes(const kvq_cache_config* cfg, size_t* bytes);
+kvq_status kvq_cache_block_bytes(const kvq_cache_config* cfg, size_t* bytes);
+
+/* Bind a cache descriptor to the caller's device buffer `dev_buf` (at least
+ * kvq_cache_bytes bytes, 256-byte aligned).  Writes the header (scales = 1.0,
+ * error word = 0) synchronously; page contents are left as they are.
+ * `*out` is freed with kvq_cache_free, which never touches device memory. */
+kvq_status kvq_cache_alloc(const kvq_cache_config* cfg, void* dev_buf, size_t bytes, kvq_cache** out);
+kvq_status kvq_cache_free(kvq_cache* cache);
+
+/* Per-tensor scales ([P1] sec. 2.1 K_fp8 = K/scale; [P5] s_t), written into
+ * the header on `stream`.  Used by KVQ_FP8_PER_TENSOR (s) and KVQ_NVFP4 (s_t);
+ * other modes ignore them.  Scales must be finite and > 0. */
+kvq_status kvq_cache_set_tensor_scales(kvq_cache* cache, float k_scale, float v_scale, void* stream);
+
+/* amax = max |x| over n elements of `x` (device, dtype kvq_dtype), written
+ * to the device float *dev_out (overwritten, not accumulated).  Exact. */
+kvq_status kvq_tensor_amax(const void* x, int dtype, size_t n, float* dev_out, void* stream);
+
+/* Set the header's scales from device amax values without a host round trip:
+ * FP8 per-tensor s = amax/448, NVFP4 s_t = amax/(448*6); an amax of 0 gives
+ * 1.0.  Both pointers are device floats (e.g. from kvq_tensor_amax). */
+kvq_status kvq_cache_set_tensor_scales_from_amax(kvq_cache* cache, const float* dev_amax_k,
+                                                 const float* dev_amax_v, void* stream);
+
+/* Copy the device error word to *flags (synchronises `stream`); if `clear`,
+ * reset it to 0 afterwards. */
+kvq_status kvq_cache_read_errors(kvq_cache* cache, uint32_t* flags, int clear, void* stream);
+
+/* Quantize-on-write ([P4] 写和读; [P1] sec. 2.1-2.3; [P2] 技术原理).
+ *  k, v          device [num_tokens][num_kv_heads][head_dim], io_dtype of the cache
+ *  slot_mapping  device int32 [num_tokens]: slot = page * page_size + row;
+ *                a negative slot skips the token; a slot past the pool skips it
+ *                and sets KVQ_DEVERR_SLOT_RANGE.
+ *  mode          must equal the cache's mode (else KVQ_ERR_MODE_MISMATCH).
+ * Per mode: FP8 per-tensor q = E4M3(x/s) with the header scale; INT8/FP8
+ * per-token-head s = max(max|x|, 1e-8)/127 (or /448), q = clip(rint(x/s)) (or
+ * E4M3(x/s)); NVFP4 s_b = E4M3(max_block|x| / (6 s_t)), q = E2M1(x/(s_t s_b));
+ * KVarN: num_tokens must be a multiple of 128 and every 128 consecutive tokens
+ * must fill one page in order (slot_mapping[128i + j] = 128 page + j); a tile
+ * that does not is skipped with KVQ_DEVERR_PARTIAL_TILE.  All divisions are
+ * IEEE round-to-nearest; results are bit-identical to the specification. */
+kvq_status kvq_quantize_write(kvq_cache* cache, const void* k, const void* v,
+                              const int32_t* slot_mapping, int num_tokens, int mode, void* stream);
+
+/* Decode plan: how many KV splits per (sequence, kv head), the tokens per
+ * split, and the workspace bytes kvq_decode_attention needs for these sizes
+ * (0 when a single split suffices).  max_seq_len is a host-side upper bound
+ * of every seq_len. */
+kvq_status kvq_decode_plan(const kvq_cache* cache, int num_seqs, int num_q_heads, int max_seq_len,
+                           int* num_splits, int* tokens_per_split, size_t* workspace_bytes);
+kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int num_seqs, int num_q_heads,
+                                      int max_seq_len, size_t* bytes);
+
+/* Paged decode attention over the packed cache ([P5] "K 与 V 的量化误差..."
+ * A = softmax(QK^T/sqrt(d)), O = AV, one query per sequence; [P3]/[P5]:
+ * dequantization happens in the kernel's load path, no dequantized copy of
+ * the cache is made).
+ *  q            device [num_seqs][num_q_heads][head_dim], io_dtype of the cache
+ *  block_table  device int32 [num_seqs][max_pages]: page ids of each sequence
+ *  seq_lens     device int32 [num_seqs]; 0 gives a zero output row
+ *  max_seq_len  host upper bound of seq_lens (<= max_pages * page_size)
+ *  softmax_scale  usually 1/sqrt(head_dim)
+ *  out          device [num_seqs][num_q_heads][head_dim], dtype out_dtype
+ *  workspace    device scratch of >= the planned bytes (may be NULL if 0)
+ * GQA: query head h reads kv head h / (num_q_heads / num_kv_heads), which
+ * must divide evenly with a group of at most 8.  KVarN: every seq_len must be
+ * a multiple of 128 (whole tiles), the query is rotated by the same
+ * normalised Hadamard transform and the output rotated back. */
+kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                                int max_pages, const int32_t* seq_lens, int num_seqs,
+                                int num_q_heads, int max_seq_len, int mode, float softmax_scale,
+                                void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

@@ -1,0 +1,601 @@
+// kvq_decode.cu -- paged decode attention over the packed quantized cache,
+// dequantization fused into the load path (modes 1-4), plus the split-KV
+// combine kernel.
+//
+// Sources (web pages, by title and section):
+//  "NVFP4 KV Cache：Blackwell 上的 4-bit 缓存量化": "K 与 V 的量化误差进入 attention 的位置不同"
+//     (A = softmax(QK^T/sqrt(d)), O = AV), "KV 的写入与读取路径" (unpack, apply block and tensor
+//     scales inside the attention tile load, no dequantized temporary), "GQA";
+//  "KV Cache 量化 · LLM Glossary": dequantize while loading inside the attention kernel;
+//  "KV 量化" (rustineverything.app), 写和读: read by block table, multiply by the descale.
+//
+// Design (GB300): one CTA per (KV split, kv head, sequence), W warps; each
+// warp owns a ring of STAGES shared-memory buffers and streams whole
+// (page, kv head) blocks into them with TMA (a tiled tensor copy whose
+// 128/64-byte swizzle makes the fragment loads bank-conflict free; a plain
+// bulk copy for head_dim 32), completion tracked by one mbarrier per stage.
+// A 16-token page is one tensor-core step: S^T = K Q^T on mma.m16n8k16 with
+// M = 16 tokens, N = 8 query heads of the GQA group, K = 16 channels; then
+// O^T += V^T P^T with M = 16 channels, N = 8 heads, K = 16 tokens.  Codes are
+// converted to f16 in registers (exact: int8, e4m3, e2m1 x e4m3 are all
+// representable), the scales are applied to the fp32 scores and to P, and the
+// fp32 probabilities enter the second product as an f16 hi + lo pair so the
+// result keeps ~22 bits.  Online softmax in base 2.  Split partials are merged
+// inside the CTA and, when a sequence has several splits, by the combine kernel.
+#include <cuda_fp16.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr int kPage = 16;
+constexpr int kWarps = 4;
+constexpr int kStages = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeArgs {
+  const uint8_t* pool;
+  const void* q;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  void* out;
+  float* ws_o;   // [B][Hq][S][D]
+  float* ws_ml;  // [B][Hq][S][2]
+  int num_pages, Hkv, Hq, G, B, max_pages, max_seq_len;
+  int tokens_per_split, num_splits;
+  int out_f32;
+  float sm_log2;  // softmax_scale * log2(e)
+  size_t block_bytes;
+  int rows_per_block;
+};
+
+template <int MODE, int D>
+struct Cfg {
+  static constexpr int RW = MODE == KVQ_NVFP4 ? D / 2 : D;  // payload row bytes
+  static constexpr int BLK = (int)block_bytes(MODE, kPage, D);
+  static constexpr bool TMA = D == 128;
+  static constexpr int STAGE = TMA ? (BLK + 1023) / 1024 * 1024 : (BLK + 127) / 128 * 128;
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int MTILES = D / 16;
+  static constexpr int V_OFF = kPage * RW;            // V payload
+  static constexpr int S_OFF = 2 * kPage * RW;        // scales region
+  // SW128 for 128-byte rows, SW64 for 64-byte rows (XOR of address bits 7.. into 4..).
+  static constexpr int SWZ_MASK = !TMA ? 0 : (RW == 128 ? 7 : 3);
+  // probabilities are scaled by 2^PSHIFT before the f16 split (range of P x scale)
+  static constexpr int pshift(bool f32io) {
+    return MODE == KVQ_INT8_PER_TOKEN_HEAD ? (f32io ? 0 : 6)
+         : MODE == KVQ_FP8_PER_TOKEN_HEAD ? (f32io ? 0 : 8) : 14;
+  }
+};
+
+template <int MASK>
+__device__ __forceinline__ int swz(int off) {
+  return off ^ (((off >> 7) & MASK) << 4);
+}
+
+template <int N>
+__device__ __forceinline__ void lds(const uint8_t* p, uint32_t* w);
+template <>
+__device__ __forceinline__ void lds<4>(const uint8_t* p, uint32_t* w) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+}
+template <>
+__device__ __forceinline__ void lds<2>(const uint8_t* p, uint32_t* w) {
+  uint2 u = *reinterpret_cast<const uint2*>(p);
+  w[0] = u.x; w[1] = u.y;
+}
+template <>
+__device__ __forceinline__ void lds<1>(const uint8_t* p, uint32_t* w) {
+  w[0] = *reinterpret_cast<const uint32_t*>(p);
+}
+
+// int8 pair (bytes 0,1 or 2,3 of w) -> exact f16x2 via 1024 + (x + 128) - 1152.
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t biased_w, uint32_t sel) {
+  const uint32_t h = prmt(biased_w, 0x64646464u, sel);
+  return h2_as_u32(__hsub2(u32_as_h2(h), __half2half2(__ushort_as_half(0x6480))));  // 0x6480 = 1152
+}
+
+template <int MODE>
+__device__ __forceinline__ void cvt_pair4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  // 4 one-byte codes -> (bytes 0,1) and (bytes 2,3) as f16x2
+  if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD) {
+    const uint32_t b = w ^ 0x80808080u;
+    lo = i8x2_to_f16x2(b, 0x4140u);
+    hi = i8x2_to_f16x2(b, 0x4342u);
+  } else {
+    lo = e4m3x2_to_f16x2(w & 0xFFFFu);
+    hi = e4m3x2_to_f16x2(w >> 16);
+  }
+}
+
+// Q as the B operand of S^T = K Q^T: b0 = Q[g][d(j,2tq..2tq+1)], b1 = Q[g][d(j,2tq+8..+9)]
+// with d(j, .) = tq*D/4 + 4j + {0,1} and {2,3}.  Heads >= G are zero.
+template <int D, bool QF32>
+__device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int g, int tq, uint32_t (*qh)[2],
+                                       uint32_t (*ql)[2]) {
+  constexpr int KSTEPS = D / 16;
+  const bool ok = g < a.G;
+  const long long row = ((long long)b * a.Hq + (long long)kvh * a.G + (ok ? g : 0)) * D + tq * (D / 4);
+#pragma unroll
+  for (int j = 0; j < KSTEPS; ++j) {
+    float x[4];
+    if constexpr (QF32) {
+      const float4 u = ok ? __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + row + 4 * j))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+      __half2 h0 = __floats2half2_rn(x[0], x[1]), h1 = __floats2half2_rn(x[2], x[3]);
+      const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+      qh[j][0] = h2_as_u32(h0);
+      qh[j][1] = h2_as_u32(h1);
+      ql[j][0] = h2_as_u32(__floats2half2_rn(x[0] - f0.x, x[1] - f0.y));
+      ql[j][1] = h2_as_u32(__floats2half2_rn(x[2] - f1.x, x[3] - f1.y));
+    } else {
+      const uint2 u = ok ? __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(a.q) + row + 4 * j))
+                         : make_uint2(0u, 0u);
+      qh[j][0] = u.x;
+      qh[j][1] = u.y;
+    }
+  }
+}
+
+template <int MODE, int D, bool QF32>
+__global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_constant__ DecodeArgs a,
+                                                               const __grid_constant__ CUtensorMap tmap) {
+  using C = Cfg<MODE, D>;
+  constexpr int KSTEPS = C::KSTEPS, MTILES = C::MTILES;
+  constexpr int PSHIFT = C::pshift(QF32);
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t bars[kWarps][kStages];
+  // 1024-byte alignment of the ring (swizzle patterns are address based)
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+
+  int n = a.seq_lens[b];
+  const int lim = min(a.max_seq_len, a.max_pages * kPage);
+  if (n > lim || n < 0) {
+    if (threadIdx.x == 0 && split == 0 && kvh == 0) set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_SEQ_LEN);
+    n = n < 0 ? 0 : lim;
+  }
+  const int t_begin = split * a.tokens_per_split;
+  const int t_end = min(n, t_begin + a.tokens_per_split);
+  if (t_begin >= t_end) {
+    if (a.num_splits == 1) {  // empty sequence: zero output rows
+      for (int i = threadIdx.x; i < a.G * D; i += blockDim.x) {
+        const long long o = ((long long)b * a.Hq + (long long)kvh * a.G + i / D) * D + i % D;
+        if (a.out_f32) static_cast<float*>(a.out)[o] = 0.0f;
+        else static_cast<__half*>(a.out)[o] = __float2half_rn(0.0f);
+      }
+    }
+    return;
+  }
+  const int p0 = t_begin / kPage, p1 = (t_end + kPage - 1) / kPage;
+  const int my_count = (p1 - p0 - warp + kWarps - 1) / kWarps;  // pages of this warp (<= 32)
+
+  uint8_t* ring = smem + warp * kStages * C::STAGE;
+  uint64_t* wb = bars[warp];
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&wb[s], 1);
+    mbar_fence_init();
+    if constexpr (C::TMA) prefetch_tmap(&tmap);
+  }
+  __syncwarp();
+
+  // lane i holds the page id of this warp's i-th page
+  int my_pid = -1;
+  if (lane < my_count) {
+    my_pid = __ldg(a.block_table + (long long)b * a.max_pages + p0 + warp + kWarps * lane);
+    if (my_pid < 0 || my_pid >= a.num_pages) {
+      set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_PAGE_RANGE);
+      my_pid = -1;
+    }
+  }
+
+  auto issue = [&](int i) {
+    const int pid = __shfl_sync(kFull, my_pid, i);
+    if (lane == 0) {
+      uint64_t* bar = &wb[i % kStages];
+      mbar_arrive_expect_tx(bar, pid >= 0 ? (uint32_t)C::BLK : 0u);
+      if (pid >= 0) {
+        uint8_t* dst = ring + (i % kStages) * C::STAGE;
+        const long long ph = (long long)pid * a.Hkv + kvh;
+        if constexpr (C::TMA)
+          tma_g2s_2d(dst, &tmap, 0, (int)((kHeaderBytes + ph * (long long)C::BLK) / C::RW), bar);
+        else
+          bulk_g2s(dst, a.pool + kHeaderBytes + ph * (long long)C::BLK, (uint32_t)C::BLK, bar);
+      }
+    }
+  };
+
+  const int npre = my_count < kStages ? my_count : kStages;
+  for (int i = 0; i < npre; ++i) issue(i);
+
+  // query fragments
+  uint32_t qh[KSTEPS][2], ql[QF32 ? KSTEPS : 1][2];
+  load_q<D, QF32>(a, b, kvh, g, tq, qh, ql);
+
+  float kfac = a.sm_log2, vfac = exp2f(-(float)PSHIFT);
+  if constexpr (MODE == KVQ_FP8_PER_TENSOR || MODE == KVQ_NVFP4) {
+    kfac *= *reinterpret_cast<const float*>(a.pool + kHdrKScaleOffset);
+    vfac *= *reinterpret_cast<const float*>(a.pool + kHdrVScaleOffset);
+  }
+  const float pmul = exp2f((float)PSHIFT);
+
+  float o[MTILES][4];
+#pragma unroll
+  for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  bool timed_out = false;
+
+  for (int i = 0; i < my_count; ++i) {
+    const int pid = __shfl_sync(kFull, my_pid, i);
+    const uint8_t* st = ring + (i % kStages) * C::STAGE;
+    if (!mbar_wait_bounded(&wb[i % kStages], (i / kStages) & 1)) {
+      timed_out = true;
+      break;
+    }
+    if (pid >= 0) {
+      const int tok0 = (p0 + warp + kWarps * i) * kPage;
+      // ---------------- S^T = K Q^T (16 tokens x 8 heads)
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        constexpr int KW = (MODE == KVQ_NVFP4 ? D / 8 : D / 4) / 4;  // words per thread per row
+        uint32_t kg[KW], kh8[KW];
+        const int rb = tq * (KW * 4);
+#pragma unroll
+        for (int w = 0; w < KW; w += 4) {
+          lds<(KW >= 4 ? 4 : KW)>(st + swz<C::SWZ_MASK>(g * C::RW + rb + 4 * w), kg + w);
+          lds<(KW >= 4 ? 4 : KW)>(st + swz<C::SWZ_MASK>((g + 8) * C::RW + rb + 4 * w), kh8 + w);
+        }
+        if constexpr (MODE == KVQ_NVFP4) {
+          // block scales of this thread's channels: blocks (tq*D/4)/16 and (tq*D/4 + D/4 - 1)/16
+          constexpr int SB = D / 16;
+          const int blk0 = (tq * (D / 4)) / 16;
+          const int base_g = C::S_OFF + g * SB, base_h = C::S_OFF + (g + 8) * SB;
+          uint32_t sg, sh;
+          if constexpr (D / 4 >= 16) {
+            sg = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(base_g + blk0));
+            sh = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(base_h + blk0));
+          } else {
+            sg = st[swz<C::SWZ_MASK>(base_g + blk0)] * 0x0101u;
+            sh = st[swz<C::SWZ_MASK>(base_h + blk0)] * 0x0101u;
+          }
+          const __half2 sg2 = u32_as_h2(e4m3x2_to_f16x2(sg)), sh2 = u32_as_h2(e4m3x2_to_f16x2(sh));
+#pragma unroll
+          for (int w = 0; w < KW; ++w) {
+            uint32_t fg[4], fh[4];
+            e2m1x8_to_f16x2x4(kg[w], fg);
+            e2m1x8_to_f16x2x4(kh8[w], fh);
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+              const int j = 2 * w + hlf;
+              const bool second = (4 * j) >= 16;  // channel offset within the thread's D/4 range
+              const __half2 sa = second ? __high2half2(sg2) : __low2half2(sg2);
+              const __half2 sb = second ? __high2half2(sh2) : __low2half2(sh2);
+              uint32_t af[4];
+              af[0] = h2_as_u32(__hmul2(u32_as_h2(fg[2 * hlf]), sa));
+              af[1] = h2_as_u32(__hmul2(u32_as_h2(fh[2 * hlf]), sb));
+              af[2] = h2_as_u32(__hmul2(u32_as_h2(fg[2 * hlf + 1]), sa));
+              af[3] = h2_as_u32(__hmul2(u32_as_h2(fh[2 * hlf + 1]), sb));
+              mma16816(c, af, qh[j][0], qh[j][1]);
+              if constexpr (QF32) mma16816(c, af, ql[j][0], ql[j][1]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < KSTEPS; ++j) {
+            uint32_t af[4];
+            cvt_pair4<MODE>(kg[j], af[0], af[2]);
+            cvt_pair4<MODE>(kh8[j], af[1], af[3]);
+            mma16816(c, af, qh[j][0], qh[j][1]);
+            if constexpr (QF32) mma16816(c, af, ql[j][0], ql[j][1]);
+          }
+        }
+      }
+      // ---------------- scores (log2 domain), mask, online softmax
+      float fg = kfac, fh = kfac, vg = pmul, vh = pmul;
+      if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD || MODE == KVQ_FP8_PER_TOKEN_HEAD) {
+        const float* ks = reinterpret_cast<const float*>(st + C::S_OFF);  // K scales, then V scales
+        fg *= ks[g];
+        fh *= ks[g + 8];
+        vg *= ks[kPage + g];
+        vh *= ks[kPage + g + 8];
+      }
+      const bool okg = tok0 + g < t_end, okh = tok0 + g + 8 < t_end;
+      float s0 = okg ? c[0] * fg : -INFINITY, s1 = okg ? c[1] * fg : -INFINITY;
+      float s2 = okh ? c[2] * fh : -INFINITY, s3 = okh ? c[3] * fh : -INFINITY;
+      float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int x = 4; x <= 16; x <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, x));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, x));
+      }
+      const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
+      const float al0 = n0 == -INFINITY ? 1.0f : exp2f(m0 - n0);
+      const float al1 = n1 == -INFINITY ? 1.0f : exp2f(m1 - n1);
+      const float p0v = n0 == -INFINITY ? 0.0f : exp2f(s0 - n0);
+      const float p2v = n0 == -INFINITY ? 0.0f : exp2f(s2 - n0);
+      const float p1v = n1 == -INFINITY ? 0.0f : exp2f(s1 - n1);
+      const float p3v = n1 == -INFINITY ? 0.0f : exp2f(s3 - n1);
+      m0 = n0;
+      m1 = n1;
+      l0 = l0 * al0 + (p0v + p2v);
+      l1 = l1 * al1 + (p1v + p3v);
+#pragma unroll
+      for (int t = 0; t < MTILES; ++t) {
+        o[t][0] *= al0; o[t][2] *= al0;
+        o[t][1] *= al1; o[t][3] *= al1;
+      }
+      // ---------------- P^T as the B operand: f16 hi + lo, transposed per 8x8 block
+      const float x0 = p0v * vg, x1 = p1v * vg, x2 = p2v * vh, x3 = p3v * vh;
+      const __half2 hg = __floats2half2_rn(x0, x1), hh = __floats2half2_rn(x2, x3);
+      const float2 fgf = __half22float2(hg), fhf = __half22float2(hh);
+      const __half2 lg = __floats2half2_rn(x0 - fgf.x, x1 - fgf.y), lh = __floats2half2_rn(x2 - fhf.x, x3 - fhf.y);
+      const uint32_t bh0 = movmatrix_t(h2_as_u32(hg)), bh1 = movmatrix_t(h2_as_u32(hh));
+      const uint32_t bl0 = movmatrix_t(h2_as_u32(lg)), bl1 = movmatrix_t(h2_as_u32(lh));
+      // ---------------- O^T += V^T P^T
+      {
+        const uint8_t* vb = st + C::V_OFF;
+        const int r0 = 2 * tq, r1 = 2 * tq + 1, r2 = 2 * tq + 8, r3 = 2 * tq + 9;
+        if constexpr (MODE == KVQ_NVFP4) {
+          constexpr int VB = D / 16;  // bytes per thread per row (D/8 channels at 4 bits)
+          constexpr int VW = VB >= 4 ? VB / 4 : 1;
+          uint32_t A0[VW], A1[VW], A2[VW], A3[VW];
+          const int cb = g * VB;
+          if constexpr (VB >= 8) {
+            lds<2>(vb + swz<C::SWZ_MASK>(C::V_OFF * 0 + r0 * C::RW + cb), A0);
+            lds<2>(vb + swz<C::SWZ_MASK>(r1 * C::RW + cb), A1);
+            lds<2>(vb + swz<C::SWZ_MASK>(r2 * C::RW + cb), A2);
+            lds<2>(vb + swz<C::SWZ_MASK>(r3 * C::RW + cb), A3);
+          } else {
+            A0[0] = *reinterpret_cast<const uint16_t*>(vb + swz<C::SWZ_MASK>(r0 * C::RW + cb));
+            A1[0] = *reinterpret_cast<const uint16_t*>(vb + swz<C::SWZ_MASK>(r1 * C::RW + cb));
+            A2[0] = *reinterpret_cast<const uint16_t*>(vb + swz<C::SWZ_MASK>(r2 * C::RW + cb));
+            A3[0] = *reinterpret_cast<const uint16_t*>(vb + swz<C::SWZ_MASK>(r3 * C::RW + cb));
+          }
+          // V block scales of rows r0..r3 for this thread's block
+          const int vblk = (g * (D / 8)) / 16;
+          const uint8_t* vs = st + C::S_OFF + kPage * (D / 16);
+          const uint32_t s01 = st[swz<C::SWZ_MASK>(C::S_OFF + kPage * (D / 16) + r0 * (D / 16) + vblk)] |
+                               (st[swz<C::SWZ_MASK>(C::S_OFF + kPage * (D / 16) + r1 * (D / 16) + vblk)] << 8);
+          const uint32_t s23 = st[swz<C::SWZ_MASK>(C::S_OFF + kPage * (D / 16) + r2 * (D / 16) + vblk)] |
+                               (st[swz<C::SWZ_MASK>(C::S_OFF + kPage * (D / 16) + r3 * (D / 16) + vblk)] << 8);
+          (void)vs;
+          const __half2 sc01 = u32_as_h2(e4m3x2_to_f16x2(s01)), sc23 = u32_as_h2(e4m3x2_to_f16x2(s23));
+#pragma unroll
+          for (int w = 0; w < VW; ++w) {
+            // pair rows (r0, r1) and (r2, r3) nibble by nibble: even channel e = 8w+2k, odd e+1
+            const uint32_t xe01 = bitsel(A0[w], A1[w] << 4, 0x0F0F0F0Fu);
+            const uint32_t xo01 = bitsel(A0[w] >> 4, A1[w], 0x0F0F0F0Fu);
+            const uint32_t xe23 = bitsel(A2[w], A3[w] << 4, 0x0F0F0F0Fu);
+            const uint32_t xo23 = bitsel(A2[w] >> 4, A3[w], 0x0F0F0F0Fu);
+            uint32_t fe01[4], fo01[4], fe23[4], fo23[4];
+            e2m1x8_to_f16x2x4(xe01, fe01);
+            e2m1x8_to_f16x2x4(xo01, fo01);
+            e2m1x8_to_f16x2x4(xe23, fe23);
+            e2m1x8_to_f16x2x4(xo23, fo23);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int t = 4 * w + k;
+              if (t < MTILES) {
+                uint32_t av[4];
+                av[0] = h2_as_u32(__hmul2(u32_as_h2(fe01[k]), sc01));
+                av[1] = h2_as_u32(__hmul2(u32_as_h2(fo01[k]), sc01));
+                av[2] = h2_as_u32(__hmul2(u32_as_h2(fe23[k]), sc23));
+                av[3] = h2_as_u32(__hmul2(u32_as_h2(fo23[k]), sc23));
+                mma16816(o[t], av, bh0, bh1);
+                mma16816(o[t], av, bl0, bl1);
+              }
+            }
+          }
+        } else {
+          constexpr int VW = D / 32;  // words per thread per row (D/8 one-byte channels)
+          uint32_t A0[VW], A1[VW], A2[VW], A3[VW];
+          const int cb = g * (D / 8);
+          lds<VW>(vb + swz<C::SWZ_MASK>(r0 * C::RW + cb) - C::V_OFF + C::V_OFF, A0);
+          lds<VW>(vb + swz<C::SWZ_MASK>(r1 * C::RW + cb), A1);
+          lds<VW>(vb + swz<C::SWZ_MASK>(r2 * C::RW + cb), A2);
+          lds<VW>(vb + swz<C::SWZ_MASK>(r3 * C::RW + cb), A3);
+#pragma unroll
+          for (int w = 0; w < VW; ++w) {
+            const uint32_t x01 = prmt(A0[w], A1[w], 0x5140u), y01 = prmt(A0[w], A1[w], 0x7362u);
+            const uint32_t x23 = prmt(A2[w], A3[w], 0x5140u), y23 = prmt(A2[w], A3[w], 0x7362u);
+            uint32_t av[4];
+            cvt_pair4<MODE>(x01, av[0], av[1]);
+            cvt_pair4<MODE>(x23, av[2], av[3]);
+            mma16816(o[2 * w], av, bh0, bh1);
+            mma16816(o[2 * w], av, bl0, bl1);
+            cvt_pair4<MODE>(y01, av[0], av[1]);
+            cvt_pair4<MODE>(y23, av[2], av[3]);
+            mma16816(o[2 * w + 1], av, bh0, bh1);
+            mma16816(o[2 * w + 1], av, bl0, bl1);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (i + kStages < my_count) {
+      if (lane == 0) fence_proxy_async_smem();
+      issue(i + kStages);
+    }
+  }
+  if (timed_out && lane == 0) set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_TIMEOUT);
+
+  // ---------------- merge the warps of this CTA
+#pragma unroll
+  for (int x = 4; x <= 16; x <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, x);
+    l1 += __shfl_xor_sync(kFull, l1, x);
+  }
+  __syncthreads();  // every warp is done with its ring: reuse it for the merge
+  float* red_o = reinterpret_cast<float*>(smem);             // [W][8][D]
+  float* red_m = red_o + kWarps * 8 * D;                     // [W][8]
+  float* red_l = red_m + kWarps * 8;                         // [W][8]
+  if (g == 0) {
+    red_m[warp * 8 + 2 * tq] = m0;
+    red_m[warp * 8 + 2 * tq + 1] = m1;
+    red_l[warp * 8 + 2 * tq] = l0;
+    red_l[warp * 8 + 2 * tq + 1] = l1;
+  }
+  {
+    float* ow = red_o + warp * 8 * D;
+    const int d0 = g * (D / 8);
+#pragma unroll
+    for (int t = 0; t < MTILES; ++t) {
+      ow[(2 * tq) * D + d0 + 2 * t] = o[t][0];
+      ow[(2 * tq + 1) * D + d0 + 2 * t] = o[t][1];
+      ow[(2 * tq) * D + d0 + 2 * t + 1] = o[t][2];
+      ow[(2 * tq + 1) * D + d0 + 2 * t + 1] = o[t][3];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < a.G * D; idx += blockDim.x) {
+    const int h = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * 8 + h]);
+    float L = 0.0f, O = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float e = exp2f(red_m[w * 8 + h] - M);
+        L += red_l[w * 8 + h] * e;
+        O += red_o[(w * 8 + h) * D + d] * e;
+      }
+    }
+    const int hq = kvh * a.G + h;
+    if (a.num_splits == 1) {
+      const float r = L > 0.0f ? O * vfac / L : 0.0f;
+      const long long oi = ((long long)b * a.Hq + hq) * D + d;
+      if (a.out_f32) static_cast<float*>(a.out)[oi] = r;
+      else static_cast<__half*>(a.out)[oi] = __float2half_rn(r);
+    } else {
+      const long long pi = ((long long)b * a.Hq + hq) * a.num_splits + split;
+      a.ws_o[pi * D + d] = O * vfac;
+      if (d == 0) {
+        a.ws_ml[2 * pi] = M;
+        a.ws_ml[2 * pi + 1] = L;
+      }
+    }
+  }
+}
+
+// Merge the splits of each (sequence, query head).
+template <int D>
+__global__ void __launch_bounds__(D) combine_kernel(const __grid_constant__ DecodeArgs a) {
+  const int b = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, d = threadIdx.x;
+  int n = a.seq_lens[b];
+  const int lim = min(a.max_seq_len, a.max_pages * kPage);
+  n = n < 0 ? 0 : (n > lim ? lim : n);
+  const int ns = (n + a.tokens_per_split - 1) / a.tokens_per_split;
+  const long long base = ((long long)b * a.Hq + hq) * a.num_splits;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, a.ws_ml[2 * (base + s)]);
+  float L = 0.0f, O = 0.0f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < ns; ++s) {
+      const float e = exp2f(a.ws_ml[2 * (base + s)] - M);
+      L += a.ws_ml[2 * (base + s) + 1] * e;
+      O += a.ws_o[(base + s) * D + d] * e;
+    }
+  }
+  const float r = L > 0.0f ? O / L : 0.0f;
+  const long long oi = ((long long)b * a.Hq + hq) * D + d;
+  if (a.out_f32) static_cast<float*>(a.out)[oi] = r;
+  else static_cast<__half*>(a.out)[oi] = __float2half_rn(r);
+}
+
+template <int MODE, int D, bool QF32>
+cudaError_t launch_mode(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s) {
+  using C = Cfg<MODE, D>;
+  const size_t ring = (size_t)kWarps * kStages * C::STAGE;
+  const size_t merge = (size_t)kWarps * 8 * (D + 2) * sizeof(float);
+  const size_t smem = (ring > merge ? ring : merge) + 1024;
+  auto kern = decode_kernel<MODE, D, QF32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_splits, a.Hkv, a.B);
+  kern<<<grid, kWarps * 32, smem, s>>>(a, c->tmap);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.num_splits == 1) return e;
+  combine_kernel<D><<<a.B * a.Hq, D, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, bool QF32>
+cudaError_t launch_d(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s) {
+  switch (c->cfg.mode) {
+    case KVQ_FP8_PER_TENSOR: return launch_mode<KVQ_FP8_PER_TENSOR, D, QF32>(c, a, s);
+    case KVQ_INT8_PER_TOKEN_HEAD: return launch_mode<KVQ_INT8_PER_TOKEN_HEAD, D, QF32>(c, a, s);
+    case KVQ_FP8_PER_TOKEN_HEAD: return launch_mode<KVQ_FP8_PER_TOKEN_HEAD, D, QF32>(c, a, s);
+    case KVQ_NVFP4: return launch_mode<KVQ_NVFP4, D, QF32>(c, a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int max_seq_len) {
+  (void)num_q_heads;
+  DecodePlan p{1, kPage, 0};
+  const int P = c->cfg.page_size;
+  const long long pages = (max_seq_len + P - 1) / P;
+  if (pages <= 0) return p;
+  const long long units = (long long)num_seqs * c->cfg.num_kv_heads;
+  const int per_warp_pages = 32;  // one page id per lane
+  const long long cap = (long long)kWarps * per_warp_pages;
+  long long splits = (8LL * num_sms() + units - 1) / (units > 0 ? units : 1);
+  const long long min_splits = (pages + cap - 1) / cap;
+  const long long max_splits = (pages + kWarps - 1) / kWarps;
+  if (splits > max_splits) splits = max_splits;
+  if (splits < min_splits) splits = min_splits;
+  if (splits < 1) splits = 1;
+  long long pps = (pages + splits - 1) / splits;
+  p.tokens_per_split = (int)(pps * P);
+  p.num_splits = (int)((max_seq_len + p.tokens_per_split - 1) / p.tokens_per_split);
+  if (p.num_splits > 1)
+    p.workspace_bytes = (size_t)num_seqs * num_q_heads * p.num_splits * (c->cfg.head_dim + 2) * sizeof(float);
+  return p;
+}
+
+cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void* q, const int32_t* block_table,
+                          int max_pages, const int32_t* seq_lens, int num_seqs, int num_q_heads, int max_seq_len,
+                          float softmax_scale, void* out, int out_dtype, void* workspace, cudaStream_t stream) {
+  DecodeArgs a;
+  a.pool = c->base;
+  a.q = q;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_ml = plan.num_splits > 1 ? a.ws_o + (size_t)num_seqs * num_q_heads * plan.num_splits * c->cfg.head_dim
+                                : nullptr;
+  a.num_pages = c->cfg.num_pages;
+  a.Hkv = c->cfg.num_kv_heads;
+  a.Hq = num_q_heads;
+  a.G = num_q_heads / c->cfg.num_kv_heads;
+  a.B = num_seqs;
+  a.max_pages = max_pages;
+  a.max_seq_len = max_seq_len;
+  a.tokens_per_split = plan.tokens_per_split;
+  a.num_splits = plan.num_splits;
+  a.out_f32 = out_dtype == KVQ_F32;
+  a.sm_log2 = softmax_scale * kLog2e;
+  a.block_bytes = c->block_bytes;
+  a.rows_per_block = c->rows_per_block;
+  if (num_seqs == 0 || max_seq_len == 0 && false) return cudaSuccess;
+  const bool qf32 = c->cfg.io_dtype == KVQ_F32;
+  if (c->cfg.head_dim == 128)
+    return qf32 ? launch_d<128, true>(c, a, stream) : launch_d<128, false>(c, a, stream);
+  if (c->cfg.head_dim == 32)
+    return qf32 ? launch_d<32, true>(c, a, stream) : launch_d<32, false>(c, a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvq

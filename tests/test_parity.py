@@ -1,0 +1,230 @@
+"""GPU parity of libkvq against the CPU oracle, through the C ABI.
+
+Quantize-on-write: pool bytes and scales bit-exact.  Decode attention: fp32
+outputs within 2e-3 max-abs of the fp64 oracle; fp16 outputs within 2e-3 of
+fp16(oracle) or one fp16 ulp of it.  Sizes here finish on the oracle in
+seconds but span several pages, several KV splits and ragged tails."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from _helpers import (FILL, check_attention, gpu_cache, gpu_calibrate, gpu_decode, header_scales, kvq,
+                      make_case, oracle_decode, oracle_pool)
+
+pytestmark = pytest.mark.gpu
+
+MODES4 = ["fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nvfp4"]
+LENS = [1, 15, 16, 17, 100, 333, 1000, 2500]
+KVARN_LENS = [128, 256, 640]
+
+
+def small_workload(mode, D=128, Hq=16, Hkv=2, io="f16", seed=7):
+    """Small shapes with the outlier structure of the mode's full-size workload."""
+    P = 128 if mode == "kvarn_k4v2_g128" else 16
+    extra = {
+        "fp8_per_tensor": dict(sink_tokens=4, sink_gain=20.0),
+        "int8_per_token_head": dict(outlier_token_frac=0.01, token_gain=30.0),
+        "fp8_per_token_head": dict(outlier_token_frac=0.01, token_gain=30.0),
+        "nvfp4": dict(outlier_channels=3, channels_per_head=True, channel_gain=10.0),
+        "kvarn_k4v2_g128": dict(outlier_channels=4, channels_per_head=True, channel_gain=15.0),
+    }[mode]
+    return wl.Workload(name=f"small_{mode}_{D}_{io}", mode=mode, num_seqs=1, num_q_heads=Hq, num_kv_heads=Hkv,
+                       head_dim=D, page_size=P, io_dtype=io, seed=seed, seq_len_range=(1, 1), **extra)
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _upload_oracle_pool(cache, pool_np, c):
+    cache.pool[256:].copy_(torch.from_numpy(pool_np[256:]).cuda())
+    kvq().kvq_cache_set_tensor_scales(cache, c.k_scale, c.v_scale)
+
+
+# ------------------------------------------------------------------ write
+@pytest.mark.parametrize("D,io", [(128, "f16"), (32, "f32"), (32, "f16"), (128, "f32")])
+@pytest.mark.parametrize("mode", MODES4)
+def test_write_bit_exact(mode, D, io):
+    K = kvq()
+    c = make_case(small_workload(mode, D=D, io=io), LENS[:6], slack_pages=2)
+    slots = c.slots.copy()
+    slots[3] = -1                                    # skipped token
+    slots[7] = c.lay.num_pages * 16 + 5              # out of range: skipped and flagged
+    cache = gpu_cache(c)
+    kd, vd = _dev(c.k), _dev(c.v)
+    if mode in ("fp8_per_tensor", "nvfp4"):
+        gpu_calibrate(cache, kd, vd)
+        ks, vs = header_scales(cache)
+        assert np.float32(ks) == np.float32(c.k_scale) and np.float32(vs) == np.float32(c.v_scale)
+    K.kvq_quantize_write(cache, kd, vd, _dev(slots))
+    flags = K.kvq_cache_read_errors(cache)
+    assert flags == 0x1, hex(flags)
+    got = cache.pool.cpu().numpy()
+    ref = oracle_pool(c, slots=slots)
+    diff = np.flatnonzero(got[256:] != ref[256:])
+    assert diff.size == 0, f"{diff.size} bytes differ, first at pool offset {256 + diff[0]}"
+
+
+def test_write_kvarn_bit_exact():
+    K = kvq()
+    c = make_case(small_workload("kvarn_k4v2_g128"), KVARN_LENS, slack_pages=1)
+    cache = gpu_cache(c)
+    K.kvq_quantize_write(cache, _dev(c.k), _dev(c.v), _dev(c.slots))
+    assert K.kvq_cache_read_errors(cache) == 0
+    got = cache.pool.cpu().numpy()
+    ref = oracle_pool(c)
+    diff = np.flatnonzero(got[256:] != ref[256:])
+    assert diff.size == 0, f"{diff.size} bytes differ, first at pool offset {256 + diff[0]}"
+
+
+def test_write_kvarn_partial_tile_is_flagged_and_skipped():
+    K = kvq()
+    c = make_case(small_workload("kvarn_k4v2_g128"), [256], slack_pages=1)
+    slots = c.slots.copy()
+    slots[128:] = slots[128:] + 1                      # second tile no longer fills a page in order
+    slots[-1] = slots[128] - 1
+    cache = gpu_cache(c)
+    K.kvq_quantize_write(cache, _dev(c.k), _dev(c.v), _dev(slots))
+    assert K.kvq_cache_read_errors(cache) == 0x4
+    got = cache.pool.cpu().numpy()
+    ref = oracle_pool(c, slots=slots)
+    assert (got[256:] == ref[256:]).all()
+
+
+def test_write_conversion_edge_values():
+    """E4M3 and E2M1 ties, signed zeros, tiny values and saturation go through the
+    hardware conversions exactly as the format definitions say."""
+    K = kvq()
+    pos = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+    mids = (pos[1:] + pos[:-1]) / 2
+    vals = np.concatenate([pos, mids, -pos, -mids, [0.0, -0.0, 1e-8, -1e-8, 500.0, -500.0, 6e4, -6e4]])
+    vals = vals.astype(np.float16)
+    D = 128
+    n = (len(vals) + D - 1) // D
+    row = np.zeros(n * D, np.float16)
+    row[:len(vals)] = vals
+    x = row.reshape(n, 1, D)
+    w = wl.Workload(name="edge", mode="fp8_per_tensor", num_seqs=1, num_q_heads=1, num_kv_heads=1, head_dim=D,
+                    page_size=16, io_dtype="f16", seed=1, seq_len=n)
+    for mode, ks in (("fp8_per_tensor", 1.0), ("nvfp4", 1.0), ("fp8_per_token_head", None),
+                     ("int8_per_token_head", None)):
+        wm = w.with_mode(mode)
+        lay = wl.paged_layout(wm, np.array([n], np.int32))
+        c = make_case(wm, [n])
+        c.k, c.v = x, (x * np.float16(0.75)).astype(np.float16)
+        c.slots = wl.slots_for_seq(wm, lay, 0)
+        c.lay = lay
+        c.k_scale = c.v_scale = 1.0
+        cache = gpu_cache(c)
+        K.kvq_cache_set_tensor_scales(cache, 1.0, 1.0)
+        K.kvq_quantize_write(cache, _dev(c.k), _dev(c.v), _dev(c.slots))
+        got = cache.pool.cpu().numpy()
+        ref = oracle_pool(c)
+        assert (got[256:] == ref[256:]).all(), mode
+    # E2M1 ties: with s_t = 1 a block whose max is 6 has s_b = 1 and x/(s_t s_b) = x
+    ties = np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25, -5.0, 0.0, -0.0, 0.1, -0.1],
+                    np.float16)
+    xt = np.tile(ties, D // 16).reshape(1, 1, D)
+    xt = np.repeat(xt, 16, axis=0)
+    wm = w.with_mode("nvfp4")
+    lay = wl.paged_layout(wm, np.array([16], np.int32))
+    c = make_case(wm, [16])
+    c.k, c.v, c.lay = xt, xt, lay
+    c.slots = wl.slots_for_seq(wm, lay, 0)
+    c.k_scale = c.v_scale = 1.0
+    cache = gpu_cache(c)
+    K.kvq_cache_set_tensor_scales(cache, 1.0, 1.0)
+    K.kvq_quantize_write(cache, _dev(c.k), _dev(c.v), _dev(c.slots))
+    got = cache.pool.cpu().numpy()
+    assert (got[256:] == oracle_pool(c)[256:]).all()
+
+
+def test_tensor_amax_exact():
+    K = kvq()
+    rng = np.random.default_rng(0)
+    for n in (1, 7, 8, 1000, 123457):
+        x = (rng.standard_normal(n) * 50).astype(np.float16)
+        out = torch.zeros(1, dtype=torch.float32, device="cuda")
+        K.kvq_tensor_amax(_dev(x), out)
+        assert out.item() == np.abs(x.astype(np.float32)).max()
+        xf = x.astype(np.float32)
+        K.kvq_tensor_amax(_dev(xf), out)
+        assert out.item() == np.abs(xf).max()
+
+
+# ------------------------------------------------------------------ decode
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+@pytest.mark.parametrize("D,io,Hq,Hkv", [(128, "f16", 16, 2), (128, "f16", 8, 2), (32, "f32", 4, 4),
+                                         (32, "f16", 16, 2), (128, "f32", 8, 1)])
+@pytest.mark.parametrize("mode", MODES4)
+def test_decode_parity(mode, D, io, Hq, Hkv, out_dtype):
+    c = make_case(small_workload(mode, D=D, io=io, Hq=Hq, Hkv=Hkv), LENS + [0], slack_pages=2)
+    pool = oracle_pool(c)
+    cache = gpu_cache(c)
+    _upload_oracle_pool(cache, pool, c)
+    out, plan = gpu_decode(cache, c, out_dtype=out_dtype)
+    assert plan[0] > 1, "the case should exercise several KV splits"
+    ref = oracle_decode(c, pool)
+    check_attention(out, ref)
+    assert kvq().kvq_cache_read_errors(cache) == 0
+
+
+@pytest.mark.parametrize("mode", MODES4)
+def test_decode_empty_and_single_token(mode):
+    c = make_case(small_workload(mode), [0, 1, 16, 0, 2], slack_pages=1)
+    pool = oracle_pool(c)
+    cache = gpu_cache(c)
+    _upload_oracle_pool(cache, pool, c)
+    out, _ = gpu_decode(cache, c)
+    ref = oracle_decode(c, pool)
+    check_attention(out, ref)
+    assert (out[0] == 0).all() and (out[3] == 0).all()
+
+
+@pytest.mark.parametrize("mode", ["int8_per_token_head", "nvfp4"])
+def test_decode_bad_page_and_long_seq_are_flagged(mode):
+    K = kvq()
+    c = make_case(small_workload(mode), [300, 200], slack_pages=1)
+    pool = oracle_pool(c)
+    cache = gpu_cache(c)
+    _upload_oracle_pool(cache, pool, c)
+    bt = c.lay.block_table.copy()
+    bt[0, 3] = 10 ** 6                                   # out-of-range page id: its tokens drop out
+    out, _ = gpu_decode(cache, c, bt=bt)
+    assert K.kvq_cache_read_errors(cache) == 0x2
+    check_attention(out, oracle_decode(c, pool, bt=bt))
+    out2, _ = gpu_decode(cache, c, max_seq_len=256)      # seq 0 (300 tokens) exceeds the bound
+    assert K.kvq_cache_read_errors(cache) & 0x8
+    check_attention(out2, oracle_decode(c, pool, lens=np.array([256, 200], np.int32)))
+
+
+def test_decode_tiny_config_end_to_end():
+    """The tiny INT8 per-token-head workload (fp32 K, V, q; D=32; B=2; T=16)
+    through write + decode on the GPU, against the oracle's write + decode."""
+    K = kvq()
+    w = wl.WORKLOADS["int8_pth_tiny"]
+    c = make_case(w, list(wl.seq_lens(w)))
+    cache = gpu_cache(c)
+    K.kvq_quantize_write(cache, _dev(c.k), _dev(c.v), _dev(c.slots))
+    pool = oracle_pool(c)
+    assert (cache.pool.cpu().numpy()[256:] == pool[256:]).all()
+    out, plan = gpu_decode(cache, c)
+    check_attention(out, oracle_decode(c, pool))
+
+
+def test_mode_mismatch_and_unsupported():
+    K = kvq()
+    c = make_case(small_workload("nvfp4"), [16])
+    cache = gpu_cache(c)
+    with pytest.raises(K.KVQError) as e:
+        K.kvq_quantize_write(cache, _dev(c.k), _dev(c.v), _dev(c.slots), mode="fp8_per_tensor")
+    assert e.value.status == 3
+    out = torch.empty((1, 16, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(K.KVQError) as e:
+        K.kvq_decode_attention(cache, _dev(c.q), _dev(c.lay.block_table), _dev(c.lay.seq_lens), out,
+                               max_seq_len=16, mode="int8_per_token_head")
+    assert e.value.status == 3
