@@ -480,6 +480,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="shrink the batch (same shapes otherwise), e.g. to size an ncu capture")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -487,6 +489,9 @@ def main(argv=None):
         w = wl.WORKLOADS["pth_b64_u1k_32k"].with_mode("fp8_per_token_head")
     else:
         w = wl.WORKLOADS[args.workload]
+    if args.num_seqs is not None:
+        import dataclasses
+        w = dataclasses.replace(w, num_seqs=args.num_seqs, name=f"{w.name}[B={args.num_seqs}]")
     res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if res is not None:
         print(json.dumps(res), flush=True)

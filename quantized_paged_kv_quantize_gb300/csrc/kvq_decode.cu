@@ -112,6 +112,17 @@ __device__ __forceinline__ void cvt_pair4(uint32_t w, uint32_t& lo, uint32_t& hi
   }
 }
 
+// Like cvt_pair4, but int8 words arrive already biased (x ^ 0x80 per byte).
+template <int MODE>
+__device__ __forceinline__ void cvt_pair4_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD) {
+    lo = i8x2_to_f16x2(w, 0x4140u);
+    hi = i8x2_to_f16x2(w, 0x4342u);
+  } else {
+    cvt_pair4<MODE>(w, lo, hi);
+  }
+}
+
 // Q as the B operand of S^T = K Q^T: b0 = Q[g][d(j,2tq..2tq+1)], b1 = Q[g][d(j,2tq+8..+9)]
 // with d(j, .) = tq*D/4 + 4j + {0,1} and {2,3}.  Heads >= G are zero.
 template <int D, bool QF32>
@@ -138,6 +149,179 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int 
                          : make_uint2(0u, 0u);
       qh[j][0] = u.x;
       qh[j][1] = u.y;
+    }
+  }
+}
+
+__device__ __forceinline__ float ex2(float x) {  // 2^x on the SFU (rel. error ~2^-22), ex2(-inf) = 0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// S^T = K Q^T for one staged page: c[0..1] = tokens g, c[2..3] = token g+8, heads 2tq, 2tq+1.
+template <int MODE, int D, bool QF32>
+__device__ __forceinline__ void qk_page(const uint8_t* st, int g, int tq, const uint32_t (*qh)[2],
+                                        const uint32_t (*ql)[2], float* c) {
+  using C = Cfg<MODE, D>;
+  constexpr int KSTEPS = C::KSTEPS;
+  constexpr int KW = (MODE == KVQ_NVFP4 ? D / 8 : D / 4) / 4;  // words per thread per row
+  uint32_t kg[KW], kh8[KW];
+  const int rb = tq * (KW * 4);
+#pragma unroll
+  for (int w = 0; w < KW; w += 4) {
+    lds<(KW >= 4 ? 4 : KW)>(st + swz<C::SWZ_MASK>(g * C::RW + rb + 4 * w), kg + w);
+    lds<(KW >= 4 ? 4 : KW)>(st + swz<C::SWZ_MASK>((g + 8) * C::RW + rb + 4 * w), kh8 + w);
+  }
+  if constexpr (MODE == KVQ_NVFP4) {
+    constexpr int SB = D / 16;
+    const int blk0 = (tq * (D / 4)) / 16;
+    const int base_g = C::S_OFF + g * SB, base_h = C::S_OFF + (g + 8) * SB;
+    uint32_t sg, sh;
+    if constexpr (D / 4 >= 16) {
+      sg = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(base_g + blk0));
+      sh = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(base_h + blk0));
+    } else {
+      sg = st[swz<C::SWZ_MASK>(base_g + blk0)] * 0x0101u;
+      sh = st[swz<C::SWZ_MASK>(base_h + blk0)] * 0x0101u;
+    }
+    const __half2 sg2 = u32_as_h2(e4m3x2_to_f16x2(sg)), sh2 = u32_as_h2(e4m3x2_to_f16x2(sh));
+#pragma unroll
+    for (int w = 0; w < KW; ++w) {
+      uint32_t fg[4], fh[4];
+      e2m1x8_to_f16x2x4(kg[w], fg);
+      e2m1x8_to_f16x2x4(kh8[w], fh);
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int j = 2 * w + hlf;
+        const bool second = (4 * j) >= 16;  // channel offset within the thread's D/4 range
+        const __half2 sa = second ? __high2half2(sg2) : __low2half2(sg2);
+        const __half2 sb = second ? __high2half2(sh2) : __low2half2(sh2);
+        uint32_t af[4];
+        af[0] = h2_as_u32(__hmul2(u32_as_h2(fg[2 * hlf]), sa));
+        af[1] = h2_as_u32(__hmul2(u32_as_h2(fh[2 * hlf]), sb));
+        af[2] = h2_as_u32(__hmul2(u32_as_h2(fg[2 * hlf + 1]), sa));
+        af[3] = h2_as_u32(__hmul2(u32_as_h2(fh[2 * hlf + 1]), sb));
+        mma16816(c, af, qh[j][0], qh[j][1]);
+        if constexpr (QF32) mma16816(c, af, ql[j][0], ql[j][1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < KSTEPS; ++j) {
+      uint32_t af[4];
+      cvt_pair4<MODE>(kg[j], af[0], af[2]);
+      cvt_pair4<MODE>(kh8[j], af[1], af[3]);
+      mma16816(c, af, qh[j][0], qh[j][1]);
+      if constexpr (QF32) mma16816(c, af, ql[j][0], ql[j][1]);
+    }
+  }
+}
+
+// O^T += V^T P^T for one staged page.  Rows (tokens) >= nvalid are zeroed before
+// use so that whatever bytes an unwritten slot holds cannot reach the output.
+template <int MODE, int D>
+__device__ __forceinline__ void pv_page(const uint8_t* st, int g, int tq, int nvalid, uint32_t bh0, uint32_t bh1,
+                                        uint32_t bl0, uint32_t bl1, float (*o)[4]) {
+  using C = Cfg<MODE, D>;
+  constexpr int MTILES = C::MTILES;
+  const int r0 = 2 * tq, r1 = 2 * tq + 1, r2 = 2 * tq + 8, r3 = 2 * tq + 9;
+  const bool partial = nvalid < kPage;
+  if constexpr (MODE == KVQ_NVFP4) {
+    constexpr int VB = D / 16;  // bytes per thread per row (D/8 channels at 4 bits)
+    constexpr int VW = VB >= 4 ? VB / 4 : 1;
+    uint32_t A0[VW], A1[VW], A2[VW], A3[VW];
+    const int cb = g * VB;
+    if constexpr (VB >= 8) {
+      lds<2>(st + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb), A0);
+      lds<2>(st + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb), A1);
+      lds<2>(st + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb), A2);
+      lds<2>(st + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb), A3);
+    } else {
+      A0[0] = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb));
+      A1[0] = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb));
+      A2[0] = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb));
+      A3[0] = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb));
+    }
+    const int vblk = (g * (D / 8)) / 16;
+    constexpr int VS = C::S_OFF + kPage * (D / 16);  // V block scales
+    uint32_t b0 = st[swz<C::SWZ_MASK>(VS + r0 * (D / 16) + vblk)], b1 = st[swz<C::SWZ_MASK>(VS + r1 * (D / 16) + vblk)];
+    uint32_t b2 = st[swz<C::SWZ_MASK>(VS + r2 * (D / 16) + vblk)], b3 = st[swz<C::SWZ_MASK>(VS + r3 * (D / 16) + vblk)];
+    if (partial) {
+#pragma unroll
+      for (int w = 0; w < VW; ++w) {
+        if (r0 >= nvalid) A0[w] = 0;
+        if (r1 >= nvalid) A1[w] = 0;
+        if (r2 >= nvalid) A2[w] = 0;
+        if (r3 >= nvalid) A3[w] = 0;
+      }
+      if (r0 >= nvalid) b0 = 0;
+      if (r1 >= nvalid) b1 = 0;
+      if (r2 >= nvalid) b2 = 0;
+      if (r3 >= nvalid) b3 = 0;
+    }
+    const __half2 sc01 = u32_as_h2(e4m3x2_to_f16x2(b0 | (b1 << 8)));
+    const __half2 sc23 = u32_as_h2(e4m3x2_to_f16x2(b2 | (b3 << 8)));
+#pragma unroll
+    for (int w = 0; w < VW; ++w) {
+      // pair rows (r0, r1) and (r2, r3) nibble by nibble: even channel e = 8w+2k, odd e+1
+      const uint32_t xe01 = bitsel(A0[w], A1[w] << 4, 0x0F0F0F0Fu);
+      const uint32_t xo01 = bitsel(A0[w] >> 4, A1[w], 0x0F0F0F0Fu);
+      const uint32_t xe23 = bitsel(A2[w], A3[w] << 4, 0x0F0F0F0Fu);
+      const uint32_t xo23 = bitsel(A2[w] >> 4, A3[w], 0x0F0F0F0Fu);
+      uint32_t fe01[4], fo01[4], fe23[4], fo23[4];
+      e2m1x8_to_f16x2x4(xe01, fe01);
+      e2m1x8_to_f16x2x4(xo01, fo01);
+      e2m1x8_to_f16x2x4(xe23, fe23);
+      e2m1x8_to_f16x2x4(xo23, fo23);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int t = 4 * w + k;
+        if (t < MTILES) {
+          uint32_t av[4];
+          av[0] = h2_as_u32(__hmul2(u32_as_h2(fe01[k]), sc01));
+          av[1] = h2_as_u32(__hmul2(u32_as_h2(fo01[k]), sc01));
+          av[2] = h2_as_u32(__hmul2(u32_as_h2(fe23[k]), sc23));
+          av[3] = h2_as_u32(__hmul2(u32_as_h2(fo23[k]), sc23));
+          mma16816(o[t], av, bh0, bh1);
+          mma16816(o[t], av, bl0, bl1);
+        }
+      }
+    }
+  } else {
+    constexpr int VW = D / 32;  // words per thread per row (D/8 one-byte channels)
+    uint32_t A0[VW], A1[VW], A2[VW], A3[VW];
+    const int cb = g * (D / 8);
+    lds<VW>(st + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb), A0);
+    lds<VW>(st + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb), A1);
+    lds<VW>(st + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb), A2);
+    lds<VW>(st + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb), A3);
+    if (partial) {
+#pragma unroll
+      for (int w = 0; w < VW; ++w) {
+        if (r0 >= nvalid) A0[w] = 0;
+        if (r1 >= nvalid) A1[w] = 0;
+        if (r2 >= nvalid) A2[w] = 0;
+        if (r3 >= nvalid) A3[w] = 0;
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < VW; ++w) {
+      uint32_t a0 = A0[w], a1 = A1[w], a2 = A2[w], a3 = A3[w];
+      if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD) {  // bias once per word: x + 128
+        a0 ^= 0x80808080u; a1 ^= 0x80808080u; a2 ^= 0x80808080u; a3 ^= 0x80808080u;
+      }
+      const uint32_t x01 = prmt(a0, a1, 0x5140u), y01 = prmt(a0, a1, 0x7362u);
+      const uint32_t x23 = prmt(a2, a3, 0x5140u), y23 = prmt(a2, a3, 0x7362u);
+      uint32_t av[4];
+      cvt_pair4_biased<MODE>(x01, av[0], av[1]);
+      cvt_pair4_biased<MODE>(x23, av[2], av[3]);
+      mma16816(o[2 * w], av, bh0, bh1);
+      mma16816(o[2 * w], av, bl0, bl1);
+      cvt_pair4_biased<MODE>(y01, av[0], av[1]);
+      cvt_pair4_biased<MODE>(y23, av[2], av[3]);
+      mma16816(o[2 * w + 1], av, bh0, bh1);
+      mma16816(o[2 * w + 1], av, bl0, bl1);
     }
   }
 }
@@ -220,12 +404,16 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_consta
   uint32_t qh[KSTEPS][2], ql[QF32 ? KSTEPS : 1][2];
   load_q<D, QF32>(a, b, kvh, g, tq, qh, ql);
 
-  float kfac = a.sm_log2, vfac = exp2f(-(float)PSHIFT);
+  // Scores in log2 units: s = c * kfac (FP8 per-tensor, NVFP4: the K tensor scale
+  // is uniform) or c * ks[t] * softmax_scale*log2(e) (per-token-head).  The
+  // probabilities enter P V scaled by 2^PSHIFT (added in the exponent); l sums the
+  // same scaled values, so O / l needs no correction.
+  float kfac = a.sm_log2, vfac = 1.0f;
   if constexpr (MODE == KVQ_FP8_PER_TENSOR || MODE == KVQ_NVFP4) {
     kfac *= *reinterpret_cast<const float*>(a.pool + kHdrKScaleOffset);
-    vfac *= *reinterpret_cast<const float*>(a.pool + kHdrVScaleOffset);
+    vfac = *reinterpret_cast<const float*>(a.pool + kHdrVScaleOffset);
   }
-  const float pmul = exp2f((float)PSHIFT);
+  constexpr bool kPerToken = MODE == KVQ_INT8_PER_TOKEN_HEAD || MODE == KVQ_FP8_PER_TOKEN_HEAD;
 
   float o[MTILES][4];
 #pragma unroll
@@ -233,196 +421,88 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_consta
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   bool timed_out = false;
 
-  for (int i = 0; i < my_count; ++i) {
-    const int pid = __shfl_sync(kFull, my_pid, i);
-    const uint8_t* st = ring + (i % kStages) * C::STAGE;
-    if (!mbar_wait_bounded(&wb[i % kStages], (i / kStages) & 1)) {
+  for (int i = 0; i < my_count; i += 2) {
+    const bool two = i + 1 < my_count;  // warp-uniform
+    const int pidA = __shfl_sync(kFull, my_pid, i);
+    const int pidB_raw = __shfl_sync(kFull, my_pid, two ? i + 1 : i);
+    const int pidB = two ? pidB_raw : -1;
+    const uint8_t* stA = ring + (i % kStages) * C::STAGE;
+    const uint8_t* stB = ring + ((i + 1) % kStages) * C::STAGE;
+    if (!mbar_wait_bounded(&wb[i % kStages], (i / kStages) & 1) ||
+        (two && !mbar_wait_bounded(&wb[(i + 1) % kStages], ((i + 1) / kStages) & 1))) {
       timed_out = true;
       break;
     }
-    if (pid >= 0) {
-      const int tok0 = (p0 + warp + kWarps * i) * kPage;
-      // ---------------- S^T = K Q^T (16 tokens x 8 heads)
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        constexpr int KW = (MODE == KVQ_NVFP4 ? D / 8 : D / 4) / 4;  // words per thread per row
-        uint32_t kg[KW], kh8[KW];
-        const int rb = tq * (KW * 4);
+    const int tokA = (p0 + warp + kWarps * i) * kPage;
+    const int tokB = tokA + kWarps * kPage;
+    const int nvA = pidA >= 0 ? min(t_end - tokA, kPage) : 0;   // valid rows of each page
+    const int nvB = pidB >= 0 ? min(t_end - tokB, kPage) : 0;
+
+    float cA[4] = {0.f, 0.f, 0.f, 0.f}, cB[4] = {0.f, 0.f, 0.f, 0.f};
+    if (nvA > 0) qk_page<MODE, D, QF32>(stA, g, tq, qh, ql, cA);
+    if (nvB > 0) qk_page<MODE, D, QF32>(stB, g, tq, qh, ql, cB);
+
+    float fA0 = kfac, fA8 = kfac, fB0 = kfac, fB8 = kfac;     // score factors of tokens g, g+8
+    float vA0 = 1.f, vA8 = 1.f, vB0 = 1.f, vB8 = 1.f;         // V per-token scales
+    if constexpr (kPerToken) {
+      const float* sa = reinterpret_cast<const float*>(stA + C::S_OFF);  // K scales, then V scales
+      const float* sb = reinterpret_cast<const float*>(stB + C::S_OFF);
+      fA0 *= sa[g]; fA8 *= sa[g + 8]; vA0 = sa[kPage + g]; vA8 = sa[kPage + g + 8];
+      fB0 *= sb[g]; fB8 *= sb[g + 8]; vB0 = sb[kPage + g]; vB8 = sb[kPage + g + 8];
+    }
+    float sA[4] = {cA[0] * fA0, cA[1] * fA0, cA[2] * fA8, cA[3] * fA8};
+    float sB[4] = {cB[0] * fB0, cB[1] * fB0, cB[2] * fB8, cB[3] * fB8};
+    if (nvA < kPage || nvB < kPage) {  // rare: a partial or missing page
+      if (g >= nvA) { sA[0] = sA[1] = -INFINITY; vA0 = 0.f; }
+      if (g + 8 >= nvA) { sA[2] = sA[3] = -INFINITY; vA8 = 0.f; }
+      if (g >= nvB) { sB[0] = sB[1] = -INFINITY; vB0 = 0.f; }
+      if (g + 8 >= nvB) { sB[2] = sB[3] = -INFINITY; vB8 = 0.f; }
+    }
+    float bm0 = fmaxf(fmaxf(sA[0], sA[2]), fmaxf(sB[0], sB[2]));
+    float bm1 = fmaxf(fmaxf(sA[1], sA[3]), fmaxf(sB[1], sB[3]));
 #pragma unroll
-        for (int w = 0; w < KW; w += 4) {
-          lds<(KW >= 4 ? 4 : KW)>(st + swz<C::SWZ_MASK>(g * C::RW + rb + 4 * w), kg + w);
-          lds<(KW >= 4 ? 4 : KW)>(st + swz<C::SWZ_MASK>((g + 8) * C::RW + rb + 4 * w), kh8 + w);
-        }
-        if constexpr (MODE == KVQ_NVFP4) {
-          // block scales of this thread's channels: blocks (tq*D/4)/16 and (tq*D/4 + D/4 - 1)/16
-          constexpr int SB = D / 16;
-          const int blk0 = (tq * (D / 4)) / 16;
-          const int base_g = C::S_OFF + g * SB, base_h = C::S_OFF + (g + 8) * SB;
-          uint32_t sg, sh;
-          if constexpr (D / 4 >= 16) {
-            sg = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(base_g + blk0));
-            sh = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(base_h + blk0));
-          } else {
-            sg = st[swz<C::SWZ_MASK>(base_g + blk0)] * 0x0101u;
-            sh = st[swz<C::SWZ_MASK>(base_h + blk0)] * 0x0101u;
-          }
-          const __half2 sg2 = u32_as_h2(e4m3x2_to_f16x2(sg)), sh2 = u32_as_h2(e4m3x2_to_f16x2(sh));
-#pragma unroll
-          for (int w = 0; w < KW; ++w) {
-            uint32_t fg[4], fh[4];
-            e2m1x8_to_f16x2x4(kg[w], fg);
-            e2m1x8_to_f16x2x4(kh8[w], fh);
-#pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-              const int j = 2 * w + hlf;
-              const bool second = (4 * j) >= 16;  // channel offset within the thread's D/4 range
-              const __half2 sa = second ? __high2half2(sg2) : __low2half2(sg2);
-              const __half2 sb = second ? __high2half2(sh2) : __low2half2(sh2);
-              uint32_t af[4];
-              af[0] = h2_as_u32(__hmul2(u32_as_h2(fg[2 * hlf]), sa));
-              af[1] = h2_as_u32(__hmul2(u32_as_h2(fh[2 * hlf]), sb));
-              af[2] = h2_as_u32(__hmul2(u32_as_h2(fg[2 * hlf + 1]), sa));
-              af[3] = h2_as_u32(__hmul2(u32_as_h2(fh[2 * hlf + 1]), sb));
-              mma16816(c, af, qh[j][0], qh[j][1]);
-              if constexpr (QF32) mma16816(c, af, ql[j][0], ql[j][1]);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < KSTEPS; ++j) {
-            uint32_t af[4];
-            cvt_pair4<MODE>(kg[j], af[0], af[2]);
-            cvt_pair4<MODE>(kh8[j], af[1], af[3]);
-            mma16816(c, af, qh[j][0], qh[j][1]);
-            if constexpr (QF32) mma16816(c, af, ql[j][0], ql[j][1]);
-          }
-        }
-      }
-      // ---------------- scores (log2 domain), mask, online softmax
-      float fg = kfac, fh = kfac, vg = pmul, vh = pmul;
-      if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD || MODE == KVQ_FP8_PER_TOKEN_HEAD) {
-        const float* ks = reinterpret_cast<const float*>(st + C::S_OFF);  // K scales, then V scales
-        fg *= ks[g];
-        fh *= ks[g + 8];
-        vg *= ks[kPage + g];
-        vh *= ks[kPage + g + 8];
-      }
-      const bool okg = tok0 + g < t_end, okh = tok0 + g + 8 < t_end;
-      float s0 = okg ? c[0] * fg : -INFINITY, s1 = okg ? c[1] * fg : -INFINITY;
-      float s2 = okh ? c[2] * fh : -INFINITY, s3 = okh ? c[3] * fh : -INFINITY;
-      float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
-#pragma unroll
-      for (int x = 4; x <= 16; x <<= 1) {
-        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, x));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, x));
-      }
-      const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
-      const float al0 = n0 == -INFINITY ? 1.0f : exp2f(m0 - n0);
-      const float al1 = n1 == -INFINITY ? 1.0f : exp2f(m1 - n1);
-      const float p0v = n0 == -INFINITY ? 0.0f : exp2f(s0 - n0);
-      const float p2v = n0 == -INFINITY ? 0.0f : exp2f(s2 - n0);
-      const float p1v = n1 == -INFINITY ? 0.0f : exp2f(s1 - n1);
-      const float p3v = n1 == -INFINITY ? 0.0f : exp2f(s3 - n1);
-      m0 = n0;
-      m1 = n1;
-      l0 = l0 * al0 + (p0v + p2v);
-      l1 = l1 * al1 + (p1v + p3v);
+    for (int x = 4; x <= 16; x <<= 1) {
+      bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, x));
+      bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, x));
+    }
+    const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
+    const float z0 = n0 == -INFINITY ? 0.0f : n0, z1 = n1 == -INFINITY ? 0.0f : n1;
+    const float al0 = ex2(m0 - z0), al1 = ex2(m1 - z1);
+    m0 = n0;
+    m1 = n1;
+    if (!__all_sync(kFull, al0 == 1.0f && al1 == 1.0f)) {
 #pragma unroll
       for (int t = 0; t < MTILES; ++t) {
         o[t][0] *= al0; o[t][2] *= al0;
         o[t][1] *= al1; o[t][3] *= al1;
       }
-      // ---------------- P^T as the B operand: f16 hi + lo, transposed per 8x8 block
-      const float x0 = p0v * vg, x1 = p1v * vg, x2 = p2v * vh, x3 = p3v * vh;
-      const __half2 hg = __floats2half2_rn(x0, x1), hh = __floats2half2_rn(x2, x3);
-      const float2 fgf = __half22float2(hg), fhf = __half22float2(hh);
-      const __half2 lg = __floats2half2_rn(x0 - fgf.x, x1 - fgf.y), lh = __floats2half2_rn(x2 - fhf.x, x3 - fhf.y);
-      const uint32_t bh0 = movmatrix_t(h2_as_u32(hg)), bh1 = movmatrix_t(h2_as_u32(hh));
-      const uint32_t bl0 = movmatrix_t(h2_as_u32(lg)), bl1 = movmatrix_t(h2_as_u32(lh));
-      // ---------------- O^T += V^T P^T
-      {
-        const uint8_t* vb = st + C::V_OFF;
-        const int r0 = 2 * tq, r1 = 2 * tq + 1, r2 = 2 * tq + 8, r3 = 2 * tq + 9;
-        if constexpr (MODE == KVQ_NVFP4) {
-          constexpr int VB = D / 16;  // bytes per thread per row (D/8 channels at 4 bits)
-          constexpr int VW = VB >= 4 ? VB / 4 : 1;
-          uint32_t A0[VW], A1[VW], A2[VW], A3[VW];
-          const int cb = g * VB;
-          if constexpr (VB >= 8) {
-            lds<2>(vb + swz<C::SWZ_MASK>(C::V_OFF * 0 + r0 * C::RW + cb), A0);
-            lds<2>(vb + swz<C::SWZ_MASK>(r1 * C::RW + cb), A1);
-            lds<2>(vb + swz<C::SWZ_MASK>(r2 * C::RW + cb), A2);
-            lds<2>(vb + swz<C::SWZ_MASK>(r3 * C::RW + cb), A3);
-          } else {
-            A0[0] = *reinterpret_cast<const uint16_t*>(vb + swz<C::SWZ_MASK>(r0 * C::RW + cb));
-            A1[0] = *reinterpret_cast<const uint16_t*>(vb + swz<C::SWZ_MASK>(r1 * C::RW + cb));
-            A2[0] = *reinterpret_cast<const uint16_t*>(vb + swz<C::SWZ_MASK>(r2 * C::RW + cb));
-            A3[0] = *reinterpret_cast<const uint16_t*>(vb + swz<C::SWZ_MASK>(r3 * C::RW + cb));
-          }
-          // V block scales of rows r0..r3 for this thread's block
-          const int vblk = (g * (D / 8)) / 16;
-          const uint8_t* vs = st + C::S_OFF + kPage * (D / 16);
-          const uint32_t s01 = st[swz<C::SWZ_MASK>(C::S_OFF + kPage * (D / 16) + r0 * (D / 16) + vblk)] |
-                               (st[swz<C::SWZ_MASK>(C::S_OFF + kPage * (D / 16) + r1 * (D / 16) + vblk)] << 8);
-          const uint32_t s23 = st[swz<C::SWZ_MASK>(C::S_OFF + kPage * (D / 16) + r2 * (D / 16) + vblk)] |
-                               (st[swz<C::SWZ_MASK>(C::S_OFF + kPage * (D / 16) + r3 * (D / 16) + vblk)] << 8);
-          (void)vs;
-          const __half2 sc01 = u32_as_h2(e4m3x2_to_f16x2(s01)), sc23 = u32_as_h2(e4m3x2_to_f16x2(s23));
+    }
+    const float e0 = (float)PSHIFT - z0, e1 = (float)PSHIFT - z1;
+    const float pA0 = ex2(sA[0] + e0), pA1 = ex2(sA[1] + e1), pA2 = ex2(sA[2] + e0), pA3 = ex2(sA[3] + e1);
+    const float pB0 = ex2(sB[0] + e0), pB1 = ex2(sB[1] + e1), pB2 = ex2(sB[2] + e0), pB3 = ex2(sB[3] + e1);
+    l0 = l0 * al0 + ((pA0 + pA2) + (pB0 + pB2));
+    l1 = l1 * al1 + ((pA1 + pA3) + (pB1 + pB3));
+    // P^T as the B operand: f16 hi + lo, each 8x8 block transposed in registers
+    uint32_t bh[4], bl[4];
+    {
+      const float x[8] = {pA0 * vA0, pA1 * vA0, pA2 * vA8, pA3 * vA8, pB0 * vB0, pB1 * vB0, pB2 * vB8, pB3 * vB8};
 #pragma unroll
-          for (int w = 0; w < VW; ++w) {
-            // pair rows (r0, r1) and (r2, r3) nibble by nibble: even channel e = 8w+2k, odd e+1
-            const uint32_t xe01 = bitsel(A0[w], A1[w] << 4, 0x0F0F0F0Fu);
-            const uint32_t xo01 = bitsel(A0[w] >> 4, A1[w], 0x0F0F0F0Fu);
-            const uint32_t xe23 = bitsel(A2[w], A3[w] << 4, 0x0F0F0F0Fu);
-            const uint32_t xo23 = bitsel(A2[w] >> 4, A3[w], 0x0F0F0F0Fu);
-            uint32_t fe01[4], fo01[4], fe23[4], fo23[4];
-            e2m1x8_to_f16x2x4(xe01, fe01);
-            e2m1x8_to_f16x2x4(xo01, fo01);
-            e2m1x8_to_f16x2x4(xe23, fe23);
-            e2m1x8_to_f16x2x4(xo23, fo23);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int t = 4 * w + k;
-              if (t < MTILES) {
-                uint32_t av[4];
-                av[0] = h2_as_u32(__hmul2(u32_as_h2(fe01[k]), sc01));
-                av[1] = h2_as_u32(__hmul2(u32_as_h2(fo01[k]), sc01));
-                av[2] = h2_as_u32(__hmul2(u32_as_h2(fe23[k]), sc23));
-                av[3] = h2_as_u32(__hmul2(u32_as_h2(fo23[k]), sc23));
-                mma16816(o[t], av, bh0, bh1);
-                mma16816(o[t], av, bl0, bl1);
-              }
-            }
-          }
-        } else {
-          constexpr int VW = D / 32;  // words per thread per row (D/8 one-byte channels)
-          uint32_t A0[VW], A1[VW], A2[VW], A3[VW];
-          const int cb = g * (D / 8);
-          lds<VW>(vb + swz<C::SWZ_MASK>(r0 * C::RW + cb) - C::V_OFF + C::V_OFF, A0);
-          lds<VW>(vb + swz<C::SWZ_MASK>(r1 * C::RW + cb), A1);
-          lds<VW>(vb + swz<C::SWZ_MASK>(r2 * C::RW + cb), A2);
-          lds<VW>(vb + swz<C::SWZ_MASK>(r3 * C::RW + cb), A3);
-#pragma unroll
-          for (int w = 0; w < VW; ++w) {
-            const uint32_t x01 = prmt(A0[w], A1[w], 0x5140u), y01 = prmt(A0[w], A1[w], 0x7362u);
-            const uint32_t x23 = prmt(A2[w], A3[w], 0x5140u), y23 = prmt(A2[w], A3[w], 0x7362u);
-            uint32_t av[4];
-            cvt_pair4<MODE>(x01, av[0], av[1]);
-            cvt_pair4<MODE>(x23, av[2], av[3]);
-            mma16816(o[2 * w], av, bh0, bh1);
-            mma16816(o[2 * w], av, bl0, bl1);
-            cvt_pair4<MODE>(y01, av[0], av[1]);
-            cvt_pair4<MODE>(y23, av[2], av[3]);
-            mma16816(o[2 * w + 1], av, bh0, bh1);
-            mma16816(o[2 * w + 1], av, bl0, bl1);
-          }
-        }
+      for (int k = 0; k < 4; ++k) {
+        const __half2 h = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
+        const float2 f = __half22float2(h);
+        const __half2 lo = __floats2half2_rn(x[2 * k] - f.x, x[2 * k + 1] - f.y);
+        bh[k] = movmatrix_t(h2_as_u32(h));
+        bl[k] = movmatrix_t(h2_as_u32(lo));
       }
     }
+    if (nvA > 0) pv_page<MODE, D>(stA, g, tq, nvA, bh[0], bh[1], bl[0], bl[1], o);
+    if (nvB > 0) pv_page<MODE, D>(stB, g, tq, nvB, bh[2], bh[3], bl[2], bl[3], o);
+
     __syncwarp();
     if (i + kStages < my_count) {
       if (lane == 0) fence_proxy_async_smem();
       issue(i + kStages);
+      if (i + 1 + kStages < my_count) issue(i + 1 + kStages);
     }
   }
   if (timed_out && lane == 0) set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_TIMEOUT);
