@@ -46,7 +46,7 @@ def _inputs():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if os.environ.get("KVQ_NVCC_FLAGS") or not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(f) <= t for f in _inputs())
@@ -57,7 +57,7 @@ def build(force: bool = False, verbose: bool = False, extra: list | None = None)
         return LIB
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
-    extra = list(extra or [])
+    extra = list(extra or []) + os.environ.get("KVQ_NVCC_FLAGS", "").split()
 
     def compile_one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))

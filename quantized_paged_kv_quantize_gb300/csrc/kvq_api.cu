@@ -311,7 +311,6 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
       return fail(KVQ_ERR_CAPACITY, "workspace needs %zu bytes, got %zu", p.workspace_bytes, workspace_bytes);
     if (!aligned(workspace, 16)) return fail(KVQ_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   }
-  if (c.mode == KVQ_KVARN_K4V2_G128) return fail(KVQ_ERR_UNSUPPORTED, "kvarn decode is not built yet");
   cudaError_t e = kvq::launch_decode(cache, p, q, block_table, max_pages, seq_lens, num_seqs, num_q_heads,
                                      max_seq_len, softmax_scale, out, out_dtype, workspace,
                                      static_cast<cudaStream_t>(stream));

@@ -33,24 +33,21 @@ namespace {
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kPage = 16;
 constexpr int kWarps = 4;
-constexpr int kStages = 4;
+// Pipeline depth (pages in flight per warp) and the resident CTAs per SM the
+// register budget is sized for, per payload width; -D overrides exist for tuning.
+#ifndef KVQ_FP4_STAGES
+#define KVQ_FP4_STAGES 4
+#endif
+#ifndef KVQ_FP4_MINB
+#define KVQ_FP4_MINB 4
+#endif
+#ifndef KVQ_B1_STAGES
+#define KVQ_B1_STAGES 2
+#endif
+#ifndef KVQ_B1_MINB
+#define KVQ_B1_MINB 5
+#endif
 constexpr float kLog2e = 1.4426950408889634f;
-
-struct DecodeArgs {
-  const uint8_t* pool;
-  const void* q;
-  const int32_t* block_table;
-  const int32_t* seq_lens;
-  void* out;
-  float* ws_o;   // [B][Hq][S][D]
-  float* ws_ml;  // [B][Hq][S][2]
-  int num_pages, Hkv, Hq, G, B, max_pages, max_seq_len;
-  int tokens_per_split, num_splits;
-  int out_f32;
-  float sm_log2;  // softmax_scale * log2(e)
-  size_t block_bytes;
-  int rows_per_block;
-};
 
 template <int MODE, int D>
 struct Cfg {
@@ -64,6 +61,8 @@ struct Cfg {
   static constexpr int S_OFF = 2 * kPage * RW;        // scales region
   // SW128 for 128-byte rows, SW64 for 64-byte rows (XOR of address bits 7.. into 4..).
   static constexpr int SWZ_MASK = !TMA ? 0 : (RW == 128 ? 7 : 3);
+  static constexpr int STAGES = MODE == KVQ_NVFP4 ? KVQ_FP4_STAGES : KVQ_B1_STAGES;
+  static constexpr int MINB = MODE == KVQ_NVFP4 ? KVQ_FP4_MINB : KVQ_B1_MINB;
   // probabilities are scaled by 2^PSHIFT before the f16 split (range of P x scale)
   static constexpr int pshift(bool f32io) {
     return MODE == KVQ_INT8_PER_TOKEN_HEAD ? (f32io ? 0 : 6)
@@ -74,23 +73,6 @@ struct Cfg {
 template <int MASK>
 __device__ __forceinline__ int swz(int off) {
   return off ^ (((off >> 7) & MASK) << 4);
-}
-
-template <int N>
-__device__ __forceinline__ void lds(const uint8_t* p, uint32_t* w);
-template <>
-__device__ __forceinline__ void lds<4>(const uint8_t* p, uint32_t* w) {
-  uint4 u = *reinterpret_cast<const uint4*>(p);
-  w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
-}
-template <>
-__device__ __forceinline__ void lds<2>(const uint8_t* p, uint32_t* w) {
-  uint2 u = *reinterpret_cast<const uint2*>(p);
-  w[0] = u.x; w[1] = u.y;
-}
-template <>
-__device__ __forceinline__ void lds<1>(const uint8_t* p, uint32_t* w) {
-  w[0] = *reinterpret_cast<const uint32_t*>(p);
 }
 
 // int8 pair (bytes 0,1 or 2,3 of w) -> exact f16x2 via 1024 + (x + 128) - 1152.
@@ -151,12 +133,6 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int 
       qh[j][1] = u.y;
     }
   }
-}
-
-__device__ __forceinline__ float ex2(float x) {  // 2^x on the SFU (rel. error ~2^-22), ex2(-inf) = 0
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 
 // S^T = K Q^T for one staged page: c[0..1] = tokens g, c[2..3] = token g+8, heads 2tq, 2tq+1.
@@ -327,13 +303,13 @@ __device__ __forceinline__ void pv_page(const uint8_t* st, int g, int tq, int nv
 }
 
 template <int MODE, int D, bool QF32>
-__global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_constant__ DecodeArgs a,
+__global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel(const __grid_constant__ DecodeArgs a,
                                                                const __grid_constant__ CUtensorMap tmap) {
   using C = Cfg<MODE, D>;
   constexpr int KSTEPS = C::KSTEPS, MTILES = C::MTILES;
   constexpr int PSHIFT = C::pshift(QF32);
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t bars[kWarps][kStages];
+  __shared__ uint64_t bars[kWarps][C::STAGES];
   // 1024-byte alignment of the ring (swizzle patterns are address based)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -362,10 +338,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_consta
   const int p0 = t_begin / kPage, p1 = (t_end + kPage - 1) / kPage;
   const int my_count = (p1 - p0 - warp + kWarps - 1) / kWarps;  // pages of this warp (<= 32)
 
-  uint8_t* ring = smem + warp * kStages * C::STAGE;
+  uint8_t* ring = smem + warp * C::STAGES * C::STAGE;
   uint64_t* wb = bars[warp];
   if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&wb[s], 1);
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(&wb[s], 1);
     mbar_fence_init();
     if constexpr (C::TMA) prefetch_tmap(&tmap);
   }
@@ -384,10 +360,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_consta
   auto issue = [&](int i) {
     const int pid = __shfl_sync(kFull, my_pid, i);
     if (lane == 0) {
-      uint64_t* bar = &wb[i % kStages];
+      uint64_t* bar = &wb[i % C::STAGES];
       mbar_arrive_expect_tx(bar, pid >= 0 ? (uint32_t)C::BLK : 0u);
       if (pid >= 0) {
-        uint8_t* dst = ring + (i % kStages) * C::STAGE;
+        uint8_t* dst = ring + (i % C::STAGES) * C::STAGE;
         const long long ph = (long long)pid * a.Hkv + kvh;
         if constexpr (C::TMA)
           tma_g2s_2d(dst, &tmap, 0, (int)((kHeaderBytes + ph * (long long)C::BLK) / C::RW), bar);
@@ -397,7 +373,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_consta
     }
   };
 
-  const int npre = my_count < kStages ? my_count : kStages;
+  const int npre = my_count < C::STAGES ? my_count : C::STAGES;
   for (int i = 0; i < npre; ++i) issue(i);
 
   // query fragments
@@ -426,10 +402,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_consta
     const int pidA = __shfl_sync(kFull, my_pid, i);
     const int pidB_raw = __shfl_sync(kFull, my_pid, two ? i + 1 : i);
     const int pidB = two ? pidB_raw : -1;
-    const uint8_t* stA = ring + (i % kStages) * C::STAGE;
-    const uint8_t* stB = ring + ((i + 1) % kStages) * C::STAGE;
-    if (!mbar_wait_bounded(&wb[i % kStages], (i / kStages) & 1) ||
-        (two && !mbar_wait_bounded(&wb[(i + 1) % kStages], ((i + 1) / kStages) & 1))) {
+    const uint8_t* stA = ring + (i % C::STAGES) * C::STAGE;
+    const uint8_t* stB = ring + ((i + 1) % C::STAGES) * C::STAGE;
+    if (!mbar_wait_bounded(&wb[i % C::STAGES], (i / C::STAGES) & 1) ||
+        (two && !mbar_wait_bounded(&wb[(i + 1) % C::STAGES], ((i + 1) / C::STAGES) & 1))) {
       timed_out = true;
       break;
     }
@@ -499,10 +475,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_consta
     if (nvB > 0) pv_page<MODE, D>(stB, g, tq, nvB, bh[2], bh[3], bl[2], bl[3], o);
 
     __syncwarp();
-    if (i + kStages < my_count) {
+    if (i + C::STAGES < my_count) {
       if (lane == 0) fence_proxy_async_smem();
-      issue(i + kStages);
-      if (i + 1 + kStages < my_count) issue(i + 1 + kStages);
+      issue(i + C::STAGES);
+      if (i + 1 + C::STAGES < my_count) issue(i + 1 + C::STAGES);
     }
   }
   if (timed_out && lane == 0) set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_TIMEOUT);
@@ -594,7 +570,7 @@ __global__ void __launch_bounds__(D) combine_kernel(const __grid_constant__ Deco
 template <int MODE, int D, bool QF32>
 cudaError_t launch_mode(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s) {
   using C = Cfg<MODE, D>;
-  const size_t ring = (size_t)kWarps * kStages * C::STAGE;
+  const size_t ring = (size_t)kWarps * C::STAGES * C::STAGE;
   const size_t merge = (size_t)kWarps * 8 * (D + 2) * sizeof(float);
   const size_t smem = (ring > merge ? ring : merge) + 1024;
   auto kern = decode_kernel<MODE, D, QF32>;
@@ -622,21 +598,23 @@ cudaError_t launch_d(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s) {
 }  // namespace
 
 DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int max_seq_len) {
-  (void)num_q_heads;
-  DecodePlan p{1, kPage, 0};
+  DecodePlan p{1, c->cfg.page_size, 0};
   const int P = c->cfg.page_size;
   const long long pages = (max_seq_len + P - 1) / P;
   if (pages <= 0) return p;
   const long long units = (long long)num_seqs * c->cfg.num_kv_heads;
-  const int per_warp_pages = 32;  // one page id per lane
-  const long long cap = (long long)kWarps * per_warp_pages;
+  // pages per split: at least one per warp (modes 1-4: a warp owns whole pages,
+  // at most 32; KVarN: the CTA shares each 128-token tile, at most 64 tiles)
+  const bool kvarn = c->cfg.mode == KVQ_KVARN_K4V2_G128;
+  const long long cap = kvarn ? 64 : (long long)kWarps * 32;
+  const long long min_pages = kvarn ? 1 : kWarps;
   long long splits = (8LL * num_sms() + units - 1) / (units > 0 ? units : 1);
   const long long min_splits = (pages + cap - 1) / cap;
-  const long long max_splits = (pages + kWarps - 1) / kWarps;
+  const long long max_splits = (pages + min_pages - 1) / min_pages;
   if (splits > max_splits) splits = max_splits;
   if (splits < min_splits) splits = min_splits;
   if (splits < 1) splits = 1;
-  long long pps = (pages + splits - 1) / splits;
+  const long long pps = (pages + splits - 1) / splits;
   p.tokens_per_split = (int)(pps * P);
   p.num_splits = (int)((max_seq_len + p.tokens_per_split - 1) / p.tokens_per_split);
   if (p.num_splits > 1)
@@ -666,10 +644,12 @@ cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void
   a.tokens_per_split = plan.tokens_per_split;
   a.num_splits = plan.num_splits;
   a.out_f32 = out_dtype == KVQ_F32;
+  a.q_f32 = c->cfg.io_dtype == KVQ_F32;
   a.sm_log2 = softmax_scale * kLog2e;
   a.block_bytes = c->block_bytes;
   a.rows_per_block = c->rows_per_block;
-  if (num_seqs == 0 || max_seq_len == 0 && false) return cudaSuccess;
+  if (num_seqs == 0) return cudaSuccess;
+  if (c->cfg.mode == KVQ_KVARN_K4V2_G128) return launch_kvarn_decode(a, stream);
   const bool qf32 = c->cfg.io_dtype == KVQ_F32;
   if (c->cfg.head_dim == 128)
     return qf32 ? launch_d<128, true>(c, a, stream) : launch_d<128, false>(c, a, stream);

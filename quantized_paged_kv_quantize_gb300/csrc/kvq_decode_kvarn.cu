@@ -1,0 +1,483 @@
+// kvq_decode_kvarn.cu -- paged decode attention over the KVarN k4v2 g128 cache.
+//
+// Source: "KVarN：华为推出的原生 vLLM KV-cache 量化后端，打破性能与精度的权衡",
+// section 技术原理: 128-token tiles; a Hadamard rotation along channels, which is
+// orthogonal and so leaves attention scores unchanged; variance normalisation;
+// asymmetric round-to-nearest whose scales are folded back at read time, keys
+// per channel and values per token.  Attention itself follows
+// "NVFP4 KV Cache：Blackwell 上的 4-bit 缓存量化", A = softmax(QK^T/sqrt(d)), O = AV.
+//
+// Stored tile (per kv head), rotated domain: x^_td = r_t c_d (scale * code + zero)
+// with K's scale/zero per channel and V's per token.  With q' = H q:
+//   s_t  = r^K_t [ sum_d (q'_d c^K_d scale^K_d) code^K_td + sum_d q'_d c^K_d zero^K_d ]
+//   o'_d = c^V_d [ sum_t (p_t r^V_t scale^V_t) code^V_td + sum_t p_t r^V_t zero^V_t ]
+//   o    = H o' / sum_t p_t
+// so every scale folds into the 8 x 128 query (once per tile) or into the
+// probabilities (once per token), and the codes enter the tensor cores as
+// integers.  A code c becomes the f16 with bit pattern c (the subnormal
+// c * 2^-24, exact) by shift-and-mask; the 2^24 comes back in the fp32 scale.
+//
+// GB300 layout: one CTA per (KV split, kv head, sequence); the CTA's warps
+// share a ring of 16 KB tile buffers filled by bulk TMA copies (one per tile).
+// Per tile the CTA folds the query (channel d per thread) into shared memory
+// in mma.sync B-fragment order; each warp then takes 2 of the tile's 8
+// 16-token sub-blocks: S^T = K Q^T and O^T += V^T P^T on mma.m16n8k16 (N = the
+// GQA group of 8 query heads), online softmax in base 2, f16 hi + lo splits
+// for the folded query and for the probabilities.
+#include <cuda_fp16.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr int kT = 128;                              // tokens per tile (= page)
+constexpr int kD = 128;                              // head_dim
+constexpr int kBlk = 16384;                          // bytes per (tile, kv head)
+constexpr int kW = 4;                                // warps per CTA
+constexpr int kVOff = kT * kD / 2;                   // V codes [128][32]
+constexpr int kKMeta = kVOff + kT * kD / 4;          // K: scale[D] zero[D] c[D] r[T]
+constexpr int kVMeta = kKMeta + 4 * (3 * kD + kT);   // V: scale[T] zero[T] r[T] c[D]
+constexpr int kPShift = 14;                          // P scaled by 2^14 before the f16 split
+constexpr int kMaxTiles = 64;                        // tiles per split (page ids kept in smem)
+#ifndef KVQ_KVARN_STAGES
+#define KVQ_KVARN_STAGES 2
+#endif
+constexpr int kS = KVQ_KVARN_STAGES;
+
+struct Shared {
+  float qrot[8][kD];     // q' = H q per head of the group
+  uint4 frag[8][32];     // per k-step and lane: {b0 hi, b1 hi, b0 lo, b1 lo}
+  float kf[kT];          // r^K_t * softmax_scale * log2(e)
+  float vf[kT];          // r^V_t * scale^V_t
+  float vz[kT];          // r^V_t * zero^V_t
+  float beta_part[kW][8];
+  float vmax_part[kW];
+  int pages[kMaxTiles];
+};
+constexpr size_t kSmem = (size_t)kS * kBlk + sizeof(Shared);
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// In-register normalised Walsh-Hadamard transform of one 128-vector held as
+// 4 consecutive values per lane (lane l: elements 4l..4l+3).
+__device__ __forceinline__ void fwht128_warp(float* v, int lane) {
+  float w0 = v[0] + v[1], w1 = v[0] - v[1], w2 = v[2] + v[3], w3 = v[2] - v[3];
+  v[0] = w0 + w2; v[2] = w0 - w2; v[1] = w1 + w3; v[3] = w1 - w3;
+#pragma unroll
+  for (int o = 1; o <= 16; o <<= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float p = __shfl_xor_sync(kFull, v[i], o);
+      v[i] = upper ? p - v[i] : v[i] + p;
+    }
+  }
+  const float c = 0.08838834764831845f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] *= c;
+}
+
+__global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ uint64_t bars[kS];
+  uint8_t* ring = smem_raw;
+  Shared& sh = *reinterpret_cast<Shared*>(smem_raw + (size_t)kS * kBlk);
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  uint8_t* pool = const_cast<uint8_t*>(a.pool);
+
+  int n = a.seq_lens[b];
+  const int lim = min(a.max_seq_len, a.max_pages * kT);
+  const bool first = tid == 0 && split == 0 && kvh == 0;
+  if (n > lim || n < 0) {
+    if (first) set_error(pool, KVQ_DEVERR_SEQ_LEN);
+    n = n < 0 ? 0 : lim;
+  }
+  if (n % kT) {  // only whole tiles are readable
+    if (first) set_error(pool, KVQ_DEVERR_PARTIAL_TILE);
+    n -= n % kT;
+  }
+  const int t_begin = split * a.tokens_per_split;
+  const int t_end = min(n, t_begin + a.tokens_per_split);
+  if (t_begin >= t_end) {
+    if (a.num_splits == 1) {
+      for (int i = tid; i < a.G * kD; i += blockDim.x) {
+        const long long o = ((long long)b * a.Hq + (long long)kvh * a.G + i / kD) * kD + i % kD;
+        if (a.out_f32) static_cast<float*>(a.out)[o] = 0.0f;
+        else static_cast<__half*>(a.out)[o] = __float2half_rn(0.0f);
+      }
+    }
+    return;
+  }
+  const int tile0 = t_begin / kT, ntiles = (t_end - t_begin) / kT;
+
+  if (tid < ntiles) {
+    int pid = __ldg(a.block_table + (long long)b * a.max_pages + tile0 + tid);
+    if (pid < 0 || pid >= a.num_pages) {
+      set_error(pool, KVQ_DEVERR_PAGE_RANGE);
+      pid = -1;
+    }
+    sh.pages[tid] = pid;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kS; ++s) mbar_init(&bars[s], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  auto issue = [&](int i) {  // thread 0 only
+    const int pid = sh.pages[i];
+    uint64_t* bar = &bars[i % kS];
+    mbar_arrive_expect_tx(bar, pid >= 0 ? (uint32_t)kBlk : 0u);
+    if (pid >= 0)
+      bulk_g2s(ring + (i % kS) * kBlk, a.pool + kHeaderBytes + ((size_t)pid * a.Hkv + kvh) * kBlk, kBlk, bar);
+  };
+  if (tid == 0)
+    for (int i = 0; i < min(kS, ntiles); ++i) issue(i);
+
+  // q' = H q for the group's heads (zero for heads >= G)
+  for (int h = warp; h < 8; h += kW) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (h < a.G) {
+      const long long row = ((long long)b * a.Hq + (long long)kvh * a.G + h) * kD + 4 * lane;
+      if (a.q_f32) {
+        const float4 u = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + row));
+        v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+      } else {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(a.q) + row));
+        const float2 f0 = __half22float2(u32_as_h2(u.x)), f1 = __half22float2(u32_as_h2(u.y));
+        v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+      }
+    }
+    fwht128_warp(v, lane);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sh.qrot[h][4 * lane + i] = v[i];
+  }
+  __syncthreads();
+
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  bool timed_out = false;
+
+  for (int i = 0; i < ntiles; ++i) {
+    const uint8_t* st = ring + (i % kS) * kBlk;
+    const bool ok = mbar_wait_bounded(&bars[i % kS], (i / kS) & 1);
+    if (__syncthreads_or(!ok)) {
+      timed_out = true;
+      break;
+    }
+    const int pid = sh.pages[i];
+    if (pid >= 0) {
+      const float* km = reinterpret_cast<const float*>(st + kKMeta);
+      const float* vm = reinterpret_cast<const float*>(st + kVMeta);
+      // ---- fold: thread tid owns channel d = tid and token t = tid
+      {
+        const int d = tid;
+        const float cs = km[2 * kD + d] * km[d];       // c_d * scale_d
+        const float cz = km[2 * kD + d] * km[kD + d];  // c_d * zero_d
+        // B-fragment slot of channel d: d = 32 tq + 8 w + k, k = 4 half + s, j = 2 w + s/2
+        const int tqd = d >> 5, w = (d & 31) >> 3, k = d & 7, s = k & 3, half = k >> 2;
+        const int j = 2 * w + (s >> 1), slot = s & 1;
+        __half* fr = reinterpret_cast<__half*>(&sh.frag[j][0]);
+        float bp[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const float qv = sh.qrot[h][d];
+          const float qt = qv * cs;
+          const __half hi = __float2half_rn(qt);
+          const __half lo = __float2half_rn(qt - __half2float(hi));
+          const int ln = 4 * h + tqd;
+          fr[ln * 8 + slot * 2 + half] = hi;
+          fr[ln * 8 + 4 + slot * 2 + half] = lo;
+          bp[h] = qv * cz;
+        }
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const float s2 = warp_sum(bp[h]);
+          if (lane == 0) sh.beta_part[warp][h] = s2;
+        }
+        const int t = tid;
+        sh.kf[t] = km[3 * kD + t] * a.sm_log2;
+        const float f = vm[2 * kT + t] * vm[t];
+        sh.vf[t] = f;
+        sh.vz[t] = vm[2 * kT + t] * vm[kT + t];
+        float fm = fabsf(f);
+#pragma unroll
+        for (int x = 16; x >= 1; x >>= 1) fm = fmaxf(fm, __shfl_xor_sync(kFull, fm, x));
+        if (lane == 0) sh.vmax_part[warp] = fm;
+      }
+      __syncthreads();
+      const float be0 = sh.beta_part[0][2 * tq] + sh.beta_part[1][2 * tq] + sh.beta_part[2][2 * tq] +
+                        sh.beta_part[3][2 * tq];
+      const float be1 = sh.beta_part[0][2 * tq + 1] + sh.beta_part[1][2 * tq + 1] + sh.beta_part[2][2 * tq + 1] +
+                        sh.beta_part[3][2 * tq + 1];
+      const float vmx = fmaxf(fmaxf(sh.vmax_part[0], sh.vmax_part[1]), fmaxf(sh.vmax_part[2], sh.vmax_part[3]));
+      int ex = 0;
+      (void)frexpf(vmx, &ex);                         // vmx < 2^ex
+      const float vnorm = ldexpf(1.0f, -ex);          // p' * vf * vnorm <= 2^kPShift
+      const float vback = ldexpf(16777216.0f, ex);    // undoes vnorm and the 2^-24 of the codes
+
+      // ---- this warp's two 16-token sub-blocks: tokens 16*sa.., 16*sb..
+      const int sa = warp, sb = warp + kW;
+      float cA[4] = {0.f, 0.f, 0.f, 0.f}, cB[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        uint32_t KA0[4], KA8[4], KB0[4], KB8[4];
+        lds<4>(st + (16 * sa + g) * 64 + tq * 16, KA0);
+        lds<4>(st + (16 * sa + g + 8) * 64 + tq * 16, KA8);
+        lds<4>(st + (16 * sb + g) * 64 + tq * 16, KB0);
+        lds<4>(st + (16 * sb + g + 8) * 64 + tq * 16, KB8);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 fq = sh.frag[j][lane];
+          const int w = j >> 1, sft = (j & 1) * 8;
+          uint32_t af[4];
+          af[0] = (KA0[w] >> sft) & 0x000F000Fu;
+          af[2] = (KA0[w] >> (sft + 4)) & 0x000F000Fu;
+          af[1] = (KA8[w] >> sft) & 0x000F000Fu;
+          af[3] = (KA8[w] >> (sft + 4)) & 0x000F000Fu;
+          mma16816(cA, af, fq.x, fq.y);
+          mma16816(cA, af, fq.z, fq.w);
+          af[0] = (KB0[w] >> sft) & 0x000F000Fu;
+          af[2] = (KB0[w] >> (sft + 4)) & 0x000F000Fu;
+          af[1] = (KB8[w] >> sft) & 0x000F000Fu;
+          af[3] = (KB8[w] >> (sft + 4)) & 0x000F000Fu;
+          mma16816(cB, af, fq.x, fq.y);
+          mma16816(cB, af, fq.z, fq.w);
+        }
+      }
+      const int ta = 16 * sa + g, tb = 16 * sb + g;
+      const float kA0 = sh.kf[ta], kA8 = sh.kf[ta + 8], kB0 = sh.kf[tb], kB8 = sh.kf[tb + 8];
+      const float sA[4] = {fmaf(cA[0], 16777216.0f, be0) * kA0, fmaf(cA[1], 16777216.0f, be1) * kA0,
+                           fmaf(cA[2], 16777216.0f, be0) * kA8, fmaf(cA[3], 16777216.0f, be1) * kA8};
+      const float sB[4] = {fmaf(cB[0], 16777216.0f, be0) * kB0, fmaf(cB[1], 16777216.0f, be1) * kB0,
+                           fmaf(cB[2], 16777216.0f, be0) * kB8, fmaf(cB[3], 16777216.0f, be1) * kB8};
+      float bm0 = fmaxf(fmaxf(sA[0], sA[2]), fmaxf(sB[0], sB[2]));
+      float bm1 = fmaxf(fmaxf(sA[1], sA[3]), fmaxf(sB[1], sB[3]));
+#pragma unroll
+      for (int x = 4; x <= 16; x <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, x));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, x));
+      }
+      const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
+      const float z0 = n0 == -INFINITY ? 0.0f : n0, z1 = n1 == -INFINITY ? 0.0f : n1;
+      const float al0 = ex2(m0 - z0), al1 = ex2(m1 - z1);
+      m0 = n0;
+      m1 = n1;
+      if (!__all_sync(kFull, al0 == 1.0f && al1 == 1.0f)) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          o[t][0] *= al0; o[t][2] *= al0;
+          o[t][1] *= al1; o[t][3] *= al1;
+        }
+      }
+      const float e0 = (float)kPShift - z0, e1 = (float)kPShift - z1;
+      const float pA0 = ex2(sA[0] + e0), pA1 = ex2(sA[1] + e1), pA2 = ex2(sA[2] + e0), pA3 = ex2(sA[3] + e1);
+      const float pB0 = ex2(sB[0] + e0), pB1 = ex2(sB[1] + e1), pB2 = ex2(sB[2] + e0), pB3 = ex2(sB[3] + e1);
+      l0 = l0 * al0 + ((pA0 + pA2) + (pB0 + pB2));
+      l1 = l1 * al1 + ((pA1 + pA3) + (pB1 + pB3));
+      // value-side bias: sum_t p'_t r_t zero_t over this warp's 32 tokens
+      const float zA0 = sh.vz[ta], zA8 = sh.vz[ta + 8], zB0 = sh.vz[tb], zB8 = sh.vz[tb + 8];
+      float bv0 = (pA0 * zA0 + pA2 * zA8) + (pB0 * zB0 + pB2 * zB8);
+      float bv1 = (pA1 * zA0 + pA3 * zA8) + (pB1 * zB0 + pB3 * zB8);
+#pragma unroll
+      for (int x = 4; x <= 16; x <<= 1) {
+        bv0 += __shfl_xor_sync(kFull, bv0, x);
+        bv1 += __shfl_xor_sync(kFull, bv1, x);
+      }
+      uint32_t bh[4], bl[4];
+      {
+        const float fA0 = sh.vf[ta] * vnorm, fA8 = sh.vf[ta + 8] * vnorm;
+        const float fB0 = sh.vf[tb] * vnorm, fB8 = sh.vf[tb + 8] * vnorm;
+        const float x[8] = {pA0 * fA0, pA1 * fA0, pA2 * fA8, pA3 * fA8, pB0 * fB0, pB1 * fB0, pB2 * fB8, pB3 * fB8};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __half2 h = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
+          const float2 f = __half22float2(h);
+          const __half2 lo = __floats2half2_rn(x[2 * k] - f.x, x[2 * k + 1] - f.y);
+          bh[k] = movmatrix_t(h2_as_u32(h));
+          bl[k] = movmatrix_t(h2_as_u32(lo));
+        }
+      }
+      // ---- O_tile^T = V^T P^T for both sub-blocks, then the per-channel fold
+      float ot[8][4];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) ot[t][0] = ot[t][1] = ot[t][2] = ot[t][3] = 0.0f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int base = 16 * (half ? sb : sa);
+        const uint8_t* vrow = st + kVOff + 4 * g;
+        const uint32_t A0 = *reinterpret_cast<const uint32_t*>(vrow + (base + 2 * tq) * 32);
+        const uint32_t A1 = *reinterpret_cast<const uint32_t*>(vrow + (base + 2 * tq + 1) * 32);
+        const uint32_t A2 = *reinterpret_cast<const uint32_t*>(vrow + (base + 2 * tq + 8) * 32);
+        const uint32_t A3 = *reinterpret_cast<const uint32_t*>(vrow + (base + 2 * tq + 9) * 32);
+        // codes 0..7 of two rows side by side (low / high halfword), then 8..15
+        const uint32_t X01 = prmt(A0, A1, 0x5410u), Y01 = prmt(A0, A1, 0x7632u);
+        const uint32_t X23 = prmt(A2, A3, 0x5410u), Y23 = prmt(A2, A3, 0x7632u);
+        const uint32_t hb0 = half ? bh[2] : bh[0], hb1 = half ? bh[3] : bh[1];
+        const uint32_t lb0 = half ? bl[2] : bl[0], lb1 = half ? bl[3] : bl[1];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const uint32_t s01 = t < 4 ? X01 : Y01, s23 = t < 4 ? X23 : Y23;
+          const int sh2 = 4 * (t & 3);  // code e = 2t (row g) and 2t+1 (row g+8), 2 bits each
+          uint32_t av[4];
+          av[0] = (s01 >> sh2) & 0x00030003u;
+          av[1] = (s01 >> (sh2 + 2)) & 0x00030003u;
+          av[2] = (s23 >> sh2) & 0x00030003u;
+          av[3] = (s23 >> (sh2 + 2)) & 0x00030003u;
+          mma16816(ot[t], av, hb0, hb1);
+          mma16816(ot[t], av, lb0, lb1);
+        }
+      }
+      {
+        float cv[16];
+        lds<4>(reinterpret_cast<const uint8_t*>(vm + 3 * kT + 16 * g), reinterpret_cast<uint32_t*>(cv));
+        lds<4>(reinterpret_cast<const uint8_t*>(vm + 3 * kT + 16 * g + 4), reinterpret_cast<uint32_t*>(cv + 4));
+        lds<4>(reinterpret_cast<const uint8_t*>(vm + 3 * kT + 16 * g + 8), reinterpret_cast<uint32_t*>(cv + 8));
+        lds<4>(reinterpret_cast<const uint8_t*>(vm + 3 * kT + 16 * g + 12), reinterpret_cast<uint32_t*>(cv + 12));
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          o[t][0] = fmaf(cv[2 * t], fmaf(ot[t][0], vback, bv0), o[t][0]);
+          o[t][1] = fmaf(cv[2 * t], fmaf(ot[t][1], vback, bv1), o[t][1]);
+          o[t][2] = fmaf(cv[2 * t + 1], fmaf(ot[t][2], vback, bv0), o[t][2]);
+          o[t][3] = fmaf(cv[2 * t + 1], fmaf(ot[t][3], vback, bv1), o[t][3]);
+        }
+      }
+    }
+    __syncthreads();  // every warp is done with this stage
+    if (tid == 0 && i + kS < ntiles) {
+      fence_proxy_async_smem();
+      issue(i + kS);
+    }
+  }
+  if (timed_out && tid == 0) set_error(pool, KVQ_DEVERR_TIMEOUT);
+
+  // ---- merge the warps (the ring is free: every issued copy was waited for)
+#pragma unroll
+  for (int x = 4; x <= 16; x <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, x);
+    l1 += __shfl_xor_sync(kFull, l1, x);
+  }
+  __syncthreads();
+  float* red_o = reinterpret_cast<float*>(ring);   // [W][8][D]
+  float* red_m = red_o + kW * 8 * kD;              // [W][8]
+  float* red_l = red_m + kW * 8;                   // [W][8]
+  float* fin = red_l + kW * 8;                     // [8][D]
+  if (g == 0) {
+    red_m[warp * 8 + 2 * tq] = m0;
+    red_m[warp * 8 + 2 * tq + 1] = m1;
+    red_l[warp * 8 + 2 * tq] = l0;
+    red_l[warp * 8 + 2 * tq + 1] = l1;
+  }
+  {
+    float* ow = red_o + warp * 8 * kD;
+    const int d0 = 16 * g;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      ow[(2 * tq) * kD + d0 + 2 * t] = o[t][0];
+      ow[(2 * tq + 1) * kD + d0 + 2 * t] = o[t][1];
+      ow[(2 * tq) * kD + d0 + 2 * t + 1] = o[t][2];
+      ow[(2 * tq + 1) * kD + d0 + 2 * t + 1] = o[t][3];
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < 8 * kD; idx += blockDim.x) {
+    const int h = idx / kD, d = idx % kD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) M = fmaxf(M, red_m[w * 8 + h]);
+    float L = 0.0f, O = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kW; ++w) {
+        const float e = ex2(red_m[w * 8 + h] - M);
+        L += red_l[w * 8 + h] * e;
+        O += red_o[(w * 8 + h) * kD + d] * e;
+      }
+    }
+    if (a.num_splits == 1) {
+      fin[idx] = L > 0.0f ? O / L : 0.0f;
+    } else if (h < a.G) {
+      const long long pi = ((long long)b * a.Hq + (long long)kvh * a.G + h) * a.num_splits + split;
+      a.ws_o[pi * kD + d] = O;
+      if (d == 0) {
+        a.ws_ml[2 * pi] = M;
+        a.ws_ml[2 * pi + 1] = L;
+      }
+    }
+  }
+  if (a.num_splits == 1) {
+    __syncthreads();
+    for (int h = warp; h < a.G; h += kW) {  // o = H o'
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = fin[h * kD + 4 * lane + i];
+      fwht128_warp(v, lane);
+      const long long ob = ((long long)b * a.Hq + (long long)kvh * a.G + h) * kD + 4 * lane;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (a.out_f32) static_cast<float*>(a.out)[ob + i] = v[i];
+        else static_cast<__half*>(a.out)[ob + i] = __float2half_rn(v[i]);
+      }
+    }
+  }
+}
+
+// Merge the splits of each (sequence, query head), then rotate back: o = H o'.
+__global__ void __launch_bounds__(kD) kvarn_combine_kernel(const __grid_constant__ DecodeArgs a) {
+  __shared__ float v[kD];
+  const int b = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, d = threadIdx.x;
+  int n = a.seq_lens[b];
+  const int lim = min(a.max_seq_len, a.max_pages * kT);
+  n = n < 0 ? 0 : (n > lim ? lim : n);
+  n -= n % kT;
+  const int ns = (n + a.tokens_per_split - 1) / a.tokens_per_split;
+  const long long base = ((long long)b * a.Hq + hq) * a.num_splits;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, a.ws_ml[2 * (base + s)]);
+  float L = 0.0f, O = 0.0f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < ns; ++s) {
+      const float e = ex2(a.ws_ml[2 * (base + s)] - M);
+      L += a.ws_ml[2 * (base + s) + 1] * e;
+      O += a.ws_o[(base + s) * kD + d] * e;
+    }
+  }
+  v[d] = L > 0.0f ? O / L : 0.0f;
+  __syncthreads();
+  for (int h = 1; h < kD; h <<= 1) {  // Sylvester butterflies across threads
+    const float mine = v[d], other = v[d ^ h];
+    __syncthreads();
+    v[d] = (d & h) ? other - mine : mine + other;
+    __syncthreads();
+  }
+  const float r = v[d] * 0.08838834764831845f;
+  const long long oi = ((long long)b * a.Hq + hq) * kD + d;
+  if (a.out_f32) static_cast<float*>(a.out)[oi] = r;
+  else static_cast<__half*>(a.out)[oi] = __float2half_rn(r);
+}
+
+}  // namespace
+
+cudaError_t launch_kvarn_decode(const DecodeArgs& a, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kvarn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_splits, a.Hkv, a.B);
+  kvarn_decode_kernel<<<grid, kW * 32, kSmem, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.num_splits == 1) return e;
+  kvarn_combine_kernel<<<a.B * a.Hq, kD, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

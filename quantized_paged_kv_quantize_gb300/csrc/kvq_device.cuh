@@ -166,9 +166,54 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   return y;
 }
 
+__device__ __forceinline__ float ex2(float x) {  // 2^x on the SFU (rel. error ~2^-22), ex2(-inf) = 0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Shared-memory loads of N 32-bit words.
+template <int N>
+__device__ __forceinline__ void lds(const uint8_t* p, uint32_t* w);
+template <>
+__device__ __forceinline__ void lds<4>(const uint8_t* p, uint32_t* w) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+}
+template <>
+__device__ __forceinline__ void lds<2>(const uint8_t* p, uint32_t* w) {
+  uint2 u = *reinterpret_cast<const uint2*>(p);
+  w[0] = u.x; w[1] = u.y;
+}
+template <>
+__device__ __forceinline__ void lds<1>(const uint8_t* p, uint32_t* w) {
+  w[0] = *reinterpret_cast<const uint32_t*>(p);
+}
+
 __device__ __forceinline__ float warp_max_xor(float v, int first, int last) {
   for (int o = first; o <= last; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
+
+// Arguments of the decode kernels (passed by value as a __grid_constant__).
+struct DecodeArgs {
+  const uint8_t* pool;
+  const void* q;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  void* out;
+  float* ws_o;   // [B][Hq][S][D]
+  float* ws_ml;  // [B][Hq][S][2]
+  int num_pages, Hkv, Hq, G, B, max_pages, max_seq_len;
+  int tokens_per_split, num_splits;
+  int out_f32;
+  int q_f32;
+  float sm_log2;  // softmax_scale * log2(e)
+  size_t block_bytes;
+  int rows_per_block;
+};
+
+// KVarN decode + combine (kvq_decode_kvarn.cu).
+cudaError_t launch_kvarn_decode(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace kvq

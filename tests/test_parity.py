@@ -228,3 +228,33 @@ def test_mode_mismatch_and_unsupported():
         K.kvq_decode_attention(cache, _dev(c.q), _dev(c.lay.block_table), _dev(c.lay.seq_lens), out,
                                max_seq_len=16, mode="int8_per_token_head")
     assert e.value.status == 3
+
+
+# ------------------------------------------------------------------ KVarN decode
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+@pytest.mark.parametrize("Hq,Hkv,io", [(16, 2, "f16"), (8, 2, "f16"), (2, 2, "f16"), (8, 1, "f32")])
+def test_decode_kvarn_parity(Hq, Hkv, io, out_dtype):
+    c = make_case(small_workload("kvarn_k4v2_g128", Hq=Hq, Hkv=Hkv, io=io), KVARN_LENS + [0, 2048],
+                  slack_pages=2)
+    pool = oracle_pool(c)
+    cache = gpu_cache(c)
+    _upload_oracle_pool(cache, pool, c)
+    out, plan = gpu_decode(cache, c, out_dtype=out_dtype)
+    assert plan[0] > 1
+    check_attention(out, oracle_decode(c, pool))
+    assert kvq().kvq_cache_read_errors(cache) == 0
+
+
+def test_decode_kvarn_single_split_and_partial_tile():
+    K = kvq()
+    c = make_case(small_workload("kvarn_k4v2_g128"), [128, 0], slack_pages=1)
+    pool = oracle_pool(c)
+    cache = gpu_cache(c)
+    _upload_oracle_pool(cache, pool, c)
+    out, plan = gpu_decode(cache, c)
+    assert plan[0] == 1
+    check_attention(out, oracle_decode(c, pool))
+    # a sequence that ends inside a tile: only whole tiles are read, and it is flagged
+    out2, _ = gpu_decode(cache, c, lens=np.array([200, 0], np.int32), max_seq_len=256)
+    assert K.kvq_cache_read_errors(cache) & 0x4
+    check_attention(out2, oracle_decode(c, pool, lens=np.array([128, 0], np.int32)))
