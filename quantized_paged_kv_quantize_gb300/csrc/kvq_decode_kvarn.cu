@@ -14,8 +14,10 @@
 //   o    = H o' / sum_t p_t
 // so every scale folds into the 8 x 128 query (once per tile) or into the
 // probabilities (once per token), and the codes enter the tensor cores as
-// integers.  A code c becomes the f16 with bit pattern c (the subnormal
-// c * 2^-24, exact) by shift-and-mask; the 2^24 comes back in the fp32 scale.
+// small exact f16 values: a key code c (0..15) becomes 1 + c/16 and a value
+// code (0..3) becomes 1 + c/4, each by one shift and one bit-select; the
+// constant 1 is taken back out with the per-tile sums of the folded query
+// and of the scaled probabilities.
 //
 // GB300 layout: one CTA per (KV split, kv head, sequence); the CTA's warps
 // share a ring of 16 KB tile buffers filled by bulk TMA copies (one per tile).
@@ -58,6 +60,19 @@ struct Shared {
   int pages[kMaxTiles];
 };
 constexpr size_t kSmem = (size_t)kS * kBlk + sizeof(Shared);
+
+// Two 4-bit key codes (bits sft..sft+3 and 16+sft..) -> f16x2 {1 + c/16}: c lands in
+// mantissa bits 6..9 of 1.0 (0x3C00).
+__device__ __forceinline__ uint32_t kcode(uint32_t w, int sft) {
+  const uint32_t x = sft >= 6 ? (w >> (sft - 6)) : (w << (6 - sft));
+  return (x & 0x03C003C0u) | 0x3C003C00u;
+}
+// Two 2-bit value codes (bits sft..sft+1 and 16+sft..) -> f16x2 {1 + c/4}: c lands in
+// mantissa bits 8..9 of 1.0.
+__device__ __forceinline__ uint32_t vcode(uint32_t w, int sft) {
+  const uint32_t x = sft >= 8 ? (w >> (sft - 8)) : (w << (8 - sft));
+  return (x & 0x03000300u) | 0x3C003C00u;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -199,7 +214,8 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
           const int ln = 4 * h + tqd;
           fr[ln * 8 + slot * 2 + half] = hi;
           fr[ln * 8 + 4 + slot * 2 + half] = lo;
-          bp[h] = qv * cz;
+          // the tensor core sees (1 + code/16): take out 16 * sum of the folded query it used
+          bp[h] = qv * cz - 16.0f * (__half2float(hi) + __half2float(lo));
         }
 #pragma unroll
         for (int h = 0; h < 8; ++h) {
@@ -225,7 +241,7 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
       int ex = 0;
       (void)frexpf(vmx, &ex);                         // vmx < 2^ex
       const float vnorm = ldexpf(1.0f, -ex);          // p' * vf * vnorm <= 2^kPShift
-      const float vback = ldexpf(16777216.0f, ex);    // undoes vnorm and the 2^-24 of the codes
+      const float vback = ldexpf(4.0f, ex);           // undoes vnorm and the 1/4 of the value codes
 
       // ---- this warp's two 16-token sub-blocks: tokens 16*sa.., 16*sb..
       const int sa = warp, sb = warp + kW;
@@ -241,26 +257,26 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
           const uint4 fq = sh.frag[j][lane];
           const int w = j >> 1, sft = (j & 1) * 8;
           uint32_t af[4];
-          af[0] = (KA0[w] >> sft) & 0x000F000Fu;
-          af[2] = (KA0[w] >> (sft + 4)) & 0x000F000Fu;
-          af[1] = (KA8[w] >> sft) & 0x000F000Fu;
-          af[3] = (KA8[w] >> (sft + 4)) & 0x000F000Fu;
+          af[0] = kcode(KA0[w], sft);
+          af[2] = kcode(KA0[w], sft + 4);
+          af[1] = kcode(KA8[w], sft);
+          af[3] = kcode(KA8[w], sft + 4);
           mma16816(cA, af, fq.x, fq.y);
           mma16816(cA, af, fq.z, fq.w);
-          af[0] = (KB0[w] >> sft) & 0x000F000Fu;
-          af[2] = (KB0[w] >> (sft + 4)) & 0x000F000Fu;
-          af[1] = (KB8[w] >> sft) & 0x000F000Fu;
-          af[3] = (KB8[w] >> (sft + 4)) & 0x000F000Fu;
+          af[0] = kcode(KB0[w], sft);
+          af[2] = kcode(KB0[w], sft + 4);
+          af[1] = kcode(KB8[w], sft);
+          af[3] = kcode(KB8[w], sft + 4);
           mma16816(cB, af, fq.x, fq.y);
           mma16816(cB, af, fq.z, fq.w);
         }
       }
       const int ta = 16 * sa + g, tb = 16 * sb + g;
       const float kA0 = sh.kf[ta], kA8 = sh.kf[ta + 8], kB0 = sh.kf[tb], kB8 = sh.kf[tb + 8];
-      const float sA[4] = {fmaf(cA[0], 16777216.0f, be0) * kA0, fmaf(cA[1], 16777216.0f, be1) * kA0,
-                           fmaf(cA[2], 16777216.0f, be0) * kA8, fmaf(cA[3], 16777216.0f, be1) * kA8};
-      const float sB[4] = {fmaf(cB[0], 16777216.0f, be0) * kB0, fmaf(cB[1], 16777216.0f, be1) * kB0,
-                           fmaf(cB[2], 16777216.0f, be0) * kB8, fmaf(cB[3], 16777216.0f, be1) * kB8};
+      const float sA[4] = {fmaf(cA[0], 16.0f, be0) * kA0, fmaf(cA[1], 16.0f, be1) * kA0,
+                           fmaf(cA[2], 16.0f, be0) * kA8, fmaf(cA[3], 16.0f, be1) * kA8};
+      const float sB[4] = {fmaf(cB[0], 16.0f, be0) * kB0, fmaf(cB[1], 16.0f, be1) * kB0,
+                           fmaf(cB[2], 16.0f, be0) * kB8, fmaf(cB[3], 16.0f, be1) * kB8};
       float bm0 = fmaxf(fmaxf(sA[0], sA[2]), fmaxf(sB[0], sB[2]));
       float bm1 = fmaxf(fmaxf(sA[1], sA[3]), fmaxf(sB[1], sB[3]));
 #pragma unroll
@@ -289,24 +305,31 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
       const float zA0 = sh.vz[ta], zA8 = sh.vz[ta + 8], zB0 = sh.vz[tb], zB8 = sh.vz[tb + 8];
       float bv0 = (pA0 * zA0 + pA2 * zA8) + (pB0 * zB0 + pB2 * zB8);
       float bv1 = (pA1 * zA0 + pA3 * zA8) + (pB1 * zB0 + pB3 * zB8);
-#pragma unroll
-      for (int x = 4; x <= 16; x <<= 1) {
-        bv0 += __shfl_xor_sync(kFull, bv0, x);
-        bv1 += __shfl_xor_sync(kFull, bv1, x);
-      }
       uint32_t bh[4], bl[4];
       {
         const float fA0 = sh.vf[ta] * vnorm, fA8 = sh.vf[ta + 8] * vnorm;
         const float fB0 = sh.vf[tb] * vnorm, fB8 = sh.vf[tb + 8] * vnorm;
         const float x[8] = {pA0 * fA0, pA1 * fA0, pA2 * fA8, pA3 * fA8, pB0 * fB0, pB1 * fB0, pB2 * fB8, pB3 * fB8};
+        float u0 = 0.0f, u1 = 0.0f;  // sum of the f16 values the tensor core sees, per head
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const __half2 h = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
           const float2 f = __half22float2(h);
           const __half2 lo = __floats2half2_rn(x[2 * k] - f.x, x[2 * k + 1] - f.y);
+          const float2 fl = __half22float2(lo);
+          u0 += f.x + fl.x;
+          u1 += f.y + fl.y;
           bh[k] = movmatrix_t(h2_as_u32(h));
           bl[k] = movmatrix_t(h2_as_u32(lo));
         }
+        // value codes enter as (1 + code/4): take out vback * sum of the probabilities used
+        bv0 = fmaf(-vback, u0, bv0);
+        bv1 = fmaf(-vback, u1, bv1);
+      }
+#pragma unroll
+      for (int x = 4; x <= 16; x <<= 1) {
+        bv0 += __shfl_xor_sync(kFull, bv0, x);
+        bv1 += __shfl_xor_sync(kFull, bv1, x);
       }
       // ---- O_tile^T = V^T P^T for both sub-blocks, then the per-channel fold
       float ot[8][4];
@@ -330,10 +353,10 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
           const uint32_t s01 = t < 4 ? X01 : Y01, s23 = t < 4 ? X23 : Y23;
           const int sh2 = 4 * (t & 3);  // code e = 2t (row g) and 2t+1 (row g+8), 2 bits each
           uint32_t av[4];
-          av[0] = (s01 >> sh2) & 0x00030003u;
-          av[1] = (s01 >> (sh2 + 2)) & 0x00030003u;
-          av[2] = (s23 >> sh2) & 0x00030003u;
-          av[3] = (s23 >> (sh2 + 2)) & 0x00030003u;
+          av[0] = vcode(s01, sh2);
+          av[1] = vcode(s01, sh2 + 2);
+          av[2] = vcode(s23, sh2);
+          av[3] = vcode(s23, sh2 + 2);
           mma16816(ot[t], av, hb0, hb1);
           mma16816(ot[t], av, lb0, lb1);
         }

@@ -255,6 +255,10 @@ def test_decode_kvarn_single_split_and_partial_tile():
     assert plan[0] == 1
     check_attention(out, oracle_decode(c, pool))
     # a sequence that ends inside a tile: only whole tiles are read, and it is flagged
-    out2, _ = gpu_decode(cache, c, lens=np.array([200, 0], np.int32), max_seq_len=256)
-    assert K.kvq_cache_read_errors(cache) & 0x4
-    check_attention(out2, oracle_decode(c, pool, lens=np.array([128, 0], np.int32)))
+    c2 = make_case(small_workload("kvarn_k4v2_g128"), [256, 0], slack_pages=1)
+    pool2 = oracle_pool(c2)
+    cache2 = gpu_cache(c2)
+    _upload_oracle_pool(cache2, pool2, c2)
+    out2, _ = gpu_decode(cache2, c2, lens=np.array([200, 0], np.int32), max_seq_len=256)
+    assert K.kvq_cache_read_errors(cache2) & 0x4
+    check_attention(out2, oracle_decode(c2, pool2, lens=np.array([128, 0], np.int32)))
