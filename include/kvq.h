@@ -28,8 +28,10 @@
  *    before anything is launched.
  *  - Pointers named dev_* or documented as device pointers are CUDA device
  *    memory owned by the caller.  The library never allocates device memory:
- *    the cache pool and the decode workspace are caller buffers.  A kvq_cache
- *    handle owns only a small host-side descriptor.
+ *    the cache pool and the decode workspace are caller buffers (the one
+ *    library-owned buffer is the fixed scratch array described at
+ *    kvq_decode_attention_noalloc).  A kvq_cache handle owns only a small
+ *    host-side descriptor.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All device
  *    work is enqueued on it asynchronously, unless a call says otherwise.
  *  - There is no fallback path: an unsupported combination of mode, head_dim,
@@ -183,6 +185,34 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
                                 int num_q_heads, int max_seq_len, int mode, float softmax_scale,
                                 void* out, int out_dtype, void* workspace, size_t workspace_bytes,
                                 void* stream);
+
+/* Allocation-free variant of kvq_decode_attention.  (No counterpart on the
+ * source pages: this is an interface for callers, not part of the method.)
+ * It is for callers that cannot allocate device memory when they decode --
+ * for example code running inside a memory pool that was sized and frozen in
+ * advance, or a host process embedding the library without any device
+ * allocator of its own -- and so cannot provide the split-KV workspace.
+ * Arguments and results are those of kvq_decode_attention minus the
+ * workspace: the split partials go to a scratch array built into the library,
+ * KVQ_NOALLOC_SCRATCH_BYTES bytes of device memory that every GPU loading the
+ * library holds until the process exits.
+ *  - A decode whose plan (kvq_decode_plan) needs more scratch than that is
+ *    rejected with KVQ_ERR_CAPACITY before anything is launched.
+ *  - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *    library routine.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    calls whose kernels overlap on the GPU (different streams, or other
+ *    host threads) race on it and must be serialised by the caller.
+ *  - Each call writes every scratch entry it reads, so nothing has to be
+ *    cleared between calls. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (32u << 20)
+kvq_status kvq_decode_attention_noalloc(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                                        int max_pages, const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                                        int max_seq_len, int mode, float softmax_scale, void* out,
+                                        int out_dtype, void* stream);
 
 #ifdef __cplusplus
 }

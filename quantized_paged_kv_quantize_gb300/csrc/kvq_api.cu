@@ -319,3 +319,86 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode.  Some callers cannot allocate device memory at the
+// point where they decode: inference loops that sized and froze their memory
+// pool up front, or hosts embedding the library with no device allocator of
+// their own (no torch, no cudaMalloc in their process model).
+// For them the split-KV scratch that kvq_decode_attention takes as a caller
+// buffer lives instead in this fixed, library-owned device array.  Every GPU
+// that loads the library keeps this array for the life of the process.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The array's
+// name in host code is only a host-side handle, never a device address, so it
+// is resolved once per device (with that device current) and cached.
+kvq_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(KVQ_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the decode scratch");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_cache* cache, const void* q,
+                                                   const int32_t* block_table, int max_pages,
+                                                   const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                                                   int max_seq_len, int mode, float softmax_scale, void* out,
+                                                   int out_dtype, void* stream) {
+  kvq_status s = check_cache(cache);
+  if (s) return s;
+  const kvq_cache_config& c = cache->cfg;
+  if (mode != c.mode)
+    return fail(KVQ_ERR_MODE_MISMATCH, "decode mode %d but the cache holds mode %d", mode, c.mode);
+  if (num_seqs < 0 || max_pages < 0 || max_seq_len < 0) return fail(KVQ_ERR_INVALID_ARG, "negative size");
+  if (num_q_heads <= 0 || num_q_heads % c.num_kv_heads != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                c.num_kv_heads);
+  if (num_q_heads / c.num_kv_heads > 8)
+    return fail(KVQ_ERR_UNSUPPORTED, "GQA group %d > 8", num_q_heads / c.num_kv_heads);
+  if ((long long)max_seq_len > (long long)max_pages * c.page_size)
+    return fail(KVQ_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
+  if (out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return fail(KVQ_ERR_UNSUPPORTED, "out_dtype %d", out_dtype);
+  if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f)
+    return fail(KVQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+  if (num_seqs == 0) return KVQ_OK;
+  if (!q || !block_table || !seq_lens || !out) return fail(KVQ_ERR_INVALID_ARG, "NULL q, table, lens or out");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return fail(KVQ_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs, num_q_heads, max_seq_len);
+  if (p.workspace_bytes > (size_t)KVQ_NOALLOC_SCRATCH_BYTES)
+    return fail(KVQ_ERR_CAPACITY,
+                "this decode needs %zu bytes of split scratch but the built-in scratch holds %zu; "
+                "use kvq_decode_attention with a caller workspace",
+                p.workspace_bytes, (size_t)KVQ_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  if (p.workspace_bytes > 0) {
+    s = noalloc_scratch(&scratch);
+    if (s) return s;
+  }
+  // Every scratch entry the combine step reads is written earlier in the same
+  // call, so nothing needs clearing between calls.
+  cudaError_t e = kvq::launch_decode(cache, p, q, block_table, max_pages, seq_lens, num_seqs, num_q_heads,
+                                     max_seq_len, softmax_scale, out, out_dtype, scratch,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return KVQ_OK;
+}

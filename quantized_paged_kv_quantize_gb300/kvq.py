@@ -34,7 +34,7 @@ EXPORTED = [
     "kvq_last_error", "kvq_version", "kvq_cache_bytes", "kvq_cache_block_bytes", "kvq_cache_alloc",
     "kvq_cache_free", "kvq_cache_set_tensor_scales", "kvq_tensor_amax",
     "kvq_cache_set_tensor_scales_from_amax", "kvq_cache_read_errors", "kvq_quantize_write",
-    "kvq_decode_plan", "kvq_decode_workspace_bytes", "kvq_decode_attention",
+    "kvq_decode_plan", "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_decode_attention_noalloc",
 ]
 
 
@@ -72,6 +72,7 @@ def _load():
                                   ctypes.POINTER(sz)]),
         "kvq_decode_workspace_bytes": (i32, [vp, i32, i32, i32, ctypes.POINTER(sz)]),
         "kvq_decode_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, f32, vp, i32, vp, sz, vp]),
+        "kvq_decode_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, f32, vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -231,3 +232,23 @@ def kvq_decode_attention(cache: KVCache, q, block_table, seq_lens, out, *, max_s
     _check(_lib.kvq_decode_attention(cache.handle, _ptr(q), _ptr(block_table), mp, _ptr(seq_lens), B, Hq,
                                      max_seq_len, cache.mode if mode is None else _mode(mode), sm, _ptr(out),
                                      od, _ptr(workspace), wb, _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def kvq_decode_attention_noalloc(cache: KVCache, q, block_table, seq_lens, out, *, max_seq_len: int,
+                                 num_seqs: Optional[int] = None, num_q_heads: Optional[int] = None,
+                                 max_pages: Optional[int] = None, softmax_scale: Optional[float] = None,
+                                 mode=None, out_dtype=None, stream=None):
+    """kvq_decode_attention for callers that cannot allocate device memory: the
+    split scratch is the library's own fixed array (NOALLOC_SCRATCH_BYTES), shared
+    by all calls, so calls must not overlap on the GPU."""
+    B = num_seqs if num_seqs is not None else q.shape[0]
+    Hq = num_q_heads if num_q_heads is not None else q.shape[1]
+    mp = max_pages if max_pages is not None else block_table.shape[1]
+    sm = softmax_scale if softmax_scale is not None else cache.cfg.head_dim ** -0.5
+    od = _dtype_code(out.dtype) if out_dtype is None else _dtype_code(out_dtype)
+    _check(_lib.kvq_decode_attention_noalloc(cache.handle, _ptr(q), _ptr(block_table), mp, _ptr(seq_lens), B,
+                                             Hq, max_seq_len, cache.mode if mode is None else _mode(mode), sm,
+                                             _ptr(out), od, _stream(stream)))
