@@ -45,7 +45,7 @@ constexpr int kWarps = 4;
 #define KVQ_B1_STAGES 2
 #endif
 #ifndef KVQ_B1_MINB
-#define KVQ_B1_MINB 5
+#define KVQ_B1_MINB 4
 #endif
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -63,10 +63,15 @@ struct Cfg {
   static constexpr int SWZ_MASK = !TMA ? 0 : (RW == 128 ? 7 : 3);
   static constexpr int STAGES = MODE == KVQ_NVFP4 ? KVQ_FP4_STAGES : KVQ_B1_STAGES;
   static constexpr int MINB = MODE == KVQ_NVFP4 ? KVQ_FP4_MINB : KVQ_B1_MINB;
-  // probabilities are scaled by 2^PSHIFT before the f16 split (range of P x scale)
+  // The running reference max may lag the true max by up to SLACK (log2 units)
+  // before it is moved, so probabilities reach 2^SLACK; they are scaled by
+  // 2^PSHIFT before the f16 split, with 2^(PSHIFT + SLACK) x (largest V scale
+  // folded into P) inside the f16 range: per-token-head V scales of fp16 inputs
+  // are at most 65504/127 (INT8) or 65504/448 (FP8).
+  static constexpr int slack(bool f32io) { return f32io ? 0 : 4; }
   static constexpr int pshift(bool f32io) {
-    return MODE == KVQ_INT8_PER_TOKEN_HEAD ? (f32io ? 0 : 6)
-         : MODE == KVQ_FP8_PER_TOKEN_HEAD ? (f32io ? 0 : 8) : 14;
+    return MODE == KVQ_INT8_PER_TOKEN_HEAD ? (f32io ? 0 : 2)
+         : MODE == KVQ_FP8_PER_TOKEN_HEAD ? (f32io ? 0 : 4) : (f32io ? 14 : 10);
   }
 };
 
@@ -135,170 +140,197 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int 
   }
 }
 
-// S^T = K Q^T for one staged page: c[0..1] = tokens g, c[2..3] = token g+8, heads 2tq, 2tq+1.
-template <int MODE, int D, bool QF32>
-__device__ __forceinline__ void qk_page(const uint8_t* st, int g, int tq, const uint32_t (*qh)[2],
-                                        const uint32_t (*ql)[2], float* c) {
+// S^T = K Q^T for NP staged pages, their k-steps interleaved so the pages'
+// MMA chains overlap: c[p][0..1] = token g, c[p][2..3] = token g+8, heads 2tq, 2tq+1.
+template <int MODE, int D, bool QF32, int NP>
+__device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq, const uint32_t (*qh)[2],
+                                         const uint32_t (*ql)[2], float (*c)[4]) {
   using C = Cfg<MODE, D>;
   constexpr int KSTEPS = C::KSTEPS;
   constexpr int KW = (MODE == KVQ_NVFP4 ? D / 8 : D / 4) / 4;  // words per thread per row
-  uint32_t kg[KW], kh8[KW];
+  uint32_t kg[NP][KW], kh8[NP][KW];
   const int rb = tq * (KW * 4);
 #pragma unroll
-  for (int w = 0; w < KW; w += 4) {
-    lds<(KW >= 4 ? 4 : KW)>(st + swz<C::SWZ_MASK>(g * C::RW + rb + 4 * w), kg + w);
-    lds<(KW >= 4 ? 4 : KW)>(st + swz<C::SWZ_MASK>((g + 8) * C::RW + rb + 4 * w), kh8 + w);
-  }
+  for (int p = 0; p < NP; ++p)
+#pragma unroll
+    for (int w = 0; w < KW; w += 4) {
+      lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>(g * C::RW + rb + 4 * w), kg[p] + w);
+      lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>((g + 8) * C::RW + rb + 4 * w), kh8[p] + w);
+    }
   if constexpr (MODE == KVQ_NVFP4) {
     constexpr int SB = D / 16;
     const int blk0 = (tq * (D / 4)) / 16;
     const int base_g = C::S_OFF + g * SB, base_h = C::S_OFF + (g + 8) * SB;
-    uint32_t sg, sh;
-    if constexpr (D / 4 >= 16) {
-      sg = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(base_g + blk0));
-      sh = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(base_h + blk0));
-    } else {
-      sg = st[swz<C::SWZ_MASK>(base_g + blk0)] * 0x0101u;
-      sh = st[swz<C::SWZ_MASK>(base_h + blk0)] * 0x0101u;
-    }
-    const __half2 sg2 = u32_as_h2(e4m3x2_to_f16x2(sg)), sh2 = u32_as_h2(e4m3x2_to_f16x2(sh));
+    __half2 sg2[NP], sh2[NP];
 #pragma unroll
-    for (int w = 0; w < KW; ++w) {
-      uint32_t fg[4], fh[4];
-      e2m1x8_to_f16x2x4(kg[w], fg);
-      e2m1x8_to_f16x2x4(kh8[w], fh);
+    for (int p = 0; p < NP; ++p) {
+      uint32_t sg, sh;
+      if constexpr (D / 4 >= 16) {
+        sg = *reinterpret_cast<const uint16_t*>(st[p] + swz<C::SWZ_MASK>(base_g + blk0));
+        sh = *reinterpret_cast<const uint16_t*>(st[p] + swz<C::SWZ_MASK>(base_h + blk0));
+      } else {
+        sg = st[p][swz<C::SWZ_MASK>(base_g + blk0)] * 0x0101u;
+        sh = st[p][swz<C::SWZ_MASK>(base_h + blk0)] * 0x0101u;
+      }
+      sg2[p] = u32_as_h2(e4m3x2_to_f16x2(sg));
+      sh2[p] = u32_as_h2(e4m3x2_to_f16x2(sh));
+    }
+#pragma unroll
+    for (int w = 0; w < KW; ++w)
 #pragma unroll
       for (int hlf = 0; hlf < 2; ++hlf) {
         const int j = 2 * w + hlf;
         const bool second = (4 * j) >= 16;  // channel offset within the thread's D/4 range
-        const __half2 sa = second ? __high2half2(sg2) : __low2half2(sg2);
-        const __half2 sb = second ? __high2half2(sh2) : __low2half2(sh2);
-        uint32_t af[4];
-        af[0] = h2_as_u32(__hmul2(u32_as_h2(fg[2 * hlf]), sa));
-        af[1] = h2_as_u32(__hmul2(u32_as_h2(fh[2 * hlf]), sb));
-        af[2] = h2_as_u32(__hmul2(u32_as_h2(fg[2 * hlf + 1]), sa));
-        af[3] = h2_as_u32(__hmul2(u32_as_h2(fh[2 * hlf + 1]), sb));
-        mma16816(c, af, qh[j][0], qh[j][1]);
-        if constexpr (QF32) mma16816(c, af, ql[j][0], ql[j][1]);
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          uint32_t fg[4], fh[4];
+          e2m1x8_to_f16x2x4(kg[p][w], fg);
+          e2m1x8_to_f16x2x4(kh8[p][w], fh);
+          const __half2 sa = second ? __high2half2(sg2[p]) : __low2half2(sg2[p]);
+          const __half2 sb = second ? __high2half2(sh2[p]) : __low2half2(sh2[p]);
+          uint32_t af[4];
+          af[0] = h2_as_u32(__hmul2(u32_as_h2(fg[2 * hlf]), sa));
+          af[1] = h2_as_u32(__hmul2(u32_as_h2(fh[2 * hlf]), sb));
+          af[2] = h2_as_u32(__hmul2(u32_as_h2(fg[2 * hlf + 1]), sa));
+          af[3] = h2_as_u32(__hmul2(u32_as_h2(fh[2 * hlf + 1]), sb));
+          mma16816(c[p], af, qh[j][0], qh[j][1]);
+          if constexpr (QF32) mma16816(c[p], af, ql[j][0], ql[j][1]);
+        }
       }
-    }
   } else {
 #pragma unroll
-    for (int j = 0; j < KSTEPS; ++j) {
-      uint32_t af[4];
-      cvt_pair4<MODE>(kg[j], af[0], af[2]);
-      cvt_pair4<MODE>(kh8[j], af[1], af[3]);
-      mma16816(c, af, qh[j][0], qh[j][1]);
-      if constexpr (QF32) mma16816(c, af, ql[j][0], ql[j][1]);
-    }
+    for (int j = 0; j < KSTEPS; ++j)
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        uint32_t af[4];
+        cvt_pair4<MODE>(kg[p][j], af[0], af[2]);
+        cvt_pair4<MODE>(kh8[p][j], af[1], af[3]);
+        mma16816(c[p], af, qh[j][0], qh[j][1]);
+        if constexpr (QF32) mma16816(c[p], af, ql[j][0], ql[j][1]);
+      }
   }
 }
 
-// O^T += V^T P^T for one staged page.  Rows (tokens) >= nvalid are zeroed before
-// use so that whatever bytes an unwritten slot holds cannot reach the output.
-template <int MODE, int D>
-__device__ __forceinline__ void pv_page(const uint8_t* st, int g, int tq, int nvalid, uint32_t bh0, uint32_t bh1,
-                                        uint32_t bl0, uint32_t bl1, float (*o)[4]) {
+// O^T += V^T P^T for NP staged pages (M-tiles interleaved across pages).  With
+// PARTIAL, rows (tokens) >= nvalid[p] are zeroed before use so that whatever
+// bytes an unwritten slot holds cannot reach the output.
+template <int MODE, int D, int NP, bool PARTIAL>
+__device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq, const int* nvalid,
+                                         const uint32_t (*bh)[2], const uint32_t (*bl)[2], float (*o)[4]) {
   using C = Cfg<MODE, D>;
   constexpr int MTILES = C::MTILES;
   const int r0 = 2 * tq, r1 = 2 * tq + 1, r2 = 2 * tq + 8, r3 = 2 * tq + 9;
-  const bool partial = nvalid < kPage;
   if constexpr (MODE == KVQ_NVFP4) {
     constexpr int VB = D / 16;  // bytes per thread per row (D/8 channels at 4 bits)
     constexpr int VW = VB >= 4 ? VB / 4 : 1;
-    uint32_t A0[VW], A1[VW], A2[VW], A3[VW];
+    uint32_t A0[NP][VW], A1[NP][VW], A2[NP][VW], A3[NP][VW];
+    __half2 sc01[NP], sc23[NP];
     const int cb = g * VB;
-    if constexpr (VB >= 8) {
-      lds<2>(st + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb), A0);
-      lds<2>(st + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb), A1);
-      lds<2>(st + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb), A2);
-      lds<2>(st + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb), A3);
-    } else {
-      A0[0] = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb));
-      A1[0] = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb));
-      A2[0] = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb));
-      A3[0] = *reinterpret_cast<const uint16_t*>(st + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb));
-    }
     const int vblk = (g * (D / 8)) / 16;
     constexpr int VS = C::S_OFF + kPage * (D / 16);  // V block scales
-    uint32_t b0 = st[swz<C::SWZ_MASK>(VS + r0 * (D / 16) + vblk)], b1 = st[swz<C::SWZ_MASK>(VS + r1 * (D / 16) + vblk)];
-    uint32_t b2 = st[swz<C::SWZ_MASK>(VS + r2 * (D / 16) + vblk)], b3 = st[swz<C::SWZ_MASK>(VS + r3 * (D / 16) + vblk)];
-    if (partial) {
 #pragma unroll
-      for (int w = 0; w < VW; ++w) {
-        if (r0 >= nvalid) A0[w] = 0;
-        if (r1 >= nvalid) A1[w] = 0;
-        if (r2 >= nvalid) A2[w] = 0;
-        if (r3 >= nvalid) A3[w] = 0;
+    for (int p = 0; p < NP; ++p) {
+      if constexpr (VB >= 8) {
+        lds<2>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb), A0[p]);
+        lds<2>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb), A1[p]);
+        lds<2>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb), A2[p]);
+        lds<2>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb), A3[p]);
+      } else {
+        A0[p][0] = *reinterpret_cast<const uint16_t*>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb));
+        A1[p][0] = *reinterpret_cast<const uint16_t*>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb));
+        A2[p][0] = *reinterpret_cast<const uint16_t*>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb));
+        A3[p][0] = *reinterpret_cast<const uint16_t*>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb));
       }
-      if (r0 >= nvalid) b0 = 0;
-      if (r1 >= nvalid) b1 = 0;
-      if (r2 >= nvalid) b2 = 0;
-      if (r3 >= nvalid) b3 = 0;
+      uint32_t b0 = st[p][swz<C::SWZ_MASK>(VS + r0 * (D / 16) + vblk)];
+      uint32_t b1 = st[p][swz<C::SWZ_MASK>(VS + r1 * (D / 16) + vblk)];
+      uint32_t b2 = st[p][swz<C::SWZ_MASK>(VS + r2 * (D / 16) + vblk)];
+      uint32_t b3 = st[p][swz<C::SWZ_MASK>(VS + r3 * (D / 16) + vblk)];
+      if constexpr (PARTIAL) {
+        const int nv = nvalid[p];
+#pragma unroll
+        for (int w = 0; w < VW; ++w) {
+          if (r0 >= nv) A0[p][w] = 0;
+          if (r1 >= nv) A1[p][w] = 0;
+          if (r2 >= nv) A2[p][w] = 0;
+          if (r3 >= nv) A3[p][w] = 0;
+        }
+        if (r0 >= nv) b0 = 0;
+        if (r1 >= nv) b1 = 0;
+        if (r2 >= nv) b2 = 0;
+        if (r3 >= nv) b3 = 0;
+      }
+      sc01[p] = u32_as_h2(e4m3x2_to_f16x2(b0 | (b1 << 8)));
+      sc23[p] = u32_as_h2(e4m3x2_to_f16x2(b2 | (b3 << 8)));
     }
-    const __half2 sc01 = u32_as_h2(e4m3x2_to_f16x2(b0 | (b1 << 8)));
-    const __half2 sc23 = u32_as_h2(e4m3x2_to_f16x2(b2 | (b3 << 8)));
 #pragma unroll
-    for (int w = 0; w < VW; ++w) {
-      // pair rows (r0, r1) and (r2, r3) nibble by nibble: even channel e = 8w+2k, odd e+1
-      const uint32_t xe01 = bitsel(A0[w], A1[w] << 4, 0x0F0F0F0Fu);
-      const uint32_t xo01 = bitsel(A0[w] >> 4, A1[w], 0x0F0F0F0Fu);
-      const uint32_t xe23 = bitsel(A2[w], A3[w] << 4, 0x0F0F0F0Fu);
-      const uint32_t xo23 = bitsel(A2[w] >> 4, A3[w], 0x0F0F0F0Fu);
-      uint32_t fe01[4], fo01[4], fe23[4], fo23[4];
-      e2m1x8_to_f16x2x4(xe01, fe01);
-      e2m1x8_to_f16x2x4(xo01, fo01);
-      e2m1x8_to_f16x2x4(xe23, fe23);
-      e2m1x8_to_f16x2x4(xo23, fo23);
+    for (int w = 0; w < VW; ++w)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int t = 4 * w + k;
-        if (t < MTILES) {
-          uint32_t av[4];
-          av[0] = h2_as_u32(__hmul2(u32_as_h2(fe01[k]), sc01));
-          av[1] = h2_as_u32(__hmul2(u32_as_h2(fo01[k]), sc01));
-          av[2] = h2_as_u32(__hmul2(u32_as_h2(fe23[k]), sc23));
-          av[3] = h2_as_u32(__hmul2(u32_as_h2(fo23[k]), sc23));
-          mma16816(o[t], av, bh0, bh1);
-          mma16816(o[t], av, bl0, bl1);
+      for (int p = 0; p < NP; ++p) {
+        // pair rows (r0, r1) and (r2, r3) nibble by nibble: even channel e = 8w+2k, odd e+1
+        const uint32_t xe01 = bitsel(A0[p][w], A1[p][w] << 4, 0x0F0F0F0Fu);
+        const uint32_t xo01 = bitsel(A0[p][w] >> 4, A1[p][w], 0x0F0F0F0Fu);
+        const uint32_t xe23 = bitsel(A2[p][w], A3[p][w] << 4, 0x0F0F0F0Fu);
+        const uint32_t xo23 = bitsel(A2[p][w] >> 4, A3[p][w], 0x0F0F0F0Fu);
+        uint32_t fe01[4], fo01[4], fe23[4], fo23[4];
+        e2m1x8_to_f16x2x4(xe01, fe01);
+        e2m1x8_to_f16x2x4(xo01, fo01);
+        e2m1x8_to_f16x2x4(xe23, fe23);
+        e2m1x8_to_f16x2x4(xo23, fo23);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int t = 4 * w + k;
+          if (t < MTILES) {
+            uint32_t av[4];
+            av[0] = h2_as_u32(__hmul2(u32_as_h2(fe01[k]), sc01[p]));
+            av[1] = h2_as_u32(__hmul2(u32_as_h2(fo01[k]), sc01[p]));
+            av[2] = h2_as_u32(__hmul2(u32_as_h2(fe23[k]), sc23[p]));
+            av[3] = h2_as_u32(__hmul2(u32_as_h2(fo23[k]), sc23[p]));
+            mma16816(o[t], av, bh[p][0], bh[p][1]);
+            mma16816(o[t], av, bl[p][0], bl[p][1]);
+          }
+        }
+      }
+  } else {
+    constexpr int VW = D / 32;  // words per thread per row (D/8 one-byte channels)
+    uint32_t A0[NP][VW], A1[NP][VW], A2[NP][VW], A3[NP][VW];
+    const int cb = g * (D / 8);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb), A0[p]);
+      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb), A1[p]);
+      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb), A2[p]);
+      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb), A3[p]);
+      if constexpr (PARTIAL) {
+        const int nv = nvalid[p];
+#pragma unroll
+        for (int w = 0; w < VW; ++w) {
+          if (r0 >= nv) A0[p][w] = 0;
+          if (r1 >= nv) A1[p][w] = 0;
+          if (r2 >= nv) A2[p][w] = 0;
+          if (r3 >= nv) A3[p][w] = 0;
         }
       }
     }
-  } else {
-    constexpr int VW = D / 32;  // words per thread per row (D/8 one-byte channels)
-    uint32_t A0[VW], A1[VW], A2[VW], A3[VW];
-    const int cb = g * (D / 8);
-    lds<VW>(st + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb), A0);
-    lds<VW>(st + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb), A1);
-    lds<VW>(st + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb), A2);
-    lds<VW>(st + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb), A3);
-    if (partial) {
 #pragma unroll
-      for (int w = 0; w < VW; ++w) {
-        if (r0 >= nvalid) A0[w] = 0;
-        if (r1 >= nvalid) A1[w] = 0;
-        if (r2 >= nvalid) A2[w] = 0;
-        if (r3 >= nvalid) A3[w] = 0;
-      }
-    }
+    for (int w = 0; w < VW; ++w)
 #pragma unroll
-    for (int w = 0; w < VW; ++w) {
-      uint32_t a0 = A0[w], a1 = A1[w], a2 = A2[w], a3 = A3[w];
-      if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD) {  // bias once per word: x + 128
-        a0 ^= 0x80808080u; a1 ^= 0x80808080u; a2 ^= 0x80808080u; a3 ^= 0x80808080u;
+      for (int p = 0; p < NP; ++p) {
+        uint32_t a0 = A0[p][w], a1 = A1[p][w], a2 = A2[p][w], a3 = A3[p][w];
+        if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD) {  // bias once per word: x + 128
+          a0 ^= 0x80808080u; a1 ^= 0x80808080u; a2 ^= 0x80808080u; a3 ^= 0x80808080u;
+        }
+        const uint32_t x01 = prmt(a0, a1, 0x5140u), y01 = prmt(a0, a1, 0x7362u);
+        const uint32_t x23 = prmt(a2, a3, 0x5140u), y23 = prmt(a2, a3, 0x7362u);
+        uint32_t av[4];
+        cvt_pair4_biased<MODE>(x01, av[0], av[1]);
+        cvt_pair4_biased<MODE>(x23, av[2], av[3]);
+        mma16816(o[2 * w], av, bh[p][0], bh[p][1]);
+        mma16816(o[2 * w], av, bl[p][0], bl[p][1]);
+        cvt_pair4_biased<MODE>(y01, av[0], av[1]);
+        cvt_pair4_biased<MODE>(y23, av[2], av[3]);
+        mma16816(o[2 * w + 1], av, bh[p][0], bh[p][1]);
+        mma16816(o[2 * w + 1], av, bl[p][0], bl[p][1]);
       }
-      const uint32_t x01 = prmt(a0, a1, 0x5140u), y01 = prmt(a0, a1, 0x7362u);
-      const uint32_t x23 = prmt(a2, a3, 0x5140u), y23 = prmt(a2, a3, 0x7362u);
-      uint32_t av[4];
-      cvt_pair4_biased<MODE>(x01, av[0], av[1]);
-      cvt_pair4_biased<MODE>(x23, av[2], av[3]);
-      mma16816(o[2 * w], av, bh0, bh1);
-      mma16816(o[2 * w], av, bl0, bl1);
-      cvt_pair4_biased<MODE>(y01, av[0], av[1]);
-      cvt_pair4_biased<MODE>(y23, av[2], av[3]);
-      mma16816(o[2 * w + 1], av, bh0, bh1);
-      mma16816(o[2 * w + 1], av, bl0, bl1);
-    }
   }
 }
 
@@ -308,6 +340,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   using C = Cfg<MODE, D>;
   constexpr int KSTEPS = C::KSTEPS, MTILES = C::MTILES;
   constexpr int PSHIFT = C::pshift(QF32);
+  constexpr float SLACK = (float)C::slack(QF32);
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ uint64_t bars[kWarps][C::STAGES];
   // 1024-byte alignment of the ring (swizzle patterns are address based)
@@ -347,28 +380,33 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   }
   __syncwarp();
 
-  // lane i holds the page id of this warp's i-th page
+  // lane i holds this warp's i-th page id and where its (page, kv head) block
+  // starts: a TMA row coordinate, or a byte offset for the plain bulk copy.
   int my_pid = -1;
+  long long my_src = 0;
   if (lane < my_count) {
     my_pid = __ldg(a.block_table + (long long)b * a.max_pages + p0 + warp + kWarps * lane);
     if (my_pid < 0 || my_pid >= a.num_pages) {
       set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_PAGE_RANGE);
       my_pid = -1;
+    } else {
+      my_src = kHeaderBytes + ((long long)my_pid * a.Hkv + kvh) * (long long)C::BLK;
+      if constexpr (C::TMA) my_src /= C::RW;
     }
   }
 
   auto issue = [&](int i) {
     const int pid = __shfl_sync(kFull, my_pid, i);
+    const long long src = __shfl_sync(kFull, my_src, i);
     if (lane == 0) {
       uint64_t* bar = &wb[i % C::STAGES];
       mbar_arrive_expect_tx(bar, pid >= 0 ? (uint32_t)C::BLK : 0u);
       if (pid >= 0) {
         uint8_t* dst = ring + (i % C::STAGES) * C::STAGE;
-        const long long ph = (long long)pid * a.Hkv + kvh;
         if constexpr (C::TMA)
-          tma_g2s_2d(dst, &tmap, 0, (int)((kHeaderBytes + ph * (long long)C::BLK) / C::RW), bar);
+          tma_g2s_2d(dst, &tmap, 0, (int)src, bar);
         else
-          bulk_g2s(dst, a.pool + kHeaderBytes + ph * (long long)C::BLK, (uint32_t)C::BLK, bar);
+          bulk_g2s(dst, a.pool + src, (uint32_t)C::BLK, bar);
       }
     }
   };
@@ -394,7 +432,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   float o[MTILES][4];
 #pragma unroll
   for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  float m0 = -1e30f, m1 = -1e30f, l0 = 0.0f, l1 = 0.0f;  // finite start: no inf - inf
   bool timed_out = false;
 
   for (int i = 0; i < my_count; i += 2) {
@@ -414,9 +452,18 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
     const int nvA = pidA >= 0 ? min(t_end - tokA, kPage) : 0;   // valid rows of each page
     const int nvB = pidB >= 0 ? min(t_end - tokB, kPage) : 0;
 
-    float cA[4] = {0.f, 0.f, 0.f, 0.f}, cB[4] = {0.f, 0.f, 0.f, 0.f};
-    if (nvA > 0) qk_page<MODE, D, QF32>(stA, g, tq, qh, ql, cA);
-    if (nvB > 0) qk_page<MODE, D, QF32>(stB, g, tq, qh, ql, cB);
+    // full pairs take a branch-free path with the two pages interleaved
+    const bool full2 = nvA == kPage && nvB == kPage;
+    const uint8_t* stAB[2] = {stA, stB};
+    float cc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (full2) {
+      qk_pages<MODE, D, QF32, 2>(stAB, g, tq, qh, ql, cc);
+    } else {
+      if (nvA > 0) qk_pages<MODE, D, QF32, 1>(stAB, g, tq, qh, ql, cc);
+      if (nvB > 0) qk_pages<MODE, D, QF32, 1>(stAB + 1, g, tq, qh, ql, cc + 1);
+    }
+    const float* cA = cc[0];
+    const float* cB = cc[1];
 
     float fA0 = kfac, fA8 = kfac, fB0 = kfac, fB8 = kfac;     // score factors of tokens g, g+8
     float vA0 = 1.f, vA8 = 1.f, vB0 = 1.f, vB8 = 1.f;         // V per-token scales
@@ -434,45 +481,60 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
       if (g >= nvB) { sB[0] = sB[1] = -INFINITY; vB0 = 0.f; }
       if (g + 8 >= nvB) { sB[2] = sB[3] = -INFINITY; vB8 = 0.f; }
     }
-    float bm0 = fmaxf(fmaxf(sA[0], sA[2]), fmaxf(sB[0], sB[2]));
-    float bm1 = fmaxf(fmaxf(sA[1], sA[3]), fmaxf(sB[1], sB[3]));
+    // Lazy reference max: move it (and rescale) only when some score exceeds it
+    // by more than SLACK -- rare once the first pages are seen.
+    const float t0 = m0 + SLACK, t1 = m1 + SLACK;
+    const bool over = (sA[0] > t0) | (sA[2] > t0) | (sB[0] > t0) | (sB[2] > t0) | (sA[1] > t1) | (sA[3] > t1) |
+                      (sB[1] > t1) | (sB[3] > t1);
+    if (__any_sync(kFull, over)) {
+      float bm0 = fmaxf(fmaxf(sA[0], sA[2]), fmaxf(sB[0], sB[2]));
+      float bm1 = fmaxf(fmaxf(sA[1], sA[3]), fmaxf(sB[1], sB[3]));
 #pragma unroll
-    for (int x = 4; x <= 16; x <<= 1) {
-      bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, x));
-      bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, x));
-    }
-    const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
-    const float z0 = n0 == -INFINITY ? 0.0f : n0, z1 = n1 == -INFINITY ? 0.0f : n1;
-    const float al0 = ex2(m0 - z0), al1 = ex2(m1 - z1);
-    m0 = n0;
-    m1 = n1;
-    if (!__all_sync(kFull, al0 == 1.0f && al1 == 1.0f)) {
+      for (int x = 4; x <= 16; x <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, x));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, x));
+      }
+      const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
+      const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);  // m starts at a finite -1e30
+      m0 = n0;
+      m1 = n1;
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
       for (int t = 0; t < MTILES; ++t) {
         o[t][0] *= al0; o[t][2] *= al0;
         o[t][1] *= al1; o[t][3] *= al1;
       }
     }
-    const float e0 = (float)PSHIFT - z0, e1 = (float)PSHIFT - z1;
+    const float e0 = (float)PSHIFT - m0, e1 = (float)PSHIFT - m1;
     const float pA0 = ex2(sA[0] + e0), pA1 = ex2(sA[1] + e1), pA2 = ex2(sA[2] + e0), pA3 = ex2(sA[3] + e1);
     const float pB0 = ex2(sB[0] + e0), pB1 = ex2(sB[1] + e1), pB2 = ex2(sB[2] + e0), pB3 = ex2(sB[3] + e1);
-    l0 = l0 * al0 + ((pA0 + pA2) + (pB0 + pB2));
-    l1 = l1 * al1 + ((pA1 + pA3) + (pB1 + pB3));
+    l0 += (pA0 + pA2) + (pB0 + pB2);
+    l1 += (pA1 + pA3) + (pB1 + pB3);
     // P^T as the B operand: f16 hi + lo, each 8x8 block transposed in registers
-    uint32_t bh[4], bl[4];
+    uint32_t bh[2][2], bl[2][2];
     {
-      const float x[8] = {pA0 * vA0, pA1 * vA0, pA2 * vA8, pA3 * vA8, pB0 * vB0, pB1 * vB0, pB2 * vB8, pB3 * vB8};
+      float x[8] = {pA0, pA1, pA2, pA3, pB0, pB1, pB2, pB3};
+      if constexpr (kPerToken) {
+        x[0] *= vA0; x[1] *= vA0; x[2] *= vA8; x[3] *= vA8;
+        x[4] *= vB0; x[5] *= vB0; x[6] *= vB8; x[7] *= vB8;
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const __half2 h = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
         const float2 f = __half22float2(h);
         const __half2 lo = __floats2half2_rn(x[2 * k] - f.x, x[2 * k + 1] - f.y);
-        bh[k] = movmatrix_t(h2_as_u32(h));
-        bl[k] = movmatrix_t(h2_as_u32(lo));
+        bh[k >> 1][k & 1] = movmatrix_t(h2_as_u32(h));
+        bl[k >> 1][k & 1] = movmatrix_t(h2_as_u32(lo));
       }
     }
-    if (nvA > 0) pv_page<MODE, D>(stA, g, tq, nvA, bh[0], bh[1], bl[0], bl[1], o);
-    if (nvB > 0) pv_page<MODE, D>(stB, g, tq, nvB, bh[2], bh[3], bl[2], bl[3], o);
+    if (full2) {
+      const int nv2[2] = {kPage, kPage};
+      pv_pages<MODE, D, 2, false>(stAB, g, tq, nv2, bh, bl, o);
+    } else {
+      if (nvA > 0) pv_pages<MODE, D, 1, true>(stAB, g, tq, &nvA, bh, bl, o);
+      if (nvB > 0) pv_pages<MODE, D, 1, true>(stAB + 1, g, tq, &nvB, bh + 1, bl + 1, o);
+    }
 
     __syncwarp();
     if (i + C::STAGES < my_count) {
