@@ -1,3 +1,4 @@
+import importlib.util
 import os
 import sys
 
@@ -8,3 +9,15 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+def pytest_sessionstart(session):
+    """Build libkvq (skipped when up to date) and the oracle before any test
+    imports them."""
+    spec = importlib.util.spec_from_file_location(
+        "kvq_build", os.path.join(ROOT, "quantized_paged_kv_quantize_gb300", "_build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import oracle
+    oracle.build()
