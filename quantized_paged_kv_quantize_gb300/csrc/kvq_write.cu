@@ -28,7 +28,7 @@ struct WriteArgs {
   const void* v;
   const int32_t* slots;
   long long num_tokens;
-  int Hkv, P, num_pages;
+  int Hkv, P, log2P, num_pages;
   size_t block_bytes;
 };
 
@@ -66,6 +66,70 @@ __device__ __forceinline__ void store_bytes<8>(uint8_t* dst, const uint32_t* w) 
   *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
 }
 
+// Encoding of the IEEE quotient RN(x/s) without a division on the common path.
+// With r = RN(1/s), rlo = RN(r(1 - 2^-20)) and rhi = RN(r(1 + 2^-20)), the
+// products RN(x rlo) and RN(x rhi) enclose RN(x/s): their relative distance to
+// x/s is at least 16u - 3u (u = 2^-24) on each side, while RN(x/s) is within u
+// of it.  Every encoder used here (round-to-nearest-even onto a grid, with
+// saturation) is monotone, so when both ends encode to the same code, that is
+// the code of RN(x/s); when they differ the quotient is computed exactly.
+// Scales whose reciprocal is not a comfortable normal number always divide.
+struct QDiv {
+  float s, rlo, rhi;
+  bool fast;
+  __device__ __forceinline__ explicit QDiv(float s_) : s(s_) {
+    const float r = __frcp_rn(s_);
+    fast = r >= 0x1p-100f && r <= 0x1p100f;
+    rlo = __fmul_rn(r, 1.0f - 0x1p-20f);
+    rhi = __fmul_rn(r, 1.0f + 0x1p-20f);
+  }
+  // E4M3 codes of x1:x0 (x0 in the low byte)
+  __device__ __forceinline__ uint32_t e4m3x2(float x1, float x0) const {
+    const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(x1, rlo), __fmul_rn(x0, rlo));
+    const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(x1, rhi), __fmul_rn(x0, rhi));
+    if (fast && lo == hi) return lo;
+    return f32x2_to_e4m3x2(__fdiv_rn(x1, s), __fdiv_rn(x0, s));
+  }
+  // Four int8 codes clamp(rint(x/s), -127, 127), x[0] in the low byte.  rint
+  // is done by adding 1.5 * 2^23: round-to-nearest-even leaves the integer in
+  // the low mantissa bits, whose low byte is the two's-complement code.  The
+  // fast path also requires both ends inside [-127, 127] (bit patterns
+  // 0x4B400000 -127 .. +127), so neither the clamp nor a NaN can reach it.
+  __device__ __forceinline__ uint32_t int8x4(const float* x) const {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    uint32_t lo[4], bad = fast ? 0u : 1u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      lo[e] = __float_as_uint(__fadd_rn(__fmul_rn(x[e], rlo), kMagic));
+      const uint32_t hi = __float_as_uint(__fadd_rn(__fmul_rn(x[e], rhi), kMagic));
+      bad |= (lo[e] ^ hi) | static_cast<uint32_t>(lo[e] - 0x4B3FFF81u > 254u);
+    }
+    if (bad == 0) return prmt(prmt(lo[0], lo[1], 0x0040u), prmt(lo[2], lo[3], 0x0040u), 0x5410u);
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float qv = fminf(fmaxf(rintf(__fdiv_rn(x[e], s)), -127.0f), 127.0f);
+      w |= (static_cast<uint32_t>(__float2int_rn(qv)) & 0xFFu) << (8 * e);
+    }
+    return w;
+  }
+  // eight E2M1 codes (pairs packed low nibble first) of x[0..n)
+  template <int N>
+  __device__ __forceinline__ uint32_t e2m1x8(const float* x) const {
+    float ylo[8], yhi[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      ylo[i] = i < N ? __fmul_rn(x[i], rlo) : 0.0f;
+      yhi[i] = i < N ? __fmul_rn(x[i], rhi) : 0.0f;
+    }
+    const uint32_t lo = f32x8_to_e2m1x8(ylo), hi = f32x8_to_e2m1x8(yhi);
+    if (fast && lo == hi) return lo;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ylo[i] = i < N ? __fdiv_rn(x[i], s) : 0.0f;
+    return f32x8_to_e2m1x8(ylo);
+  }
+};
+
 // Group max over TPR consecutive lanes (TPR a power of two <= 32).
 template <int TPR>
 __device__ __forceinline__ float group_max(float v) {
@@ -75,30 +139,29 @@ __device__ __forceinline__ float group_max(float v) {
 }
 
 // One (token, kv head, side) row of D values per group of TPR threads; each
-// thread converts VEC = 16 bytes of input.  Modes 1-4.
+// thread converts VEC = 16 bytes of input.  Grid: (token blocks, kv head,
+// side), so no index needs a division; a block's consecutive tokens land in
+// consecutive rows of the same pages.  Modes 1-4.
 template <int MODE, typename T, int D>
 __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
   constexpr int VEC = 16 / sizeof(T);
   constexpr int TPR = D / VEC;
+  constexpr int TOK = 256 / TPR;  // tokens per block
   static_assert(TPR >= 2 && TPR <= 32 && (TPR & (TPR - 1)) == 0, "row group");
-  const long long rows_per_side = a.num_tokens * a.Hkv;
-  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = gid / TPR;
-  const int j = static_cast<int>(gid % TPR);
+  const int h = blockIdx.y, side = blockIdx.z;
+  const long long token = (long long)blockIdx.x * TOK + threadIdx.x / TPR;
+  const int j = threadIdx.x % TPR;
 
-  bool active = row < 2 * rows_per_side;
-  const int side = active && row >= rows_per_side ? 1 : 0;
-  const long long r = active ? row - side * rows_per_side : 0;
-  const long long token = r / a.Hkv;
-  const int h = static_cast<int>(r % a.Hkv);
+  bool active = token < a.num_tokens;
   int slot = active ? __ldg(a.slots + token) : -1;
   active = active && slot >= 0;
-  const long long page = slot / a.P;
-  const int off = slot % a.P;
+  const int page = slot >> a.log2P;
+  const int off = slot & (a.P - 1);
   if (active && page >= a.num_pages) {
     if (j == 0) set_error(a.pool, KVQ_DEVERR_SLOT_RANGE);
     active = false;
   }
+  const long long r = token * a.Hkv + h;  // (token, head) row of the input
 
   float x[VEC];
   if (active) {
@@ -108,17 +171,13 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) x[i] = 0.0f;
   }
-  uint8_t* blk = a.pool + kHeaderBytes + (size_t)(page * a.Hkv + h) * a.block_bytes;
+  uint8_t* blk = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes;
 
   if constexpr (MODE == KVQ_FP8_PER_TENSOR) {
-    const float s = *reinterpret_cast<const float*>(a.pool + (side ? kHdrVScaleOffset : kHdrKScaleOffset));
+    const QDiv q(*reinterpret_cast<const float*>(a.pool + (side ? kHdrVScaleOffset : kHdrKScaleOffset)));
     uint32_t w[VEC / 4];
 #pragma unroll
-    for (int i = 0; i < VEC; i += 4) {
-      uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(x[i + 1], s), __fdiv_rn(x[i], s));
-      uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(x[i + 3], s), __fdiv_rn(x[i + 2], s));
-      w[i / 4] = lo | (hi << 16);
-    }
+    for (int i = 0; i < VEC; i += 4) w[i / 4] = q.e4m3x2(x[i + 1], x[i]) | (q.e4m3x2(x[i + 3], x[i + 2]) << 16);
     if (active) store_bytes<VEC>(blk + (size_t)side * a.P * D + (size_t)off * D + j * VEC, w);
   } else if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD || MODE == KVQ_FP8_PER_TOKEN_HEAD) {
     float amax = 0.0f;
@@ -126,22 +185,14 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
     for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
     amax = group_max<TPR>(amax);
     const float s = __fdiv_rn(fmaxf(amax, 1e-8f), MODE == KVQ_INT8_PER_TOKEN_HEAD ? 127.0f : 448.0f);
+    const QDiv q(s);
     uint32_t w[VEC / 4];
 #pragma unroll
     for (int i = 0; i < VEC; i += 4) {
       if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float qv = rintf(__fdiv_rn(x[i + e], s));
-          qv = fminf(fmaxf(qv, -127.0f), 127.0f);
-          word |= (static_cast<uint32_t>(__float2int_rn(qv)) & 0xFFu) << (8 * e);
-        }
-        w[i / 4] = word;
+        w[i / 4] = q.int8x4(x + i);
       } else {
-        uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(x[i + 1], s), __fdiv_rn(x[i], s));
-        uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(x[i + 3], s), __fdiv_rn(x[i + 2], s));
-        w[i / 4] = lo | (hi << 16);
+        w[i / 4] = q.e4m3x2(x[i + 1], x[i]) | (q.e4m3x2(x[i + 3], x[i + 2]) << 16);
       }
     }
     if (active) {
@@ -159,10 +210,8 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
     const uint32_t sb = f32x2_to_e4m3x2(0.0f, __fdiv_rn(amax, six_st)) & 0xFFu;
     const float sbf = e4m3_to_f32(sb);
     const float den = __fmul_rn(st, sbf);
-    float y[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = (i < VEC && sbf != 0.0f) ? __fdiv_rn(x[i], den) : 0.0f;
-    uint32_t w[1] = {f32x8_to_e2m1x8(y)};
+    uint32_t w[1] = {0u};
+    if (sbf != 0.0f) w[0] = QDiv(den).e2m1x8<VEC>(x);
     if (active) {
       store_bytes<VEC / 2>(blk + (size_t)side * a.P * D / 2 + (size_t)off * D / 2 + j * VEC / 2, w);
       if ((j % TPB) == 0)
@@ -401,12 +450,11 @@ __global__ void scales_from_amax_kernel(uint8_t* pool, const float* ak, const fl
 
 template <int MODE, typename T, int D>
 cudaError_t launch_rows(const WriteArgs& a, cudaStream_t s) {
-  constexpr int TPR = D / (16 / sizeof(T));
-  const long long threads = 2LL * a.num_tokens * a.Hkv * TPR;
-  const long long blocks = (threads + 255) / 256;
+  constexpr int TOK = 256 / (D / (16 / sizeof(T)));
+  const long long blocks = (a.num_tokens + TOK - 1) / TOK;
   if (blocks == 0) return cudaSuccess;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  write_rows_kernel<MODE, T, D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  if (blocks > 0x7fffffffLL || a.Hkv > 65535) return cudaErrorInvalidValue;
+  write_rows_kernel<MODE, T, D><<<dim3(static_cast<unsigned>(blocks), a.Hkv, 2), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -449,6 +497,8 @@ cudaError_t launch_write(const kvq_cache* c, const void* k, const void* v, const
   a.num_tokens = num_tokens;
   a.Hkv = c->cfg.num_kv_heads;
   a.P = c->cfg.page_size;
+  a.log2P = 0;
+  while ((1 << a.log2P) < a.P) ++a.log2P;  // page sizes are powers of two
   a.num_pages = c->cfg.num_pages;
   a.block_bytes = c->block_bytes;
   const int mode = c->cfg.mode, D = c->cfg.head_dim;
