@@ -24,6 +24,8 @@
 // inside the CTA and, when a sequence has several splits, by the combine kernel.
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -47,6 +49,9 @@ constexpr int kWarps = 4;
 #ifndef KVQ_B1_MINB
 #define KVQ_B1_MINB 4
 #endif
+// A warp's page ids for one split live in shared memory (at most this many
+// pages per warp, so at most kWarps * kIdsPerWarp pages per split).
+constexpr int kIdsPerWarp = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int MODE, int D>
@@ -353,6 +358,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   constexpr bool PLO = C::plo(QF32);
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ uint64_t bars[kWarps][C::STAGES];
+  __shared__ int page_ids[kWarps * kIdsPerWarp];
   // 1024-byte alignment of the ring (swizzle patterns are address based)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -390,24 +396,24 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   }
   __syncwarp();
 
-  // lane i holds this warp's i-th page id and where its (page, kv head) block
-  // starts: a TMA row coordinate, or a byte offset for the plain bulk copy.
-  int my_pid = -1;
-  long long my_src = 0;
-  if (lane < my_count) {
-    my_pid = __ldg(a.block_table + (long long)b * a.max_pages + p0 + warp + kWarps * lane);
-    if (my_pid < 0 || my_pid >= a.num_pages) {
+  // the warp's page ids (an out-of-range id is flagged and its page skipped)
+  int* ids = page_ids + warp * kIdsPerWarp;
+  for (int k = lane; k < my_count; k += 32) {
+    int pid = __ldg(a.block_table + (long long)b * a.max_pages + p0 + warp + kWarps * k);
+    if (pid < 0 || pid >= a.num_pages) {
       set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_PAGE_RANGE);
-      my_pid = -1;
-    } else {
-      my_src = kHeaderBytes + ((long long)my_pid * a.Hkv + kvh) * (long long)C::BLK;
-      if constexpr (C::TMA) my_src /= C::RW;
+      pid = -1;
     }
+    ids[k] = pid;
   }
+  __syncwarp();
 
+  // stream page i of this warp into stage i % STAGES: a TMA row coordinate or a
+  // byte offset for the plain bulk copy
   auto issue = [&](int i) {
-    const int pid = __shfl_sync(kFull, my_pid, i);
-    const long long src = __shfl_sync(kFull, my_src, i);
+    const int pid = ids[i];
+    long long src = kHeaderBytes + ((long long)pid * a.Hkv + kvh) * (long long)C::BLK;
+    if constexpr (C::TMA) src /= C::RW;
     if (lane == 0) {
       uint64_t* bar = &wb[i % C::STAGES];
       mbar_arrive_expect_tx(bar, pid >= 0 ? (uint32_t)C::BLK : 0u);
@@ -453,8 +459,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
 
   for (int i = 0; i < my_count; i += 2) {
     const bool two = i + 1 < my_count;  // warp-uniform
-    const int pidA = __shfl_sync(kFull, my_pid, i);
-    const int pidB_raw = __shfl_sync(kFull, my_pid, two ? i + 1 : i);
+    const int pidA = ids[i];
+    const int pidB_raw = ids[two ? i + 1 : i];
     const int pidB = two ? pidB_raw : -1;
     const uint8_t* stA = ring + (i % C::STAGES) * C::STAGE;
     const uint8_t* stB = ring + ((i + 1) % C::STAGES) * C::STAGE;
@@ -665,12 +671,52 @@ __global__ void __launch_bounds__(D) combine_kernel(const __grid_constant__ Deco
   else static_cast<__half*>(a.out)[oi] = __float2half_rn(r);
 }
 
+template <int MODE, int D>
+constexpr size_t decode_smem() {  // dynamic shared memory: the stage rings, reused by the merge
+  using C = Cfg<MODE, D>;
+  constexpr size_t ring = (size_t)kWarps * C::STAGES * C::STAGE;
+  constexpr size_t merge = (size_t)kWarps * 8 * (D + 2) * sizeof(float);
+  return (ring > merge ? ring : merge) + 1024;
+}
+
+// Resident CTAs per SM of one decode kernel instance (occupancy query, cached;
+// the register budget's target if the query fails).
+template <int MODE, int D, bool QF32>
+int resident_ctas() {
+  static std::atomic<int> cached{0};
+  int n = cached.load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  auto kern = decode_kernel<MODE, D, QF32>;
+  constexpr size_t smem = decode_smem<MODE, D>();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, smem) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = Cfg<MODE, D>::MINB;
+  }
+  cached.store(n, std::memory_order_relaxed);
+  return n;
+}
+
+template <int D, bool QF32>
+int resident_ctas_d(int mode) {
+  switch (mode) {
+    case KVQ_FP8_PER_TENSOR: return resident_ctas<KVQ_FP8_PER_TENSOR, D, QF32>();
+    case KVQ_INT8_PER_TOKEN_HEAD: return resident_ctas<KVQ_INT8_PER_TOKEN_HEAD, D, QF32>();
+    case KVQ_FP8_PER_TOKEN_HEAD: return resident_ctas<KVQ_FP8_PER_TOKEN_HEAD, D, QF32>();
+    case KVQ_NVFP4: return resident_ctas<KVQ_NVFP4, D, QF32>();
+    default: return 1;
+  }
+}
+
+int resident_ctas_of(const kvq_cache* c) {
+  const bool f32 = c->cfg.io_dtype == KVQ_F32;
+  if (c->cfg.head_dim == 128) return f32 ? resident_ctas_d<128, true>(c->cfg.mode) : resident_ctas_d<128, false>(c->cfg.mode);
+  return f32 ? resident_ctas_d<32, true>(c->cfg.mode) : resident_ctas_d<32, false>(c->cfg.mode);
+}
+
 template <int MODE, int D, bool QF32>
 cudaError_t launch_mode(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s) {
-  using C = Cfg<MODE, D>;
-  const size_t ring = (size_t)kWarps * C::STAGES * C::STAGE;
-  const size_t merge = (size_t)kWarps * 8 * (D + 2) * sizeof(float);
-  const size_t smem = (ring > merge ? ring : merge) + 1024;
+  constexpr size_t smem = decode_smem<MODE, D>();
   auto kern = decode_kernel<MODE, D, QF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -695,22 +741,49 @@ cudaError_t launch_d(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// Split plan.  Sequence lengths are known only on the device, so the plan
+// takes every sequence to be max_seq_len long.
+//  Modes 1-4: one CTA per (split, kv head, sequence), R of them resident per
+//  SM.  A plan with s splits is estimated at
+//      ceil(units * s / (R * SMs)) waves  x  (ceil(pages / s) + kSplitCost),
+//  kSplitCost being the cost of one CTA beyond its pages (start-up, pipeline
+//  fill, merge, partial write) in page units, fitted to GB300 timings; the
+//  smallest estimate wins, ties going to fewer splits.  Each warp takes at
+//  least one and at most kIdsPerWarp pages.
+//  KVarN: the CTA shares each 128-token tile; about 8 CTAs per SM, at most 64
+//  tiles per split.
+constexpr long long kSplitCost = 16;
+
 DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int max_seq_len) {
   DecodePlan p{1, c->cfg.page_size, 0};
   const int P = c->cfg.page_size;
   const long long pages = (max_seq_len + P - 1) / P;
   if (pages <= 0) return p;
   const long long units = (long long)num_seqs * c->cfg.num_kv_heads;
-  // pages per split: at least one per warp (modes 1-4: a warp owns whole pages,
-  // at most 32; KVarN: the CTA shares each 128-token tile, at most 64 tiles)
   const bool kvarn = c->cfg.mode == KVQ_KVARN_K4V2_G128;
-  const long long cap = kvarn ? 64 : (long long)kWarps * 32;
+  const long long cap = kvarn ? 64 : (long long)kWarps * kIdsPerWarp;
   const long long min_pages = kvarn ? 1 : kWarps;
-  long long splits = (8LL * num_sms() + units - 1) / (units > 0 ? units : 1);
   const long long min_splits = (pages + cap - 1) / cap;
   const long long max_splits = (pages + min_pages - 1) / min_pages;
-  if (splits > max_splits) splits = max_splits;
-  if (splits < min_splits) splits = min_splits;
+  long long splits;
+  if (kvarn) {
+    splits = (8LL * num_sms() + units - 1) / (units > 0 ? units : 1);
+    if (splits > max_splits) splits = max_splits;
+    if (splits < min_splits) splits = min_splits;
+  } else {
+    const long long slots = (long long)resident_ctas_of(c) * num_sms();
+    long long best = -1;
+    splits = min_splits;
+    const long long hi = max_splits < min_splits + 256 ? max_splits : min_splits + 256;
+    for (long long s = min_splits; s <= hi; ++s) {
+      const long long waves = (units * s + slots - 1) / slots;
+      const long long cost = waves * ((pages + s - 1) / s + kSplitCost);
+      if (best < 0 || cost < best) {
+        best = cost;
+        splits = s;
+      }
+    }
+  }
   if (splits < 1) splits = 1;
   const long long pps = (pages + splits - 1) / splits;
   p.tokens_per_split = (int)(pps * P);
