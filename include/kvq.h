@@ -19,7 +19,8 @@
  *       stored inside the page next to the data.
  *  [P5] "NVFP4 KV Cache：Blackwell 上的 4-bit 缓存量化": two-level scaling,
  *       KV write/read paths, attention A = softmax(QK^T/sqrt(d)), O = AV;
- *       "unsupported combinations fail fast, never fall back silently".
+ *       an unsupported combination is an immediate error, not a silent
+ *       fallback.
  *
  * Conventions
  *  - Every call returns a kvq_status; KVQ_OK is 0.  On error,

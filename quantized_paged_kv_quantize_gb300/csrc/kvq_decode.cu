@@ -649,23 +649,13 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
 // Merge the splits of each (sequence, query head).
 template <int D>
 __global__ void __launch_bounds__(D) combine_kernel(const __grid_constant__ DecodeArgs a) {
+  __shared__ float wts[D], red[D / 32];
   const int b = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, d = threadIdx.x;
   int n = a.seq_lens[b];
   const int lim = min(a.max_seq_len, a.max_pages * kPage);
   n = n < 0 ? 0 : (n > lim ? lim : n);
   const int ns = (n + a.tokens_per_split - 1) / a.tokens_per_split;
-  const long long base = ((long long)b * a.Hq + hq) * a.num_splits;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, a.ws_ml[2 * (base + s)]);
-  float L = 0.0f, O = 0.0f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < ns; ++s) {
-      const float e = exp2f(a.ws_ml[2 * (base + s)] - M);
-      L += a.ws_ml[2 * (base + s) + 1] * e;
-      O += a.ws_o[(base + s) * D + d] * e;
-    }
-  }
-  const float r = L > 0.0f ? O / L : 0.0f;
+  const float r = merge_split_row<D>(a, ((long long)b * a.Hq + hq) * a.num_splits, ns, wts, red);
   const long long oi = ((long long)b * a.Hq + hq) * D + d;
   if (a.out_f32) static_cast<float*>(a.out)[oi] = r;
   else static_cast<__half*>(a.out)[oi] = __float2half_rn(r);

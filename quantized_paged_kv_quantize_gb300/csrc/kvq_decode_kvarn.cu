@@ -457,25 +457,15 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
 
 // Merge the splits of each (sequence, query head), then rotate back: o = H o'.
 __global__ void __launch_bounds__(kD) kvarn_combine_kernel(const __grid_constant__ DecodeArgs a) {
-  __shared__ float v[kD];
+  __shared__ float v[kD], wts[kD], red[kD / 32];
   const int b = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, d = threadIdx.x;
   int n = a.seq_lens[b];
   const int lim = min(a.max_seq_len, a.max_pages * kT);
   n = n < 0 ? 0 : (n > lim ? lim : n);
   n -= n % kT;
   const int ns = (n + a.tokens_per_split - 1) / a.tokens_per_split;
-  const long long base = ((long long)b * a.Hq + hq) * a.num_splits;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, a.ws_ml[2 * (base + s)]);
-  float L = 0.0f, O = 0.0f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < ns; ++s) {
-      const float e = ex2(a.ws_ml[2 * (base + s)] - M);
-      L += a.ws_ml[2 * (base + s) + 1] * e;
-      O += a.ws_o[(base + s) * kD + d] * e;
-    }
-  }
-  v[d] = L > 0.0f ? O / L : 0.0f;
+  const float r0 = merge_split_row<kD>(a, ((long long)b * a.Hq + hq) * a.num_splits, ns, wts, red);
+  v[d] = r0;
   __syncthreads();
   for (int h = 1; h < kD; h <<= 1) {  // Sylvester butterflies across threads
     const float mine = v[d], other = v[d ^ h];

@@ -213,6 +213,61 @@ struct DecodeArgs {
   int rows_per_block;
 };
 
+// Split-KV merge of one (sequence, query head) row by a CTA of D threads,
+// thread d owning channel d; base indexes the row's first split partial.
+// M = max_s m_s, w_s = 2^(m_s - M), result sum_s o_s w_s / sum_s l_s w_s (0
+// for a row with no tokens).  The weights go through shared memory (wts[D],
+// red[D / 32]) in chunks of D splits and each thread keeps eight partial loads
+// in flight, so a row costs a few memory round trips whatever the split count.
+template <int D>
+__device__ float merge_split_row(const DecodeArgs& a, long long base, int ns, float* wts, float* red) {
+  constexpr int NW = D / 32;
+  const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + base;
+  float M = -INFINITY;
+  for (int s = d; s < ns; s += D) M = fmaxf(M, ml[s].x);
+  M = warp_max_xor(M, 1, 16);
+  if (NW > 1) {
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
+  }
+  float lsum = 0.0f, acc = 0.0f;
+  if (M != -INFINITY) {  // uniform across the CTA
+    for (int c = 0; c < ns; c += D) {
+      float w = 0.0f;
+      if (c + d < ns) {
+        const float2 v = ml[c + d];
+        w = exp2f(v.x - M);
+        lsum += v.y * w;
+      }
+      wts[d] = w;
+      __syncthreads();
+      const int cn = min(D, ns - c);
+      const float* src = a.ws_o + (base + c) * D + d;
+      for (int j0 = 0; j0 < cn; j0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = j0 + j < cn ? src[(long long)(j0 + j) * D] : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc += v[j] * (j0 + j < cn ? wts[j0 + j] : 0.0f);
+      }
+      __syncthreads();
+    }
+  }
+  for (int o = 16; o >= 1; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+  if (NW > 1) {
+    if (lane == 0) red[warp] = lsum;
+    __syncthreads();
+    lsum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) lsum += red[w];
+  }
+  return lsum > 0.0f ? acc / lsum : 0.0f;
+}
+
 // KVarN decode + combine (kvq_decode_kvarn.cu).
 cudaError_t launch_kvarn_decode(const DecodeArgs& a, cudaStream_t stream);
 
