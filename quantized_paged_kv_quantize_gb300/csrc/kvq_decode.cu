@@ -732,17 +732,21 @@ cudaError_t launch_d(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s) {
 }  // namespace
 
 // Split plan.  Sequence lengths are known only on the device, so the plan
-// takes every sequence to be max_seq_len long.
-//  Modes 1-4: one CTA per (split, kv head, sequence), R of them resident per
-//  SM.  A plan with s splits is estimated at
-//      ceil(units * s / (R * SMs)) waves  x  (ceil(pages / s) + kSplitCost),
-//  kSplitCost being the cost of one CTA beyond its pages (start-up, pipeline
-//  fill, merge, partial write) in page units, fitted to GB300 timings; the
-//  smallest estimate wins, ties going to fewer splits.  Each warp takes at
-//  least one and at most kIdsPerWarp pages.
-//  KVarN: the CTA shares each 128-token tile; about 8 CTAs per SM, at most 64
-//  tiles per split.
-constexpr long long kSplitCost = 16;
+// takes every sequence to be max_seq_len long.  One CTA per (split, kv head,
+// sequence), R of them resident per SM; pages per split pps = ceil(pages / s).
+//  Modes 1-4 (16-token pages, 1 to kIdsPerWarp per warp) stream at the memory
+//  system's pace: a plan with s splits is estimated at
+//      ceil(units * s / (R * SMs)) waves  x  (pps + kSplitCostPages).
+//  KVarN (the CTA shares each 128-token tile, at most 64 per split) is bound
+//  by instruction issue, so a partial wave runs faster and what counts is the
+//  busiest SM: ceil(units * s / SMs) x (pps + kSplitCostTiles), with at least
+//  one full wave of CTAs (R per SM) to hide latency when there is work for it.
+// The overheads are a CTA's cost beyond its pages (start-up, pipeline fill,
+// merge, partial write) in page units, fitted to GB300 timings; the smallest
+// estimate wins, ties going to the split that divides the pages most evenly,
+// then to fewer splits.
+constexpr long long kSplitCostPages = 16;
+constexpr long long kSplitCostTiles = 2;
 
 DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int max_seq_len) {
   DecodePlan p{1, c->cfg.page_size, 0};
@@ -753,25 +757,26 @@ DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int ma
   const bool kvarn = c->cfg.mode == KVQ_KVARN_K4V2_G128;
   const long long cap = kvarn ? 64 : (long long)kWarps * kIdsPerWarp;
   const long long min_pages = kvarn ? 1 : kWarps;
-  const long long min_splits = (pages + cap - 1) / cap;
+  long long min_splits = (pages + cap - 1) / cap;
   const long long max_splits = (pages + min_pages - 1) / min_pages;
-  long long splits;
-  if (kvarn) {
-    splits = (8LL * num_sms() + units - 1) / (units > 0 ? units : 1);
-    if (splits > max_splits) splits = max_splits;
-    if (splits < min_splits) splits = min_splits;
-  } else {
-    const long long slots = (long long)resident_ctas_of(c) * num_sms();
-    long long best = -1;
-    splits = min_splits;
-    const long long hi = max_splits < min_splits + 256 ? max_splits : min_splits + 256;
-    for (long long s = min_splits; s <= hi; ++s) {
-      const long long waves = (units * s + slots - 1) / slots;
-      const long long cost = waves * ((pages + s - 1) / s + kSplitCost);
-      if (best < 0 || cost < best) {
-        best = cost;
-        splits = s;
-      }
+  const long long sms = num_sms();
+  const long long slots = (long long)(kvarn ? kvarn_resident_ctas() : resident_ctas_of(c)) * sms;
+  if (kvarn) {  // one full wave when the tiles allow it
+    long long full = (slots + units - 1) / units;
+    if (full > max_splits) full = max_splits;
+    if (full > min_splits) min_splits = full;
+  }
+  long long best = -1, best_ragged = 0, splits = min_splits;
+  const long long hi = max_splits < min_splits + 256 ? max_splits : min_splits + 256;
+  for (long long s = min_splits; s <= hi; ++s) {
+    const long long pps = (pages + s - 1) / s;
+    const long long cost = kvarn ? (units * s + sms - 1) / sms * (pps + kSplitCostTiles)
+                                 : (units * s + slots - 1) / slots * (pps + kSplitCostPages);
+    const long long ragged = s * pps - pages;  // ties: the evener split
+    if (best < 0 || cost < best || (cost == best && ragged < best_ragged)) {
+      best = cost;
+      best_ragged = ragged;
+      splits = s;
     }
   }
   if (splits < 1) splits = 1;

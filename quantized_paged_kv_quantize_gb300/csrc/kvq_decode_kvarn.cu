@@ -28,6 +28,8 @@
 // for the folded query and for the probabilities.
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -49,13 +51,23 @@ constexpr int kMaxTiles = 64;                        // tiles per split (page id
 #endif
 constexpr int kS = KVQ_KVARN_STAGES;
 
+// The folded query is the B operand of S^T = K Q^T.  Entry (k-step j, lane
+// 4h + tq) holds head h's channels base, base+4, base+1, base+5 with
+// base = 32 tq + 8 (j >> 1) + 2 (j & 1), as {b0, b1} in f16 hi then lo; the
+// key-code unpacking (kcode) produces the A operand in the same channel order.
+// Entries are stored at [j][(4h + tq) ^ 4j]: the MMA warps' loads (one j at a
+// time) and the fold's stores (one h at a time) are both conflict-free.
+__host__ __device__ constexpr int frag_base(int j, int tq) { return 32 * tq + 8 * (j >> 1) + 2 * (j & 1); }
+
 struct Shared {
-  float qrot[8][kD];     // q' = H q per head of the group
-  uint4 frag[8][32];     // per k-step and lane: {b0 hi, b1 hi, b0 lo, b1 lo}
+  float qrot[8][kD];     // q' = H q per head of the group (set-up only)
+  uint4 frag[8][32];     // folded query, see above
+  float4 cs[32];         // per tile, entry order (4 j + tq): c_d * scale_d of K
+  float4 cz[32];         //                                   c_d * zero_d of K
   float kf[kT];          // r^K_t * softmax_scale * log2(e)
   float vf[kT];          // r^V_t * scale^V_t
   float vz[kT];          // r^V_t * zero^V_t
-  float beta_part[kW][8];
+  float beta[8];         // per head: sum_d q'_d c_d zero_d - 16 sum_d (folded query used)
   float vmax_part[kW];
   int pages[kMaxTiles];
 };
@@ -177,6 +189,17 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
     for (int i = 0; i < 4; ++i) sh.qrot[h][4 * lane + i] = v[i];
   }
   __syncthreads();
+  // this lane's fold entry: k-step fj, channel group ftq, for heads warp and warp + 4
+  const int fj = lane >> 2, ftq = lane & 3, fbase = frag_base(fj, ftq);
+  float qv[2][4];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const float* qr = sh.qrot[warp + kW * hh];
+    qv[hh][0] = qr[fbase];
+    qv[hh][1] = qr[fbase + 4];
+    qv[hh][2] = qr[fbase + 1];
+    qv[hh][3] = qr[fbase + 5];
+  }
 
   float o[8][4];
 #pragma unroll
@@ -195,33 +218,14 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
     if (pid >= 0) {
       const float* km = reinterpret_cast<const float*>(st + kKMeta);
       const float* vm = reinterpret_cast<const float*>(st + kVMeta);
-      // ---- fold: thread tid owns channel d = tid and token t = tid
+      // ---- fold, part 1: thread tid owns channel d = tid and token t = tid
       {
         const int d = tid;
-        const float cs = km[2 * kD + d] * km[d];       // c_d * scale_d
-        const float cz = km[2 * kD + d] * km[kD + d];  // c_d * zero_d
-        // B-fragment slot of channel d: d = 32 tq + 8 w + k, k = 4 half + s, j = 2 w + s/2
-        const int tqd = d >> 5, w = (d & 31) >> 3, k = d & 7, s = k & 3, half = k >> 2;
-        const int j = 2 * w + (s >> 1), slot = s & 1;
-        __half* fr = reinterpret_cast<__half*>(&sh.frag[j][0]);
-        float bp[8];
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          const float qv = sh.qrot[h][d];
-          const float qt = qv * cs;
-          const __half hi = __float2half_rn(qt);
-          const __half lo = __float2half_rn(qt - __half2float(hi));
-          const int ln = 4 * h + tqd;
-          fr[ln * 8 + slot * 2 + half] = hi;
-          fr[ln * 8 + 4 + slot * 2 + half] = lo;
-          // the tensor core sees (1 + code/16): take out 16 * sum of the folded query it used
-          bp[h] = qv * cz - 16.0f * (__half2float(hi) + __half2float(lo));
-        }
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          const float s2 = warp_sum(bp[h]);
-          if (lane == 0) sh.beta_part[warp][h] = s2;
-        }
+        // entry (j, tq) and position of channel d (inverse of frag_base)
+        const int tqd = d >> 5, w = (d & 31) >> 3, k = d & 7, sd = k & 3, half = k >> 2;
+        const int pos = 4 * (4 * (2 * w + (sd >> 1)) + tqd) + 2 * (sd & 1) + half;
+        reinterpret_cast<float*>(sh.cs)[pos] = km[2 * kD + d] * km[d];       // c_d * scale_d
+        reinterpret_cast<float*>(sh.cz)[pos] = km[2 * kD + d] * km[kD + d];  // c_d * zero_d
         const int t = tid;
         sh.kf[t] = km[3 * kD + t] * a.sm_log2;
         const float f = vm[2 * kT + t] * vm[t];
@@ -233,10 +237,35 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
         if (lane == 0) sh.vmax_part[warp] = fm;
       }
       __syncthreads();
-      const float be0 = sh.beta_part[0][2 * tq] + sh.beta_part[1][2 * tq] + sh.beta_part[2][2 * tq] +
-                        sh.beta_part[3][2 * tq];
-      const float be1 = sh.beta_part[0][2 * tq + 1] + sh.beta_part[1][2 * tq + 1] + sh.beta_part[2][2 * tq + 1] +
-                        sh.beta_part[3][2 * tq + 1];
+      // ---- fold, part 2: warp w folds heads w and w + 4, lane = entry 4 j + tq
+      {
+        const float4 cs4 = sh.cs[lane], cz4 = sh.cz[lane];
+        const float csv[4] = {cs4.x, cs4.y, cs4.z, cs4.w}, czv[4] = {cz4.x, cz4.y, cz4.z, cz4.w};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int h = warp + kW * hh;
+          __half hi[4], lo[4];
+          float bp = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float qt = qv[hh][i] * csv[i];
+            hi[i] = __float2half_rn(qt);
+            lo[i] = __float2half_rn(qt - __half2float(hi[i]));
+            // the tensor core sees (1 + code/16): take out 16 * the folded query it used
+            bp += qv[hh][i] * czv[i] - 16.0f * (__half2float(hi[i]) + __half2float(lo[i]));
+          }
+          uint4 e;
+          e.x = h2_as_u32(__halves2half2(hi[0], hi[1]));
+          e.y = h2_as_u32(__halves2half2(hi[2], hi[3]));
+          e.z = h2_as_u32(__halves2half2(lo[0], lo[1]));
+          e.w = h2_as_u32(__halves2half2(lo[2], lo[3]));
+          sh.frag[fj][(4 * h + ftq) ^ (4 * fj)] = e;
+          bp = warp_sum(bp);
+          if (lane == 0) sh.beta[h] = bp;
+        }
+      }
+      __syncthreads();
+      const float be0 = sh.beta[2 * tq], be1 = sh.beta[2 * tq + 1];
       const float vmx = fmaxf(fmaxf(sh.vmax_part[0], sh.vmax_part[1]), fmaxf(sh.vmax_part[2], sh.vmax_part[3]));
       int ex = 0;
       (void)frexpf(vmx, &ex);                         // vmx < 2^ex
@@ -254,7 +283,7 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
         lds<4>(st + (16 * sb + g + 8) * 64 + tq * 16, KB8);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint4 fq = sh.frag[j][lane];
+          const uint4 fq = sh.frag[j][lane ^ (4 * j)];
           const int w = j >> 1, sft = (j & 1) * 8;
           uint32_t af[4];
           af[0] = kcode(KA0[w], sft);
@@ -480,6 +509,21 @@ __global__ void __launch_bounds__(kD) kvarn_combine_kernel(const __grid_constant
 }
 
 }  // namespace
+
+int kvarn_resident_ctas() {
+  static std::atomic<int> cached{0};
+  int n = cached.load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaFuncSetAttribute(kvarn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmem)) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kvarn_decode_kernel, kW * 32, kSmem) != cudaSuccess ||
+      n <= 0) {
+    (void)cudaGetLastError();
+    n = 4;
+  }
+  cached.store(n, std::memory_order_relaxed);
+  return n;
+}
 
 cudaError_t launch_kvarn_decode(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kvarn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

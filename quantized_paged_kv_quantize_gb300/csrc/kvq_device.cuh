@@ -270,5 +270,6 @@ __device__ float merge_split_row(const DecodeArgs& a, long long base, int ns, fl
 
 // KVarN decode + combine (kvq_decode_kvarn.cu).
 cudaError_t launch_kvarn_decode(const DecodeArgs& a, cudaStream_t stream);
+int kvarn_resident_ctas();  // resident KVarN decode CTAs per SM (occupancy query)
 
 }  // namespace kvq
