@@ -222,33 +222,117 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
 }
 
 // ------------------------------------------------------------------ KVarN
-// One CTA per (128-token tile, kv head, side).  The tile is held in shared
-// memory as Y[token][channel] (row stride 129 floats: both row-wise and
-// column-wise warp accesses are bank-conflict free).
+// One CTA of 256 threads per (128-token tile, kv head, side).
+//  1. Load + rotate: thread (token t, half) holds channels 64 half .. +63;
+//     Walsh-Hadamard stages h = 1 .. 32 run in registers, h = 64 between the
+//     two halves' lanes, then the fp32 1/sqrt(128) (0x3DB504F3).  The tile is
+//     staged in shared memory once (row stride 144 floats).
+//  2. Normalise: thread (warp w, lane l) holds y[i][j] for tokens
+//     t = tl + 16 i and channels d = dl + 16 j (i, j = 0..7), with dl = l & 15
+//     and tl = (l >> 4) | (w << 1).  The canonical 128-sum (v[i] += v[i + off],
+//     off = 64, 32, .., 1) therefore takes its first three levels inside the
+//     thread on either axis.  Token sums finish with lane shuffles on
+//     d bits 3, 2, 1, 0 -- recursive halving, so that afterwards each lane
+//     owns one of its eight tokens and computes that token's sqrt and
+//     reciprocal once; channel sums finish through shared memory on t bits
+//     3, 2, 1, 0 (one thread per channel).  Every fp32 operation is the
+//     specification's, rounded alone (-fmad=false).
+//  3. Round: asymmetric RTN, keys per channel over tokens (4 bits), values
+//     per token over channels (2 bits); codes staged as bytes in shared
+//     memory, then packed and stored as 16-byte rows.
 constexpr int kKvTile = 128;
-constexpr int kKvStride = 129;
 constexpr int kKvThreads = 256;
-constexpr size_t kKvSmem = sizeof(float) * (kKvTile * kKvStride + 4 * kKvTile) + kKvTile * kKvTile;
+constexpr int kKvYS = 144;  // floats per staged token row (banks: +16 per row)
+constexpr int kKvCS = 144;  // bytes per staged code row
+struct KvSmem {
+  float Y[kKvTile * kKvYS];     // rotated tile; later the code bytes
+  float part[16 * kKvYS];       // per-channel partial sums / minima [t_lo][d]
+  float part2[16 * kKvYS];      // per-channel maxima [t_lo][d]
+  float st0[kKvTile], st1[kKvTile];  // per-line statistics
+  float fr[kKvTile], fc[kKvTile];    // final factors r_t, c_d
+};
+constexpr size_t kKvSmem = sizeof(KvSmem);
 
-// Canonical 128-sum: lane l holds elements l, l+32, l+64, l+96; the pairwise
-// tree adds v[i] + v[i+off] for off = 64, 32 (in thread) then 16 .. 1 (lanes).
-__device__ __forceinline__ float tree_sum128(const float* v) {
-  float s = __fadd_rn(__fadd_rn(v[0], v[2]), __fadd_rn(v[1], v[3]));
+// In-thread levels 64, 32, 16 of the canonical sum over eight values whose
+// index bits are the line's bits 6, 5, 4 (v[k] = element 16 k + lo).
+__device__ __forceinline__ float tree8(const float* v) {
+  const float a0 = __fadd_rn(v[0], v[4]), a1 = __fadd_rn(v[1], v[5]);
+  const float a2 = __fadd_rn(v[2], v[6]), a3 = __fadd_rn(v[3], v[7]);
+  return __fadd_rn(__fadd_rn(a0, a2), __fadd_rn(a1, a3));
+}
+
+// Canonical levels 8, 4, 2, 1 over lane bits 3..0 for the thread's eight
+// tokens (p[i] = partial of token tl + 16 i).  Returns the full sum of token
+// tl + 16 (4 b3 + 2 b2 + b1), b = lane bits; lanes differing in bit 0 agree.
+__device__ __forceinline__ float row_tree(const float* p, int lane) {
+  const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+  float q[4];
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(kFull, s, o));
-  return s;
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b3 ? p[i + 4] : p[i], send = b3 ? p[i] : p[i + 4];
+    q[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 8));
+  }
+  float q2[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b2 ? q[i + 2] : q[i], send = b2 ? q[i] : q[i + 2];
+    q2[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 4));
+  }
+  const float q3 = __fadd_rn(b1 ? q2[1] : q2[0], __shfl_xor_sync(kFull, b1 ? q2[0] : q2[1], 2));
+  return __fadd_rn(q3, __shfl_xor_sync(kFull, q3, 1));
+}
+// Lane holding row_tree's result for the thread's token index i.
+__device__ __forceinline__ int row_owner(int lane, int i) {
+  return (lane & 16) | (((i >> 2) & 1) << 3) | (((i >> 1) & 1) << 2) | ((i & 1) << 1);
+}
+// Same recursive halving for a minimum and a maximum (order-free).
+__device__ __forceinline__ void row_minmax(const float* mn8, const float* mx8, int lane, float& mn, float& mx) {
+  const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+  float a[4], b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a[i] = fminf(b3 ? mn8[i + 4] : mn8[i], __shfl_xor_sync(kFull, b3 ? mn8[i] : mn8[i + 4], 8));
+    b[i] = fmaxf(b3 ? mx8[i + 4] : mx8[i], __shfl_xor_sync(kFull, b3 ? mx8[i] : mx8[i + 4], 8));
+  }
+  float a2[2], b2v[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    a2[i] = fminf(b2 ? a[i + 2] : a[i], __shfl_xor_sync(kFull, b2 ? a[i] : a[i + 2], 4));
+    b2v[i] = fmaxf(b2 ? b[i + 2] : b[i], __shfl_xor_sync(kFull, b2 ? b[i] : b[i + 2], 4));
+  }
+  float a3 = fminf(b1 ? a2[1] : a2[0], __shfl_xor_sync(kFull, b1 ? a2[0] : a2[1], 2));
+  float b3v = fmaxf(b1 ? b2v[1] : b2v[0], __shfl_xor_sync(kFull, b1 ? b2v[0] : b2v[1], 2));
+  mn = fminf(a3, __shfl_xor_sync(kFull, a3, 1));
+  mx = fmaxf(b3v, __shfl_xor_sync(kFull, b3v, 1));
+}
+// Canonical levels 8, 4, 2, 1 over the 16 partials of one channel (row i of
+// part = t_lo i).
+__device__ __forceinline__ float col_tree(const float* part, int d) {
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = part[i * kKvYS + d];
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1)
+#pragma unroll
+    for (int i = 0; i < off; ++i) v[i] = __fadd_rn(v[i], v[i + off]);
+  return v[0];
+}
+
+// code = clamp(rint(x / s), 0, steps) for x >= 0 (x = y - min); s == 0 gives 0.
+__device__ __forceinline__ uint32_t rtn_code(float x, const QDiv& q, float steps) {
+  if (q.s == 0.0f) return 0u;
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it leaves rint(v) in the low bits
+  const uint32_t lo = __float_as_uint(__fadd_rn(__fmul_rn(x, q.rlo), kMagic));
+  const uint32_t hi = __float_as_uint(__fadd_rn(__fmul_rn(x, q.rhi), kMagic));
+  if (q.fast && lo == hi && lo - 0x4B400000u <= static_cast<uint32_t>(steps)) return lo & 0xFFu;
+  const float qv = fminf(fmaxf(rintf(__fdiv_rn(x, q.s)), 0.0f), steps);
+  return static_cast<uint32_t>(__float2int_rn(qv));
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kKvThreads) kvarn_write_kernel(WriteArgs a) {
+__global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a) {
   extern __shared__ __align__(16) unsigned char kv_smem[];
-  float* Y = reinterpret_cast<float*>(kv_smem);
-  float* fac_r = Y + kKvTile * kKvStride;  // per-token factor r_t
-  float* fac_c = fac_r + kKvTile;          // per-channel factor c_d
-  float* qscale = fac_c + kKvTile;         // RTN scale (K: per channel, V: per token)
-  float* qzero = qscale + kKvTile;         // RTN zero (minimum)
-  uint8_t* codes = reinterpret_cast<uint8_t*>(qzero + kKvTile);  // [128][128]
-
+  KvSmem& sm = *reinterpret_cast<KvSmem*>(kv_smem);
   const int tile = blockIdx.x, h = blockIdx.y, side = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int D = 128;
@@ -264,161 +348,235 @@ __global__ void __launch_bounds__(kKvThreads) kvarn_write_kernel(WriteArgs a) {
     return;
   }
   const int page = s0 / kKvTile;
-  if (tid < kKvTile) { fac_r[tid] = 1.0f; fac_c[tid] = 1.0f; }
 
-  // Stage 1-2: load each token's 128 channels (lane holds d = 4l..4l+3),
-  // Walsh-Hadamard butterflies h = 1, 2 (in thread), 4 .. 64 (lanes), then
-  // the 1/sqrt(128) normalisation (fp32 0x3DB504F3).
-  const T* src = static_cast<const T*>(side ? a.v : a.k);
-  const float inv_sqrt128 = __int_as_float(0x3DB504F3);
-  for (int t = warp; t < kKvTile; t += kKvThreads / 32) {
-    const T* row = src + ((t0 + t) * a.Hkv + h) * D + 4 * lane;
-    float v[4];
-    if constexpr (sizeof(T) == 2) {
-      uint2 u = __ldg(reinterpret_cast<const uint2*>(row));
-      float2 p0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-      float2 p1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-      v[0] = p0.x; v[1] = p0.y; v[2] = p1.x; v[3] = p1.y;
-    } else {
-      float4 u = __ldg(reinterpret_cast<const float4*>(row));
-      v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  // ---- 1. load + Walsh-Hadamard along channels
+  {
+    const int t = tid >> 1, half = tid & 1;
+    const T* row = static_cast<const T*>(side ? a.v : a.k) + ((t0 + t) * a.Hkv + h) * D + 64 * half;
+    float v[64];
+#pragma unroll
+    for (int c = 0; c < 64; c += 16 / (int)sizeof(T)) load16<T>(row + c, v + c);
+#pragma unroll
+    for (int hh = 1; hh <= 32; hh <<= 1)
+#pragma unroll
+      for (int i = 0; i < 64; i += 2 * hh)
+#pragma unroll
+        for (int j = i; j < i + hh; ++j) {
+          const float x = v[j], y = v[j + hh];
+          v[j] = __fadd_rn(x, y);
+          v[j + hh] = __fsub_rn(x, y);
+        }
+    const float c = __int_as_float(0x3DB504F3);
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      const float p = __shfl_xor_sync(kFull, v[j], 1);  // the other half of the token
+      v[j] = __fmul_rn(half ? __fsub_rn(p, v[j]) : __fadd_rn(v[j], p), c);
     }
-    float w0 = __fadd_rn(v[0], v[1]), w1 = __fsub_rn(v[0], v[1]);
-    float w2 = __fadd_rn(v[2], v[3]), w3 = __fsub_rn(v[2], v[3]);
-    v[0] = __fadd_rn(w0, w2); v[2] = __fsub_rn(w0, w2);
-    v[1] = __fadd_rn(w1, w3); v[3] = __fsub_rn(w1, w3);
+    float* dst = sm.Y + t * kKvYS + 64 * half;
 #pragma unroll
-    for (int o = 1; o <= 16; o <<= 1) {
-      const bool upper = (lane & o) != 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float p = __shfl_xor_sync(kFull, v[i], o);
-        v[i] = upper ? __fsub_rn(p, v[i]) : __fadd_rn(v[i], p);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) Y[t * kKvStride + 4 * lane + i] = __fmul_rn(v[i], inv_sqrt128);
+    for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
   }
   __syncthreads();
 
-  // Stage 3: eight alternating std normalisation steps, tokens first.
+  // ---- 2. eight alternating std normalisation steps, tokens first
+  const int dl = lane & 15, tl = (lane >> 4) | (warp << 1);
+  float y[8][8], rf[8], cf[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    rf[i] = 1.0f;
+    cf[i] = 1.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[i][j] = sm.Y[(tl + 16 * i) * kKvYS + dl + 16 * j];
+  }
   for (int step = 0; step < 8; ++step) {
-    const bool per_token = (step & 1) == 0;
-    for (int L = warp; L < kKvTile; L += kKvThreads / 32) {
-      float v[4];
+    if ((step & 1) == 0) {  // per token: sums over channels
+      float p[8], mean[8];
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
-        v[m] = per_token ? Y[L * kKvStride + lane + 32 * m] : Y[(lane + 32 * m) * kKvStride + L];
-      const float mean = __fmul_rn(tree_sum128(v), 0.0078125f);
-      float sq[4];
+      for (int i = 0; i < 8; ++i) p[i] = tree8(y[i]);
+      const float mine = __fmul_rn(row_tree(p, lane), 0.0078125f);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float d = __fsub_rn(v[m], mean);
-        sq[m] = __fmul_rn(d, d);
-      }
-      const float var = __fmul_rn(tree_sum128(sq), 0.0078125f);
-      const float sd = __fsqrt_rn(var);
-      if (!(sd < 1e-8f)) {
-        const float inv = __frcp_rn(sd);
+      for (int i = 0; i < 8; ++i) mean[i] = __shfl_sync(kFull, mine, row_owner(lane, i));
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float y = __fmul_rn(v[m], inv);
-          if (per_token) Y[L * kKvStride + lane + 32 * m] = y;
-          else Y[(lane + 32 * m) * kKvStride + L] = y;
+      for (int i = 0; i < 8; ++i) {
+        float d2[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float dv = __fsub_rn(y[i][j], mean[i]);
+          d2[j] = __fmul_rn(dv, dv);
         }
-        if (lane == 0) {
-          if (per_token) fac_r[L] = __fmul_rn(fac_r[L], sd);
-          else fac_c[L] = __fmul_rn(fac_c[L], sd);
+        p[i] = tree8(d2);
+      }
+      const float sd = __fsqrt_rn(__fmul_rn(row_tree(p, lane), 0.0078125f));
+      const float inv = __frcp_rn(sd);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int src = row_owner(lane, i);
+        const float s = __shfl_sync(kFull, sd, src), iv = __shfl_sync(kFull, inv, src);
+        if (!(s < 1e-8f)) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) y[i][j] = __fmul_rn(y[i][j], iv);
+          rf[i] = __fmul_rn(rf[i], s);
         }
       }
+    } else {  // per channel: sums over tokens
+      float col[8], mean[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) col[i] = y[i][j];
+        sm.part[tl * kKvYS + dl + 16 * j] = tree8(col);
+      }
+      __syncthreads();
+      if (tid < D) sm.st0[tid] = __fmul_rn(col_tree(sm.part, tid), 0.0078125f);
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mean[j] = sm.st0[dl + 16 * j];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float dv = __fsub_rn(y[i][j], mean[j]);
+          col[i] = __fmul_rn(dv, dv);
+        }
+        sm.part[tl * kKvYS + dl + 16 * j] = tree8(col);
+      }
+      __syncthreads();
+      if (tid < D) {
+        const float sd = __fsqrt_rn(__fmul_rn(col_tree(sm.part, tid), 0.0078125f));
+        sm.st0[tid] = sd;
+        sm.st1[tid] = __frcp_rn(sd);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float s = sm.st0[dl + 16 * j], iv = sm.st1[dl + 16 * j];
+        if (!(s < 1e-8f)) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) y[i][j] = __fmul_rn(y[i][j], iv);
+          cf[j] = __fmul_rn(cf[j], s);
+        }
+      }
+    }
+  }
+  // the factors, once per line
+  if (dl == 0)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sm.fr[tl + 16 * i] = rf[i];
+  if (tl == 0)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sm.fc[dl + 16 * j] = cf[j];
+
+  // ---- 3. asymmetric round-to-nearest
+  uint8_t* blk = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes;
+  uint8_t* codes = reinterpret_cast<uint8_t*>(sm.Y);  // [128][kKvCS]; Y is in registers now
+  __syncthreads();  // every thread has read its y from sm.Y
+  if (side == 0) {  // keys: per channel over the tile's tokens, 4 bits
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float mn = y[0][j], mx = y[0][j];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) {
+        mn = fminf(mn, y[i][j]);
+        mx = fmaxf(mx, y[i][j]);
+      }
+      sm.part[tl * kKvYS + dl + 16 * j] = mn;
+      sm.part2[tl * kKvYS + dl + 16 * j] = mx;
     }
     __syncthreads();
-  }
-
-  // Stage 4: asymmetric round-to-nearest.  K: per channel over the tile's
-  // tokens, 4 bits; V: per token over the channels, 2 bits.
-  {
-    const bool by_channel = side == 0;
-    const float steps = by_channel ? 15.0f : 3.0f;
-    for (int L = warp; L < kKvTile; L += kKvThreads / 32) {
-      float v[4];
+    float* meta = reinterpret_cast<float*>(blk + kKvTile * D / 2 + kKvTile * D / 4);
+    if (tid < D) {
+      float mn = sm.part[tid], mx = sm.part2[tid];
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
-        v[m] = by_channel ? Y[(lane + 32 * m) * kKvStride + L] : Y[L * kKvStride + lane + 32 * m];
-      float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
-      float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      for (int i = 1; i < 16; ++i) {
+        mn = fminf(mn, sm.part[i * kKvYS + tid]);
+        mx = fmaxf(mx, sm.part2[i * kKvYS + tid]);
       }
-      const float sc = __fdiv_rn(__fsub_rn(mx, mn), steps);
+      const float sc = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+      sm.st0[tid] = sc;
+      sm.st1[tid] = mn;
+      meta[tid] = sc;
+      meta[D + tid] = mn;
+      meta[2 * D + tid] = sm.fc[tid];
+      meta[3 * D + tid] = sm.fr[tid];
+    }
+    __syncthreads();
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        float qv = 0.0f;
-        if (sc != 0.0f) {
-          qv = rintf(__fdiv_rn(__fsub_rn(v[m], mn), sc));
-          qv = fminf(fmaxf(qv, 0.0f), steps);
-        }
-        const int e = lane + 32 * m;
-        codes[by_channel ? e * kKvTile + L : L * kKvTile + e] = static_cast<uint8_t>(__float2int_rn(qv));
+    for (int j = 0; j < 8; ++j) {
+      const int d = dl + 16 * j;
+      const float mn = sm.st1[d];
+      const QDiv q(sm.st0[d]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        codes[(tl + 16 * i) * kKvCS + d] = static_cast<uint8_t>(rtn_code(__fsub_rn(y[i][j], mn), q, 15.0f));
+    }
+  } else {  // values: per token over the channels, 2 bits
+    float mn8[8], mx8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      mn8[i] = y[i][0];
+      mx8[i] = y[i][0];
+#pragma unroll
+      for (int j = 1; j < 8; ++j) {
+        mn8[i] = fminf(mn8[i], y[i][j]);
+        mx8[i] = fmaxf(mx8[i], y[i][j]);
       }
-      if (lane == 0) { qscale[L] = sc; qzero[L] = mn; }
+    }
+    float mn, mx;
+    row_minmax(mn8, mx8, lane, mn, mx);
+    const float sc = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+    float* meta = reinterpret_cast<float*>(blk + kKvTile * D / 2 + kKvTile * D / 4 + 4 * (3 * D + kKvTile));
+    if ((lane & 1) == 0) {  // lanes 2k (+16) own token tl + 16 (4 b3 + 2 b2 + b1)
+      const int t = tl + 16 * (((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1));
+      meta[t] = sc;
+      meta[kKvTile + t] = mn;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int src = row_owner(lane, i);
+      const float mni = __shfl_sync(kFull, mn, src);
+      const QDiv q(__shfl_sync(kFull, sc, src));
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        codes[(tl + 16 * i) * kKvCS + dl + 16 * j] = static_cast<uint8_t>(rtn_code(__fsub_rn(y[i][j], mni), q, 3.0f));
+    }
+    __syncthreads();  // fr, fc complete
+    if (tid < kKvTile) {
+      meta[2 * kKvTile + tid] = sm.fr[tid];
+      meta[3 * kKvTile + tid] = sm.fc[tid];
     }
   }
   __syncthreads();
 
-  // Pack and store payload + metadata of this side.
-  uint8_t* blk = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes;
-  if (side == 0) {
-    uint8_t* pay = blk;  // [128][64]: even channel in the low nibble
-    for (int c = tid; c < kKvTile * 4; c += kKvThreads) {  // 16-byte chunks: 32 channels of one token
+  // ---- pack the code bytes and store 16-byte rows
+  if (side == 0) {  // [128][64]: even channel in the low nibble; 32 codes per chunk
+    uint8_t* pay = blk;
+    for (int c = tid; c < kKvTile * 4; c += kKvThreads) {
       const int t = c >> 2, k0 = (c & 3) * 32;
-      uint32_t w[4];
+      const uint4 u0 = *reinterpret_cast<const uint4*>(codes + t * kKvCS + k0);
+      const uint4 u1 = *reinterpret_cast<const uint4*>(codes + t * kKvCS + k0 + 16);
+      const uint32_t in[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      uint32_t out[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int d = k0 + 8 * q + 2 * b;
-          word |= (uint32_t)(codes[t * kKvTile + d] | (codes[t * kKvTile + d + 1] << 4)) << (8 * b);
-        }
-        w[q] = word;
+        const uint32_t x0 = in[2 * q] | (in[2 * q] >> 4), x1 = in[2 * q + 1] | (in[2 * q + 1] >> 4);
+        out[q] = prmt(x0, x1, 0x6420u);  // bytes 0, 2 of each: (c0 | c1 << 4), (c2 | c3 << 4)
       }
-      *reinterpret_cast<uint4*>(pay + t * 64 + (c & 3) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(pay + t * 64 + (c & 3) * 16) = make_uint4(out[0], out[1], out[2], out[3]);
     }
-    float* meta = reinterpret_cast<float*>(blk + kKvTile * D / 2 + kKvTile * D / 4);
-    if (tid < kKvTile) {
-      meta[tid] = qscale[tid];
-      meta[D + tid] = qzero[tid];
-      meta[2 * D + tid] = fac_c[tid];
-      meta[3 * D + tid] = fac_r[tid];
-    }
-  } else {
-    uint8_t* pay = blk + kKvTile * D / 2;  // [128][32]: element 4i+j in bits 2j..2j+1
-    for (int c = tid; c < kKvTile * 2; c += kKvThreads) {  // 16-byte chunks: 64 channels of one token
-      const int t = c >> 1, k0 = (c & 1) * 64;
-      uint32_t w[4];
+  } else {  // [128][32]: element 4i + j in bits 2j..2j+1; 64 codes per chunk
+    uint8_t* pay = blk + kKvTile * D / 2;
+    const int t = tid >> 1, k0 = (tid & 1) * 64;
+    uint32_t out[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t word = 0;
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = *reinterpret_cast<const uint4*>(codes + t * kKvCS + k0 + 16 * q);
+      const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+      uint32_t b[4];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int d = k0 + 16 * q + 4 * b;
-          const uint8_t* cp = codes + t * kKvTile + d;
-          word |= (uint32_t)(cp[0] | (cp[1] << 2) | (cp[2] << 4) | (cp[3] << 6)) << (8 * b);
-        }
-        w[q] = word;
-      }
-      *reinterpret_cast<uint4*>(pay + t * 32 + (c & 1) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int e = 0; e < 4; ++e) b[e] = (in[e] | (in[e] >> 6) | (in[e] >> 12) | (in[e] >> 18)) & 0xFFu;
+      out[q] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
     }
-    float* meta = reinterpret_cast<float*>(blk + kKvTile * D / 2 + kKvTile * D / 4 + 4 * (3 * D + kKvTile));
-    if (tid < kKvTile) {
-      meta[tid] = qscale[tid];
-      meta[kKvTile + tid] = qzero[tid];
-      meta[2 * kKvTile + tid] = fac_r[tid];
-      meta[3 * kKvTile + tid] = fac_c[tid];
-    }
+    *reinterpret_cast<uint4*>(pay + t * 32 + (tid & 1) * 16) = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 
@@ -473,13 +631,9 @@ template <typename T>
 cudaError_t launch_kvarn(const WriteArgs& a, cudaStream_t s) {
   const long long tiles = a.num_tokens / kKvTile;
   if (tiles == 0) return cudaSuccess;
-  static bool attr_set = false;  // one attribute per instantiation, set before first launch
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kvarn_write_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kKvSmem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = cudaFuncSetAttribute(kvarn_write_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kKvSmem));
+  if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(tiles), a.Hkv, 2);
   kvarn_write_kernel<T><<<grid, kKvThreads, kKvSmem, s>>>(a);
   return cudaGetLastError();

@@ -69,14 +69,39 @@ def test_write_bit_exact(mode, D, io):
     assert diff.size == 0, f"{diff.size} bytes differ, first at pool offset {256 + diff[0]}"
 
 
-def test_write_kvarn_bit_exact():
+@pytest.mark.parametrize("io", ["f16", "f32"])
+def test_write_kvarn_bit_exact(io):
     K = kvq()
-    c = make_case(small_workload("kvarn_k4v2_g128"), KVARN_LENS, slack_pages=1)
+    c = make_case(small_workload("kvarn_k4v2_g128", io=io), KVARN_LENS, slack_pages=1)
     cache = gpu_cache(c)
     K.kvq_quantize_write(cache, _dev(c.k), _dev(c.v), _dev(c.slots))
     assert K.kvq_cache_read_errors(cache) == 0
     got = cache.pool.cpu().numpy()
     ref = oracle_pool(c)
+    diff = np.flatnonzero(got[256:] != ref[256:])
+    assert diff.size == 0, f"{diff.size} bytes differ, first at pool offset {256 + diff[0]}"
+
+
+def test_write_kvarn_degenerate_tiles():
+    """Tiles whose normalisation steps meet std < 1e-8 (left unchanged) and
+    whose rounding meets zero ranges (all codes 0): an all-zero tile, a tile of
+    one constant, a tile whose tokens are all equal, and one constant channel."""
+    K = kvq()
+    c = make_case(small_workload("kvarn_k4v2_g128"), [512], slack_pages=1)
+    k, v = c.k.copy(), c.v.copy()
+    k[0:128] = 0
+    v[0:128] = 0
+    k[128:256] = np.asarray(0.75, k.dtype)
+    v[128:256] = np.asarray(-1.5, v.dtype)
+    k[256:384] = k[256:257]                 # every token of the tile equal
+    v[256:384] = v[256:257]
+    k[384:512, :, 5] = np.asarray(2.0, k.dtype)   # one constant channel
+    v[384:512, :, 7] = np.asarray(-3.0, v.dtype)
+    cache = gpu_cache(c)
+    K.kvq_quantize_write(cache, _dev(k), _dev(v), _dev(c.slots))
+    assert K.kvq_cache_read_errors(cache) == 0
+    got = cache.pool.cpu().numpy()
+    ref = oracle_pool(c, k=k, v=v)
     diff = np.flatnonzero(got[256:] != ref[256:])
     assert diff.size == 0, f"{diff.size} bytes differ, first at pool offset {256 + diff[0]}"
 
