@@ -51,6 +51,24 @@ __device__ __forceinline__ void load16<float>(const float* p, float* f) {
   f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
 }
 
+// 16 loaded bytes -> fp32 values (exact widening of fp16; fp32 as is).
+template <typename T>
+__device__ __forceinline__ void widen16(const uint4& u, float* f);
+template <>
+__device__ __forceinline__ void widen16<__half>(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(u32_as_h2(w[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+template <>
+__device__ __forceinline__ void widen16<float>(const uint4& u, float* f) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y); f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+
 template <int N>
 __device__ __forceinline__ void store_bytes(uint8_t* dst, const uint32_t* w);
 template <>
@@ -236,7 +254,8 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
 //     owns one of its eight tokens and computes that token's sqrt and
 //     reciprocal once; channel sums finish through shared memory on t bits
 //     3, 2, 1, 0 (one thread per channel).  Every fp32 operation is the
-//     specification's, rounded alone (-fmad=false).
+//     specification's, rounded alone (-fmad=false); a line whose std is below
+//     1e-8 is multiplied by exactly 1 instead of being skipped.
 //  3. Round: asymmetric RTN, keys per channel over tokens (4 bits), values
 //     per token over channels (2 bits); codes staged as bytes in shared
 //     memory, then packed and stored as 16-byte rows.
@@ -252,6 +271,10 @@ struct KvSmem {
   float fr[kKvTile], fc[kKvTile];    // final factors r_t, c_d
 };
 constexpr size_t kKvSmem = sizeof(KvSmem);
+#ifndef KVQ_KVARN_PAIR_UNROLL
+#define KVQ_KVARN_PAIR_UNROLL 1
+#endif
+constexpr int kKvPairUnroll = KVQ_KVARN_PAIR_UNROLL;  // normalisation pairs unrolled
 
 // In-thread levels 64, 32, 16 of the canonical sum over eight values whose
 // index bits are the line's bits 6, 5, 4 (v[k] = element 16 k + lo).
@@ -337,8 +360,20 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int D = 128;
 
-  // A tile must be 128 consecutive slots starting a page.
   const long long t0 = (long long)tile * kKvTile;
+  // This thread's half token (64 channels), loaded before the slot check so
+  // that the two memory latencies overlap (rows t0 .. t0 + 127 always exist).
+  const int t = tid >> 1, half = tid & 1;
+  constexpr int NRAW = 64 * (int)sizeof(T) / 16;
+  uint4 raw[NRAW];
+  {
+    const uint4* row = reinterpret_cast<const uint4*>(static_cast<const T*>(side ? a.v : a.k) +
+                                                      ((t0 + t) * a.Hkv + h) * D + 64 * half);
+#pragma unroll
+    for (int k = 0; k < NRAW; ++k) raw[k] = __ldg(row + k);
+  }
+
+  // A tile must be 128 consecutive slots starting a page.
   const int s0 = __ldg(a.slots + t0);
   int ok = 1;
   if (tid < kKvTile) ok = (__ldg(a.slots + t0 + tid) == s0 + tid);
@@ -348,14 +383,16 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
     return;
   }
   const int page = s0 / kKvTile;
+  if (tid < kKvTile) {
+    sm.fr[tid] = 1.0f;  // token factors r_t
+    sm.fc[tid] = 1.0f;  // channel factors c_d
+  }
 
-  // ---- 1. load + Walsh-Hadamard along channels
+  // ---- 1. Walsh-Hadamard along channels
   {
-    const int t = tid >> 1, half = tid & 1;
-    const T* row = static_cast<const T*>(side ? a.v : a.k) + ((t0 + t) * a.Hkv + h) * D + 64 * half;
     float v[64];
 #pragma unroll
-    for (int c = 0; c < 64; c += 16 / (int)sizeof(T)) load16<T>(row + c, v + c);
+    for (int k = 0; k < NRAW; ++k) widen16<T>(raw[k], v + k * (16 / (int)sizeof(T)));
 #pragma unroll
     for (int hh = 1; hh <= 32; hh <<= 1)
 #pragma unroll
@@ -380,46 +417,49 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
 
   // ---- 2. eight alternating std normalisation steps, tokens first
   const int dl = lane & 15, tl = (lane >> 4) | (warp << 1);
-  float y[8][8], rf[8], cf[8];
+  // the lane that finishes token tl + 16 rr's sums (lanes 2k and 2k+1 agree)
+  const int rr = ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+  float y[8][8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    rf[i] = 1.0f;
-    cf[i] = 1.0f;
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) y[i][j] = sm.Y[(tl + 16 * i) * kKvYS + dl + 16 * j];
-  }
-  for (int step = 0; step < 8; ++step) {
-    if ((step & 1) == 0) {  // per token: sums over channels
-      float p[8], mean[8];
+  // Steps alternate tokens, channels, ...; written as four (token, channel)
+  // pairs so that no branch joins the two forms of the loop body.
+#pragma unroll kKvPairUnroll
+  for (int pair = 0; pair < 4; ++pair) {
+    {  // per token: sums over channels
+      float p[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) p[i] = tree8(y[i]);
       const float mine = __fmul_rn(row_tree(p, lane), 0.0078125f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mean[i] = __shfl_sync(kFull, mine, row_owner(lane, i));
-#pragma unroll
       for (int i = 0; i < 8; ++i) {
+        const float mean = __shfl_sync(kFull, mine, row_owner(lane, i));
         float d2[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float dv = __fsub_rn(y[i][j], mean[i]);
+          const float dv = __fsub_rn(y[i][j], mean);
           d2[j] = __fmul_rn(dv, dv);
         }
         p[i] = tree8(d2);
       }
-      const float sd = __fsqrt_rn(__fmul_rn(row_tree(p, lane), 0.0078125f));
-      const float inv = __frcp_rn(sd);
+      float sd = __fsqrt_rn(__fmul_rn(row_tree(p, lane), 0.0078125f));
+      float inv = __frcp_rn(sd);
+      if (sd < 1e-8f) {  // std below 1e-8: the token stays as it is
+        sd = 1.0f;
+        inv = 1.0f;
+      }
+      if ((lane & 1) == 0) sm.fr[tl + 16 * rr] = __fmul_rn(sm.fr[tl + 16 * rr], sd);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int src = row_owner(lane, i);
-        const float s = __shfl_sync(kFull, sd, src), iv = __shfl_sync(kFull, inv, src);
-        if (!(s < 1e-8f)) {
+        const float iv = __shfl_sync(kFull, inv, row_owner(lane, i));
 #pragma unroll
-          for (int j = 0; j < 8; ++j) y[i][j] = __fmul_rn(y[i][j], iv);
-          rf[i] = __fmul_rn(rf[i], s);
-        }
+        for (int j = 0; j < 8; ++j) y[i][j] = __fmul_rn(y[i][j], iv);
       }
-    } else {  // per channel: sums over tokens
-      float col[8], mean[8];
+    }
+    {  // per channel: sums over tokens
+      float col[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
 #pragma unroll
@@ -430,12 +470,11 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
       if (tid < D) sm.st0[tid] = __fmul_rn(col_tree(sm.part, tid), 0.0078125f);
       __syncthreads();
 #pragma unroll
-      for (int j = 0; j < 8; ++j) mean[j] = sm.st0[dl + 16 * j];
-#pragma unroll
       for (int j = 0; j < 8; ++j) {
+        const float mean = sm.st0[dl + 16 * j];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float dv = __fsub_rn(y[i][j], mean[j]);
+          const float dv = __fsub_rn(y[i][j], mean);
           col[i] = __fmul_rn(dv, dv);
         }
         sm.part[tl * kKvYS + dl + 16 * j] = tree8(col);
@@ -443,29 +482,19 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
       __syncthreads();
       if (tid < D) {
         const float sd = __fsqrt_rn(__fmul_rn(col_tree(sm.part, tid), 0.0078125f));
-        sm.st0[tid] = sd;
-        sm.st1[tid] = __frcp_rn(sd);
+        const bool keep = sd < 1e-8f;  // std below 1e-8: the channel stays as it is
+        sm.st1[tid] = keep ? 1.0f : __frcp_rn(sd);
+        sm.fc[tid] = __fmul_rn(sm.fc[tid], keep ? 1.0f : sd);
       }
       __syncthreads();
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float s = sm.st0[dl + 16 * j], iv = sm.st1[dl + 16 * j];
-        if (!(s < 1e-8f)) {
+        const float iv = sm.st1[dl + 16 * j];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) y[i][j] = __fmul_rn(y[i][j], iv);
-          cf[j] = __fmul_rn(cf[j], s);
-        }
+        for (int i = 0; i < 8; ++i) y[i][j] = __fmul_rn(y[i][j], iv);
       }
     }
   }
-  // the factors, once per line
-  if (dl == 0)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sm.fr[tl + 16 * i] = rf[i];
-  if (tl == 0)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) sm.fc[dl + 16 * j] = cf[j];
-
   // ---- 3. asymmetric round-to-nearest
   uint8_t* blk = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes;
   uint8_t* codes = reinterpret_cast<uint8_t*>(sm.Y);  // [128][kKvCS]; Y is in registers now
@@ -539,7 +568,6 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
       for (int j = 0; j < 8; ++j)
         codes[(tl + 16 * i) * kKvCS + dl + 16 * j] = static_cast<uint8_t>(rtn_code(__fsub_rn(y[i][j], mni), q, 3.0f));
     }
-    __syncthreads();  // fr, fc complete
     if (tid < kKvTile) {
       meta[2 * kKvTile + tid] = sm.fr[tid];
       meta[3 * kKvTile + tid] = sm.fc[tid];
