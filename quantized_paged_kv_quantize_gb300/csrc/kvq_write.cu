@@ -396,13 +396,12 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
 #pragma unroll
     for (int hh = 1; hh <= 32; hh <<= 1)
 #pragma unroll
-      for (int i = 0; i < 64; i += 2 * hh)
-#pragma unroll
-        for (int j = i; j < i + hh; ++j) {
-          const float x = v[j], y = v[j + hh];
-          v[j] = __fadd_rn(x, y);
-          v[j + hh] = __fsub_rn(x, y);
-        }
+      for (int k = 0; k < 32; ++k) {  // the 32 butterflies (j, j + hh) of this stage
+        const int j = (k / hh) * 2 * hh + k % hh;
+        const float x = v[j], y = v[j + hh];
+        v[j] = __fadd_rn(x, y);
+        v[j + hh] = __fsub_rn(x, y);
+      }
     const float c = __int_as_float(0x3DB504F3);
 #pragma unroll
     for (int j = 0; j < 64; ++j) {
