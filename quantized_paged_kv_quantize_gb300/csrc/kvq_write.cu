@@ -156,38 +156,17 @@ __device__ __forceinline__ float group_max(float v) {
   return v;
 }
 
-// One (token, kv head, side) row of D values per group of TPR threads; each
-// thread converts VEC = 16 bytes of input.  Grid: (token blocks, kv head,
-// side), so no index needs a division; a block's consecutive tokens land in
-// consecutive rows of the same pages.  Modes 1-4.
-template <int MODE, typename T, int D>
-__global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
-  constexpr int VEC = 16 / sizeof(T);
-  constexpr int TPR = D / VEC;
-  constexpr int TOK = 256 / TPR;  // tokens per block
-  static_assert(TPR >= 2 && TPR <= 32 && (TPR & (TPR - 1)) == 0, "row group");
-  const int h = blockIdx.y, side = blockIdx.z;
-  const long long token = (long long)blockIdx.x * TOK + threadIdx.x / TPR;
-  const int j = threadIdx.x % TPR;
-
-  bool active = token < a.num_tokens;
-  int slot = active ? __ldg(a.slots + token) : -1;
-  active = active && slot >= 0;
+// Quantize one (token, kv head, side) row of D values, held by a group of TPR
+// threads with VEC values each (thread j: values j*VEC ..), and store it at
+// slot (skipped when slot < 0; flagged and skipped when out of range).
+template <int MODE, int D, int VEC, int TPR>
+__device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side, int slot, int j, const float* x) {
+  bool active = slot >= 0;
   const int page = slot >> a.log2P;
   const int off = slot & (a.P - 1);
   if (active && page >= a.num_pages) {
     if (j == 0) set_error(a.pool, KVQ_DEVERR_SLOT_RANGE);
     active = false;
-  }
-  const long long r = token * a.Hkv + h;  // (token, head) row of the input
-
-  float x[VEC];
-  if (active) {
-    const T* src = static_cast<const T*>(side ? a.v : a.k) + r * D + j * VEC;
-    load16<T>(src, x);
-  } else {
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) x[i] = 0.0f;
   }
   uint8_t* blk = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes;
 
@@ -236,6 +215,47 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
         blk[(size_t)a.P * D + (size_t)side * a.P * D / 16 + (size_t)off * D / 16 + (j * VEC) / 16] =
             static_cast<uint8_t>(sb);
     }
+  }
+}
+
+// Rows of D values, one per group of TPR threads (VEC = 16 bytes of input per
+// thread), kRowsPerThread rows per thread with every load issued before the
+// first row is converted, so that enough bytes are in flight to cover HBM
+// latency.  Grid: (token blocks, kv head, side), so no index needs a division;
+// a block's consecutive tokens land in consecutive rows of the same pages.
+// Modes 1-4.
+#ifndef KVQ_WRITE_ROWS
+#define KVQ_WRITE_ROWS 4
+#endif
+constexpr int kRowsPerThread = KVQ_WRITE_ROWS;
+
+template <int MODE, typename T, int D>
+__global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
+  constexpr int VEC = 16 / sizeof(T);
+  constexpr int TPR = D / VEC;
+  constexpr int TOK = 256 / TPR;  // tokens per block and row pass
+  constexpr int R = kRowsPerThread;
+  static_assert(TPR >= 2 && TPR <= 32 && (TPR & (TPR - 1)) == 0, "row group");
+  const int h = blockIdx.y, side = blockIdx.z;
+  const long long tok0 = (long long)blockIdx.x * (TOK * R) + threadIdx.x / TPR;
+  const int j = threadIdx.x % TPR;
+  const T* src = static_cast<const T*>(side ? a.v : a.k);
+
+  int slot[R];
+  uint4 raw[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const long long token = tok0 + (long long)r * TOK;
+    const bool in = token < a.num_tokens;
+    slot[r] = in ? __ldg(a.slots + token) : -1;
+    raw[r] = in ? __ldg(reinterpret_cast<const uint4*>(src + (token * a.Hkv + h) * D + j * VEC))
+                : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    float x[VEC];
+    widen16<T>(raw[r], x);
+    quantize_row<MODE, D, VEC, TPR>(a, h, side, slot[r], j, x);
   }
 }
 
@@ -635,7 +655,7 @@ __global__ void scales_from_amax_kernel(uint8_t* pool, const float* ak, const fl
 
 template <int MODE, typename T, int D>
 cudaError_t launch_rows(const WriteArgs& a, cudaStream_t s) {
-  constexpr int TOK = 256 / (D / (16 / sizeof(T)));
+  constexpr int TOK = 256 / (D / (16 / sizeof(T))) * kRowsPerThread;
   const long long blocks = (a.num_tokens + TOK - 1) / TOK;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL || a.Hkv > 65535) return cudaErrorInvalidValue;
