@@ -213,6 +213,42 @@ def flush_l2(buf):
     buf.zero_()
 
 
+# --------------------------------------------------------------------------- recorded DRAM traffic
+CSRC = os.path.join(ROOT, "quantized_paged_kv_quantize_gb300", "csrc")
+KERNEL_SOURCES = {
+    "decode_kernel": ["kvq_decode.cu", "kvq_device.cuh", "kvq_internal.h", "../_build.py"],
+    "kvarn_decode_kernel": ["kvq_decode_kvarn.cu", "kvq_device.cuh", "kvq_internal.h", "../_build.py"],
+}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+
+
+def kernel_sources_hash(kernel: str) -> str:
+    """sha256 of the sources a decode kernel is built from (its file, the shared
+    device header and the build flags), to tell whether a recorded capture still
+    describes the kernel that runs."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str, kv_tokens: int):
+    """DRAM bytes (read + write) per launch of the kernel on this workload, from the
+    ncu capture recorded in profiles/traffic.txt, scaled from the capture's cached
+    tokens to kv_tokens; None when there is no record or the kernel's sources have
+    changed since it was taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    want = kernel_sources_hash(kernel)
+    for line in open(TRAFFIC_FILE):
+        f = line.split()
+        if len(f) == 5 and not line.startswith("#") and f[0] == workload and f[1] == kernel and f[4] == want:
+            return int(round(float(f[3]) * kv_tokens / float(f[2])))
+    return None
+
+
 def run_ours(args, w: wl.Workload):
     import torch
     import torch.distributed as dist
@@ -298,6 +334,8 @@ def run_ours(args, w: wl.Workload):
     dec_avg = float(np.mean(dec_ms))
     peak, peak_kind = measured_peaks()
     dec_gbs = dbytes / (dec_avg * 1e-3) / 1e9
+    dec_kernel = "kvarn_decode_kernel" if w.mode == "kvarn_k4v2_g128" else "decode_kernel"
+    traffic = recorded_traffic(w.name.split("[")[0], dec_kernel, int(gw.lay.seq_lens.sum()))
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region)
     q_h = gw.q.cpu().pin_memory()
@@ -368,8 +406,9 @@ def run_ours(args, w: wl.Workload):
                       "bulk_bytes": wbytes, "tokens_heads_per_s": gw.lay.num_tokens * w.num_kv_heads / (fill_ms * 1e-3),
                       "calibrate_ms": round(calib_ms, 4) if w.mode in ("fp8_per_tensor", "nvfp4") else None},
             "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(dec_gbs / peak, 4), "traffic": None,
-                         "kernel": "decode_kernel + combine_kernel", "peak_kind": peak_kind},
+                         "frac": round(dec_gbs / peak, 4), "traffic": traffic,
+                         "kernel": dec_kernel, "peak_kind": peak_kind,
+                         "timed": dec_kernel + (" + its split combine" if gw.plan[0] > 1 else "")},
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": gw.launches_per_step() * args.steps,
