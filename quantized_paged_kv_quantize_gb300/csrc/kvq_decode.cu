@@ -86,6 +86,13 @@ struct Cfg {
   // the tensor core), so the output is a weighted mean whose weights carry a
   // relative error of at most 2^-11 each.
   static constexpr bool plo(bool f32io) { return f32io || MODE != KVQ_NVFP4; }
+  // Token held by MMA row m (S^T rows, P^T k-index) of a page.  For 64-byte
+  // rows (NVFP4) rows 2 and 3 of every 4 trade places: under the 64-byte
+  // swizzle the V rows 2tq, 2tq+1, 2tq+8, 2tq+9 that a quad reads then fall in
+  // distinct banks (the identity order left them 2-way conflicted), and the K
+  // rows g, g+8 stay conflict-free.  Any order is valid as long as K rows, V
+  // rows and the masks all use it, since P^T comes from the S^T fragment.
+  static __device__ __forceinline__ int tok(int m) { return MODE == KVQ_NVFP4 ? m ^ ((m >> 1) & 1) : m; }
 };
 
 template <int MASK>
@@ -163,17 +170,18 @@ __device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq
   constexpr int KW = (MODE == KVQ_NVFP4 ? D / 8 : D / 4) / 4;  // words per thread per row
   uint32_t kg[NP][KW], kh8[NP][KW];
   const int rb = tq * (KW * 4);
+  const int tg = C::tok(g);  // tokens of MMA rows g and g + 8 (tok keeps bit 3)
 #pragma unroll
   for (int p = 0; p < NP; ++p)
 #pragma unroll
     for (int w = 0; w < KW; w += 4) {
-      lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>(g * C::RW + rb + 4 * w), kg[p] + w);
-      lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>((g + 8) * C::RW + rb + 4 * w), kh8[p] + w);
+      lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>(tg * C::RW + rb + 4 * w), kg[p] + w);
+      lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>((tg + 8) * C::RW + rb + 4 * w), kh8[p] + w);
     }
   if constexpr (MODE == KVQ_NVFP4) {
     constexpr int SB = D / 16;
     const int blk0 = (tq * (D / 4)) / 16;
-    const int base_g = C::S_OFF + g * SB, base_h = C::S_OFF + (g + 8) * SB;
+    const int base_g = C::S_OFF + tg * SB, base_h = C::S_OFF + (tg + 8) * SB;
     __half2 sg2[NP], sh2[NP];
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
@@ -232,7 +240,7 @@ __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq
                                          const uint32_t (*bh)[2], const uint32_t (*bl)[2], float (*o)[4]) {
   using C = Cfg<MODE, D>;
   constexpr int MTILES = C::MTILES;
-  const int r0 = 2 * tq, r1 = 2 * tq + 1, r2 = 2 * tq + 8, r3 = 2 * tq + 9;
+  const int r0 = C::tok(2 * tq), r1 = C::tok(2 * tq + 1), r2 = r0 + 8, r3 = r1 + 8;  // tokens
   if constexpr (MODE == KVQ_NVFP4) {
     constexpr int VB = D / 16;  // bytes per thread per row (D/8 channels at 4 bits)
     constexpr int VW = VB >= 4 ? VB / 4 : 1;
@@ -365,6 +373,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, tq = lane & 3;
+  const int tg = C::tok(g);  // token of MMA rows g (and tg + 8 of row g + 8)
 
   int n = a.seq_lens[b];
   const int lim = min(a.max_seq_len, a.max_pages * kPage);
@@ -492,16 +501,16 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
     if constexpr (kPerToken) {
       const float* sa = reinterpret_cast<const float*>(stA + C::S_OFF);  // K scales, then V scales
       const float* sb = reinterpret_cast<const float*>(stB + C::S_OFF);
-      fA0 *= sa[g]; fA8 *= sa[g + 8]; vA0 = sa[kPage + g]; vA8 = sa[kPage + g + 8];
+      fA0 *= sa[tg]; fA8 *= sa[tg + 8]; vA0 = sa[kPage + tg]; vA8 = sa[kPage + tg + 8];
       fB0 *= sb[g]; fB8 *= sb[g + 8]; vB0 = sb[kPage + g]; vB8 = sb[kPage + g + 8];
     }
     float sA[4] = {cA[0] * fA0, cA[1] * fA0, cA[2] * fA8, cA[3] * fA8};
     float sB[4] = {cB[0] * fB0, cB[1] * fB0, cB[2] * fB8, cB[3] * fB8};
     if (nvA < kPage || nvB < kPage) {  // rare: a partial or missing page
-      if (g >= nvA) { sA[0] = sA[1] = -INFINITY; vA0 = 0.f; }
-      if (g + 8 >= nvA) { sA[2] = sA[3] = -INFINITY; vA8 = 0.f; }
-      if (g >= nvB) { sB[0] = sB[1] = -INFINITY; vB0 = 0.f; }
-      if (g + 8 >= nvB) { sB[2] = sB[3] = -INFINITY; vB8 = 0.f; }
+      if (tg >= nvA) { sA[0] = sA[1] = -INFINITY; vA0 = 0.f; }
+      if (tg + 8 >= nvA) { sA[2] = sA[3] = -INFINITY; vA8 = 0.f; }
+      if (tg >= nvB) { sB[0] = sB[1] = -INFINITY; vB0 = 0.f; }
+      if (tg + 8 >= nvB) { sB[2] = sB[3] = -INFINITY; vB8 = 0.f; }
     }
     // Lazy reference max: move it (and rescale) only when some score exceeds it
     // by more than SLACK -- rare once the first pages are seen.
