@@ -81,11 +81,6 @@ struct Cfg {
     return MODE == KVQ_INT8_PER_TOKEN_HEAD ? (f32io ? 0 : 2)
          : MODE == KVQ_FP8_PER_TOKEN_HEAD ? (f32io ? 0 : 4) : (f32io ? 14 : 10);
   }
-  // Whether P enters P V as an f16 hi + lo pair (~22 bits).  NVFP4 with f16 io
-  // uses the hi part alone and takes l from the same f16 weights (a ones tile on
-  // the tensor core), so the output is a weighted mean whose weights carry a
-  // relative error of at most 2^-11 each.
-  static constexpr bool plo(bool f32io) { return f32io || MODE != KVQ_NVFP4; }
   // Token held by MMA row m (S^T rows, P^T k-index) of a page.  For 64-byte
   // rows (NVFP4) rows 2 and 3 of every 4 trade places: under the 64-byte
   // swizzle the V rows 2tq, 2tq+1, 2tq+8, 2tq+9 that a quad reads then fall in
@@ -235,7 +230,7 @@ __device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq
 // O^T += V^T P^T for NP staged pages (M-tiles interleaved across pages).  With
 // PARTIAL, rows (tokens) >= nvalid[p] are zeroed before use so that whatever
 // bytes an unwritten slot holds cannot reach the output.
-template <int MODE, int D, int NP, bool PARTIAL, bool PLO>
+template <int MODE, int D, int NP, bool PARTIAL>
 __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq, const int* nvalid,
                                          const uint32_t (*bh)[2], const uint32_t (*bl)[2], float (*o)[4]) {
   using C = Cfg<MODE, D>;
@@ -307,12 +302,11 @@ __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq
             av[2] = h2_as_u32(__hmul2(u32_as_h2(fe23[k]), sc23[p]));
             av[3] = h2_as_u32(__hmul2(u32_as_h2(fo23[k]), sc23[p]));
             mma16816(o[t], av, bh[p][0], bh[p][1]);
-            if constexpr (PLO) mma16816(o[t], av, bl[p][0], bl[p][1]);
+            mma16816(o[t], av, bl[p][0], bl[p][1]);
           }
         }
       }
   } else {
-    static_assert(PLO, "one-byte modes always use the hi + lo split");
     constexpr int VW = D / 32;  // words per thread per row (D/8 one-byte channels)
     uint32_t A0[NP][VW], A1[NP][VW], A2[NP][VW], A3[NP][VW];
     const int cb = g * (D / 8);
@@ -363,7 +357,6 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   constexpr int KSTEPS = C::KSTEPS, MTILES = C::MTILES;
   constexpr int PSHIFT = C::pshift(QF32);
   constexpr float SLACK = (float)C::slack(QF32);
-  constexpr bool PLO = C::plo(QF32);
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ uint64_t bars[kWarps][C::STAGES];
   __shared__ int page_ids[kWarps * kIdsPerWarp];
@@ -458,12 +451,6 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
 #pragma unroll
   for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
   float m0 = -1e30f, m1 = -1e30f, l0 = 0.0f, l1 = 0.0f;  // finite start: no inf - inf
-  // Without the lo split, l accumulates on the tensor core: ones(16x16) x P^T
-  // gives, in every row, the sum over the page's tokens of the f16 weights
-  // (lacc[0], lacc[1] = heads 2tq, 2tq+1; rows g and g+8 hold the same sums).
-  float lacc[4] = {0.f, 0.f, 0.f, 0.f};
-  constexpr uint32_t kOnes = 0x3C003C00u;
-  const uint32_t ones[4] = {kOnes, kOnes, kOnes, kOnes};
   bool timed_out = false;
 
   for (int i = 0; i < my_count; i += 2) {
@@ -529,13 +516,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
       const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);  // m starts at a finite -1e30
       m0 = n0;
       m1 = n1;
-      if constexpr (PLO) {
-        l0 *= al0;
-        l1 *= al1;
-      } else {
-        lacc[0] *= al0;
-        lacc[1] *= al1;
-      }
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
       for (int t = 0; t < MTILES; ++t) {
         o[t][0] *= al0; o[t][2] *= al0;
@@ -545,10 +527,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
     const float e0 = (float)PSHIFT - m0, e1 = (float)PSHIFT - m1;
     const float pA0 = ex2(sA[0] + e0), pA1 = ex2(sA[1] + e1), pA2 = ex2(sA[2] + e0), pA3 = ex2(sA[3] + e1);
     const float pB0 = ex2(sB[0] + e0), pB1 = ex2(sB[1] + e1), pB2 = ex2(sB[2] + e0), pB3 = ex2(sB[3] + e1);
-    if constexpr (PLO) {
-      l0 += (pA0 + pA2) + (pB0 + pB2);
-      l1 += (pA1 + pA3) + (pB1 + pB3);
-    }
+    l0 += (pA0 + pA2) + (pB0 + pB2);
+    l1 += (pA1 + pA3) + (pB1 + pB3);
     // P^T as the B operand: f16 hi + lo, each 8x8 block transposed in registers
     uint32_t bh[2][2], bl[2][2];
     {
@@ -560,26 +540,18 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const __half2 h = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
+        const float2 f = __half22float2(h);
+        const __half2 lo = __floats2half2_rn(x[2 * k] - f.x, x[2 * k + 1] - f.y);
         bh[k >> 1][k & 1] = movmatrix_t(h2_as_u32(h));
-        if constexpr (PLO) {
-          const float2 f = __half22float2(h);
-          const __half2 lo = __floats2half2_rn(x[2 * k] - f.x, x[2 * k + 1] - f.y);
-          bl[k >> 1][k & 1] = movmatrix_t(h2_as_u32(lo));
-        } else {
-          bl[k >> 1][k & 1] = 0u;
-        }
+        bl[k >> 1][k & 1] = movmatrix_t(h2_as_u32(lo));
       }
-    }
-    if constexpr (!PLO) {  // absent or partial pages have zero weights
-      mma16816(lacc, ones, bh[0][0], bh[0][1]);
-      mma16816(lacc, ones, bh[1][0], bh[1][1]);
     }
     if (full2) {
       const int nv2[2] = {kPage, kPage};
-      pv_pages<MODE, D, 2, false, PLO>(stAB, g, tq, nv2, bh, bl, o);
+      pv_pages<MODE, D, 2, false>(stAB, g, tq, nv2, bh, bl, o);
     } else {
-      if (nvA > 0) pv_pages<MODE, D, 1, true, PLO>(stAB, g, tq, &nvA, bh, bl, o);
-      if (nvB > 0) pv_pages<MODE, D, 1, true, PLO>(stAB + 1, g, tq, &nvB, bh + 1, bl + 1, o);
+      if (nvA > 0) pv_pages<MODE, D, 1, true>(stAB, g, tq, &nvA, bh, bl, o);
+      if (nvB > 0) pv_pages<MODE, D, 1, true>(stAB + 1, g, tq, &nvB, bh + 1, bl + 1, o);
     }
 
     __syncwarp();
@@ -592,15 +564,10 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   if (timed_out && lane == 0) set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_TIMEOUT);
 
   // ---------------- merge the warps of this CTA
-  if constexpr (PLO) {
 #pragma unroll
-    for (int x = 4; x <= 16; x <<= 1) {
-      l0 += __shfl_xor_sync(kFull, l0, x);
-      l1 += __shfl_xor_sync(kFull, l1, x);
-    }
-  } else {
-    l0 = lacc[0];
-    l1 = lacc[1];
+  for (int x = 4; x <= 16; x <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, x);
+    l1 += __shfl_xor_sync(kFull, l1, x);
   }
   __syncthreads();  // every warp is done with its ring: reuse it for the merge
   float* red_o = reinterpret_cast<float*>(smem);             // [W][8][D]
