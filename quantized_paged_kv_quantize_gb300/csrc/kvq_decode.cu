@@ -88,6 +88,10 @@ struct Cfg {
   // rows g, g+8 stay conflict-free.  Any order is valid as long as K rows, V
   // rows and the masks all use it, since P^T comes from the S^T fragment.
   static __device__ __forceinline__ int tok(int m) { return MODE == KVQ_NVFP4 ? m ^ ((m >> 1) & 1) : m; }
+  // The CTA's warps share one copy of the query fragments in shared memory
+  // (one 64-bit load per k-step) instead of 16 registers each: faster for the
+  // one-byte modes, slower for NVFP4 (measured on GB300).
+  static constexpr bool QSMEM = MODE != KVQ_NVFP4;
 };
 
 template <int MASK>
@@ -159,7 +163,7 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int 
 // MMA chains overlap: c[p][0..1] = token g, c[p][2..3] = token g+8, heads 2tq, 2tq+1.
 template <int MODE, int D, bool QF32, int NP>
 __device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq, const uint32_t (*qh)[2],
-                                         const uint32_t (*ql)[2], float (*c)[4]) {
+                                         const uint32_t (*ql)[2], const uint2* qs, int lane, float (*c)[4]) {
   using C = Cfg<MODE, D>;
   constexpr int KSTEPS = C::KSTEPS;
   constexpr int KW = (MODE == KVQ_NVFP4 ? D / 8 : D / 4) / 4;  // words per thread per row
@@ -214,6 +218,7 @@ __device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq
         }
       }
   } else {
+    static_assert(C::QSMEM, "one-byte modes read the query fragments from shared memory");
 #pragma unroll
     for (int j = 0; j < KSTEPS; ++j)
 #pragma unroll
@@ -221,8 +226,12 @@ __device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq
         uint32_t af[4];
         cvt_pair4<MODE>(kg[p][j], af[0], af[2]);
         cvt_pair4<MODE>(kh8[p][j], af[1], af[3]);
-        mma16816(c[p], af, qh[j][0], qh[j][1]);
-        if constexpr (QF32) mma16816(c[p], af, ql[j][0], ql[j][1]);
+        const uint2 qv = qs[j * 32 + lane];
+        mma16816(c[p], af, qv.x, qv.y);
+        if constexpr (QF32) {
+          const uint2 qw = qs[(KSTEPS + j) * 32 + lane];
+          mma16816(c[p], af, qw.x, qw.y);
+        }
       }
   }
 }
@@ -292,19 +301,20 @@ __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq
         e2m1x8_to_f16x2x4(xo01, fo01);
         e2m1x8_to_f16x2x4(xe23, fe23);
         e2m1x8_to_f16x2x4(xo23, fo23);
+        // hi products of the word's tiles first, then lo: each tile's two MMAs
+        // are then separated by the other tiles' instead of issued back to back
+        uint32_t av[4][4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int t = 4 * w + k;
-          if (t < MTILES) {
-            uint32_t av[4];
-            av[0] = h2_as_u32(__hmul2(u32_as_h2(fe01[k]), sc01[p]));
-            av[1] = h2_as_u32(__hmul2(u32_as_h2(fo01[k]), sc01[p]));
-            av[2] = h2_as_u32(__hmul2(u32_as_h2(fe23[k]), sc23[p]));
-            av[3] = h2_as_u32(__hmul2(u32_as_h2(fo23[k]), sc23[p]));
-            mma16816(o[t], av, bh[p][0], bh[p][1]);
-            mma16816(o[t], av, bl[p][0], bl[p][1]);
-          }
+          av[k][0] = h2_as_u32(__hmul2(u32_as_h2(fe01[k]), sc01[p]));
+          av[k][1] = h2_as_u32(__hmul2(u32_as_h2(fo01[k]), sc01[p]));
+          av[k][2] = h2_as_u32(__hmul2(u32_as_h2(fe23[k]), sc23[p]));
+          av[k][3] = h2_as_u32(__hmul2(u32_as_h2(fo23[k]), sc23[p]));
+          if (4 * w + k < MTILES) mma16816(o[4 * w + k], av[k], bh[p][0], bh[p][1]);
         }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (4 * w + k < MTILES) mma16816(o[4 * w + k], av[k], bl[p][0], bl[p][1]);
       }
   } else {
     constexpr int VW = D / 32;  // words per thread per row (D/8 one-byte channels)
@@ -337,15 +347,15 @@ __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq
         }
         const uint32_t x01 = prmt(a0, a1, 0x5140u), y01 = prmt(a0, a1, 0x7362u);
         const uint32_t x23 = prmt(a2, a3, 0x5140u), y23 = prmt(a2, a3, 0x7362u);
-        uint32_t av[4];
+        uint32_t av[4], aw[4];
         cvt_pair4_biased<MODE>(x01, av[0], av[1]);
         cvt_pair4_biased<MODE>(x23, av[2], av[3]);
-        mma16816(o[2 * w], av, bh[p][0], bh[p][1]);
+        cvt_pair4_biased<MODE>(y01, aw[0], aw[1]);
+        cvt_pair4_biased<MODE>(y23, aw[2], aw[3]);
+        mma16816(o[2 * w], av, bh[p][0], bh[p][1]);  // hi of both tiles, then lo
+        mma16816(o[2 * w + 1], aw, bh[p][0], bh[p][1]);
         mma16816(o[2 * w], av, bl[p][0], bl[p][1]);
-        cvt_pair4_biased<MODE>(y01, av[0], av[1]);
-        cvt_pair4_biased<MODE>(y23, av[2], av[3]);
-        mma16816(o[2 * w + 1], av, bh[p][0], bh[p][1]);
-        mma16816(o[2 * w + 1], av, bl[p][0], bl[p][1]);
+        mma16816(o[2 * w + 1], aw, bl[p][0], bl[p][1]);
       }
   }
 }
@@ -432,9 +442,20 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   const int npre = my_count < C::STAGES ? my_count : C::STAGES;
   for (int i = 0; i < npre; ++i) issue(i);
 
-  // query fragments
+  // query fragments: in registers, or one copy in shared memory (C::QSMEM)
+  __shared__ uint2 qsm[C::QSMEM ? (QF32 ? 2 : 1) * KSTEPS * 32 : 1];
   uint32_t qh[KSTEPS][2], ql[QF32 ? KSTEPS : 1][2];
-  load_q<D, QF32>(a, b, kvh, g, tq, qh, ql);
+  if (!C::QSMEM || warp == 0) load_q<D, QF32>(a, b, kvh, g, tq, qh, ql);
+  if constexpr (C::QSMEM) {
+    if (warp == 0) {
+#pragma unroll
+      for (int j = 0; j < KSTEPS; ++j) {
+        qsm[j * 32 + lane] = make_uint2(qh[j][0], qh[j][1]);
+        if constexpr (QF32) qsm[(KSTEPS + j) * 32 + lane] = make_uint2(ql[j][0], ql[j][1]);
+      }
+    }
+    __syncthreads();
+  }
 
   // Scores in log2 units: s = c * kfac (FP8 per-tensor, NVFP4: the K tensor scale
   // is uniform) or c * ks[t] * softmax_scale*log2(e) (per-token-head).  The
@@ -475,10 +496,10 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
     const uint8_t* stAB[2] = {stA, stB};
     float cc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     if (full2) {
-      qk_pages<MODE, D, QF32, 2>(stAB, g, tq, qh, ql, cc);
+      qk_pages<MODE, D, QF32, 2>(stAB, g, tq, qh, ql, qsm, lane, cc);
     } else {
-      if (nvA > 0) qk_pages<MODE, D, QF32, 1>(stAB, g, tq, qh, ql, cc);
-      if (nvB > 0) qk_pages<MODE, D, QF32, 1>(stAB + 1, g, tq, qh, ql, cc + 1);
+      if (nvA > 0) qk_pages<MODE, D, QF32, 1>(stAB, g, tq, qh, ql, qsm, lane, cc);
+      if (nvB > 0) qk_pages<MODE, D, QF32, 1>(stAB + 1, g, tq, qh, ql, qsm, lane, cc + 1);
     }
     const float* cA = cc[0];
     const float* cB = cc[1];
