@@ -522,12 +522,9 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
     }
     // Lazy reference max: move it (and rescale) only when some score exceeds it
     // by more than SLACK -- rare once the first pages are seen.
-    const float t0 = m0 + SLACK, t1 = m1 + SLACK;
-    const bool over = (sA[0] > t0) | (sA[2] > t0) | (sB[0] > t0) | (sB[2] > t0) | (sA[1] > t1) | (sA[3] > t1) |
-                      (sB[1] > t1) | (sB[3] > t1);
-    if (__any_sync(kFull, over)) {
-      float bm0 = fmaxf(fmaxf(sA[0], sA[2]), fmaxf(sB[0], sB[2]));
-      float bm1 = fmaxf(fmaxf(sA[1], sA[3]), fmaxf(sB[1], sB[3]));
+    float bm0 = fmaxf(fmaxf(sA[0], sA[2]), fmaxf(sB[0], sB[2]));  // this thread's max, heads 2tq, 2tq+1
+    float bm1 = fmaxf(fmaxf(sA[1], sA[3]), fmaxf(sB[1], sB[3]));
+    if (__any_sync(kFull, (bm0 > m0 + SLACK) | (bm1 > m1 + SLACK))) {
 #pragma unroll
       for (int x = 4; x <= 16; x <<= 1) {
         bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, x));
@@ -560,9 +557,13 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const __half2 h = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
-        const float2 f = __half22float2(h);
-        const __half2 lo = __floats2half2_rn(x[2 * k] - f.x, x[2 * k + 1] - f.y);
+        // hi = x cut to 10 mantissa bits (exact in f16 over P's range; below
+        // 2^-14 the f16 conversion rounds it, an error under 2^-24), lo = the
+        // exact remainder rounded to f16: together ~22 bits of x
+        const float h0 = __uint_as_float(__float_as_uint(x[2 * k]) & 0xFFFFE000u);
+        const float h1 = __uint_as_float(__float_as_uint(x[2 * k + 1]) & 0xFFFFE000u);
+        const __half2 h = __floats2half2_rn(h0, h1);
+        const __half2 lo = __floats2half2_rn(x[2 * k] - h0, x[2 * k + 1] - h1);
         bh[k >> 1][k & 1] = movmatrix_t(h2_as_u32(h));
         bl[k >> 1][k & 1] = movmatrix_t(h2_as_u32(lo));
       }
