@@ -96,11 +96,13 @@ typedef struct kvq_cache kvq_cache;
  * Token t of page p is row t of that block.  Per mode (P = page_size, D = head_dim):
  *   FP8 per-tensor : K[P][D] e4m3 | V[P][D] e4m3                    (2PD bytes)
  *   INT8 / FP8 PTH : K[P][D] | V[P][D] | K scale[P] f32 | V scale[P] f32
- *   NVFP4          : K[P][D/2] | V[P][D/2] | K s_b[P][D/16] e4m3 | V s_b[P][D/16] e4m3
+ *   NVFP4          : K[P][D/2] | V[P/2][D] | K s_b[P][D/16] e4m3 | V s_b[P][D/16] e4m3
  *   KVarN (P=D=128): K[128][64] u4 | V[128][32] u2 |
  *                    K scale[D] zero[D] c[D] r[P] f32 | V scale[P] zero[P] r[P] c[D] f32
- * 4-bit codes: the even head_dim index in the low nibble.  2-bit codes:
- * element 4i+j in bits 2j..2j+1 of byte i.  The header holds, at byte 16 and
+ * 4-bit codes: the even head_dim index in the low nibble, except NVFP4 V,
+ * whose byte [k][d] holds channel d of tokens 2k (low nibble) and 2k+1 -- the
+ * pairing decode's tensor-core fragments take, with no nibble shuffling.
+ * 2-bit codes: element 4i+j in bits 2j..2j+1 of byte i.  The header holds, at byte 16 and
  * 20, the per-tensor K and V scales (FP8 per-tensor s; NVFP4 s_t), and at
  * byte 12 the device error word.  This is the same content as the in-page
  * layouts of [P4] (data plus one fp32 scale per token-head; head_size/2 bytes

@@ -337,10 +337,11 @@ void kvqo_hadamard_f64(double* x, int n) {
 /*   pool = 256-byte header, then one block per (page, kv head), page-major.    */
 /*   FP8 per-tensor : K[P][D] e4m3 | V[P][D] e4m3                               */
 /*   INT8/FP8 PTH   : K[P][D] | V[P][D] | K scale[P] f32 | V scale[P] f32       */
-/*   NVFP4          : K[P][D/2] | V[P][D/2] | K s_b[P][D/16] | V s_b[P][D/16]   */
+/*   NVFP4          : K[P][D/2] | V[P/2][D] | K s_b[P][D/16] | V s_b[P][D/16]   */
 /*   KVarN (P=D=128): K[128][64] 4-bit | V[128][32] 2-bit |                      */
 /*                    K scale[D] zero[D] c[D] r[P] | V scale[P] zero[P] r[P] c[D] */
-/* 4-bit: even index in the low nibble; 2-bit: element 4i+j in bits 2j..2j+1.   */
+/* 4-bit: even index in the low nibble (NVFP4 V: byte [k][d] holds channel d  */
+/* of tokens 2k (low nibble) and 2k+1); 2-bit: element 4i+j in bits 2j..2j+1.  */
 /* ------------------------------------------------------------------------- */
 size_t kvqo_header_bytes(void) { return 256; }
 
@@ -456,11 +457,22 @@ int kvqo_write(int mode, uint8_t* pool, int num_pages, int P, int Hkv, int D, co
             kvqo_quant_row_fp8_pth(x, D, blk + (size_t)side * P * D + (size_t)off * D, &s);
             put_f32(blk + (size_t)2 * P * D + (size_t)side * 4 * P + 4 * off, s);
             break;
-          case KVQO_NVFP4:
-            kvqo_quant_row_nvfp4(x, D, side ? v_scale : k_scale,
-                                 blk + (size_t)side * P * D / 2 + (size_t)off * D / 2,
-                                 blk + (size_t)P * D + (size_t)side * P * D / 16 + (size_t)off * D / 16);
+          case KVQO_NVFP4: {
+            uint8_t* bs = blk + (size_t)P * D + (size_t)side * P * D / 16 + (size_t)off * D / 16;
+            if (!side) {
+              kvqo_quant_row_nvfp4(x, D, k_scale, blk + (size_t)off * D / 2, bs);
+            } else {  /* V: this token's nibble of each byte of its token pair's row */
+              uint8_t packed[512], *pair = blk + (size_t)P * D / 2 + (size_t)(off / 2) * D;
+              int d, sh = 4 * (off & 1);
+              if (D > 1024) return -1;
+              kvqo_quant_row_nvfp4(x, D, v_scale, packed, bs);
+              for (d = 0; d < D; d++) {
+                uint8_t code = (d & 1) ? (uint8_t)(packed[d / 2] >> 4) : (uint8_t)(packed[d / 2] & 15);
+                pair[d] = (uint8_t)((pair[d] & ~(15 << sh)) | (code << sh));
+              }
+            }
             break;
+          }
           default: return -1;
         }
       }
@@ -496,10 +508,12 @@ int kvqo_dequant_row(int mode, const uint8_t* pool, int num_pages, int P, int Hk
     }
     case KVQO_NVFP4: {
       double st = side ? v_scale : k_scale;
-      const uint8_t* row = blk + (size_t)side * P * D / 2 + (size_t)t * D / 2;
+      const uint8_t* row = blk + (size_t)t * D / 2;                               /* K */
+      const uint8_t* pair = blk + (size_t)P * D / 2 + (size_t)(t / 2) * D;         /* V */
       const uint8_t* bs = blk + (size_t)P * D + (size_t)side * P * D / 16 + (size_t)t * D / 16;
       for (d = 0; d < D; d++) {
-        uint8_t nib = (d & 1) ? (uint8_t)(row[d / 2] >> 4) : (uint8_t)(row[d / 2] & 15);
+        uint8_t nib = side ? (uint8_t)((pair[d] >> (4 * (t & 1))) & 15)
+                           : ((d & 1) ? (uint8_t)(row[d / 2] >> 4) : (uint8_t)(row[d / 2] & 15));
         out[d] = st * kvqo_e4m3_decode(bs[d / 16]) * kvqo_e2m1_decode(nib);
       }
       return 0;

@@ -81,13 +81,14 @@ struct Cfg {
     return MODE == KVQ_INT8_PER_TOKEN_HEAD ? (f32io ? 0 : 2)
          : MODE == KVQ_FP8_PER_TOKEN_HEAD ? (f32io ? 0 : 4) : (f32io ? 14 : 10);
   }
-  // Token held by MMA row m (S^T rows, P^T k-index) of a page.  For 64-byte
-  // rows (NVFP4) rows 2 and 3 of every 4 trade places: under the 64-byte
-  // swizzle the V rows 2tq, 2tq+1, 2tq+8, 2tq+9 that a quad reads then fall in
-  // distinct banks (the identity order left them 2-way conflicted), and the K
-  // rows g, g+8 stay conflict-free.  Any order is valid as long as K rows, V
-  // rows and the masks all use it, since P^T comes from the S^T fragment.
-  static __device__ __forceinline__ int tok(int m) { return MODE == KVQ_NVFP4 ? m ^ ((m >> 1) & 1) : m; }
+  // Channel group (D/8 channels) whose V rows the lanes of MMA row g load and
+  // whose outputs they hold.  NVFP4 at D = 128 reads V token-pair rows with
+  // 128-bit loads under the 64-byte swizzle: the order 0, 4, 1, 5, 2, 6, 3, 7
+  // puts the two groups of each 8-lane phase in different bank halves, so the
+  // loads are conflict-free (the identity order is 2-way conflicted).
+  static __device__ __forceinline__ int cgrp(int g) {
+    return (MODE == KVQ_NVFP4 && D == 128) ? ((g >> 1) | ((g & 1) << 2)) : g;
+  }
   // The CTA's warps share one copy of the query fragments in shared memory
   // (one 64-bit load per k-step) instead of 16 registers each: faster for the
   // one-byte modes, slower for NVFP4 (measured on GB300).
@@ -169,18 +170,17 @@ __device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq
   constexpr int KW = (MODE == KVQ_NVFP4 ? D / 8 : D / 4) / 4;  // words per thread per row
   uint32_t kg[NP][KW], kh8[NP][KW];
   const int rb = tq * (KW * 4);
-  const int tg = C::tok(g);  // tokens of MMA rows g and g + 8 (tok keeps bit 3)
 #pragma unroll
   for (int p = 0; p < NP; ++p)
 #pragma unroll
     for (int w = 0; w < KW; w += 4) {
-      lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>(tg * C::RW + rb + 4 * w), kg[p] + w);
-      lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>((tg + 8) * C::RW + rb + 4 * w), kh8[p] + w);
+      lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>(g * C::RW + rb + 4 * w), kg[p] + w);
+      lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>((g + 8) * C::RW + rb + 4 * w), kh8[p] + w);
     }
   if constexpr (MODE == KVQ_NVFP4) {
     constexpr int SB = D / 16;
     const int blk0 = (tq * (D / 4)) / 16;
-    const int base_g = C::S_OFF + tg * SB, base_h = C::S_OFF + (tg + 8) * SB;
+    const int base_g = C::S_OFF + g * SB, base_h = C::S_OFF + (g + 8) * SB;
     __half2 sg2[NP], sh2[NP];
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
@@ -244,41 +244,30 @@ __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq
                                          const uint32_t (*bh)[2], const uint32_t (*bl)[2], float (*o)[4]) {
   using C = Cfg<MODE, D>;
   constexpr int MTILES = C::MTILES;
-  const int r0 = C::tok(2 * tq), r1 = C::tok(2 * tq + 1), r2 = r0 + 8, r3 = r1 + 8;  // tokens
+  const int r0 = 2 * tq, r1 = 2 * tq + 1, r2 = 2 * tq + 8, r3 = 2 * tq + 9;  // tokens
   if constexpr (MODE == KVQ_NVFP4) {
-    constexpr int VB = D / 16;  // bytes per thread per row (D/8 channels at 4 bits)
-    constexpr int VW = VB >= 4 ? VB / 4 : 1;
-    uint32_t A0[NP][VW], A1[NP][VW], A2[NP][VW], A3[NP][VW];
+    // V payload: token-pair rows [kPage / 2][D] bytes, byte (k, d) holding
+    // channel d of tokens 2k (low nibble) and 2k + 1, so one E2M1 pair
+    // conversion gives the A fragment's (token 2tq, 2tq + 1) f16x2 directly.
+    // Lanes (g, tq) read pair rows tq and tq + 4, channels cgb .. cgb + D/8 - 1;
+    // tile t uses channel cgb + 2t in MMA row g and cgb + 2t + 1 in row g + 8.
+    constexpr int CPG = D / 8;       // channels (bytes) per lane per pair row
+    constexpr int VW = CPG / 4;      // words
+    uint32_t W0[NP][VW], W2[NP][VW];
     __half2 sc01[NP], sc23[NP];
-    const int cb = g * VB;
-    const int vblk = (g * (D / 8)) / 16;
-    constexpr int VS = C::S_OFF + kPage * (D / 16);  // V block scales
+    const int cgb = CPG * C::cgrp(g);
+    const int vblk = cgb / 16;
+    constexpr int VS = C::S_OFF + kPage * (D / 16);  // V block scales [kPage][D/16]
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-      if constexpr (VB >= 8) {
-        lds<2>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb), A0[p]);
-        lds<2>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb), A1[p]);
-        lds<2>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb), A2[p]);
-        lds<2>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb), A3[p]);
-      } else {
-        A0[p][0] = *reinterpret_cast<const uint16_t*>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb));
-        A1[p][0] = *reinterpret_cast<const uint16_t*>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb));
-        A2[p][0] = *reinterpret_cast<const uint16_t*>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb));
-        A3[p][0] = *reinterpret_cast<const uint16_t*>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb));
-      }
+      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + tq * D + cgb), W0[p]);
+      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + (tq + 4) * D + cgb), W2[p]);
       uint32_t b0 = st[p][swz<C::SWZ_MASK>(VS + r0 * (D / 16) + vblk)];
       uint32_t b1 = st[p][swz<C::SWZ_MASK>(VS + r1 * (D / 16) + vblk)];
       uint32_t b2 = st[p][swz<C::SWZ_MASK>(VS + r2 * (D / 16) + vblk)];
       uint32_t b3 = st[p][swz<C::SWZ_MASK>(VS + r3 * (D / 16) + vblk)];
-      if constexpr (PARTIAL) {
+      if constexpr (PARTIAL) {  // a zero scale zeroes the token: E2M1 codes are all finite
         const int nv = nvalid[p];
-#pragma unroll
-        for (int w = 0; w < VW; ++w) {
-          if (r0 >= nv) A0[p][w] = 0;
-          if (r1 >= nv) A1[p][w] = 0;
-          if (r2 >= nv) A2[p][w] = 0;
-          if (r3 >= nv) A3[p][w] = 0;
-        }
         if (r0 >= nv) b0 = 0;
         if (r1 >= nv) b1 = 0;
         if (r2 >= nv) b2 = 0;
@@ -288,33 +277,25 @@ __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq
       sc23[p] = u32_as_h2(e4m3x2_to_f16x2(b2 | (b3 << 8)));
     }
 #pragma unroll
-    for (int w = 0; w < VW; ++w)
+    for (int p = 0; p < NP; ++p)
 #pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        // pair rows (r0, r1) and (r2, r3) nibble by nibble: even channel e = 8w+2k, odd e+1
-        const uint32_t xe01 = bitsel(A0[p][w], A1[p][w] << 4, 0x0F0F0F0Fu);
-        const uint32_t xo01 = bitsel(A0[p][w] >> 4, A1[p][w], 0x0F0F0F0Fu);
-        const uint32_t xe23 = bitsel(A2[p][w], A3[p][w] << 4, 0x0F0F0F0Fu);
-        const uint32_t xo23 = bitsel(A2[p][w] >> 4, A3[p][w], 0x0F0F0F0Fu);
-        uint32_t fe01[4], fo01[4], fe23[4], fo23[4];
-        e2m1x8_to_f16x2x4(xe01, fe01);
-        e2m1x8_to_f16x2x4(xo01, fo01);
-        e2m1x8_to_f16x2x4(xe23, fe23);
-        e2m1x8_to_f16x2x4(xo23, fo23);
-        // hi products of the word's tiles first, then lo: each tile's two MMAs
-        // are then separated by the other tiles' instead of issued back to back
-        uint32_t av[4][4];
+      for (int w = 0; w < VW; ++w) {
+        uint32_t f0[4], f2[4];  // byte e of the word: channel cgb + 4w + e
+        e2m1x8_to_f16x2x4(W0[p][w], f0);
+        e2m1x8_to_f16x2x4(W2[p][w], f2);
+        // hi products of the word's two tiles first, then lo, so that a tile's
+        // two MMAs are not issued back to back into the same accumulator
+        uint32_t av[2][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          av[k][0] = h2_as_u32(__hmul2(u32_as_h2(fe01[k]), sc01[p]));
-          av[k][1] = h2_as_u32(__hmul2(u32_as_h2(fo01[k]), sc01[p]));
-          av[k][2] = h2_as_u32(__hmul2(u32_as_h2(fe23[k]), sc23[p]));
-          av[k][3] = h2_as_u32(__hmul2(u32_as_h2(fo23[k]), sc23[p]));
-          if (4 * w + k < MTILES) mma16816(o[4 * w + k], av[k], bh[p][0], bh[p][1]);
+        for (int u = 0; u < 2; ++u) {
+          av[u][0] = h2_as_u32(__hmul2(u32_as_h2(f0[2 * u]), sc01[p]));
+          av[u][1] = h2_as_u32(__hmul2(u32_as_h2(f0[2 * u + 1]), sc01[p]));
+          av[u][2] = h2_as_u32(__hmul2(u32_as_h2(f2[2 * u]), sc23[p]));
+          av[u][3] = h2_as_u32(__hmul2(u32_as_h2(f2[2 * u + 1]), sc23[p]));
+          mma16816(o[2 * w + u], av[u], bh[p][0], bh[p][1]);
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (4 * w + k < MTILES) mma16816(o[4 * w + k], av[k], bl[p][0], bl[p][1]);
+        for (int u = 0; u < 2; ++u) mma16816(o[2 * w + u], av[u], bl[p][0], bl[p][1]);
       }
   } else {
     constexpr int VW = D / 32;  // words per thread per row (D/8 one-byte channels)
@@ -376,7 +357,6 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, tq = lane & 3;
-  const int tg = C::tok(g);  // token of MMA rows g (and tg + 8 of row g + 8)
 
   int n = a.seq_lens[b];
   const int lim = min(a.max_seq_len, a.max_pages * kPage);
@@ -509,16 +489,16 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
     if constexpr (kPerToken) {
       const float* sa = reinterpret_cast<const float*>(stA + C::S_OFF);  // K scales, then V scales
       const float* sb = reinterpret_cast<const float*>(stB + C::S_OFF);
-      fA0 *= sa[tg]; fA8 *= sa[tg + 8]; vA0 = sa[kPage + tg]; vA8 = sa[kPage + tg + 8];
+      fA0 *= sa[g]; fA8 *= sa[g + 8]; vA0 = sa[kPage + g]; vA8 = sa[kPage + g + 8];
       fB0 *= sb[g]; fB8 *= sb[g + 8]; vB0 = sb[kPage + g]; vB8 = sb[kPage + g + 8];
     }
     float sA[4] = {cA[0] * fA0, cA[1] * fA0, cA[2] * fA8, cA[3] * fA8};
     float sB[4] = {cB[0] * fB0, cB[1] * fB0, cB[2] * fB8, cB[3] * fB8};
     if (nvA < kPage || nvB < kPage) {  // rare: a partial or missing page
-      if (tg >= nvA) { sA[0] = sA[1] = -INFINITY; vA0 = 0.f; }
-      if (tg + 8 >= nvA) { sA[2] = sA[3] = -INFINITY; vA8 = 0.f; }
-      if (tg >= nvB) { sB[0] = sB[1] = -INFINITY; vB0 = 0.f; }
-      if (tg + 8 >= nvB) { sB[2] = sB[3] = -INFINITY; vB8 = 0.f; }
+      if (g >= nvA) { sA[0] = sA[1] = -INFINITY; vA0 = 0.f; }
+      if (g + 8 >= nvA) { sA[2] = sA[3] = -INFINITY; vA8 = 0.f; }
+      if (g >= nvB) { sB[0] = sB[1] = -INFINITY; vB0 = 0.f; }
+      if (g + 8 >= nvB) { sB[2] = sB[3] = -INFINITY; vB8 = 0.f; }
     }
     // Lazy reference max: move it (and rescale) only when some score exceeds it
     // by more than SLACK -- rare once the first pages are seen.
@@ -603,7 +583,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   }
   {
     float* ow = red_o + warp * 8 * D;
-    const int d0 = g * (D / 8);
+    const int d0 = C::cgrp(g) * (D / 8);
 #pragma unroll
     for (int t = 0; t < MTILES; ++t) {
       ow[(2 * tq) * D + d0 + 2 * t] = o[t][0];

@@ -156,6 +156,28 @@ __device__ __forceinline__ float group_max(float v) {
   return v;
 }
 
+// NVFP4 codes of a thread's VEC values (its 16-value block shared with TPB =
+// 16 / VEC lanes): the E4M3 block scale byte sb and the E2M1 codes packed two
+// per byte, even channel in the low nibble (sb = 0 gives all-zero codes).
+template <int VEC, int TPB>
+__device__ __forceinline__ void nvfp4_codes(const float* x, float st, uint32_t& w, uint32_t& sb) {
+  const float six_st = __fmul_rn(6.0f, st);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  amax = group_max<TPB>(amax);
+  sb = f32x2_to_e4m3x2(0.0f, __fdiv_rn(amax, six_st)) & 0xFFu;
+  const float sbf = e4m3_to_f32(sb);
+  w = sbf != 0.0f ? QDiv(__fmul_rn(st, sbf)).e2m1x8<VEC>(x) : 0u;
+}
+
+// The n = 4 or 8 codes packed in w (two per byte) spread one per byte, in the
+// low nibble: bytes c0, c1, c2, c3 (| c4..c7).
+__device__ __forceinline__ uint2 spread_codes(uint32_t w) {
+  const uint32_t even = w & 0x0F0F0F0Fu, odd = (w >> 4) & 0x0F0F0F0Fu;
+  return make_uint2(prmt(even, odd, 0x5140u), prmt(even, odd, 0x7362u));
+}
+
 // Quantize one (token, kv head, side) row of D values, held by a group of TPR
 // threads with VEC values each (thread j: values j*VEC ..), and store it at
 // slot (skipped when slot < 0; flagged and skipped when out of range).
@@ -196,24 +218,104 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
       store_bytes<VEC>(blk + (size_t)side * a.P * D + (size_t)off * D + j * VEC, w);
       if (j == 0) *reinterpret_cast<float*>(blk + (size_t)2 * a.P * D + (size_t)side * 4 * a.P + 4 * off) = s;
     }
-  } else if constexpr (MODE == KVQ_NVFP4) {
+  } else if constexpr (MODE == KVQ_NVFP4) {  // keys; values go through nvfp4_values_pass
     constexpr int TPB = 16 / VEC;  // threads per 16-value block
-    const float st = *reinterpret_cast<const float*>(a.pool + (side ? kHdrVScaleOffset : kHdrKScaleOffset));
-    const float six_st = __fmul_rn(6.0f, st);
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    amax = group_max<TPB>(amax);
-    const uint32_t sb = f32x2_to_e4m3x2(0.0f, __fdiv_rn(amax, six_st)) & 0xFFu;
-    const float sbf = e4m3_to_f32(sb);
-    const float den = __fmul_rn(st, sbf);
-    uint32_t w[1] = {0u};
-    if (sbf != 0.0f) w[0] = QDiv(den).e2m1x8<VEC>(x);
+    uint32_t w[1], sb;
+    nvfp4_codes<VEC, TPB>(x, *reinterpret_cast<const float*>(a.pool + kHdrKScaleOffset), w[0], sb);
     if (active) {
-      store_bytes<VEC / 2>(blk + (size_t)side * a.P * D / 2 + (size_t)off * D / 2 + j * VEC / 2, w);
-      if ((j % TPB) == 0)
-        blk[(size_t)a.P * D + (size_t)side * a.P * D / 16 + (size_t)off * D / 16 + (j * VEC) / 16] =
-            static_cast<uint8_t>(sb);
+      store_bytes<VEC / 2>(blk + (size_t)off * D / 2 + j * VEC / 2, w);
+      if ((j % TPB) == 0) blk[(size_t)a.P * D + (size_t)off * D / 16 + (j * VEC) / 16] = static_cast<uint8_t>(sb);
+    }
+  }
+}
+
+
+// NVFP4 values: token-pair rows, byte (k, d) of a page holding channel d of
+// tokens 2k (low nibble) and 2k + 1.  A token with an even slot whose
+// successor in the batch holds the next slot stores the pair's bytes whole and
+// the successor stores nothing; every other token writes its own nibbles with
+// 32-bit atomic AND/OR (two tokens never share a nibble, so these commute),
+// e.g. the one new token of a decode step.  The successor's codes come from
+// the next row group of the same warp (a shuffle) when a warp holds two row
+// groups (TPR = 16), else through shared memory (whole CTA, one barrier).
+template <int D, int VEC, int TPR, int NTOK, int R, typename T>
+__device__ __forceinline__ void nvfp4_values_pass(const WriteArgs& a, int h, const int* slot, const uint4* raw,
+                                                  int j) {
+  constexpr int TPB = 16 / VEC;
+  constexpr int TOK = NTOK / R;
+  constexpr bool kInWarp = TPR == 16;
+  __shared__ uint32_t codes[kInWarp ? 1 : NTOK * TPR];
+  __shared__ int vslot[kInWarp ? 1 : NTOK];
+  const int g = threadIdx.x / TPR;
+  const float st = *reinterpret_cast<const float*>(a.pool + kHdrVScaleOffset);
+  uint32_t wr[R];
+  int sr[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    float x[VEC];
+    widen16<T>(raw[r], x);
+    const int s = slot[r];
+    bool active = s >= 0;
+    const int page = s >> a.log2P, off = s & (a.P - 1);
+    if (active && page >= a.num_pages) {
+      if (j == 0) set_error(a.pool, KVQ_DEVERR_SLOT_RANGE);
+      active = false;
+    }
+    uint32_t sb;
+    nvfp4_codes<VEC, TPB>(x, st, wr[r], sb);
+    sr[r] = active ? s : -1;
+    if (active && (j % TPB) == 0) {
+      uint8_t* blk = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes;
+      blk[(size_t)a.P * D + (size_t)a.P * D / 16 + (size_t)off * D / 16 + (j * VEC) / 16] = static_cast<uint8_t>(sb);
+    }
+    if constexpr (!kInWarp) {
+      const int li = g + TOK * r;
+      codes[li * TPR + j] = wr[r];
+      if (j == 0) vslot[li] = sr[r];
+    }
+  }
+  if constexpr (!kInWarp) __syncthreads();
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int s = sr[r];
+    int next, prev;
+    uint32_t other;
+    if constexpr (kInWarp) {  // lanes 0-15: row group g (even), lanes 16-31: g + 1
+      const bool lower = (threadIdx.x & 16) == 0;
+      const int up = __shfl_down_sync(0xffffffffu, s, 16), down = __shfl_up_sync(0xffffffffu, s, 16);
+      other = __shfl_down_sync(0xffffffffu, wr[r], 16);
+      next = lower ? up : -1;
+      prev = lower ? -1 : down;
+    } else {
+      const int li = g + TOK * r;
+      next = li + 1 < NTOK ? vslot[li + 1] : -1;
+      prev = li > 0 ? vslot[li - 1] : -1;
+      other = li + 1 < NTOK ? codes[(li + 1) * TPR + j] : 0u;
+    }
+    if (s < 0 || ((s & 1) && prev == s - 1)) continue;  // nothing, or written with the pair's first token
+    const int page = s >> a.log2P, off = s & (a.P - 1);
+    uint8_t* dst = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes + (size_t)a.P * D / 2 +
+                   (size_t)(off >> 1) * D + j * VEC;
+    if (!(s & 1) && next == s + 1) {
+      // even channels: my low nibbles | the successor's low nibbles << 4; odd
+      // channels: my high nibbles >> 4 | the successor's high nibbles; then
+      // interleave the bytes back into channel order
+      const uint32_t ev = bitsel(wr[r], other << 4, 0x0F0F0F0Fu);
+      const uint32_t od = bitsel(wr[r] >> 4, other, 0x0F0F0F0Fu);
+      const uint2 both = make_uint2(prmt(ev, od, 0x5140u), prmt(ev, od, 0x7362u));
+      if constexpr (VEC == 8) *reinterpret_cast<uint2*>(dst) = both;
+      else *reinterpret_cast<uint32_t*>(dst) = both.x;
+    } else {
+      const uint2 mine = spread_codes(wr[r]);
+      const int sh = 4 * (off & 1);
+      const uint32_t m = 0x0F0F0F0Fu << sh;
+      unsigned int* wd = reinterpret_cast<unsigned int*>(dst);
+      atomicAnd(wd, ~m);
+      atomicOr(wd, mine.x << sh);
+      if constexpr (VEC == 8) {
+        atomicAnd(wd + 1, ~m);
+        atomicOr(wd + 1, mine.y << sh);
+      }
     }
   }
 }
@@ -250,6 +352,12 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
     slot[r] = in ? __ldg(a.slots + token) : -1;
     raw[r] = in ? __ldg(reinterpret_cast<const uint4*>(src + (token * a.Hkv + h) * D + j * VEC))
                 : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if constexpr (MODE == KVQ_NVFP4) {
+    if (side == 1) {
+      nvfp4_values_pass<D, VEC, TPR, TOK * R, R, T>(a, h, slot, raw, j);
+      return;
+    }
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) {

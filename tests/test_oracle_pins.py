@@ -217,6 +217,38 @@ def test_per_token_head_scale_counts():
     assert oracle.block_bytes("fp8_per_tensor", P, D) // P * Hkv == 4096 // 2
 
 
+def test_nvfp4_value_bytes_pair_tokens():
+    """The pool's NVFP4 value payload pairs tokens: byte [k][d] of a page holds
+    channel d of tokens 2k (low nibble) and 2k+1, each the code quant_row gives
+    for that token alone; keys and block scales stay per token; the bytes do
+    not depend on the order the tokens are written in."""
+    P, Hkv, D = 16, 1, 128
+    rng = np.random.default_rng(5)
+    k = rng.standard_normal((P, Hkv, D)).astype(np.float32)
+    v = (rng.standard_normal((P, Hkv, D)) * 3).astype(np.float32)
+    ks = oracle.nvfp4_tensor_scale(oracle.amax(k))
+    vs = oracle.nvfp4_tensor_scale(oracle.amax(v))
+    pool = np.zeros(oracle.pool_bytes("nvfp4", 1, P, Hkv, D), np.uint8)
+    assert oracle.write("nvfp4", pool, 1, P, Hkv, D, k, v, np.arange(P, dtype=np.int32), ks, vs) == 0
+    perm = rng.permutation(P)
+    pool2 = np.zeros_like(pool)
+    assert oracle.write("nvfp4", pool2, 1, P, Hkv, D, k[perm], v[perm], perm.astype(np.int32), ks, vs) == 0
+    assert np.array_equal(pool, pool2)
+    blk = pool[256:]
+    vpay, kbs = P * D // 2, P * D
+    vbs = kbs + P * D // 16
+    for t in range(P):
+        qk, bk = oracle.quant_row("nvfp4", k[t, 0], ks)
+        qv, bv = oracle.quant_row("nvfp4", v[t, 0], vs)
+        assert np.array_equal(blk[t * D // 2:(t + 1) * D // 2], qk)                 # K row t
+        assert np.array_equal(blk[kbs + t * D // 16:kbs + (t + 1) * D // 16], bk)   # K block scales
+        assert np.array_equal(blk[vbs + t * D // 16:vbs + (t + 1) * D // 16], bv)   # V block scales
+        codes = np.empty(D, np.uint8)
+        codes[0::2], codes[1::2] = qv & 15, qv >> 4
+        pair = blk[vpay + (t // 2) * D:vpay + (t // 2 + 1) * D]
+        assert np.array_equal((pair >> (4 * (t & 1))) & 15, codes)                  # V nibbles of token t
+
+
 def test_nvfp4_two_block_worked_example():
     """Two blocks, one in [-0.7, 0.7], one in [-5.5, 5.5], each get their own scale
     and both map their max to (about) 6 and use many grid points."""

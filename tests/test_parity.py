@@ -70,6 +70,38 @@ def test_write_bit_exact(mode, D, io):
 
 
 @pytest.mark.parametrize("io", ["f16", "f32"])
+@pytest.mark.parametrize("order", ["reversed", "random", "split_calls", "one_by_one"])
+def test_write_nvfp4_values_any_batch_order(order, io):
+    """NVFP4 values share a byte between tokens 2k and 2k+1: written as whole
+    pairs when the two tokens are neighbours in the batch, else nibble by
+    nibble.  Any batch order, split over any number of calls, must give the
+    oracle's bytes."""
+    K = kvq()
+    c = make_case(small_workload("nvfp4", io=io), [1, 15, 16, 17, 100, 333], slack_pages=2)
+    cache = gpu_cache(c)
+    kd, vd = _dev(c.k), _dev(c.v)
+    gpu_calibrate(cache, kd, vd)
+    n = len(c.slots)
+    rng = np.random.default_rng(11)
+    if order == "reversed":
+        calls = [np.arange(n)[::-1]]
+    elif order == "random":
+        calls = [rng.permutation(n)]
+    elif order == "split_calls":               # every other token, then the rest, in two calls
+        calls = [np.arange(0, n, 2), np.arange(1, n, 2)]
+    else:
+        calls = [np.array([i]) for i in rng.permutation(n)[:40]] + [np.arange(n)]
+    for idx in calls:
+        idx = np.ascontiguousarray(idx)
+        K.kvq_quantize_write(cache, _dev(c.k[idx]), _dev(c.v[idx]), _dev(c.slots[idx]))
+    assert K.kvq_cache_read_errors(cache) == 0
+    got = cache.pool.cpu().numpy()
+    ref = oracle_pool(c)
+    diff = np.flatnonzero(got[256:] != ref[256:])
+    assert diff.size == 0, f"{diff.size} bytes differ, first at pool offset {256 + diff[0]}"
+
+
+@pytest.mark.parametrize("io", ["f16", "f32"])
 def test_write_kvarn_bit_exact(io):
     K = kvq()
     c = make_case(small_workload("kvarn_k4v2_g128", io=io), KVARN_LENS, slack_pages=1)
