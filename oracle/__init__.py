@@ -31,6 +31,8 @@ MODES = {
     "int8_per_token_head": 2,
     "fp8_per_token_head": 3,
     "nvfp4": 4,
+    "int4_per_token_head": 5,
+    "nvfp4_4over6": 6,
     "kvarn_k4v2_g128": 16,
 }
 
@@ -65,6 +67,7 @@ def lib():
             "kvqo_e2m1_decode": (ctypes.c_double, [ctypes.c_uint8]),
             "kvqo_e2m1_encode": (ctypes.c_uint8, [ctypes.c_float]),
             "kvqo_int8_encode": (ctypes.c_int, [ctypes.c_float]),
+            "kvqo_int4_encode": (ctypes.c_int, [ctypes.c_float]),
             "kvqo_fp8_tensor_scale": (ctypes.c_float, [ctypes.c_float]),
             "kvqo_nvfp4_tensor_scale": (ctypes.c_float, [ctypes.c_float]),
             "kvqo_amax": (ctypes.c_float, [f32p, ctypes.c_size_t]),
@@ -72,6 +75,9 @@ def lib():
             "kvqo_quant_row_int8_pth": (None, [f32p, ctypes.c_int, i8p, f32p]),
             "kvqo_quant_row_fp8_pth": (None, [f32p, ctypes.c_int, u8p, f32p]),
             "kvqo_quant_row_nvfp4": (None, [f32p, ctypes.c_int, ctypes.c_float, u8p, u8p]),
+            "kvqo_quant_row_int4_pth": (None, [f32p, ctypes.c_int, u8p, f32p]),
+            "kvqo_quant_row_nvfp4_4over6": (None, [f32p, ctypes.c_int, ctypes.c_float, u8p, u8p, u8p]),
+            "kvqo_nvfp4_block_sse": (ctypes.c_float, [f32p, u8p, ctypes.c_float]),
             "kvqo_inv_sqrt128": (ctypes.c_float, []),
             "kvqo_fwht128_f32": (None, [f32p]),
             "kvqo_sum128": (ctypes.c_float, [f32p]),
@@ -132,6 +138,10 @@ def int8_encode(v: float) -> int:
     return lib().kvqo_int8_encode(float(v))
 
 
+def int4_encode(v: float) -> int:
+    return lib().kvqo_int4_encode(float(v))
+
+
 def fp8_tensor_scale(amax: float) -> float:
     return lib().kvqo_fp8_tensor_scale(float(amax))
 
@@ -149,7 +159,7 @@ def tensor_scale(mode, amax_value: float) -> float:
     m = mode_id(mode)
     if m == 1:
         return fp8_tensor_scale(amax_value)
-    if m == 4:
+    if m in (4, 6):
         return nvfp4_tensor_scale(amax_value)
     return 1.0
 
@@ -180,7 +190,36 @@ def quant_row(mode, x: np.ndarray, tensor_scale_value: float = 1.0):
         L.kvqo_quant_row_nvfp4(_p(x, ctypes.c_float), D, tensor_scale_value, _p(q, ctypes.c_uint8),
                                _p(bs, ctypes.c_uint8))
         return q, bs
+    if m == 5:
+        q = np.zeros(D // 2, np.uint8)
+        s = np.zeros(1, np.float32)
+        L.kvqo_quant_row_int4_pth(_p(x, ctypes.c_float), D, _p(q, ctypes.c_uint8), _p(s, ctypes.c_float))
+        return q, s.view(np.uint8)
+    if m == 6:
+        q, bs, _ = nvfp4_4over6_row(x, tensor_scale_value)
+        return q, bs
     raise ValueError(f"no row quantizer for mode {mode}")
+
+
+def nvfp4_4over6_row(x: np.ndarray, s_t: float):
+    """nvfp4_4over6 coding of one D-vector: (packed codes, block scales, the
+    choice per block: 6 for the max/6 scale, 4 for the max/4 scale)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    D = x.size
+    q = np.zeros(D // 2, np.uint8)
+    bs = np.zeros(D // 16, np.uint8)
+    ch = np.zeros(D // 16, np.uint8)
+    lib().kvqo_quant_row_nvfp4_4over6(_p(x, ctypes.c_float), D, s_t, _p(q, ctypes.c_uint8),
+                                      _p(bs, ctypes.c_uint8), _p(ch, ctypes.c_uint8))
+    return q, bs, ch
+
+
+def nvfp4_block_sse(x: np.ndarray, codes: np.ndarray, den: float) -> float:
+    """The fp32 squared reconstruction error the 4over6 choice compares."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    assert x.size == 16 and c.size == 16
+    return lib().kvqo_nvfp4_block_sse(_p(x, ctypes.c_float), _p(c, ctypes.c_uint8), den)
 
 
 # ---- KVarN --------------------------------------------------------------------

@@ -121,6 +121,17 @@ int kvqo_int8_encode(float v) {
   return (int)r;
 }
 
+/* INT4 code [P4 "scale 和数据放在一起" names int4_per_token_head and its
+ * head_size/2 bytes per head, nothing more]: read as the 4-bit analogue of
+ * the int8 rule, q = clip(round(v), -7, 7), round half-to-even; the code is
+ * stored as a 4-bit two's-complement nibble. */
+int kvqo_int4_encode(float v) {
+  float r = rintf(v);
+  if (r > 7.0f) r = 7.0f;
+  if (r < -7.0f) r = -7.0f;
+  return (int)r;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Scales                                                                     */
 /* ------------------------------------------------------------------------- */
@@ -189,6 +200,73 @@ void kvqo_quant_row_nvfp4(const float* x, int D, float s_t, uint8_t* packed, uin
     for (i = 0; i < 16; i++) codes[i] = (sbf == 0.0f) ? 0 : kvqo_e2m1_encode(x[16 * b + i] / den);
     for (i = 0; i < 8; i++) packed[8 * b + i] = (uint8_t)(codes[2 * i] | (codes[2 * i + 1] << 4));
   }
+}
+
+/* Squared reconstruction error of one 16-value NVFP4 block, fp32: x^_i =
+ * E2M1value(code_i) * den, e_i = (x_i - x^_i)^2, summed as a pairwise tree of
+ * neighbours ((e0 + e1) + (e2 + e3)) + ... , each operation rounded once. */
+float kvqo_nvfp4_block_sse(const float* x, const uint8_t* codes, float den) {
+  float e[16];
+  int i, w;
+  for (i = 0; i < 16; i++) {
+    float xh = (float)kvqo_e2m1_decode(codes[i]) * den;
+    float d = x[i] - xh;
+    e[i] = d * d;
+  }
+  for (w = 1; w < 16; w <<= 1)
+    for (i = 0; i < 16; i += 2 * w) e[i] = e[i] + e[i + w];
+  return e[0];
+}
+
+/* nvfp4_4over6 [P5 "用一组数直观看缩放的作用", last paragraph: a max-based scale
+ * is not always the one with the smallest reconstruction error; the mode picks,
+ * per block, between scales of the max/6 and the max/4 kind by reconstruction
+ * error].  Both candidates are plain NVFP4 blocks under the same s_t:
+ *   max/6: s_b = E4M3(amax_b / (6 s_t))  (block max lands near code 6)
+ *   max/4: s_b = E4M3(amax_b / (4 s_t))  (block max lands near code 4)
+ * each coded as in kvqo_quant_row_nvfp4; the block keeps the candidate with the
+ * smaller kvqo_nvfp4_block_sse, max/6 on a tie.  Storage and reconstruction are
+ * NVFP4's. */
+void kvqo_quant_row_nvfp4_4over6(const float* x, int D, float s_t, uint8_t* packed, uint8_t* bs,
+                                 uint8_t* choice_out) {
+  float six_st = 6.0f * s_t, four_st = 4.0f * s_t;
+  int b, i, c;
+  for (b = 0; b < D / 16; b++) {
+    const float* xb = x + 16 * b;
+    float amax = 0.0f, err[2];
+    uint8_t sb[2], codes[2][16];
+    for (i = 0; i < 16; i++) amax = fmaxf(amax, fabsf(xb[i]));
+    for (c = 0; c < 2; c++) {
+      float sbf, den;
+      sb[c] = kvqo_e4m3_encode(amax / (c == 0 ? six_st : four_st));
+      sbf = (float)kvqo_e4m3_decode(sb[c]);
+      den = s_t * sbf;
+      for (i = 0; i < 16; i++) codes[c][i] = (sbf == 0.0f) ? 0 : kvqo_e2m1_encode(xb[i] / den);
+      err[c] = kvqo_nvfp4_block_sse(xb, codes[c], den);
+    }
+    c = err[1] < err[0] ? 1 : 0;
+    bs[b] = sb[c];
+    if (choice_out) choice_out[b] = (uint8_t)(c ? 4 : 6);
+    for (i = 0; i < 8; i++) packed[8 * b + i] = (uint8_t)(codes[c][2 * i] | (codes[c][2 * i + 1] << 4));
+  }
+}
+
+/* int4_per_token_head [P4 "scale 和数据放在一起": per token and kv head a
+ * dynamic fp32 scale stored in the page after head_size/2 bytes of data]:
+ * the per-token-head rule of [P1 sec. 2.2] with MAX = 7 (the largest
+ * magnitude of the symmetric 4-bit range, as 127 is for int8) and [P3]'s
+ * clamp of the max at 1e-8: s = max(max|x|, 1e-8) / 7, q = clip(rint(x/s),
+ * -7, 7).  Two codes per byte, the even head_dim index in the low nibble. */
+void kvqo_quant_row_int4_pth(const float* x, int D, uint8_t* packed, float* s_out) {
+  float amax = 0.0f, s;
+  int d;
+  for (d = 0; d < D; d++) amax = fmaxf(amax, fabsf(x[d]));
+  s = fmaxf(amax, 1e-8f) / 7.0f;
+  for (d = 0; d < D; d += 2) {
+    int lo = kvqo_int4_encode(x[d] / s) & 15, hi = kvqo_int4_encode(x[d + 1] / s) & 15;
+    packed[d / 2] = (uint8_t)(lo | (hi << 4));
+  }
+  *s_out = s;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -337,11 +415,13 @@ void kvqo_hadamard_f64(double* x, int n) {
 /*   pool = 256-byte header, then one block per (page, kv head), page-major.    */
 /*   FP8 per-tensor : K[P][D] e4m3 | V[P][D] e4m3                               */
 /*   INT8/FP8 PTH   : K[P][D] | V[P][D] | K scale[P] f32 | V scale[P] f32       */
-/*   NVFP4          : K[P][D/2] | V[P/2][D] | K s_b[P][D/16] | V s_b[P][D/16]   */
+/*   NVFP4, 4over6  : K[P][D/2] | V[P/2][D] | K s_b[P][D/16] | V s_b[P][D/16]   */
+/*   INT4 PTH       : K[P][D/2] | V[P/2][D] | K scale[P] f32 | V scale[P] f32   */
 /*   KVarN (P=D=128): K[128][64] 4-bit | V[128][32] 2-bit |                      */
 /*                    K scale[D] zero[D] c[D] r[P] | V scale[P] zero[P] r[P] c[D] */
-/* 4-bit: even index in the low nibble (NVFP4 V: byte [k][d] holds channel d  */
-/* of tokens 2k (low nibble) and 2k+1); 2-bit: element 4i+j in bits 2j..2j+1.  */
+/* 4-bit: even index in the low nibble (4-bit V of NVFP4 and INT4: byte [k][d] */
+/* holds channel d of tokens 2k (low nibble) and 2k+1); 2-bit: element 4i+j in */
+/* bits 2j..2j+1.                                                              */
 /* ------------------------------------------------------------------------- */
 size_t kvqo_header_bytes(void) { return 256; }
 
@@ -350,7 +430,9 @@ size_t kvqo_block_bytes(int mode, int P, int D) {
     case KVQO_FP8_PER_TENSOR: return (size_t)2 * P * D;
     case KVQO_INT8_PER_TOKEN_HEAD:
     case KVQO_FP8_PER_TOKEN_HEAD: return (size_t)2 * P * D + (size_t)8 * P;
-    case KVQO_NVFP4: return (size_t)P * D + (size_t)P * D / 8;
+    case KVQO_NVFP4:
+    case KVQO_NVFP4_4OVER6: return (size_t)P * D + (size_t)P * D / 8;
+    case KVQO_INT4_PER_TOKEN_HEAD: return (size_t)P * D + (size_t)8 * P;
     case KVQO_KVARN_K4V2_G128:
       return (size_t)P * D / 2 + (size_t)P * D / 4 + (size_t)4 * (3 * D + P) + (size_t)4 * (3 * P + D);
     default: return 0;
@@ -367,6 +449,16 @@ static uint8_t* block_at(uint8_t* pool, int mode, int P, int Hkv, int D, int64_t
 
 static void put_f32(uint8_t* p, float v) { memcpy(p, &v, 4); }
 static float get_f32(const uint8_t* p) { float v; memcpy(&v, p, 4); return v; }
+
+/* Token `off`'s value codes (packed two per byte, even channel low) into its
+ * nibble of each byte of its token pair's row. */
+static void put_pair_nibbles(uint8_t* pair, int D, const uint8_t* packed, int off) {
+  int d, sh = 4 * (off & 1);
+  for (d = 0; d < D; d++) {
+    uint8_t code = (d & 1) ? (uint8_t)(packed[d / 2] >> 4) : (uint8_t)(packed[d / 2] & 15);
+    pair[d] = (uint8_t)((pair[d] & ~(15 << sh)) | (code << sh));
+  }
+}
 
 static void write_kvarn_side(uint8_t* blk, int is_value, const uint8_t* codes, const float* scale,
                              const float* zero, const float* r, const float* c) {
@@ -457,20 +549,22 @@ int kvqo_write(int mode, uint8_t* pool, int num_pages, int P, int Hkv, int D, co
             kvqo_quant_row_fp8_pth(x, D, blk + (size_t)side * P * D + (size_t)off * D, &s);
             put_f32(blk + (size_t)2 * P * D + (size_t)side * 4 * P + 4 * off, s);
             break;
-          case KVQO_NVFP4: {
-            uint8_t* bs = blk + (size_t)P * D + (size_t)side * P * D / 16 + (size_t)off * D / 16;
-            if (!side) {
-              kvqo_quant_row_nvfp4(x, D, k_scale, blk + (size_t)off * D / 2, bs);
-            } else {  /* V: this token's nibble of each byte of its token pair's row */
-              uint8_t packed[512], *pair = blk + (size_t)P * D / 2 + (size_t)(off / 2) * D;
-              int d, sh = 4 * (off & 1);
-              if (D > 1024) return -1;
-              kvqo_quant_row_nvfp4(x, D, v_scale, packed, bs);
-              for (d = 0; d < D; d++) {
-                uint8_t code = (d & 1) ? (uint8_t)(packed[d / 2] >> 4) : (uint8_t)(packed[d / 2] & 15);
-                pair[d] = (uint8_t)((pair[d] & ~(15 << sh)) | (code << sh));
-              }
+          case KVQO_NVFP4:
+          case KVQO_NVFP4_4OVER6:
+          case KVQO_INT4_PER_TOKEN_HEAD: {
+            /* K: row `off` of [P][D/2]; V: this token's nibbles of its token pair's row */
+            uint8_t packed[512];
+            uint8_t* dst = side ? packed : blk + (size_t)off * D / 2;
+            if (D > 1024) return -1;
+            if (mode == KVQO_INT4_PER_TOKEN_HEAD) {
+              kvqo_quant_row_int4_pth(x, D, dst, &s);
+              put_f32(blk + (size_t)P * D + (size_t)side * 4 * P + 4 * off, s);
+            } else {
+              uint8_t* bs = blk + (size_t)P * D + (size_t)side * P * D / 16 + (size_t)off * D / 16;
+              if (mode == KVQO_NVFP4) kvqo_quant_row_nvfp4(x, D, side ? v_scale : k_scale, dst, bs);
+              else kvqo_quant_row_nvfp4_4over6(x, D, side ? v_scale : k_scale, dst, bs, NULL);
             }
+            if (side) put_pair_nibbles(blk + (size_t)P * D / 2 + (size_t)(off / 2) * D, D, packed, off);
             break;
           }
           default: return -1;
@@ -506,7 +600,18 @@ int kvqo_dequant_row(int mode, const uint8_t* pool, int num_pages, int P, int Hk
         out[d] = s * (mode == KVQO_INT8_PER_TOKEN_HEAD ? (double)(int8_t)row[d] : kvqo_e4m3_decode(row[d]));
       return 0;
     }
-    case KVQO_NVFP4: {
+    case KVQO_INT4_PER_TOKEN_HEAD: {
+      const uint8_t* row = blk + (size_t)t * D / 2;                               /* K */
+      const uint8_t* pair = blk + (size_t)P * D / 2 + (size_t)(t / 2) * D;         /* V */
+      double s = get_f32(blk + (size_t)P * D + (size_t)side * 4 * P + 4 * t);
+      for (d = 0; d < D; d++) {
+        int nib = side ? (pair[d] >> (4 * (t & 1))) & 15 : ((d & 1) ? row[d / 2] >> 4 : row[d / 2] & 15);
+        out[d] = s * (double)(nib >= 8 ? nib - 16 : nib);
+      }
+      return 0;
+    }
+    case KVQO_NVFP4:
+    case KVQO_NVFP4_4OVER6: {
       double st = side ? v_scale : k_scale;
       const uint8_t* row = blk + (size_t)t * D / 2;                               /* K */
       const uint8_t* pair = blk + (size_t)P * D / 2 + (size_t)(t / 2) * D;         /* V */

@@ -28,6 +28,8 @@ enum {
   KVQO_INT8_PER_TOKEN_HEAD = 2,
   KVQO_FP8_PER_TOKEN_HEAD = 3,
   KVQO_NVFP4 = 4,
+  KVQO_INT4_PER_TOKEN_HEAD = 5,
+  KVQO_NVFP4_4OVER6 = 6,
   KVQO_KVARN_K4V2_G128 = 16
 };
 
@@ -37,6 +39,7 @@ uint8_t kvqo_e4m3_encode(float v);          /* RNE, saturating to +-448 */
 double kvqo_e2m1_decode(uint8_t nibble);
 uint8_t kvqo_e2m1_encode(float v);          /* RNE, saturating to +-6 */
 int kvqo_int8_encode(float v);              /* clamp(rint(v), -127, 127) */
+int kvqo_int4_encode(float v);              /* clamp(rint(v), -7, 7) */
 
 /* ---- scales ---- */
 float kvqo_fp8_tensor_scale(float amax);    /* amax/448, 1.0 for an all-zero tensor */
@@ -48,6 +51,13 @@ void kvqo_quant_row_fp8_pt(const float* x, int D, float s, uint8_t* q);
 void kvqo_quant_row_int8_pth(const float* x, int D, int8_t* q, float* s);
 void kvqo_quant_row_fp8_pth(const float* x, int D, uint8_t* q, float* s);
 void kvqo_quant_row_nvfp4(const float* x, int D, float s_t, uint8_t* packed, uint8_t* block_scales);
+void kvqo_quant_row_int4_pth(const float* x, int D, uint8_t* packed, float* s);
+/* nvfp4_4over6: per block, the max/6 or the max/4 block scale, whichever
+ * reconstructs the block with the smaller fp32 sum of squared errors;
+ * choice_out (may be NULL) gets 6 or 4 per block. */
+void kvqo_quant_row_nvfp4_4over6(const float* x, int D, float s_t, uint8_t* packed, uint8_t* block_scales,
+                                 uint8_t* choice_out);
+float kvqo_nvfp4_block_sse(const float* x, const uint8_t* codes, float den); /* 16 values */
 
 /* ---- KVarN k4v2 g128 pieces ---- */
 float kvqo_inv_sqrt128(void);

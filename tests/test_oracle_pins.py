@@ -123,6 +123,45 @@ def test_int8_pth_row_properties():
     assert (q == 0).all() and sb.view(np.float32)[0] == np.float32(np.float32(1e-8) / np.float32(127))
 
 
+# --------------------------------------------------------------------------- INT4
+def test_int4_encoder_half_even_and_clip():
+    assert [oracle.int4_encode(x) for x in (0.5, 1.5, 2.5, -2.5, -0.5, 6.5, 7.4, 7.6, 100.0, -100.0)] \
+        == [0, 2, 2, -2, 0, 6, 7, 7, 7, -7]
+
+
+def _nibbles(q):
+    """Packed bytes -> signed 4-bit codes (even index from the low nibble)."""
+    n = np.stack([q & 15, q >> 4], 1).reshape(-1).astype(np.int64)
+    return np.where(n >= 8, n - 16, n)
+
+
+def test_int4_pth_row_properties():
+    """s = fp32(max|x|)/7; codes are numpy's half-even round of the fp32
+    quotient, clipped to +-7; the row max maps to +-7; error <= s/2."""
+    rng = np.random.default_rng(4)
+    for _ in range(200):
+        x = (rng.standard_normal(32) * rng.uniform(1e-3, 50)).astype(np.float32)
+        q, sb = oracle.quant_row("int4_per_token_head", x)
+        s = np.float32(sb.view(np.float32)[0])
+        assert s == np.float32(np.float32(np.abs(x).max()) / np.float32(7.0))
+        codes = _nibbles(q)
+        ref = np.clip(np.round(x / s), -7, 7).astype(np.int64)   # fp32 quotient, half-even
+        assert np.array_equal(codes, ref)
+        assert np.abs(codes).max() == 7
+        assert np.abs(codes * np.float64(s) - x).max() <= float(s) / 2 * (1 + 1e-6) + 1e-12
+    q, sb = oracle.quant_row("int4_per_token_head", np.zeros(32, np.float32))
+    assert (q == 0).all() and sb.view(np.float32)[0] == np.float32(np.float32(1e-8) / np.float32(7))
+
+
+def test_int4_pth_page_bytes():
+    """The page's per-token-head content formula: int4 keeps head_size/2 bytes
+    of data per side plus the two fp32 scales."""
+    g = _kv("per_token_head_bytes.txt")
+    P, D = 16, int(g["head_size"])
+    assert oracle.block_bytes("int8_per_token_head", P, D) == P * g["int8_bytes"]
+    assert oracle.block_bytes("int4_per_token_head", P, D) == P * g["int4_bytes"]
+
+
 def test_fake_quant_bytes_and_ratio():
     """The page's printed byte counts and ratio, from the oracle's page layout."""
     g = _kv("fake_quant_int8.txt")
@@ -217,32 +256,34 @@ def test_per_token_head_scale_counts():
     assert oracle.block_bytes("fp8_per_tensor", P, D) // P * Hkv == 4096 // 2
 
 
-def test_nvfp4_value_bytes_pair_tokens():
-    """The pool's NVFP4 value payload pairs tokens: byte [k][d] of a page holds
+@pytest.mark.parametrize("mode", ["nvfp4", "nvfp4_4over6", "int4_per_token_head"])
+def test_4bit_value_bytes_pair_tokens(mode):
+    """The pool's 4-bit value payload pairs tokens: byte [k][d] of a page holds
     channel d of tokens 2k (low nibble) and 2k+1, each the code quant_row gives
-    for that token alone; keys and block scales stay per token; the bytes do
-    not depend on the order the tokens are written in."""
+    for that token alone; keys and scales stay per token; the bytes do not
+    depend on the order the tokens are written in."""
     P, Hkv, D = 16, 1, 128
     rng = np.random.default_rng(5)
     k = rng.standard_normal((P, Hkv, D)).astype(np.float32)
     v = (rng.standard_normal((P, Hkv, D)) * 3).astype(np.float32)
-    ks = oracle.nvfp4_tensor_scale(oracle.amax(k))
-    vs = oracle.nvfp4_tensor_scale(oracle.amax(v))
-    pool = np.zeros(oracle.pool_bytes("nvfp4", 1, P, Hkv, D), np.uint8)
-    assert oracle.write("nvfp4", pool, 1, P, Hkv, D, k, v, np.arange(P, dtype=np.int32), ks, vs) == 0
+    ks = oracle.tensor_scale(mode, oracle.amax(k))
+    vs = oracle.tensor_scale(mode, oracle.amax(v))
+    pool = np.zeros(oracle.pool_bytes(mode, 1, P, Hkv, D), np.uint8)
+    assert oracle.write(mode, pool, 1, P, Hkv, D, k, v, np.arange(P, dtype=np.int32), ks, vs) == 0
     perm = rng.permutation(P)
     pool2 = np.zeros_like(pool)
-    assert oracle.write("nvfp4", pool2, 1, P, Hkv, D, k[perm], v[perm], perm.astype(np.int32), ks, vs) == 0
+    assert oracle.write(mode, pool2, 1, P, Hkv, D, k[perm], v[perm], perm.astype(np.int32), ks, vs) == 0
     assert np.array_equal(pool, pool2)
     blk = pool[256:]
     vpay, kbs = P * D // 2, P * D
-    vbs = kbs + P * D // 16
+    sw = 4 if mode == "int4_per_token_head" else D // 16     # scale bytes per token and side
+    vbs = kbs + P * sw
     for t in range(P):
-        qk, bk = oracle.quant_row("nvfp4", k[t, 0], ks)
-        qv, bv = oracle.quant_row("nvfp4", v[t, 0], vs)
+        qk, bk = oracle.quant_row(mode, k[t, 0], ks)
+        qv, bv = oracle.quant_row(mode, v[t, 0], vs)
         assert np.array_equal(blk[t * D // 2:(t + 1) * D // 2], qk)                 # K row t
-        assert np.array_equal(blk[kbs + t * D // 16:kbs + (t + 1) * D // 16], bk)   # K block scales
-        assert np.array_equal(blk[vbs + t * D // 16:vbs + (t + 1) * D // 16], bv)   # V block scales
+        assert np.array_equal(blk[kbs + t * sw:kbs + (t + 1) * sw], bk)             # K scale(s)
+        assert np.array_equal(blk[vbs + t * sw:vbs + (t + 1) * sw], bv)             # V scale(s)
         codes = np.empty(D, np.uint8)
         codes[0::2], codes[1::2] = qv & 15, qv >> 4
         pair = blk[vpay + (t // 2) * D:vpay + (t // 2 + 1) * D]
@@ -283,6 +324,107 @@ def test_nvfp4_error_bound_random():
             xh = np.array([oracle.e2m1_decode(int(c)) for c in codes[16 * b:16 * b + 16]]) * den
             # half the widest E2M1 gap (4 -> 6) times the block denominator, plus clipping
             assert np.abs(xh - seg).max() <= den + max(0.0, np.abs(seg).max() - 6 * den) + 1e-7
+
+
+# --------------------------------------------------------------------------- NVFP4 4over6
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e2m1_brute(y: float) -> int:
+    """Nearest E2M1 code by search over the value set; a tie takes the even code."""
+    a = min(abs(y), 6.0)
+    d = np.abs(_E2M1_GRID - a)
+    best = np.flatnonzero(d == d.min())
+    mag = int(best[0] if len(best) == 1 or best[0] % 2 == 0 else best[1])
+    return mag | (8 if math.copysign(1.0, y) < 0 else 0)
+
+
+def _e4m3_torch(v: np.float32) -> int:
+    """E4M3 code of a non-negative fp32 by torch's float8 cast (saturated at 448)."""
+    v = min(float(v), 448.0)
+    return int(torch.tensor([v], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+
+
+def _candidate(xb: np.ndarray, st: np.float32, c: float):
+    """One 4over6 candidate of a 16-value block, computed apart from the oracle:
+    torch's E4M3 cast for the block scale, a search over the E2M1 value set for
+    the codes, and the fp64 squared error of the reconstruction."""
+    amax = np.float32(np.abs(xb).max())
+    sb = _e4m3_torch(np.float32(amax / np.float32(np.float32(c) * st)))
+    sbf = np.float32(oracle.e4m3_decode(sb))
+    den = np.float32(st * sbf)
+    codes = [0] * 16 if sbf == 0 else [_e2m1_brute(float(np.float32(v / den))) for v in xb]
+    xh = np.array([oracle.e2m1_decode(cc) for cc in codes]) * float(den)
+    return sb, codes, float(np.sum((xh - xb.astype(np.float64)) ** 2)), den
+
+
+def test_nvfp4_4over6_isolated_outlier_worked_example():
+    """The page's case for 4over6: one outlier sets the block max and the other
+    15 values lose precision under the max/6 scale.  Block: one 6.0 and fifteen
+    2.5 with s_t = 2^-8, so s_b = 256 (max/6, divisor 1) or 384 (max/4, divisor
+    1.5), both exact in E4M3.  max/6: 2.5 -> 2 (tie to even), squared error
+    15 * 0.25 = 3.75.  max/4: 6 -> 4 (exact), 2.5 / 1.5 -> 1.5 (reconstructs
+    2.25), squared error 15 * 0.0625 = 0.9375.  max/4 wins."""
+    x = np.array([6.0] + [2.5] * 15, np.float32)
+    st = 2.0 ** -8
+    q, bs, ch = oracle.nvfp4_4over6_row(np.tile(x, 8), st)
+    assert (ch == 4).all()
+    assert oracle.e4m3_decode(bs[0]) == 384.0
+    codes = np.stack([q & 15, q >> 4], 1).reshape(-1)[:16]
+    assert codes[0] == 0b110 and (codes[1:] == 0b011).all()        # 4.0 and 1.5
+    c6 = [0b111] + [0b100] * 15                                     # 6.0 and 2.0 (tie 2.5 -> 2)
+    assert oracle.nvfp4_block_sse(x, np.array(c6, np.uint8), 1.0) == 3.75
+    assert oracle.nvfp4_block_sse(x, codes.astype(np.uint8), 1.5) == 0.9375
+    # the plain NVFP4 mode keeps the max/6 coding of the same block
+    qn, bn = oracle.quant_row("nvfp4", np.tile(x, 8), st)
+    assert oracle.e4m3_decode(bn[0]) == 256.0
+    assert list(np.stack([qn & 15, qn >> 4], 1).reshape(-1)[:16]) == c6
+
+
+def test_nvfp4_4over6_grid_blocks():
+    """A block on the max/6 grid reconstructs exactly under max/6 and keeps it;
+    a block on the max/4 grid reconstructs exactly only under max/4."""
+    st = 2.0 ** -8                                                  # divisors 1 and 1.5 as above
+    on6 = np.array([6, -4, 3, 2, 1.5, 1, 0.5, 0, -6, 4, -3, -2, -1.5, -1, -0.5, 0], np.float32)
+    on4 = (np.array([4, -3, 2, 1.5, 1, 0.5, 0, -4, 3, -2, -1.5, -1, -0.5, 0, 4, 3], np.float32) * 1.5)
+    for blk, want in ((on6, 6), (on4, 4)):
+        q, bs, ch = oracle.nvfp4_4over6_row(np.tile(blk, 8), st)
+        assert (ch == want).all()
+        den = float(np.float32(st) * np.float32(oracle.e4m3_decode(bs[0])))
+        codes = np.stack([q & 15, q >> 4], 1).reshape(-1)[:16]
+        assert np.array_equal(np.array([oracle.e2m1_decode(c) for c in codes]) * den, blk.astype(np.float64))
+
+
+def test_nvfp4_4over6_matches_brute_force():
+    """Random blocks (normal, with and without an outlier): the oracle's block
+    scale, codes and choice equal an independent computation of both
+    candidates wherever their fp64 errors are not within rounding of a tie, and
+    the chosen reconstruction is never worse than max/6 beyond rounding."""
+    rng = np.random.default_rng(21)
+    n4 = n6 = 0
+    for trial in range(300):
+        x = rng.standard_normal(128).astype(np.float32) * np.float32(rng.uniform(0.05, 30))
+        if trial % 2:
+            x[rng.integers(0, 128, 4)] *= np.float32(rng.uniform(3, 12))
+        st = np.float32(oracle.nvfp4_tensor_scale(oracle.amax(x) * rng.uniform(1.0, 2.0)))
+        q, bs, ch = oracle.nvfp4_4over6_row(x, float(st))
+        codes = np.stack([q & 15, q >> 4], 1).reshape(-1)
+        for b in range(8):
+            xb = x[16 * b:16 * b + 16]
+            sb6, c6, e6, _ = _candidate(xb, st, 6.0)
+            sb4, c4, e4, _ = _candidate(xb, st, 4.0)
+            got = list(codes[16 * b:16 * b + 16])
+            if ch[b] == 6:
+                assert (bs[b], got) == (sb6, c6)
+                n6 += 1
+            else:
+                assert (bs[b], got) == (sb4, c4)
+                n4 += 1
+            if abs(e4 - e6) > 1e-5 * max(e4, e6):
+                assert ch[b] == (4 if e4 < e6 else 6), (trial, b, e4, e6)
+            chosen = e4 if ch[b] == 4 else e6
+            assert chosen <= e6 * (1 + 1e-5) + 1e-30
+    assert n4 > 100 and n6 > 100                                    # both choices exercised
 
 
 # --------------------------------------------------------------------------- KVarN
@@ -398,7 +540,8 @@ def _dequant_seq(mode, w, lay, pool, b, ks=1.0, vs=1.0):
     return K, V
 
 
-MODES_SMALL = ["fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nvfp4"]
+MODES_SMALL = ["fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nvfp4", "int4_per_token_head",
+               "nvfp4_4over6"]
 
 
 @pytest.mark.parametrize("mode", MODES_SMALL + ["kvarn_k4v2_g128"])
