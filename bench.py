@@ -35,7 +35,14 @@ METRIC = "decode-attn HBM GB/s (packed KV+scales) & % of peak; quantize-write GB
 DEFAULT_WORKLOAD = "nvfp4_b32_s32768"
 L2_BYTES = 129 * 2 ** 20
 BYTES_PER_TOKEN_HEAD = {"fp8_per_tensor": 256, "int8_per_token_head": 264, "fp8_per_token_head": 264,
-                        "nvfp4": 144, "kvarn_k4v2_g128": 128}
+                        "nvfp4": 144, "int4_per_token_head": 136, "nvfp4_4over6": 144, "kvarn_k4v2_g128": 128}
+TENSOR_SCALED = ("fp8_per_tensor", "nvfp4", "nvfp4_4over6")
+# mode variants of a workload: the same shapes and inputs, another quantization mode
+VARIANTS = {
+    "pth_b64_u1k_32k:fp8": ("pth_b64_u1k_32k", "fp8_per_token_head"),
+    "pth_b64_u1k_32k:int4": ("pth_b64_u1k_32k", "int4_per_token_head"),
+    "nvfp4_b32_s32768:4over6": ("nvfp4_b32_s32768", "nvfp4_4over6"),
+}
 
 
 def measured_peaks():
@@ -52,7 +59,7 @@ def bytes_per_token_head(w: wl.Workload) -> float:
 
 
 def decode_bytes(w: wl.Workload, lens: np.ndarray) -> int:
-    scale_bytes = 8 if w.mode in ("fp8_per_tensor", "nvfp4") else 0
+    scale_bytes = 8 if w.mode in TENSOR_SCALED else 0
     return wl.decode_bytes(w, lens, bytes_per_token_head(w), scale_bytes)
 
 
@@ -124,7 +131,7 @@ class GpuWorkload:
             self.step_slots = self.slots.index_select(0, tidx).contiguous()
 
     def calibrate(self):
-        if self.w.mode in ("fp8_per_tensor", "nvfp4"):
+        if self.w.mode in TENSOR_SCALED:
             self.kvq.kvq_tensor_amax(self.K, self.amax[0:1])
             self.kvq.kvq_tensor_amax(self.V, self.amax[1:2])
             self.kvq.kvq_cache_set_tensor_scales_from_amax(self.cache, self.amax[0:1], self.amax[1:2])
@@ -404,7 +411,7 @@ def run_ours(args, w: wl.Workload):
                        "tokens_heads_per_s": tokens_heads / (dec_avg * 1e-3)},
             "write": {"bulk_gbs": round(wbytes / (fill_ms * 1e-3) / 1e9, 2), "bulk_ms": round(fill_ms, 4),
                       "bulk_bytes": wbytes, "tokens_heads_per_s": gw.lay.num_tokens * w.num_kv_heads / (fill_ms * 1e-3),
-                      "calibrate_ms": round(calib_ms, 4) if w.mode in ("fp8_per_tensor", "nvfp4") else None},
+                      "calibrate_ms": round(calib_ms, 4) if w.mode in TENSOR_SCALED else None},
             "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(dec_gbs / peak, 4), "traffic": traffic,
                          "kernel": dec_kernel, "peak_kind": peak_kind,
@@ -435,7 +442,7 @@ def _oracle_seq_pool(w: wl.Workload, b: int):
         P = w.page_size
         npg = (n + P - 1) // P
         ks = vs = 1.0
-        if w.mode in ("fp8_per_tensor", "nvfp4"):
+        if w.mode in TENSOR_SCALED:
             ks = oracle.tensor_scale(w.mode, oracle.amax(k.astype(np.float32)))
             vs = oracle.tensor_scale(w.mode, oracle.amax(v.astype(np.float32)))
         pool = np.zeros(oracle.pool_bytes(w.mode, npg, P, w.num_kv_heads, w.head_dim), np.uint8)
@@ -515,7 +522,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS) + ["pth_b64_u1k_32k:fp8"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS) + sorted(VARIANTS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -524,8 +531,9 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.workload == "pth_b64_u1k_32k:fp8":
-        w = wl.WORKLOADS["pth_b64_u1k_32k"].with_mode("fp8_per_token_head")
+    if args.workload in VARIANTS:
+        base, mode = VARIANTS[args.workload]
+        w = wl.WORKLOADS[base].with_mode(mode)
     else:
         w = wl.WORKLOADS[args.workload]
     if args.num_seqs is not None:

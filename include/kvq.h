@@ -20,7 +20,10 @@
  *  [P5] "NVFP4 KV Cache：Blackwell 上的 4-bit 缓存量化": two-level scaling,
  *       KV write/read paths, attention A = softmax(QK^T/sqrt(d)), O = AV;
  *       an unsupported combination is an immediate error, not a silent
- *       fallback.
+ *       fallback; "用一组数直观看缩放的作用" (the nvfp4_4over6 mode picks a
+ *       max/6 or max/4 block scale by reconstruction error).
+ *  [P4] also names int4_per_token_head: head_size/2 bytes of data plus one
+ *       fp32 scale per token and kv head.
  *
  * Conventions
  *  - Every call returns a kvq_status; KVQ_OK is 0.  On error,
@@ -67,6 +70,8 @@ typedef enum {
   KVQ_INT8_PER_TOKEN_HEAD = 2, /* int8 payload, fp32 scale per token x kv head, s = max|x|/127 */
   KVQ_FP8_PER_TOKEN_HEAD = 3,  /* E4M3 payload, fp32 scale per token x kv head, s = max|x|/448 */
   KVQ_NVFP4 = 4,               /* E2M1 payload, E4M3 scale per 16 values, fp32 global scale */
+  KVQ_INT4_PER_TOKEN_HEAD = 5, /* signed 4-bit payload, fp32 scale per token x kv head, s = max|x|/7 */
+  KVQ_NVFP4_4OVER6 = 6,        /* NVFP4 storage; each block scale is max/6 or max/4, by error */
   KVQ_KVARN_K4V2_G128 = 16     /* 4-bit keys, 2-bit values, 128-token tiles */
 } kvq_mode;
 
@@ -96,12 +101,14 @@ typedef struct kvq_cache kvq_cache;
  * Token t of page p is row t of that block.  Per mode (P = page_size, D = head_dim):
  *   FP8 per-tensor : K[P][D] e4m3 | V[P][D] e4m3                    (2PD bytes)
  *   INT8 / FP8 PTH : K[P][D] | V[P][D] | K scale[P] f32 | V scale[P] f32
- *   NVFP4          : K[P][D/2] | V[P/2][D] | K s_b[P][D/16] e4m3 | V s_b[P][D/16] e4m3
+ *   NVFP4, 4over6  : K[P][D/2] | V[P/2][D] | K s_b[P][D/16] e4m3 | V s_b[P][D/16] e4m3
+ *   INT4 PTH       : K[P][D/2] | V[P/2][D] | K scale[P] f32 | V scale[P] f32
  *   KVarN (P=D=128): K[128][64] u4 | V[128][32] u2 |
  *                    K scale[D] zero[D] c[D] r[P] f32 | V scale[P] zero[P] r[P] c[D] f32
- * 4-bit codes: the even head_dim index in the low nibble, except NVFP4 V,
- * whose byte [k][d] holds channel d of tokens 2k (low nibble) and 2k+1 -- the
- * pairing decode's tensor-core fragments take, with no nibble shuffling.
+ * 4-bit codes (E2M1, or two's-complement int4): the even head_dim index in the
+ * low nibble, except 4-bit V (NVFP4, INT4), whose byte [k][d] holds channel d
+ * of tokens 2k (low nibble) and 2k+1 -- the pairing decode's tensor-core
+ * fragments take, with no nibble shuffling.
  * 2-bit codes: element 4i+j in bits 2j..2j+1 of byte i.  The header holds, at byte 16 and
  * 20, the per-tensor K and V scales (FP8 per-tensor s; NVFP4 s_t), and at
  * byte 12 the device error word.  This is the same content as the in-page
@@ -125,8 +132,8 @@ kvq_status kvq_cache_alloc(const kvq_cache_config* cfg, void* dev_buf, size_t by
 kvq_status kvq_cache_free(kvq_cache* cache);
 
 /* Per-tensor scales ([P1] sec. 2.1 K_fp8 = K/scale; [P5] s_t), written into
- * the header on `stream`.  Used by KVQ_FP8_PER_TENSOR (s) and KVQ_NVFP4 (s_t);
- * other modes ignore them.  Scales must be finite and > 0. */
+ * the header on `stream`.  Used by KVQ_FP8_PER_TENSOR (s) and the two NVFP4
+ * modes (s_t); other modes ignore them.  Scales must be finite and > 0. */
 kvq_status kvq_cache_set_tensor_scales(kvq_cache* cache, float k_scale, float v_scale, void* stream);
 
 /* amax = max |x| over n elements of `x` (device, dtype kvq_dtype), written
@@ -134,7 +141,7 @@ kvq_status kvq_cache_set_tensor_scales(kvq_cache* cache, float k_scale, float v_
 kvq_status kvq_tensor_amax(const void* x, int dtype, size_t n, float* dev_out, void* stream);
 
 /* Set the header's scales from device amax values without a host round trip:
- * FP8 per-tensor s = amax/448, NVFP4 s_t = amax/(448*6); an amax of 0 gives
+ * FP8 per-tensor s = amax/448, NVFP4 (both modes) s_t = amax/(448*6); an amax of 0 gives
  * 1.0.  Both pointers are device floats (e.g. from kvq_tensor_amax). */
 kvq_status kvq_cache_set_tensor_scales_from_amax(kvq_cache* cache, const float* dev_amax_k,
                                                  const float* dev_amax_v, void* stream);
@@ -151,7 +158,12 @@ kvq_status kvq_cache_read_errors(kvq_cache* cache, uint32_t* flags, int clear, v
  *  mode          must equal the cache's mode (else KVQ_ERR_MODE_MISMATCH).
  * Per mode: FP8 per-tensor q = E4M3(x/s) with the header scale; INT8/FP8
  * per-token-head s = max(max|x|, 1e-8)/127 (or /448), q = clip(rint(x/s)) (or
- * E4M3(x/s)); NVFP4 s_b = E4M3(max_block|x| / (6 s_t)), q = E2M1(x/(s_t s_b));
+ * E4M3(x/s)); INT4 per-token-head s = max(max|x|, 1e-8)/7, q = clip(rint(x/s),
+ * -7, 7); NVFP4 s_b = E4M3(max_block|x| / (6 s_t)), q = E2M1(x/(s_t s_b));
+ * NVFP4 4over6: the same block coded with s_b = E4M3(max_block|x| / (4 s_t))
+ * as well, keeping the coding whose fp32 sum of squared reconstruction errors
+ * (x - s_t s_b q)^2, summed as a pairwise tree of neighbours, is smaller
+ * (max/6 on a tie);
  * KVarN: num_tokens must be a multiple of 128 and every 128 consecutive tokens
  * must fill one page in order (slot_mapping[128i + j] = 128 page + j); a tile
  * that does not is skipped with KVQ_DEVERR_PARTIAL_TILE.  All divisions are

@@ -32,7 +32,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 bool valid_mode(int m) {
   return m == KVQ_FP8_PER_TENSOR || m == KVQ_INT8_PER_TOKEN_HEAD || m == KVQ_FP8_PER_TOKEN_HEAD || m == KVQ_NVFP4 ||
-         m == KVQ_KVARN_K4V2_G128;
+         m == KVQ_INT4_PER_TOKEN_HEAD || m == KVQ_NVFP4_4OVER6 || m == KVQ_KVARN_K4V2_G128;
 }
 
 kvq_status check_config(const kvq_cache_config* cfg) {
@@ -133,10 +133,12 @@ kvq_status kvq_cache_alloc(const kvq_cache_config* cfg, void* dev_buf, size_t by
   memset(&c->tmap, 0, sizeof c->tmap);
 
   // The decode kernels of modes 1-4 at head_dim 128 stage pages with a tiled
-  // TMA copy: the pool seen as rows of 128 (1-byte codes) or 64 (E2M1) bytes,
+  // TMA copy: the pool seen as rows of 128 (1-byte codes) or 64 (4-bit codes) bytes,
   // one box = one (page, kv head) block, hardware-swizzled in shared memory.
   if (cfg->mode != KVQ_KVARN_K4V2_G128 && cfg->head_dim == 128) {
-    const int rw = cfg->mode == KVQ_NVFP4 ? 64 : 128;
+    const bool four_bit = cfg->mode == KVQ_NVFP4 || cfg->mode == KVQ_NVFP4_4OVER6 ||
+                          cfg->mode == KVQ_INT4_PER_TOKEN_HEAD;
+    const int rw = four_bit ? 64 : 128;
     const unsigned long long rows = need / rw;
     const int rpb = static_cast<int>(c->block_bytes / rw);
     if (rows >= (1ull << 31)) {
@@ -218,7 +220,7 @@ kvq_status kvq_cache_set_tensor_scales_from_amax(kvq_cache* cache, const float* 
   kvq_status s = check_cache(cache);
   if (s) return s;
   if (!dev_amax_k || !dev_amax_v) return fail(KVQ_ERR_INVALID_ARG, "NULL amax pointer");
-  if (cache->cfg.mode != KVQ_FP8_PER_TENSOR && cache->cfg.mode != KVQ_NVFP4)
+  if (cache->cfg.mode != KVQ_FP8_PER_TENSOR && cache->cfg.mode != KVQ_NVFP4 && cache->cfg.mode != KVQ_NVFP4_4OVER6)
     return fail(KVQ_ERR_MODE_MISMATCH, "mode %d has no per-tensor scale", cache->cfg.mode);
   const float div = cache->cfg.mode == KVQ_FP8_PER_TENSOR ? 448.0f : 2688.0f;
   cudaError_t e =

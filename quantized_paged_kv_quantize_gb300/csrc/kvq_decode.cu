@@ -56,7 +56,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int MODE, int D>
 struct Cfg {
-  static constexpr int RW = MODE == KVQ_NVFP4 ? D / 2 : D;  // payload row bytes
+  // 4-bit payloads (NVFP4 -- also the storage of NVFP4 4over6 -- and INT4):
+  // K rows of D/2 bytes, V token-pair rows of D bytes.
+  static constexpr bool FOUR = MODE == KVQ_NVFP4 || MODE == KVQ_INT4_PER_TOKEN_HEAD;
+  static constexpr int RW = FOUR ? D / 2 : D;  // payload row bytes
   static constexpr int BLK = (int)block_bytes(MODE, kPage, D);
   static constexpr bool TMA = D == 128;
   // stage stride: a multiple of the swizzle pattern's period (1024 B for SW128,
@@ -69,35 +72,52 @@ struct Cfg {
   static constexpr int S_OFF = 2 * kPage * RW;        // scales region
   // SW128 for 128-byte rows, SW64 for 64-byte rows (XOR of address bits 7.. into 4..).
   static constexpr int SWZ_MASK = !TMA ? 0 : (RW == 128 ? 7 : 3);
-  static constexpr int STAGES = MODE == KVQ_NVFP4 ? KVQ_FP4_STAGES : KVQ_B1_STAGES;
-  static constexpr int MINB = MODE == KVQ_NVFP4 ? KVQ_FP4_MINB : KVQ_B1_MINB;
+  static constexpr int STAGES = FOUR ? KVQ_FP4_STAGES : KVQ_B1_STAGES;
+  static constexpr int MINB = FOUR ? KVQ_FP4_MINB : KVQ_B1_MINB;
   // The running reference max may lag the true max by up to SLACK (log2 units)
   // before it is moved, so probabilities reach 2^SLACK; they are scaled by
   // 2^PSHIFT before the f16 split, with 2^(PSHIFT + SLACK) x (largest V scale
   // folded into P) inside the f16 range: per-token-head V scales of fp16 inputs
-  // are at most 65504/127 (INT8) or 65504/448 (FP8).
+  // are at most 65504/127 (INT8), 65504/448 (FP8) or 65504/7 (INT4).
   static constexpr int slack(bool f32io) { return f32io ? 0 : 4; }
   static constexpr int pshift(bool f32io) {
     return MODE == KVQ_INT8_PER_TOKEN_HEAD ? (f32io ? 0 : 2)
-         : MODE == KVQ_FP8_PER_TOKEN_HEAD ? (f32io ? 0 : 4) : (f32io ? 14 : 10);
+         : MODE == KVQ_FP8_PER_TOKEN_HEAD ? (f32io ? 0 : 4)
+         : MODE == KVQ_INT4_PER_TOKEN_HEAD ? (f32io ? 0 : -2) : (f32io ? 14 : 10);
   }
   // Channel group (D/8 channels) whose V rows the lanes of MMA row g load and
-  // whose outputs they hold.  NVFP4 at D = 128 reads V token-pair rows with
+  // whose outputs they hold.  4-bit V at D = 128 is read as token-pair rows with
   // 128-bit loads under the 64-byte swizzle: the order 0, 4, 1, 5, 2, 6, 3, 7
   // puts the two groups of each 8-lane phase in different bank halves, so the
   // loads are conflict-free (the identity order is 2-way conflicted).
   static __device__ __forceinline__ int cgrp(int g) {
-    return (MODE == KVQ_NVFP4 && D == 128) ? ((g >> 1) | ((g & 1) << 2)) : g;
+    return (FOUR && D == 128) ? ((g >> 1) | ((g & 1) << 2)) : g;
   }
   // The CTA's warps share one copy of the query fragments in shared memory
   // (one 64-bit load per k-step) instead of 16 registers each: faster for the
   // one-byte modes, slower for NVFP4 (measured on GB300).
-  static constexpr bool QSMEM = MODE != KVQ_NVFP4;
+  static constexpr bool QSMEM = !FOUR;
 };
 
 template <int MASK>
 __device__ __forceinline__ int swz(int off) {
   return off ^ (((off >> 7) & MASK) << 4);
+}
+
+// Four bytes of two's-complement 4-bit pairs -> four exact f16x2 (byte i ->
+// out[i], low nibble -> low half).  The biased nibble b = n + 8 goes into an
+// f16 mantissa as 1024 + b (low half) and 1024 + 16 b (high half); one f16x2
+// fma maps them to n: (1024 + b) * 1 - 1032 and (1024 + 16 b) * 2^-4 - 72.
+__device__ __forceinline__ void s4x8_to_f16x2x4(uint32_t w, uint32_t* out) {
+  const uint32_t b = w ^ 0x88888888u;
+  const __half2 mul = __halves2half2(__ushort_as_half(0x3C00), __ushort_as_half(0x2C00));  // 1, 2^-4
+  const __half2 add = __halves2half2(__ushort_as_half(0xE408), __ushort_as_half(0xD480));  // -1032, -72
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t y = prmt(b, 0u, 0x4040u + 0x0101u * i);  // byte i in both halves
+    const uint32_t t = bitsel(y, 0x64006400u, 0x00F0000Fu);
+    out[i] = h2_as_u32(__hfma2(u32_as_h2(t), mul, add));
+  }
 }
 
 // int8 pair (bytes 0,1 or 2,3 of w) -> exact f16x2 via 1024 + (x + 128) - 1152.
@@ -167,7 +187,7 @@ __device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq
                                          const uint32_t (*ql)[2], const uint2* qs, int lane, float (*c)[4]) {
   using C = Cfg<MODE, D>;
   constexpr int KSTEPS = C::KSTEPS;
-  constexpr int KW = (MODE == KVQ_NVFP4 ? D / 8 : D / 4) / 4;  // words per thread per row
+  constexpr int KW = (C::FOUR ? D / 8 : D / 4) / 4;  // words per thread per row
   uint32_t kg[NP][KW], kh8[NP][KW];
   const int rb = tq * (KW * 4);
 #pragma unroll
@@ -177,7 +197,23 @@ __device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq
       lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>(g * C::RW + rb + 4 * w), kg[p] + w);
       lds<(KW >= 4 ? 4 : KW)>(st[p] + swz<C::SWZ_MASK>((g + 8) * C::RW + rb + 4 * w), kh8[p] + w);
     }
-  if constexpr (MODE == KVQ_NVFP4) {
+  if constexpr (MODE == KVQ_INT4_PER_TOKEN_HEAD) {  // per-token K scale: applied to the scores
+#pragma unroll
+    for (int w = 0; w < KW; ++w)
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        uint32_t fg[4], fh[4];
+        s4x8_to_f16x2x4(kg[p][w], fg);
+        s4x8_to_f16x2x4(kh8[p][w], fh);
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          const int j = 2 * w + hlf;
+          const uint32_t af[4] = {fg[2 * hlf], fh[2 * hlf], fg[2 * hlf + 1], fh[2 * hlf + 1]};
+          mma16816(c[p], af, qh[j][0], qh[j][1]);
+          if constexpr (QF32) mma16816(c[p], af, ql[j][0], ql[j][1]);
+        }
+      }
+  } else if constexpr (MODE == KVQ_NVFP4) {
     constexpr int SB = D / 16;
     const int blk0 = (tq * (D / 4)) / 16;
     const int base_g = C::S_OFF + g * SB, base_h = C::S_OFF + (g + 8) * SB;
@@ -245,7 +281,39 @@ __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq
   using C = Cfg<MODE, D>;
   constexpr int MTILES = C::MTILES;
   const int r0 = 2 * tq, r1 = 2 * tq + 1, r2 = 2 * tq + 8, r3 = 2 * tq + 9;  // tokens
-  if constexpr (MODE == KVQ_NVFP4) {
+  if constexpr (MODE == KVQ_INT4_PER_TOKEN_HEAD) {
+    // Token-pair rows as for NVFP4 below; the per-token V scale is folded into
+    // P, and a token past seq_len has p = 0 with finite codes, so nothing is
+    // masked here.
+    constexpr int CPG = D / 8;
+    constexpr int VW = CPG / 4;
+    uint32_t W0[NP][VW], W2[NP][VW];
+    const int cgb = CPG * C::cgrp(g);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + tq * D + cgb), W0[p]);
+      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + (tq + 4) * D + cgb), W2[p]);
+    }
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+      for (int w = 0; w < VW; ++w) {
+        uint32_t f0[4], f2[4];  // byte e of the word: channel cgb + 4w + e
+        s4x8_to_f16x2x4(W0[p][w], f0);
+        s4x8_to_f16x2x4(W2[p][w], f2);
+        uint32_t av[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          av[u][0] = f0[2 * u];
+          av[u][1] = f0[2 * u + 1];
+          av[u][2] = f2[2 * u];
+          av[u][3] = f2[2 * u + 1];
+          mma16816(o[2 * w + u], av[u], bh[p][0], bh[p][1]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) mma16816(o[2 * w + u], av[u], bl[p][0], bl[p][1]);
+      }
+  } else if constexpr (MODE == KVQ_NVFP4) {
     // V payload: token-pair rows [kPage / 2][D] bytes, byte (k, d) holding
     // channel d of tokens 2k (low nibble) and 2k + 1, so one E2M1 pair
     // conversion gives the A fragment's (token 2tq, 2tq + 1) f16x2 directly.
@@ -446,7 +514,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
     kfac *= *reinterpret_cast<const float*>(a.pool + kHdrKScaleOffset);
     vfac = *reinterpret_cast<const float*>(a.pool + kHdrVScaleOffset);
   }
-  constexpr bool kPerToken = MODE == KVQ_INT8_PER_TOKEN_HEAD || MODE == KVQ_FP8_PER_TOKEN_HEAD;
+  constexpr bool kPerToken =
+      MODE == KVQ_INT8_PER_TOKEN_HEAD || MODE == KVQ_FP8_PER_TOKEN_HEAD || MODE == KVQ_INT4_PER_TOKEN_HEAD;
 
   float o[MTILES][4];
 #pragma unroll
@@ -671,7 +740,9 @@ int resident_ctas_d(int mode) {
     case KVQ_FP8_PER_TENSOR: return resident_ctas<KVQ_FP8_PER_TENSOR, D, QF32>();
     case KVQ_INT8_PER_TOKEN_HEAD: return resident_ctas<KVQ_INT8_PER_TOKEN_HEAD, D, QF32>();
     case KVQ_FP8_PER_TOKEN_HEAD: return resident_ctas<KVQ_FP8_PER_TOKEN_HEAD, D, QF32>();
-    case KVQ_NVFP4: return resident_ctas<KVQ_NVFP4, D, QF32>();
+    case KVQ_NVFP4:
+    case KVQ_NVFP4_4OVER6: return resident_ctas<KVQ_NVFP4, D, QF32>();
+    case KVQ_INT4_PER_TOKEN_HEAD: return resident_ctas<KVQ_INT4_PER_TOKEN_HEAD, D, QF32>();
     default: return 1;
   }
 }
@@ -702,7 +773,9 @@ cudaError_t launch_d(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s) {
     case KVQ_FP8_PER_TENSOR: return launch_mode<KVQ_FP8_PER_TENSOR, D, QF32>(c, a, s);
     case KVQ_INT8_PER_TOKEN_HEAD: return launch_mode<KVQ_INT8_PER_TOKEN_HEAD, D, QF32>(c, a, s);
     case KVQ_FP8_PER_TOKEN_HEAD: return launch_mode<KVQ_FP8_PER_TOKEN_HEAD, D, QF32>(c, a, s);
-    case KVQ_NVFP4: return launch_mode<KVQ_NVFP4, D, QF32>(c, a, s);
+    case KVQ_NVFP4:  // NVFP4 4over6 shares NVFP4's storage: only the write differs
+    case KVQ_NVFP4_4OVER6: return launch_mode<KVQ_NVFP4, D, QF32>(c, a, s);
+    case KVQ_INT4_PER_TOKEN_HEAD: return launch_mode<KVQ_INT4_PER_TOKEN_HEAD, D, QF32>(c, a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -23,7 +23,8 @@ __host__ __device__ constexpr size_t block_bytes(int mode, int P, int D) {
   return mode == KVQ_FP8_PER_TENSOR ? (size_t)2 * P * D
        : (mode == KVQ_INT8_PER_TOKEN_HEAD || mode == KVQ_FP8_PER_TOKEN_HEAD)
              ? (size_t)2 * P * D + (size_t)8 * P
-       : mode == KVQ_NVFP4 ? (size_t)P * D + (size_t)P * D / 8
+       : (mode == KVQ_NVFP4 || mode == KVQ_NVFP4_4OVER6) ? (size_t)P * D + (size_t)P * D / 8
+       : mode == KVQ_INT4_PER_TOKEN_HEAD ? (size_t)P * D + (size_t)8 * P
        : mode == KVQ_KVARN_K4V2_G128
              ? (size_t)P * D / 2 + (size_t)P * D / 4 + (size_t)4 * (3 * D + P) + (size_t)4 * (3 * P + D)
              : 0;

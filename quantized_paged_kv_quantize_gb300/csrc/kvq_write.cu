@@ -131,6 +131,32 @@ struct QDiv {
     }
     return w;
   }
+  // N <= 8 signed 4-bit codes clamp(rint(x/s), -7, 7) of x[0..N), two's
+  // complement, packed two per byte with x[0] in the low nibble.  Same rint
+  // as int8x4; the fast path requires both ends inside [-7, 7] (bit patterns
+  // 0x4B400000 -7 .. +7), whose low nibble is then the code.
+  template <int N>
+  __device__ __forceinline__ uint32_t int4x8(const float* x) const {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    uint32_t lo[N], bad = fast ? 0u : 1u;
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      lo[e] = __float_as_uint(__fadd_rn(__fmul_rn(x[e], rlo), kMagic));
+      const uint32_t hi = __float_as_uint(__fadd_rn(__fmul_rn(x[e], rhi), kMagic));
+      bad |= (lo[e] ^ hi) | static_cast<uint32_t>(lo[e] - 0x4B3FFFF9u > 14u);
+    }
+    if (bad != 0) {
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        const float qv = fminf(fmaxf(rintf(__fdiv_rn(x[e], s)), -7.0f), 7.0f);
+        lo[e] = static_cast<uint32_t>(__float2int_rn(qv));
+      }
+    }
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < N; ++e) w |= (lo[e] & 0xFu) << (4 * e);
+    return w;
+  }
   // eight E2M1 codes (pairs packed low nibble first) of x[0..n)
   template <int N>
   __device__ __forceinline__ uint32_t e2m1x8(const float* x) const {
@@ -156,10 +182,40 @@ __device__ __forceinline__ float group_max(float v) {
   return v;
 }
 
+// Squared reconstruction error of a 16-value block whose codes (w, this
+// thread's VEC of them) reconstruct as E2M1(code) * den: fp32, every operation
+// rounded alone, summed as a pairwise tree of neighbours -- within the thread
+// for its VEC consecutive values, then across the TPB lanes of the block
+// (xor 1, 2: each level adds two neighbouring subtrees, and fp32 addition is
+// commutative, so every lane holds the same total).
+template <int VEC, int TPB>
+__device__ __forceinline__ float block_sse(const float* x, uint32_t w, float den) {
+  uint32_t h[4];
+  e2m1x8_to_f16x2x4(w, h);
+  float e[VEC];
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) {
+    const __half2 p = u32_as_h2(h[i / 2]);
+    const float val = (i & 1) ? __high2float(p) : __low2float(p);
+    const float d = __fsub_rn(x[i], __fmul_rn(val, den));
+    e[i] = __fmul_rn(d, d);
+  }
+#pragma unroll
+  for (int st = 1; st < VEC; st <<= 1)
+#pragma unroll
+    for (int i = 0; i < VEC; i += 2 * st) e[i] = __fadd_rn(e[i], e[i + st]);
+  float t = e[0];
+#pragma unroll
+  for (int o = 1; o < TPB; o <<= 1) t = __fadd_rn(t, __shfl_xor_sync(kFull, t, o));
+  return t;
+}
+
 // NVFP4 codes of a thread's VEC values (its 16-value block shared with TPB =
 // 16 / VEC lanes): the E4M3 block scale byte sb and the E2M1 codes packed two
 // per byte, even channel in the low nibble (sb = 0 gives all-zero codes).
-template <int VEC, int TPB>
+// F46 (nvfp4_4over6): the block is also coded with the max/4 scale
+// E4M3(amax / (4 s_t)), and that coding is kept when its block_sse is smaller.
+template <int VEC, int TPB, bool F46>
 __device__ __forceinline__ void nvfp4_codes(const float* x, float st, uint32_t& w, uint32_t& sb) {
   const float six_st = __fmul_rn(6.0f, st);
   float amax = 0.0f;
@@ -168,8 +224,22 @@ __device__ __forceinline__ void nvfp4_codes(const float* x, float st, uint32_t& 
   amax = group_max<TPB>(amax);
   sb = f32x2_to_e4m3x2(0.0f, __fdiv_rn(amax, six_st)) & 0xFFu;
   const float sbf = e4m3_to_f32(sb);
-  w = sbf != 0.0f ? QDiv(__fmul_rn(st, sbf)).e2m1x8<VEC>(x) : 0u;
+  const float den = __fmul_rn(st, sbf);
+  w = sbf != 0.0f ? QDiv(den).e2m1x8<VEC>(x) : 0u;
+  if constexpr (F46) {
+    const uint32_t sb4 = f32x2_to_e4m3x2(0.0f, __fdiv_rn(amax, __fmul_rn(4.0f, st))) & 0xFFu;
+    const float sbf4 = e4m3_to_f32(sb4);
+    const float den4 = __fmul_rn(st, sbf4);
+    const uint32_t w4 = sbf4 != 0.0f ? QDiv(den4).e2m1x8<VEC>(x) : 0u;
+    if (block_sse<VEC, TPB>(x, w4, den4) < block_sse<VEC, TPB>(x, w, den)) {
+      w = w4;
+      sb = sb4;
+    }
+  }
 }
+
+template <int MODE>
+constexpr bool kFourBit = MODE == KVQ_NVFP4 || MODE == KVQ_NVFP4_4OVER6 || MODE == KVQ_INT4_PER_TOKEN_HEAD;
 
 // The n = 4 or 8 codes packed in w (two per byte) spread one per byte, in the
 // low nibble: bytes c0, c1, c2, c3 (| c4..c7).
@@ -218,29 +288,43 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
       store_bytes<VEC>(blk + (size_t)side * a.P * D + (size_t)off * D + j * VEC, w);
       if (j == 0) *reinterpret_cast<float*>(blk + (size_t)2 * a.P * D + (size_t)side * 4 * a.P + 4 * off) = s;
     }
-  } else if constexpr (MODE == KVQ_NVFP4) {  // keys; values go through nvfp4_values_pass
+  } else if constexpr (MODE == KVQ_NVFP4 || MODE == KVQ_NVFP4_4OVER6) {  // keys; values: pair_values_pass
     constexpr int TPB = 16 / VEC;  // threads per 16-value block
     uint32_t w[1], sb;
-    nvfp4_codes<VEC, TPB>(x, *reinterpret_cast<const float*>(a.pool + kHdrKScaleOffset), w[0], sb);
+    nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, *reinterpret_cast<const float*>(a.pool + kHdrKScaleOffset),
+                                                   w[0], sb);
     if (active) {
       store_bytes<VEC / 2>(blk + (size_t)off * D / 2 + j * VEC / 2, w);
       if ((j % TPB) == 0) blk[(size_t)a.P * D + (size_t)off * D / 16 + (j * VEC) / 16] = static_cast<uint8_t>(sb);
+    }
+  } else if constexpr (MODE == KVQ_INT4_PER_TOKEN_HEAD) {  // keys; values: pair_values_pass
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = group_max<TPR>(amax);
+    const float s = __fdiv_rn(fmaxf(amax, 1e-8f), 7.0f);
+    uint32_t w[1] = {QDiv(s).int4x8<VEC>(x)};
+    if (active) {
+      store_bytes<VEC / 2>(blk + (size_t)off * D / 2 + j * VEC / 2, w);
+      if (j == 0) *reinterpret_cast<float*>(blk + (size_t)a.P * D + 4 * off) = s;
     }
   }
 }
 
 
-// NVFP4 values: token-pair rows, byte (k, d) of a page holding channel d of
-// tokens 2k (low nibble) and 2k + 1.  A token with an even slot whose
-// successor in the batch holds the next slot stores the pair's bytes whole and
-// the successor stores nothing; every other token writes its own nibbles with
-// 32-bit atomic AND/OR (two tokens never share a nibble, so these commute),
-// e.g. the one new token of a decode step.  The successor's codes come from
-// the next row group of the same warp (a shuffle) when a warp holds two row
-// groups (TPR = 16), else through shared memory (whole CTA, one barrier).
-template <int D, int VEC, int TPR, int NTOK, int R, typename T>
-__device__ __forceinline__ void nvfp4_values_pass(const WriteArgs& a, int h, const int* slot, const uint4* raw,
-                                                  int j) {
+// 4-bit values (NVFP4, NVFP4 4over6, INT4): token-pair rows, byte (k, d) of a
+// page holding channel d of tokens 2k (low nibble) and 2k + 1.  A token with
+// an even slot whose successor in the batch holds the next slot stores the
+// pair's bytes whole and the successor stores nothing; every other token
+// writes its own nibbles with 32-bit atomic AND/OR (two tokens never share a
+// nibble, so these commute), e.g. the one new token of a decode step.  The
+// successor's codes come from the next row group of the same warp (a shuffle)
+// when a warp holds two row groups (TPR = 16), else through shared memory
+// (whole CTA, one barrier).  Scales (NVFP4 block scales, the INT4 token
+// scale) are per token and stored directly.
+template <int MODE, int D, int VEC, int TPR, int NTOK, int R, typename T>
+__device__ __forceinline__ void pair_values_pass(const WriteArgs& a, int h, const int* slot, const uint4* raw,
+                                                 int j) {
   constexpr int TPB = 16 / VEC;
   constexpr int TOK = NTOK / R;
   constexpr bool kInWarp = TPR == 16;
@@ -261,13 +345,22 @@ __device__ __forceinline__ void nvfp4_values_pass(const WriteArgs& a, int h, con
       if (j == 0) set_error(a.pool, KVQ_DEVERR_SLOT_RANGE);
       active = false;
     }
-    uint32_t sb;
-    nvfp4_codes<VEC, TPB>(x, st, wr[r], sb);
-    sr[r] = active ? s : -1;
-    if (active && (j % TPB) == 0) {
-      uint8_t* blk = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes;
-      blk[(size_t)a.P * D + (size_t)a.P * D / 16 + (size_t)off * D / 16 + (j * VEC) / 16] = static_cast<uint8_t>(sb);
+    uint8_t* blk = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes;
+    if constexpr (MODE == KVQ_INT4_PER_TOKEN_HEAD) {
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      amax = group_max<TPR>(amax);
+      const float sc = __fdiv_rn(fmaxf(amax, 1e-8f), 7.0f);
+      wr[r] = QDiv(sc).int4x8<VEC>(x);
+      if (active && j == 0) *reinterpret_cast<float*>(blk + (size_t)a.P * D + (size_t)4 * a.P + 4 * off) = sc;
+    } else {
+      uint32_t sb;
+      nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, st, wr[r], sb);
+      if (active && (j % TPB) == 0)
+        blk[(size_t)a.P * D + (size_t)a.P * D / 16 + (size_t)off * D / 16 + (j * VEC) / 16] = static_cast<uint8_t>(sb);
     }
+    sr[r] = active ? s : -1;
     if constexpr (!kInWarp) {
       const int li = g + TOK * r;
       codes[li * TPR + j] = wr[r];
@@ -353,9 +446,9 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
     raw[r] = in ? __ldg(reinterpret_cast<const uint4*>(src + (token * a.Hkv + h) * D + j * VEC))
                 : make_uint4(0u, 0u, 0u, 0u);
   }
-  if constexpr (MODE == KVQ_NVFP4) {
+  if constexpr (kFourBit<MODE>) {
     if (side == 1) {
-      nvfp4_values_pass<D, VEC, TPR, TOK * R, R, T>(a, h, slot, raw, j);
+      pair_values_pass<MODE, D, VEC, TPR, TOK * R, R, T>(a, h, slot, raw, j);
       return;
     }
   }
@@ -778,6 +871,8 @@ cudaError_t launch_mode(int mode, const WriteArgs& a, cudaStream_t s) {
     case KVQ_INT8_PER_TOKEN_HEAD: return launch_rows<KVQ_INT8_PER_TOKEN_HEAD, T, D>(a, s);
     case KVQ_FP8_PER_TOKEN_HEAD: return launch_rows<KVQ_FP8_PER_TOKEN_HEAD, T, D>(a, s);
     case KVQ_NVFP4: return launch_rows<KVQ_NVFP4, T, D>(a, s);
+    case KVQ_INT4_PER_TOKEN_HEAD: return launch_rows<KVQ_INT4_PER_TOKEN_HEAD, T, D>(a, s);
+    case KVQ_NVFP4_4OVER6: return launch_rows<KVQ_NVFP4_4OVER6, T, D>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

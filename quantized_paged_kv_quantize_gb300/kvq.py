@@ -25,6 +25,8 @@ MODES = {
     "int8_per_token_head": 2,
     "fp8_per_token_head": 3,
     "nvfp4": 4,
+    "int4_per_token_head": 5,
+    "nvfp4_4over6": 6,
     "kvarn_k4v2_g128": 16,
 }
 KVQ_F16, KVQ_F32 = 0, 1

@@ -12,8 +12,9 @@ import torch
 import oracle
 import workloads as wl
 
-MODE_NAMES = ["fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nvfp4", "kvarn_k4v2_g128"]
-TENSOR_SCALED = {"fp8_per_tensor", "nvfp4"}
+MODE_NAMES = ["fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nvfp4", "int4_per_token_head",
+              "nvfp4_4over6", "kvarn_k4v2_g128"]
+TENSOR_SCALED = {"fp8_per_tensor", "nvfp4", "nvfp4_4over6"}
 FILL = 0xCD  # untouched bytes of both pools
 
 

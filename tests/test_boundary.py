@@ -44,13 +44,16 @@ def test_version_and_sizes(K):
     assert K.kvq_cache_block_bytes(K.make_config(1, 16, 1, 128, "int8_per_token_head")) == 4224
     assert K.kvq_cache_block_bytes(K.make_config(1, 16, 1, 128, "fp8_per_token_head")) == 4224
     assert K.kvq_cache_block_bytes(K.make_config(1, 16, 1, 128, "nvfp4")) == 2304
+    assert K.kvq_cache_block_bytes(K.make_config(1, 16, 1, 128, "nvfp4_4over6")) == 2304
+    assert K.kvq_cache_block_bytes(K.make_config(1, 16, 1, 128, "int4_per_token_head")) == 2176
     assert K.kvq_cache_block_bytes(K.make_config(1, 128, 1, 128, "kvarn_k4v2_g128")) == 16384
     assert K.kvq_cache_bytes(K.make_config(10, 16, 8, 128, "nvfp4")) == 256 + 10 * 8 * 2304
 
 
 def test_layout_matches_oracle(K):
     import oracle
-    for mode in ("fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nvfp4"):
+    for mode in ("fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nvfp4", "int4_per_token_head",
+                 "nvfp4_4over6"):
         for D in (32, 128):
             cfg = K.make_config(7, 16, 3, D, mode)
             assert K.kvq_cache_bytes(cfg) == oracle.pool_bytes(mode, 7, 16, 3, D)

@@ -21,6 +21,8 @@ CASES = [
     ("pth_b64_u1k_32k", None, None),            # shortest and longest sequence
     ("pth_b64_u1k_32k", "fp8_per_token_head", None),
     ("nvfp4_b32_s32768", None, [5]),
+    ("pth_b64_u1k_32k", "int4_per_token_head", None),
+    ("nvfp4_b32_s32768", "nvfp4_4over6", [7]),
     ("kvarn_b16_s16384", None, [3]),
 ]
 
@@ -51,7 +53,7 @@ def test_full_size_sampled_parity(name, mode, sample):
         sample = [int(np.argmin(lens)), int(np.argmax(lens))]
     P, Hkv, D = w.page_size, w.num_kv_heads, w.head_dim
     ks = vs = 1.0
-    if w.mode in ("fp8_per_tensor", "nvfp4"):
+    if w.mode in ("fp8_per_tensor", "nvfp4", "nvfp4_4over6"):
         ak = max(oracle.amax(k.astype(np.float32)) for k, _ in gw.host)
         av = max(oracle.amax(v.astype(np.float32)) for _, v in gw.host)
         ks, vs = oracle.tensor_scale(w.mode, ak), oracle.tensor_scale(w.mode, av)

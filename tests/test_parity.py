@@ -12,12 +12,14 @@ import torch
 
 import oracle
 import workloads as wl
-from _helpers import (FILL, check_attention, gpu_cache, gpu_calibrate, gpu_decode, header_scales, kvq,
-                      make_case, oracle_decode, oracle_pool)
+from _helpers import (FILL, TENSOR_SCALED, check_attention, gpu_cache, gpu_calibrate, gpu_decode, header_scales,
+                      kvq, make_case, oracle_decode, oracle_pool)
 
 pytestmark = pytest.mark.gpu
 
-MODES4 = ["fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nvfp4"]
+MODES4 = ["fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nvfp4", "int4_per_token_head",
+          "nvfp4_4over6"]
+FOUR_BIT = ["nvfp4", "nvfp4_4over6", "int4_per_token_head"]
 LENS = [1, 15, 16, 17, 100, 333, 1000, 2500]
 KVARN_LENS = [128, 256, 640]
 
@@ -30,6 +32,8 @@ def small_workload(mode, D=128, Hq=16, Hkv=2, io="f16", seed=7):
         "int8_per_token_head": dict(outlier_token_frac=0.01, token_gain=30.0),
         "fp8_per_token_head": dict(outlier_token_frac=0.01, token_gain=30.0),
         "nvfp4": dict(outlier_channels=3, channels_per_head=True, channel_gain=10.0),
+        "nvfp4_4over6": dict(outlier_channels=3, channels_per_head=True, channel_gain=10.0),
+        "int4_per_token_head": dict(outlier_token_frac=0.01, token_gain=30.0),
         "kvarn_k4v2_g128": dict(outlier_channels=4, channels_per_head=True, channel_gain=15.0),
     }[mode]
     return wl.Workload(name=f"small_{mode}_{D}_{io}", mode=mode, num_seqs=1, num_q_heads=Hq, num_kv_heads=Hkv,
@@ -56,7 +60,7 @@ def test_write_bit_exact(mode, D, io):
     slots[7] = c.lay.num_pages * 16 + 5              # out of range: skipped and flagged
     cache = gpu_cache(c)
     kd, vd = _dev(c.k), _dev(c.v)
-    if mode in ("fp8_per_tensor", "nvfp4"):
+    if mode in TENSOR_SCALED:
         gpu_calibrate(cache, kd, vd)
         ks, vs = header_scales(cache)
         assert np.float32(ks) == np.float32(c.k_scale) and np.float32(vs) == np.float32(c.v_scale)
@@ -71,16 +75,18 @@ def test_write_bit_exact(mode, D, io):
 
 @pytest.mark.parametrize("io", ["f16", "f32"])
 @pytest.mark.parametrize("order", ["reversed", "random", "split_calls", "one_by_one"])
-def test_write_nvfp4_values_any_batch_order(order, io):
-    """NVFP4 values share a byte between tokens 2k and 2k+1: written as whole
+@pytest.mark.parametrize("mode", FOUR_BIT)
+def test_write_4bit_values_any_batch_order(mode, order, io):
+    """4-bit values share a byte between tokens 2k and 2k+1: written as whole
     pairs when the two tokens are neighbours in the batch, else nibble by
     nibble.  Any batch order, split over any number of calls, must give the
     oracle's bytes."""
     K = kvq()
-    c = make_case(small_workload("nvfp4", io=io), [1, 15, 16, 17, 100, 333], slack_pages=2)
+    c = make_case(small_workload(mode, io=io), [1, 15, 16, 17, 100, 333], slack_pages=2)
     cache = gpu_cache(c)
     kd, vd = _dev(c.k), _dev(c.v)
-    gpu_calibrate(cache, kd, vd)
+    if mode in TENSOR_SCALED:
+        gpu_calibrate(cache, kd, vd)
     n = len(c.slots)
     rng = np.random.default_rng(11)
     if order == "reversed":
@@ -168,7 +174,7 @@ def test_write_conversion_edge_values():
     w = wl.Workload(name="edge", mode="fp8_per_tensor", num_seqs=1, num_q_heads=1, num_kv_heads=1, head_dim=D,
                     page_size=16, io_dtype="f16", seed=1, seq_len=n)
     for mode, ks in (("fp8_per_tensor", 1.0), ("nvfp4", 1.0), ("fp8_per_token_head", None),
-                     ("int8_per_token_head", None)):
+                     ("int8_per_token_head", None), ("nvfp4_4over6", 1.0), ("int4_per_token_head", None)):
         wm = w.with_mode(mode)
         lay = wl.paged_layout(wm, np.array([n], np.int32))
         c = make_case(wm, [n])
@@ -182,22 +188,46 @@ def test_write_conversion_edge_values():
         got = cache.pool.cpu().numpy()
         ref = oracle_pool(c)
         assert (got[256:] == ref[256:]).all(), mode
-    # E2M1 ties: with s_t = 1 a block whose max is 6 has s_b = 1 and x/(s_t s_b) = x
+    # E2M1 ties: with s_t = 1 a block whose max is 6 has s_b = 1 and x/(s_t s_b) = x;
+    # INT4 ties: a row whose max is 7 has s = 1 and x/s = x
     ties = np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25, -5.0, 0.0, -0.0, 0.1, -0.1],
                     np.float16)
-    xt = np.tile(ties, D // 16).reshape(1, 1, D)
-    xt = np.repeat(xt, 16, axis=0)
-    wm = w.with_mode("nvfp4")
-    lay = wl.paged_layout(wm, np.array([16], np.int32))
-    c = make_case(wm, [16])
-    c.k, c.v, c.lay = xt, xt, lay
-    c.slots = wl.slots_for_seq(wm, lay, 0)
-    c.k_scale = c.v_scale = 1.0
+    ties4 = np.array([7.0, 0.5, 1.5, 2.5, 3.5, 4.5, 5.5, 6.5, -0.5, -1.5, -2.5, -6.5, 0.0, -0.0, 6.9, -7.0],
+                     np.float16)
+    for mode, t in (("nvfp4", ties), ("nvfp4_4over6", ties), ("int4_per_token_head", ties4)):
+        xt = np.tile(t, D // 16).reshape(1, 1, D)
+        xt = np.repeat(xt, 16, axis=0)
+        wm = w.with_mode(mode)
+        lay = wl.paged_layout(wm, np.array([16], np.int32))
+        c = make_case(wm, [16])
+        c.k, c.v, c.lay = xt, xt, lay
+        c.slots = wl.slots_for_seq(wm, lay, 0)
+        c.k_scale = c.v_scale = 1.0
+        cache = gpu_cache(c)
+        K.kvq_cache_set_tensor_scales(cache, 1.0, 1.0)
+        K.kvq_quantize_write(cache, _dev(c.k), _dev(c.v), _dev(c.slots))
+        got = cache.pool.cpu().numpy()
+        assert (got[256:] == oracle_pool(c)[256:]).all(), mode
+
+
+def test_write_4over6_uses_both_scales():
+    """The 4over6 write matches the oracle and really differs from plain NVFP4:
+    a sizeable share of blocks keep the max/4 scale."""
+    K = kvq()
+    c = make_case(small_workload("nvfp4_4over6"), [16, 100, 333], slack_pages=1)
     cache = gpu_cache(c)
-    K.kvq_cache_set_tensor_scales(cache, 1.0, 1.0)
-    K.kvq_quantize_write(cache, _dev(c.k), _dev(c.v), _dev(c.slots))
+    kd, vd = _dev(c.k), _dev(c.v)
+    gpu_calibrate(cache, kd, vd)
+    K.kvq_quantize_write(cache, kd, vd, _dev(c.slots))
     got = cache.pool.cpu().numpy()
     assert (got[256:] == oracle_pool(c)[256:]).all()
+    n4 = n = 0
+    for t in range(0, len(c.slots), 7):
+        for x, s_t in ((c.k[t, 0], c.k_scale), (c.v[t, 0], c.v_scale)):
+            _, _, ch = oracle.nvfp4_4over6_row(x.astype(np.float32), s_t)
+            n4 += int((ch == 4).sum())
+            n += ch.size
+    assert 0.1 < n4 / n < 0.9, n4 / n
 
 
 def test_tensor_amax_exact():
@@ -242,7 +272,7 @@ def test_decode_empty_and_single_token(mode):
     assert (out[0] == 0).all() and (out[3] == 0).all()
 
 
-@pytest.mark.parametrize("mode", ["int8_per_token_head", "nvfp4"])
+@pytest.mark.parametrize("mode", ["int8_per_token_head", "nvfp4", "int4_per_token_head"])
 def test_decode_bad_page_and_long_seq_are_flagged(mode):
     K = kvq()
     c = make_case(small_workload(mode), [300, 200], slack_pages=1)
