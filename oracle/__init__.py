@@ -94,6 +94,9 @@ def lib():
                                                 ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                                 ctypes.c_float, ctypes.c_int64, ctypes.c_int,
                                                 ctypes.c_int, f64p]),
+            "kvqo_decode_kvarn_tail": (ctypes.c_int, [u8p, ctypes.c_int, ctypes.c_int, f32p, i32p, ctypes.c_int,
+                                                      i32p, ctypes.c_int, ctypes.c_int, ctypes.c_double, f32p,
+                                                      f32p, i32p, ctypes.c_int, f64p]),
             "kvqo_decode": (ctypes.c_int, [ctypes.c_int, u8p, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                            ctypes.c_float, f32p, i32p, ctypes.c_int, i32p,
@@ -319,6 +322,31 @@ def decode(mode, pool: np.ndarray, num_pages: int, page_size: int, num_kv_heads:
                            bt.shape[1], _p(sl, ctypes.c_int32), B, Hq, softmax_scale,
                            None if rr is None else _p(rr, ctypes.c_int32),
                            0 if rr is None else len(rr), _p(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle decode rejected its arguments")
+    return out
+
+
+def decode_kvarn_tail(pool: np.ndarray, num_pages: int, num_kv_heads: int, q: np.ndarray,
+                      block_table: np.ndarray, seq_lens: np.ndarray, softmax_scale: float,
+                      tail_k: np.ndarray, tail_v: np.ndarray,
+                      rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """KVarN decode over quantized whole tiles plus each sequence's raw open
+    tile (tail_k / tail_v [num_seqs][128][Hkv][128]); fp64 output [B][Hq][128]."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    B, Hq, D = q.shape
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    tk = np.ascontiguousarray(tail_k, dtype=np.float32)
+    tv = np.ascontiguousarray(tail_v, dtype=np.float32)
+    assert tk.shape == (B, 128, num_kv_heads, D) and tv.shape == tk.shape
+    out = np.zeros((B, Hq, D), np.float64)
+    rr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    rc = lib().kvqo_decode_kvarn_tail(_p(pool, ctypes.c_uint8), num_pages, num_kv_heads, _p(q, ctypes.c_float),
+                                      _p(bt, ctypes.c_int32), bt.shape[1], _p(sl, ctypes.c_int32), B, Hq,
+                                      softmax_scale, _p(tk, ctypes.c_float), _p(tv, ctypes.c_float),
+                                      None if rr is None else _p(rr, ctypes.c_int32),
+                                      0 if rr is None else len(rr), _p(out, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle decode rejected its arguments")
     return out

@@ -707,3 +707,66 @@ int kvqo_decode(int mode, const uint8_t* pool, int num_pages, int P, int Hkv, in
   free(acc);
   return 0;
 }
+
+/* KVarN with an open tile [P2 注意事项: a tile is one 128-token page, and the
+ * backend keeps a small fixed decode workspace].  Read as: a sequence's last,
+ * incomplete tile is not quantized yet; its raw rows sit in a tail buffer and
+ * attention covers the quantized tiles plus those raw rows.  Written in the
+ * input domain: each stored row is dequantized and rotated back (x^ = H x^',
+ * H symmetric orthonormal), then o = sum_t softmax_t(q . k_t * scale) v_t over
+ * the sequence's tokens, max-subtracted, in fp64.  Tokens of an out-of-range
+ * page are left out; an empty sequence gives 0. */
+int kvqo_decode_kvarn_tail(const uint8_t* pool, int num_pages, int Hkv, const float* q,
+                           const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
+                           int Hq, double softmax_scale, const float* tail_k, const float* tail_v,
+                           const int32_t* rows, int n_rows, double* out) {
+  const int P = 128, D = 128;
+  int G, nr, ri, d;
+  double kv[128], vv[128], acc[128];
+  if (Hkv <= 0 || Hq % Hkv != 0) return -1;
+  G = Hq / Hkv;
+  nr = rows ? n_rows : B * Hq;
+  for (ri = 0; ri < nr; ri++) {
+    int row = rows ? rows[ri] : ri;
+    int b = row / Hq, hq = row % Hq, kvh = hq / G, n = seq_lens[b], nf = n - n % P, t, valid = 0;
+    double m = -INFINITY, l = 0.0, *s;
+    double* o = out + (size_t)row * D;
+    const float* qr = q + (size_t)row * D;
+    s = (double*)malloc(sizeof(double) * (n > 0 ? n : 1));
+    for (t = 0; t < n; t++) {               /* pass 1: scores */
+      double dot = 0.0;
+      if (t < nf) {
+        int32_t page = (t / P < max_pages) ? block_table[(size_t)b * max_pages + t / P] : -1;
+        if (page < 0 || page >= num_pages) { s[t] = -INFINITY; continue; }
+        kvqo_dequant_row(KVQO_KVARN_K4V2_G128, pool, num_pages, P, Hkv, D, 1.0f, 1.0f,
+                         (int64_t)page * P + t % P, kvh, 0, kv);
+        kvqo_hadamard_f64(kv, D);
+      } else {
+        for (d = 0; d < D; d++) kv[d] = tail_k[(((size_t)b * P + (t - nf)) * Hkv + kvh) * D + d];
+      }
+      for (d = 0; d < D; d++) dot += (double)qr[d] * kv[d];
+      s[t] = dot * softmax_scale;
+      if (s[t] > m) m = s[t];
+      valid++;
+    }
+    for (d = 0; d < D; d++) acc[d] = 0.0;
+    for (t = 0; t < n && valid; t++) {      /* pass 2: weights and values */
+      double p;
+      if (s[t] == -INFINITY) continue;
+      p = exp(s[t] - m);
+      l += p;
+      if (t < nf) {
+        int32_t page = block_table[(size_t)b * max_pages + t / P];
+        kvqo_dequant_row(KVQO_KVARN_K4V2_G128, pool, num_pages, P, Hkv, D, 1.0f, 1.0f,
+                         (int64_t)page * P + t % P, kvh, 1, vv);
+        kvqo_hadamard_f64(vv, D);
+      } else {
+        for (d = 0; d < D; d++) vv[d] = tail_v[(((size_t)b * P + (t - nf)) * Hkv + kvh) * D + d];
+      }
+      for (d = 0; d < D; d++) acc[d] += p * vv[d];
+    }
+    for (d = 0; d < D; d++) o[d] = valid ? acc[d] / l : 0.0;
+    free(s);
+  }
+  return 0;
+}

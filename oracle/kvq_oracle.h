@@ -93,6 +93,16 @@ int kvqo_decode(int mode, const uint8_t* pool, int num_pages, int page_size, int
                 int num_seqs, int num_q_heads, double softmax_scale, const int32_t* rows,
                 int n_rows, double* out);
 
+/* KVarN decode with an open tile: sequence b's first seq_len - seq_len % 128
+ * tokens come from its quantized tiles (dequantized and rotated back to the
+ * input domain, x^ = H x^'), the remaining seq_len % 128 from rows 0.. of its
+ * raw tail (tail_k / tail_v [num_seqs][128][Hkv][D] fp32); fp64 attention over
+ * all of them.  Returns 0 or -1. */
+int kvqo_decode_kvarn_tail(const uint8_t* pool, int num_pages, int num_kv_heads, const float* q,
+                           const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                           int num_seqs, int num_q_heads, double softmax_scale, const float* tail_k,
+                           const float* tail_v, const int32_t* rows, int n_rows, double* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -582,6 +582,61 @@ def test_decode_matches_torch_sdpa(mode):
             assert np.abs(K.transpose(1, 0, 2) - x).max() <= 0.5 * np.abs(x).max()
 
 
+def test_kvarn_tail_decode_matches_torch_sdpa():
+    """KVarN with open tiles: sequences of 0, 1, 100, 128, 200 and 383 tokens,
+    whole tiles quantized, the rest raw in the tail.  Against torch SDPA in fp64
+    over [scipy-Hadamard-rotated dequantized tiles; raw tail rows], and equal to
+    the whole-tile decode when no tail row is used."""
+    from scipy.linalg import hadamard
+    lens = np.array([0, 1, 100, 128, 200, 383], np.int32)
+    mode, P, D, Hkv, Hq = "kvarn_k4v2_g128", 128, 128, 2, 8
+    full = (lens // P) * P
+    w = wl.Workload(name="t", mode=mode, num_seqs=len(lens), num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                    page_size=P, io_dtype="f32", seed=77, seq_len_range=(1, 1))
+    lay = wl.paged_layout(w, np.maximum(lens, 1).astype(np.int32), slack_pages=1)
+    tail_k = np.zeros((len(lens), P, Hkv, D), np.float32)
+    tail_v = np.zeros_like(tail_k)
+    pool = np.zeros(oracle.pool_bytes(mode, lay.num_pages, P, Hkv, D), np.uint8)
+    seqs = []
+    for b, n in enumerate(lens):
+        k, v = wl.gen_kv_seq(w, b, int(n))
+        seqs.append((k.astype(np.float64), v.astype(np.float64)))
+        nf = int(full[b])
+        if nf:
+            slots = wl.slots_for_seq(w, lay, b)[:nf]
+            assert oracle.write(mode, pool, lay.num_pages, P, Hkv, D, k[:nf], v[:nf], slots) == 0
+        tail_k[b, :n - nf], tail_v[b, :n - nf] = k[nf:], v[nf:]
+    q = wl.gen_q(w).astype(np.float32)
+    sm = 1 / math.sqrt(D)
+    out = oracle.decode_kvarn_tail(pool, lay.num_pages, Hkv, q, lay.block_table, lens, sm, tail_k, tail_v)
+    H = hadamard(D).astype(np.float64) / math.sqrt(D)
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert (out[b] == 0).all()
+            continue
+        nf = int(full[b])
+        K = np.zeros((Hkv, n, D))
+        V = np.zeros_like(K)
+        for t in range(n):
+            for h in range(Hkv):
+                if t < nf:
+                    slot = int(lay.block_table[b, t // P]) * P + t % P
+                    K[h, t] = oracle.dequant_row(mode, pool, lay.num_pages, P, Hkv, D, 1.0, 1.0, slot, h, 0) @ H
+                    V[h, t] = oracle.dequant_row(mode, pool, lay.num_pages, P, Hkv, D, 1.0, 1.0, slot, h, 1) @ H
+                else:
+                    K[h, t], V[h, t] = seqs[b][0][t, h], seqs[b][1][t, h]
+        for hq in range(Hq):
+            qq = torch.from_numpy(q[b, hq].astype(np.float64))[None, None, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qq, torch.from_numpy(K[hq // (Hq // Hkv)])[None, None],
+                torch.from_numpy(V[hq // (Hq // Hkv)])[None, None], scale=sm)[0, 0, 0].numpy()
+            assert np.allclose(out[b, hq], ref, rtol=1e-9, atol=1e-9), (b, hq)
+    whole = np.array([l for l in lens if l % P == 0 and l > 0])
+    rows = [b * Hq + h for b in range(len(lens)) if lens[b] % P == 0 and lens[b] > 0 for h in range(Hq)]
+    ref_whole = oracle.decode(mode, pool, lay.num_pages, P, Hkv, D, q, lay.block_table, lens, sm, rows=rows)
+    assert whole.size and np.allclose(out.reshape(-1, D)[rows], ref_whole.reshape(-1, D)[rows], rtol=1e-12, atol=1e-12)
+
+
 def test_decode_special_cases():
     w = wl.Workload(name="t", mode="int8_per_token_head", num_seqs=3, num_q_heads=4, num_kv_heads=2,
                     head_dim=32, page_size=16, io_dtype="f32", seed=5, seq_len_range=(1, 1))
