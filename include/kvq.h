@@ -83,6 +83,7 @@ typedef enum { KVQ_F16 = 0, KVQ_F32 = 1 } kvq_dtype;
 #define KVQ_DEVERR_PARTIAL_TILE 0x4u /* KVarN: a write or a sequence that is not whole tiles */
 #define KVQ_DEVERR_SEQ_LEN 0x8u      /* a seq_len above max_seq_len or max_pages * page_size */
 #define KVQ_DEVERR_TIMEOUT 0x10u     /* a bounded wait on a copy ran out (work skipped) */
+#define KVQ_DEVERR_SEQ_ID 0x20u      /* kvq_kvarn_append: a seq_id outside [0, num_seqs) */
 
 typedef struct {
   int32_t num_pages;    /* pages in the pool */
@@ -200,6 +201,46 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
                                 int num_q_heads, int max_seq_len, int mode, float softmax_scale,
                                 void* out, int out_dtype, void* workspace, size_t workspace_bytes,
                                 void* stream);
+
+/* ---- KVarN open tiles ---------------------------------------------------
+ * [P2] 注意事项: a KVarN tile is exactly one 128-token page, and the backend
+ * keeps a small fixed decode workspace.  A sequence's last, incomplete tile is
+ * therefore held raw in a caller-owned tail buffer until its 128th token
+ * arrives, when it is quantized into its page; decode reads the quantized
+ * tiles plus the raw tail rows.
+ *
+ * Tail buffer (device, caller-owned, io_dtype): K rows [num_seqs][128][Hkv][D]
+ * followed by V rows of the same shape; row r of sequence b holds token
+ * 128 * floor(seq_len_b / 128) + r of that sequence, as written. */
+kvq_status kvq_kvarn_tail_bytes(const kvq_cache* cache, int num_seqs, size_t* bytes);
+
+/* Append tokens to their sequences' open tiles.  Token i (k, v [num_tokens][Hkv][D])
+ * belongs to sequence seq_ids[i] at slot slot_mapping[i] = 128 * page + r: it is
+ * copied to row r of that sequence's tail, and if r == 127 the tile is complete
+ * and the sequence's 128 tail rows are quantized into `page` exactly as a
+ * whole-tile kvq_quantize_write would.  Within one call a sequence's tokens
+ * must belong to one tile (a decode step appends one token per sequence; a
+ * prefill writes its whole tiles with kvq_quantize_write and appends the rest);
+ * otherwise the completed tile's rows may be overwritten first.  A negative
+ * slot skips the token; a slot past the pool (KVQ_DEVERR_SLOT_RANGE) or a
+ * seq_id outside [0, num_seqs) (KVQ_DEVERR_SEQ_ID) skips it and flags it.
+ * Cache mode must be KVQ_KVARN_K4V2_G128; `tail` is 16-byte aligned and at
+ * least kvq_kvarn_tail_bytes(num_seqs). */
+kvq_status kvq_kvarn_append(kvq_cache* cache, const void* k, const void* v, const int32_t* slot_mapping,
+                            const int32_t* seq_ids, int num_tokens, void* tail, int num_seqs, void* stream);
+
+/* KVarN decode over whole tiles plus each sequence's open tile: any seq_len;
+ * its first seq_len - seq_len % 128 tokens are read from the quantized pages
+ * (as kvq_decode_attention does) and the last seq_len % 128 from rows 0.. of
+ * the sequence's tail (raw, in the input domain).  The tail must hold
+ * num_seqs sequences.  Workspace: kvq_kvarn_decode_workspace_bytes (never 0:
+ * the tail is merged with the tiles' partial results by a second kernel). */
+kvq_status kvq_kvarn_decode_workspace_bytes(const kvq_cache* cache, int num_seqs, int num_q_heads,
+                                            int max_seq_len, size_t* bytes);
+kvq_status kvq_kvarn_decode_attention(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                                      int max_pages, const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                                      int max_seq_len, float softmax_scale, const void* tail, void* out,
+                                      int out_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Allocation-free variant of kvq_decode_attention.  (No counterpart on the
  * source pages: this is an interface for callers, not part of the method.)

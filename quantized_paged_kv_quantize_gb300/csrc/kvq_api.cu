@@ -320,6 +320,89 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
   return KVQ_OK;
 }
 
+// ---- KVarN open tiles
+kvq_status kvq_kvarn_tail_bytes(const kvq_cache* cache, int num_seqs, size_t* bytes) {
+  kvq_status s = check_cache(cache);
+  if (s) return s;
+  if (!bytes) return fail(KVQ_ERR_INVALID_ARG, "bytes is NULL");
+  if (cache->cfg.mode != KVQ_KVARN_K4V2_G128)
+    return fail(KVQ_ERR_MODE_MISMATCH, "mode %d has no open tiles (KVarN only)", cache->cfg.mode);
+  if (num_seqs < 0) return fail(KVQ_ERR_INVALID_ARG, "num_seqs < 0");
+  const size_t esz = cache->cfg.io_dtype == KVQ_F16 ? 2 : 4;
+  *bytes = (size_t)2 * num_seqs * 128 * cache->cfg.num_kv_heads * cache->cfg.head_dim * esz;
+  return KVQ_OK;
+}
+
+kvq_status kvq_kvarn_append(kvq_cache* cache, const void* k, const void* v, const int32_t* slot_mapping,
+                            const int32_t* seq_ids, int num_tokens, void* tail, int num_seqs, void* stream) {
+  kvq_status s = check_cache(cache);
+  if (s) return s;
+  if (cache->cfg.mode != KVQ_KVARN_K4V2_G128)
+    return fail(KVQ_ERR_MODE_MISMATCH, "kvq_kvarn_append needs a KVarN cache (mode %d)", cache->cfg.mode);
+  if (num_tokens < 0 || num_seqs < 0) return fail(KVQ_ERR_INVALID_ARG, "negative size");
+  if (num_tokens == 0) return KVQ_OK;
+  if (!k || !v || !slot_mapping || !seq_ids || !tail)
+    return fail(KVQ_ERR_INVALID_ARG, "NULL k, v, slot_mapping, seq_ids or tail");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(tail, 16) || !aligned(slot_mapping, 4) || !aligned(seq_ids, 4))
+    return fail(KVQ_ERR_INVALID_ARG, "k, v and tail must be 16-byte aligned");
+  cudaError_t e = kvq::launch_kvarn_append(cache, k, v, slot_mapping, seq_ids, num_tokens, tail, num_seqs,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return KVQ_OK;
+}
+
+kvq_status kvq_kvarn_decode_workspace_bytes(const kvq_cache* cache, int num_seqs, int num_q_heads, int max_seq_len,
+                                            size_t* bytes) {
+  kvq_status s = check_cache(cache);
+  if (s) return s;
+  if (!bytes) return fail(KVQ_ERR_INVALID_ARG, "bytes is NULL");
+  if (cache->cfg.mode != KVQ_KVARN_K4V2_G128)
+    return fail(KVQ_ERR_MODE_MISMATCH, "mode %d has no open tiles (KVarN only)", cache->cfg.mode);
+  if (num_seqs < 0 || num_q_heads <= 0 || max_seq_len < 0)
+    return fail(KVQ_ERR_INVALID_ARG, "bad sizes (num_seqs %d, num_q_heads %d, max_seq_len %d)", num_seqs,
+                num_q_heads, max_seq_len);
+  const kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs, num_q_heads, max_seq_len);
+  *bytes = (size_t)num_seqs * num_q_heads * p.num_splits * (cache->cfg.head_dim + 2) * sizeof(float);
+  return KVQ_OK;
+}
+
+kvq_status kvq_kvarn_decode_attention(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                                      int max_pages, const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                                      int max_seq_len, float softmax_scale, const void* tail, void* out,
+                                      int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  kvq_status s = check_cache(cache);
+  if (s) return s;
+  const kvq_cache_config& c = cache->cfg;
+  if (c.mode != KVQ_KVARN_K4V2_G128)
+    return fail(KVQ_ERR_MODE_MISMATCH, "kvq_kvarn_decode_attention needs a KVarN cache (mode %d)", c.mode);
+  if (num_seqs < 0 || max_pages < 0 || max_seq_len < 0) return fail(KVQ_ERR_INVALID_ARG, "negative size");
+  if (num_q_heads <= 0 || num_q_heads % c.num_kv_heads != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                c.num_kv_heads);
+  if (num_q_heads / c.num_kv_heads > 8)
+    return fail(KVQ_ERR_UNSUPPORTED, "GQA group %d > 8", num_q_heads / c.num_kv_heads);
+  if ((long long)max_seq_len > (long long)max_pages * c.page_size)
+    return fail(KVQ_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
+  if (out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return fail(KVQ_ERR_UNSUPPORTED, "out_dtype %d", out_dtype);
+  if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f)
+    return fail(KVQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+  if (num_seqs == 0) return KVQ_OK;
+  if (!q || !block_table || !seq_lens || !out || !tail)
+    return fail(KVQ_ERR_INVALID_ARG, "NULL q, table, lens, tail or out");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(tail, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return fail(KVQ_ERR_INVALID_ARG, "q, tail and out must be 16-byte aligned");
+  const kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs, num_q_heads, max_seq_len);
+  const size_t need = (size_t)num_seqs * num_q_heads * p.num_splits * (c.head_dim + 2) * sizeof(float);
+  if (!workspace || workspace_bytes < need)
+    return fail(KVQ_ERR_CAPACITY, "workspace needs %zu bytes, got %zu", need, workspace ? workspace_bytes : 0);
+  if (!aligned(workspace, 16)) return fail(KVQ_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  cudaError_t e = kvq::launch_decode(cache, p, q, block_table, max_pages, seq_lens, num_seqs, num_q_heads,
+                                     max_seq_len, softmax_scale, out, out_dtype, workspace,
+                                     static_cast<cudaStream_t>(stream), tail);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return KVQ_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

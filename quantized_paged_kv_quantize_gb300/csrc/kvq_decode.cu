@@ -841,7 +841,8 @@ DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int ma
 
 cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void* q, const int32_t* block_table,
                           int max_pages, const int32_t* seq_lens, int num_seqs, int num_q_heads, int max_seq_len,
-                          float softmax_scale, void* out, int out_dtype, void* workspace, cudaStream_t stream) {
+                          float softmax_scale, void* out, int out_dtype, void* workspace, cudaStream_t stream,
+                          const void* kvarn_tail) {
   DecodeArgs a;
   a.pool = c->base;
   a.q = q;
@@ -849,7 +850,7 @@ cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void
   a.seq_lens = seq_lens;
   a.out = out;
   a.ws_o = static_cast<float*>(workspace);
-  a.ws_ml = plan.num_splits > 1 ? a.ws_o + (size_t)num_seqs * num_q_heads * plan.num_splits * c->cfg.head_dim
+  a.ws_ml = (plan.num_splits > 1 || kvarn_tail) ? a.ws_o + (size_t)num_seqs * num_q_heads * plan.num_splits * c->cfg.head_dim
                                 : nullptr;
   a.num_pages = c->cfg.num_pages;
   a.Hkv = c->cfg.num_kv_heads;
@@ -864,6 +865,7 @@ cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void
   a.q_f32 = c->cfg.io_dtype == KVQ_F32;
   a.sm_log2 = softmax_scale * kLog2e;
   a.block_bytes = c->block_bytes;
+  a.tail = static_cast<const uint8_t*>(kvarn_tail);
   a.rows_per_block = c->rows_per_block;
   if (num_seqs == 0) return cudaSuccess;
   if (c->cfg.mode == KVQ_KVARN_K4V2_G128) return launch_kvarn_decode(a, stream);

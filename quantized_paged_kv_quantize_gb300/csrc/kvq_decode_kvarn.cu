@@ -129,14 +129,16 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
     if (first) set_error(pool, KVQ_DEVERR_SEQ_LEN);
     n = n < 0 ? 0 : lim;
   }
-  if (n % kT) {  // only whole tiles are readable
-    if (first) set_error(pool, KVQ_DEVERR_PARTIAL_TILE);
+  if (n % kT) {  // only whole tiles are quantized: the rest is read from the tail, if there is one
+    if (first && a.tail == nullptr) set_error(pool, KVQ_DEVERR_PARTIAL_TILE);
     n -= n % kT;
   }
+  // with a tail, every CTA leaves a partial result for the merge kernel
+  const bool direct = a.num_splits == 1 && a.tail == nullptr;
   const int t_begin = split * a.tokens_per_split;
   const int t_end = min(n, t_begin + a.tokens_per_split);
   if (t_begin >= t_end) {
-    if (a.num_splits == 1) {
+    if (direct) {
       for (int i = tid; i < a.G * kD; i += blockDim.x) {
         const long long o = ((long long)b * a.Hq + (long long)kvh * a.G + i / kD) * kD + i % kD;
         if (a.out_f32) static_cast<float*>(a.out)[o] = 0.0f;
@@ -456,7 +458,7 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
         O += red_o[(w * 8 + h) * kD + d] * e;
       }
     }
-    if (a.num_splits == 1) {
+    if (direct) {
       fin[idx] = L > 0.0f ? O / L : 0.0f;
     } else if (h < a.G) {
       const long long pi = ((long long)b * a.Hq + (long long)kvh * a.G + h) * a.num_splits + split;
@@ -467,7 +469,7 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
       }
     }
   }
-  if (a.num_splits == 1) {
+  if (direct) {
     __syncthreads();
     for (int h = warp; h < a.G; h += kW) {  // o = H o'
       float v[4];
@@ -485,15 +487,23 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
 }
 
 // Merge the splits of each (sequence, query head), then rotate back: o = H o'.
+// With a tail (open tiles), the merged tile result stays unnormalised, is
+// rotated back (H is linear) and joins the tail rows' terms, computed in the
+// input domain: scores q . k_t in fp32 (warp w takes rows w, w + 4, ..; lane l
+// channels 4l .. 4l + 3), then one max-subtracted softmax over both parts.
 __global__ void __launch_bounds__(kD) kvarn_combine_kernel(const __grid_constant__ DecodeArgs a) {
-  __shared__ float v[kD], wts[kD], red[kD / 32];
+  __shared__ float v[kD], wts[kD], red[kD / 32], tsc[kT];
   const int b = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, d = threadIdx.x;
+  const int lane = d & 31, warp = d >> 5;
   int n = a.seq_lens[b];
   const int lim = min(a.max_seq_len, a.max_pages * kT);
   n = n < 0 ? 0 : (n > lim ? lim : n);
+  const int nt = a.tail ? n % kT : 0;  // tail rows
   n -= n % kT;
   const int ns = (n + a.tokens_per_split - 1) / a.tokens_per_split;
-  const float r0 = merge_split_row<kD>(a, ((long long)b * a.Hq + hq) * a.num_splits, ns, wts, red);
+  float M = -INFINITY, L = 0.0f;
+  const float r0 = merge_split_row<kD>(a, ((long long)b * a.Hq + hq) * a.num_splits, ns, wts, red,
+                                       a.tail ? &M : nullptr, &L);
   v[d] = r0;
   __syncthreads();
   for (int h = 1; h < kD; h <<= 1) {  // Sylvester butterflies across threads
@@ -502,7 +512,52 @@ __global__ void __launch_bounds__(kD) kvarn_combine_kernel(const __grid_constant
     v[d] = (d & h) ? other - mine : mine + other;
     __syncthreads();
   }
-  const float r = v[d] * 0.08838834764831845f;
+  float r = v[d] * 0.08838834764831845f;
+  if (a.tail) {
+    const int kvh = hq / a.G;
+    const size_t esz = a.q_f32 ? 4 : 2;
+    const size_t row_elems = (size_t)a.Hkv * kD;                    // one tail row (token)
+    const uint8_t* tk = a.tail + ((size_t)b * kT * row_elems + (size_t)kvh * kD) * esz;
+    const uint8_t* tv = tk + (size_t)a.B * kT * row_elems * esz;    // the V rows follow the K rows
+    auto ld4 = [&](const uint8_t* base, size_t elem, float* x) {  // 4 consecutive elements
+      if (a.q_f32) {
+        const float4 u = __ldg(reinterpret_cast<const float4*>(base + elem * 4));
+        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+      } else {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(base + elem * 2));
+        const float2 f0 = __half22float2(u32_as_h2(u.x)), f1 = __half22float2(u32_as_h2(u.y));
+        x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
+      }
+    };
+    float qv[4];
+    ld4(static_cast<const uint8_t*>(a.q), ((size_t)b * a.Hq + hq) * kD + 4 * lane, qv);
+    for (int t = warp; t < nt; t += kD / 32) {
+      float kx[4];
+      ld4(tk, (size_t)t * row_elems + 4 * lane, kx);
+      float dot = qv[0] * kx[0] + qv[1] * kx[1] + qv[2] * kx[2] + qv[3] * kx[3];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
+      if (lane == 0) tsc[t] = dot * a.sm_log2;
+    }
+    __syncthreads();
+    // the tiles' (M, L, H acc) carry the 2^kPShift of the decode kernel's P: their max is M - kPShift
+    const float Mq = M - (float)kPShift;
+    float mt = Mq;
+    for (int t = 0; t < nt; ++t) mt = fmaxf(mt, tsc[t]);
+    float Lt = 0.0f, Ot = 0.0f;
+    if (mt != -INFINITY) {
+      const float wq = exp2f(Mq - mt);
+      Lt = L * wq;
+      Ot = r * wq;  // H acc, normalised rotation
+      for (int t = 0; t < nt; ++t) {
+        const float w = exp2f(tsc[t] - mt);
+        const uint8_t* vr = tv + ((size_t)t * row_elems + d) * esz;
+        Lt += w;
+        Ot += w * (a.q_f32 ? *reinterpret_cast<const float*>(vr) : __half2float(*reinterpret_cast<const __half*>(vr)));
+      }
+    }
+    r = Lt > 0.0f ? Ot / Lt : 0.0f;
+  }
   const long long oi = ((long long)b * a.Hq + hq) * kD + d;
   if (a.out_f32) static_cast<float*>(a.out)[oi] = r;
   else static_cast<__half*>(a.out)[oi] = __float2half_rn(r);
@@ -532,7 +587,7 @@ cudaError_t launch_kvarn_decode(const DecodeArgs& a, cudaStream_t s) {
   dim3 grid(a.num_splits, a.Hkv, a.B);
   kvarn_decode_kernel<<<grid, kW * 32, kSmem, s>>>(a);
   e = cudaGetLastError();
-  if (e != cudaSuccess || a.num_splits == 1) return e;
+  if (e != cudaSuccess || (a.num_splits == 1 && a.tail == nullptr)) return e;
   kvarn_combine_kernel<<<a.B * a.Hq, kD, 0, s>>>(a);
   return cudaGetLastError();
 }

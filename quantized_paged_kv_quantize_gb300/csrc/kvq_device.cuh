@@ -212,6 +212,9 @@ struct DecodeArgs {
   float sm_log2;  // softmax_scale * log2(e)
   size_t block_bytes;
   int rows_per_block;
+  // KVarN open tiles (kvq_kvarn_decode_attention): the tail buffer, K rows
+  // [B][128][Hkv][D] then V rows, io dtype; null for whole-tile decode
+  const uint8_t* tail;
 };
 
 // Split-KV merge of one (sequence, query head) row by a CTA of D threads,
@@ -221,7 +224,8 @@ struct DecodeArgs {
 // red[D / 32]) in chunks of D splits and each thread keeps eight partial loads
 // in flight, so a row costs a few memory round trips whatever the split count.
 template <int D>
-__device__ float merge_split_row(const DecodeArgs& a, long long base, int ns, float* wts, float* red) {
+__device__ float merge_split_row(const DecodeArgs& a, long long base, int ns, float* wts, float* red,
+                                 float* m_out = nullptr, float* l_out = nullptr) {
   constexpr int NW = D / 32;
   const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
   const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + base;
@@ -265,6 +269,11 @@ __device__ float merge_split_row(const DecodeArgs& a, long long base, int ns, fl
     lsum = 0.0f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) lsum += red[w];
+  }
+  if (m_out) {  // unnormalised: the caller merges more terms (M = -inf: no split had tokens)
+    *m_out = M;
+    *l_out = lsum;
+    return acc;
   }
   return lsum > 0.0f ? acc / lsum : 0.0f;
 }

@@ -32,6 +32,9 @@ int num_sms();
 
 cudaError_t launch_write(const kvq_cache* c, const void* k, const void* v, const int32_t* slots,
                          int num_tokens, cudaStream_t stream);
+cudaError_t launch_kvarn_append(const kvq_cache* c, const void* k, const void* v, const int32_t* slots,
+                                const int32_t* seq_ids, int num_tokens, void* tail, int num_seqs,
+                                cudaStream_t stream);
 cudaError_t launch_amax(const void* x, int dtype, size_t n, float* out, cudaStream_t stream);
 cudaError_t launch_scales_from_amax(uint8_t* pool, const float* amax_k, const float* amax_v, float div,
                                     cudaStream_t stream);
@@ -40,6 +43,6 @@ DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int ma
 cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void* q, const int32_t* block_table,
                           int max_pages, const int32_t* seq_lens, int num_seqs, int num_q_heads,
                           int max_seq_len, float softmax_scale, void* out, int out_dtype, void* workspace,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const void* kvarn_tail = nullptr);
 
 }  // namespace kvq

@@ -30,6 +30,11 @@ struct WriteArgs {
   long long num_tokens;
   int Hkv, P, log2P, num_pages;
   size_t block_bytes;
+  // KVarN open tiles (kvq_kvarn_append): sequence of each token, and the tail
+  // buffer, K rows [num_seqs][128][Hkv][D] then V rows, io dtype
+  const int32_t* seq_ids;
+  uint8_t* tail;
+  int num_seqs;
 };
 
 template <typename T>
@@ -573,37 +578,54 @@ __device__ __forceinline__ uint32_t rtn_code(float x, const QDiv& q, float steps
   return static_cast<uint32_t>(__float2int_rn(qv));
 }
 
-template <typename T>
+// TAIL = false: tile blockIdx.x is batch rows 128 x .. 128 x + 127 of k / v.
+// TAIL = true (kvq_kvarn_append): CTA blockIdx.x looks at batch token x; when
+// that token filled the last row of its tile (slot % 128 == 127), the tile is
+// the 128 rows of its sequence's tail, written to the token's page.
+template <typename T, bool TAIL>
 __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a) {
   extern __shared__ __align__(16) unsigned char kv_smem[];
   KvSmem& sm = *reinterpret_cast<KvSmem*>(kv_smem);
-  const int tile = blockIdx.x, h = blockIdx.y, side = blockIdx.z;
+  const int h = blockIdx.y, side = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int D = 128;
 
-  const long long t0 = (long long)tile * kKvTile;
+  const long long t0 = TAIL ? 0 : (long long)blockIdx.x * kKvTile;
+  const T* src;
+  int page = 0;
+  if constexpr (TAIL) {  // uniform per CTA; argument errors were flagged by the tail copy
+    const int slot = __ldg(a.slots + blockIdx.x), seq = __ldg(a.seq_ids + blockIdx.x);
+    if (slot < 0 || slot % kKvTile != kKvTile - 1 || slot / kKvTile >= a.num_pages || seq < 0 || seq >= a.num_seqs)
+      return;
+    page = slot / kKvTile;
+    const size_t side_bytes = (size_t)a.num_seqs * kKvTile * a.Hkv * D * sizeof(T);
+    src = reinterpret_cast<const T*>(a.tail + side * side_bytes) + (size_t)seq * kKvTile * a.Hkv * D;
+  } else {
+    src = static_cast<const T*>(side ? a.v : a.k);
+  }
   // This thread's half token (64 channels), loaded before the slot check so
   // that the two memory latencies overlap (rows t0 .. t0 + 127 always exist).
   const int t = tid >> 1, half = tid & 1;
   constexpr int NRAW = 64 * (int)sizeof(T) / 16;
   uint4 raw[NRAW];
   {
-    const uint4* row = reinterpret_cast<const uint4*>(static_cast<const T*>(side ? a.v : a.k) +
-                                                      ((t0 + t) * a.Hkv + h) * D + 64 * half);
+    const uint4* row = reinterpret_cast<const uint4*>(src + ((t0 + t) * a.Hkv + h) * D + 64 * half);
 #pragma unroll
     for (int k = 0; k < NRAW; ++k) raw[k] = __ldg(row + k);
   }
 
-  // A tile must be 128 consecutive slots starting a page.
-  const int s0 = __ldg(a.slots + t0);
-  int ok = 1;
-  if (tid < kKvTile) ok = (__ldg(a.slots + t0 + tid) == s0 + tid);
-  ok = __syncthreads_and(ok && s0 >= 0 && (s0 % kKvTile) == 0 && s0 / kKvTile < a.num_pages);
-  if (!ok) {
-    if (tid == 0 && h == 0 && side == 0) set_error(a.pool, KVQ_DEVERR_PARTIAL_TILE);
-    return;
+  if constexpr (!TAIL) {
+    // A tile must be 128 consecutive slots starting a page.
+    const int s0 = __ldg(a.slots + t0);
+    int ok = 1;
+    if (tid < kKvTile) ok = (__ldg(a.slots + t0 + tid) == s0 + tid);
+    ok = __syncthreads_and(ok && s0 >= 0 && (s0 % kKvTile) == 0 && s0 / kKvTile < a.num_pages);
+    if (!ok) {
+      if (tid == 0 && h == 0 && side == 0) set_error(a.pool, KVQ_DEVERR_PARTIAL_TILE);
+      return;
+    }
+    page = s0 / kKvTile;
   }
-  const int page = s0 / kKvTile;
   if (tid < kKvTile) {
     sm.fr[tid] = 1.0f;  // token factors r_t
     sm.fc[tid] = 1.0f;  // channel factors c_d
@@ -877,16 +899,65 @@ cudaError_t launch_mode(int mode, const WriteArgs& a, cudaStream_t s) {
   }
 }
 
-template <typename T>
+template <typename T, bool TAIL>
 cudaError_t launch_kvarn(const WriteArgs& a, cudaStream_t s) {
-  const long long tiles = a.num_tokens / kKvTile;
+  const long long tiles = TAIL ? a.num_tokens : a.num_tokens / kKvTile;
   if (tiles == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kvarn_write_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (tiles > 0x7fffffffLL || a.Hkv > 65535) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kvarn_write_kernel<T, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kKvSmem));
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(tiles), a.Hkv, 2);
-  kvarn_write_kernel<T><<<grid, kKvThreads, kKvSmem, s>>>(a);
+  kvarn_write_kernel<T, TAIL><<<grid, kKvThreads, kKvSmem, s>>>(a);
   return cudaGetLastError();
+}
+
+// KVarN open tiles: token i's K and V rows (16 bytes per thread) go to row
+// slot % 128 of sequence seq_ids[i]'s tail.  A negative slot skips the token;
+// a slot past the pool or a sequence id outside [0, num_seqs) skips it and
+// sets its error bit.
+template <typename T>
+__global__ void __launch_bounds__(256) kvarn_tail_copy_kernel(WriteArgs a) {
+  constexpr int D = 128, CH = D * (int)sizeof(T) / 16;  // 16-byte chunks per row
+  const long long n = a.num_tokens * a.Hkv * 2 * CH;
+  const size_t side_bytes = (size_t)a.num_seqs * kKvTile * a.Hkv * D * sizeof(T);
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(idx % CH);
+    const long long r = idx / CH;
+    const int side = (int)(r % 2);
+    const long long th = r / 2;
+    const int h = (int)(th % a.Hkv);
+    const long long i = th / a.Hkv;
+    const int slot = __ldg(a.slots + i), seq = __ldg(a.seq_ids + i);
+    if (slot < 0) continue;
+    if (slot / kKvTile >= a.num_pages) {
+      if (c == 0 && h == 0 && side == 0) set_error(a.pool, KVQ_DEVERR_SLOT_RANGE);
+      continue;
+    }
+    if (seq < 0 || seq >= a.num_seqs) {
+      if (c == 0 && h == 0 && side == 0) set_error(a.pool, KVQ_DEVERR_SEQ_ID);
+      continue;
+    }
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(side ? a.v : a.k) +
+                                                         (i * a.Hkv + h) * D) + c);
+    uint4* dst = reinterpret_cast<uint4*>(a.tail + side * side_bytes +
+                                          ((((size_t)seq * kKvTile + slot % kKvTile) * a.Hkv + h) * D) * sizeof(T));
+    dst[c] = v;
+  }
+}
+
+template <typename T>
+cudaError_t launch_kvarn_tail(const WriteArgs& a, cudaStream_t s) {
+  const long long chunks = a.num_tokens * a.Hkv * 2 * (128 * (long long)sizeof(T) / 16);
+  long long blocks = (chunks + 255) / 256;
+  const long long cap = (long long)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks == 0) return cudaSuccess;
+  kvarn_tail_copy_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_kvarn<T, true>(a, s);
 }
 
 }  // namespace
@@ -907,11 +978,34 @@ cudaError_t launch_write(const kvq_cache* c, const void* k, const void* v, const
   a.block_bytes = c->block_bytes;
   const int mode = c->cfg.mode, D = c->cfg.head_dim;
   const bool f16 = c->cfg.io_dtype == KVQ_F16;
+  a.seq_ids = nullptr;
+  a.tail = nullptr;
+  a.num_seqs = 0;
   if (mode == KVQ_KVARN_K4V2_G128)
-    return f16 ? launch_kvarn<__half>(a, stream) : launch_kvarn<float>(a, stream);
+    return f16 ? launch_kvarn<__half, false>(a, stream) : launch_kvarn<float, false>(a, stream);
   if (D == 128) return f16 ? launch_mode<__half, 128>(mode, a, stream) : launch_mode<float, 128>(mode, a, stream);
   if (D == 32) return f16 ? launch_mode<__half, 32>(mode, a, stream) : launch_mode<float, 32>(mode, a, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_kvarn_append(const kvq_cache* c, const void* k, const void* v, const int32_t* slots,
+                                const int32_t* seq_ids, int num_tokens, void* tail, int num_seqs,
+                                cudaStream_t stream) {
+  WriteArgs a;
+  a.pool = c->base;
+  a.k = k;
+  a.v = v;
+  a.slots = slots;
+  a.num_tokens = num_tokens;
+  a.Hkv = c->cfg.num_kv_heads;
+  a.P = c->cfg.page_size;
+  a.log2P = 7;
+  a.num_pages = c->cfg.num_pages;
+  a.block_bytes = c->block_bytes;
+  a.seq_ids = seq_ids;
+  a.tail = static_cast<uint8_t*>(tail);
+  a.num_seqs = num_seqs;
+  return c->cfg.io_dtype == KVQ_F16 ? launch_kvarn_tail<__half>(a, stream) : launch_kvarn_tail<float>(a, stream);
 }
 
 cudaError_t launch_amax(const void* x, int dtype, size_t n, float* out, cudaStream_t stream) {

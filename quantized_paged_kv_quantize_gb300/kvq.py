@@ -30,13 +30,15 @@ MODES = {
     "kvarn_k4v2_g128": 16,
 }
 KVQ_F16, KVQ_F32 = 0, 1
-DEVERR = {0x1: "SLOT_RANGE", 0x2: "PAGE_RANGE", 0x4: "PARTIAL_TILE", 0x8: "SEQ_LEN", 0x10: "TIMEOUT"}
+DEVERR = {0x1: "SLOT_RANGE", 0x2: "PAGE_RANGE", 0x4: "PARTIAL_TILE", 0x8: "SEQ_LEN", 0x10: "TIMEOUT",
+          0x20: "SEQ_ID"}
 
 EXPORTED = [
     "kvq_last_error", "kvq_version", "kvq_cache_bytes", "kvq_cache_block_bytes", "kvq_cache_alloc",
     "kvq_cache_free", "kvq_cache_set_tensor_scales", "kvq_tensor_amax",
     "kvq_cache_set_tensor_scales_from_amax", "kvq_cache_read_errors", "kvq_quantize_write",
     "kvq_decode_plan", "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_decode_attention_noalloc",
+    "kvq_kvarn_tail_bytes", "kvq_kvarn_append", "kvq_kvarn_decode_workspace_bytes", "kvq_kvarn_decode_attention",
 ]
 
 
@@ -75,6 +77,10 @@ def _load():
         "kvq_decode_workspace_bytes": (i32, [vp, i32, i32, i32, ctypes.POINTER(sz)]),
         "kvq_decode_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, f32, vp, i32, vp, sz, vp]),
         "kvq_decode_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, f32, vp, i32, vp]),
+        "kvq_kvarn_tail_bytes": (i32, [vp, i32, ctypes.POINTER(sz)]),
+        "kvq_kvarn_append": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, vp]),
+        "kvq_kvarn_decode_workspace_bytes": (i32, [vp, i32, i32, i32, ctypes.POINTER(sz)]),
+        "kvq_kvarn_decode_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, f32, vp, vp, i32, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -254,3 +260,42 @@ def kvq_decode_attention_noalloc(cache: KVCache, q, block_table, seq_lens, out, 
     _check(_lib.kvq_decode_attention_noalloc(cache.handle, _ptr(q), _ptr(block_table), mp, _ptr(seq_lens), B,
                                              Hq, max_seq_len, cache.mode if mode is None else _mode(mode), sm,
                                              _ptr(out), od, _stream(stream)))
+
+
+# ---- KVarN open tiles
+def kvq_kvarn_tail_bytes(cache: KVCache, num_seqs: int) -> int:
+    b = ctypes.c_size_t()
+    _check(_lib.kvq_kvarn_tail_bytes(cache.handle, num_seqs, ctypes.byref(b)))
+    return b.value
+
+
+def kvq_kvarn_append(cache: KVCache, k, v, slot_mapping, seq_ids, tail, num_seqs: int,
+                     num_tokens: Optional[int] = None, stream=None):
+    """Copy tokens into their sequences' open tiles (the tail buffer); a token that
+    fills row 127 of its tile has the tile quantized into its page."""
+    n = num_tokens if num_tokens is not None else int(slot_mapping.numel())
+    _check(_lib.kvq_kvarn_append(cache.handle, _ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(seq_ids), n,
+                                 _ptr(tail), num_seqs, _stream(stream)))
+
+
+def kvq_kvarn_decode_workspace_bytes(cache: KVCache, num_seqs: int, num_q_heads: int, max_seq_len: int) -> int:
+    ws = ctypes.c_size_t()
+    _check(_lib.kvq_kvarn_decode_workspace_bytes(cache.handle, num_seqs, num_q_heads, max_seq_len,
+                                                 ctypes.byref(ws)))
+    return ws.value
+
+
+def kvq_kvarn_decode_attention(cache: KVCache, q, block_table, seq_lens, tail, out, *, max_seq_len: int,
+                               workspace, num_seqs: Optional[int] = None, num_q_heads: Optional[int] = None,
+                               max_pages: Optional[int] = None, softmax_scale: Optional[float] = None,
+                               out_dtype=None, workspace_bytes: Optional[int] = None, stream=None):
+    """KVarN decode over the quantized whole tiles plus each sequence's open tile."""
+    B = num_seqs if num_seqs is not None else q.shape[0]
+    Hq = num_q_heads if num_q_heads is not None else q.shape[1]
+    mp = max_pages if max_pages is not None else block_table.shape[1]
+    sm = softmax_scale if softmax_scale is not None else cache.cfg.head_dim ** -0.5
+    od = _dtype_code(out.dtype) if out_dtype is None else _dtype_code(out_dtype)
+    wb = workspace_bytes if workspace_bytes is not None else workspace.numel() * workspace.element_size()
+    _check(_lib.kvq_kvarn_decode_attention(cache.handle, _ptr(q), _ptr(block_table), mp, _ptr(seq_lens), B, Hq,
+                                           max_seq_len, sm, _ptr(tail), _ptr(out), od, _ptr(workspace), wb,
+                                           _stream(stream)))
