@@ -637,6 +637,50 @@ def test_kvarn_tail_decode_matches_torch_sdpa():
     assert whole.size and np.allclose(out.reshape(-1, D)[rows], ref_whole.reshape(-1, D)[rows], rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("mode", ["int8_per_token_head", "nvfp4"])
+def test_decode_multi_matches_masked_sdpa(mode):
+    """Several queries per sequence: torch SDPA in fp64 with an explicit causal
+    mask (query i of nq stands at position n - nq + i) over the dequantized
+    K/V; nq = 1 is the plain decode; a query before the first token gets 0."""
+    lens = [37, 16, 3, 50]
+    nq = 4
+    w = wl.Workload(name="t", mode=mode, num_seqs=len(lens), num_q_heads=8, num_kv_heads=2,
+                    head_dim=128, page_size=16, io_dtype="f16", seed=43, seq_len_range=(1, 1))
+    lay = wl.paged_layout(w, np.array(lens, np.int32), slack_pages=1)
+    ks_, vs_, ss_ = [], [], []
+    for b in range(len(lens)):
+        k, v = wl.gen_kv_seq(w, b, lens[b])
+        ks_.append(k); vs_.append(v); ss_.append(wl.slots_for_seq(w, lay, b))
+    k, v, slots = np.concatenate(ks_), np.concatenate(vs_), np.concatenate(ss_)
+    kscale = oracle.tensor_scale(mode, oracle.amax(k.astype(np.float32)))
+    vscale = oracle.tensor_scale(mode, oracle.amax(v.astype(np.float32)))
+    pool = _fill(mode, w, lay, k, v, slots, kscale, vscale)
+    rng = np.random.default_rng(8)
+    q = rng.standard_normal((len(lens), nq, 8, 128)).astype(np.float32)
+    sm = 1 / math.sqrt(128)
+    out = oracle.decode_multi(mode, pool, lay.num_pages, 16, 2, 128, q, lay.block_table, lay.seq_lens, sm,
+                              kscale, vscale)
+    for b, n in enumerate(lens):
+        K, V = _dequant_seq(mode, w, lay, pool, b, kscale, vscale)
+        pos = n - nq + np.arange(nq)                                    # query positions
+        allowed = np.arange(n)[None, :] <= pos[:, None]                 # causal mask [nq][n]
+        for hq in range(8):
+            qq = torch.from_numpy(q[b, :, hq].astype(np.float64))[None, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qq, torch.from_numpy(K[hq // 4])[None, None], torch.from_numpy(V[hq // 4])[None, None],
+                attn_mask=torch.from_numpy(allowed)[None, None], scale=sm)[0, 0].numpy()
+            for i in range(nq):
+                if pos[i] < 0:
+                    assert (out[b, i, hq] == 0).all()
+                else:
+                    assert np.allclose(out[b, i, hq], ref[i], rtol=1e-9, atol=1e-9), (b, i, hq)
+    one = oracle.decode_multi(mode, pool, lay.num_pages, 16, 2, 128, q[:, -1:], lay.block_table, lay.seq_lens, sm,
+                              kscale, vscale)
+    plain = oracle.decode(mode, pool, lay.num_pages, 16, 2, 128, q[:, -1], lay.block_table, lay.seq_lens, sm,
+                          kscale, vscale)
+    assert np.array_equal(one[:, 0], plain)
+
+
 def test_decode_special_cases():
     w = wl.Workload(name="t", mode="int8_per_token_head", num_seqs=3, num_q_heads=4, num_kv_heads=2,
                     head_dim=32, page_size=16, io_dtype="f32", seed=5, seq_len_range=(1, 1))
