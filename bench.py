@@ -43,6 +43,8 @@ VARIANTS = {
     "pth_b64_u1k_32k:int4": ("pth_b64_u1k_32k", "int4_per_token_head"),
     "nvfp4_b32_s32768:4over6": ("nvfp4_b32_s32768", "nvfp4_4over6"),
 }
+# speculative-decoding shape: 4 causal queries per sequence over the same pages
+SPEC_VARIANTS = {"nvfp4_b32_s32768:spec4": ("nvfp4_b32_s32768", 4)}
 
 
 def measured_peaks():
@@ -101,21 +103,24 @@ class GpuWorkload:
             if keep_host:
                 self.host.append((k, v))
             off += n
-        self.q = torch.from_numpy(wl.gen_q(w)).to(device)
+        nq = w.num_queries
+        q = wl.gen_q(w, w.num_seqs * nq)
+        self.q = torch.from_numpy(q.reshape(w.num_seqs, nq, w.num_q_heads, w.head_dim) if nq > 1 else q).to(device)
         self.block_table = torch.from_numpy(self.lay.block_table).to(device)
         self.seq_lens = torch.from_numpy(lens).to(device)
         self.max_seq_len = int(lens.max())
         self.cfg = kvq.make_config(self.lay.num_pages, w.page_size, w.num_kv_heads, w.head_dim, w.mode, tdt)
         self.pool = torch.zeros(kvq.kvq_cache_bytes(self.cfg), dtype=torch.uint8, device=device)
         self.cache = kvq.kvq_cache_alloc(self.cfg, self.pool)
-        ns, tps, wsb = kvq.kvq_decode_plan(self.cache, w.num_seqs, w.num_q_heads, self.max_seq_len)
+        ns, tps, wsb = kvq.kvq_decode_plan(self.cache, w.num_seqs * nq, w.num_q_heads, self.max_seq_len)
         self.plan = (ns, tps, wsb)
         self.ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device=device)
-        self.out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=tdt, device=device)
+        self.out = torch.empty(tuple(self.q.shape), dtype=tdt, device=device)
         self.amax = torch.zeros(2, dtype=torch.float32, device=device)
-        # the decode step's append: the newest token of every sequence
-        last = (self.lay.token_offset[1:] - 1).astype(np.int64)
-        last = last[lens > 0]
+        # the decode step's append: the newest token of every sequence (the newest
+        # nq tokens when nq queries are verified per step)
+        ends = self.lay.token_offset[1:].astype(np.int64)
+        last = np.concatenate([np.arange(max(e - min(nq, int(n)), 0), e) for e, n in zip(ends, lens) if n > 0])
         idx = torch.from_numpy(last).to(device)
         self.step_k = self.K.index_select(0, idx).contiguous()
         self.step_v = self.V.index_select(0, idx).contiguous()
@@ -142,10 +147,15 @@ class GpuWorkload:
     def write_step(self):
         self.kvq.kvq_quantize_write(self.cache, self.step_k, self.step_v, self.step_slots)
 
-    def decode(self, out=None):
-        self.kvq.kvq_decode_attention(self.cache, self.q, self.block_table, self.seq_lens,
-                                      self.out if out is None else out, max_seq_len=self.max_seq_len,
-                                      workspace=self.ws)
+    def decode(self, out=None, q=None):
+        q = self.q if q is None else q
+        out = self.out if out is None else out
+        if self.w.num_queries > 1:
+            self.kvq.kvq_decode_attention_multi(self.cache, q, self.block_table, self.seq_lens, out,
+                                                max_seq_len=self.max_seq_len, workspace=self.ws)
+        else:
+            self.kvq.kvq_decode_attention(self.cache, q, self.block_table, self.seq_lens, out,
+                                          max_seq_len=self.max_seq_len, workspace=self.ws)
 
     def launches_per_step(self) -> int:
         return 1 + 1 + (1 if self.plan[0] > 1 else 0)
@@ -364,8 +374,7 @@ def run_ours(args, w: wl.Workload):
         v_d.copy_(v_h, non_blocking=True)
         s_d.copy_(s_h, non_blocking=True)
         gw.kvq.kvq_quantize_write(gw.cache, k_d, v_d, s_d)
-        gw.kvq.kvq_decode_attention(gw.cache, q_d, gw.block_table, gw.seq_lens, gw.out,
-                                    max_seq_len=gw.max_seq_len, workspace=gw.ws)
+        gw.decode(q=q_d)
         out_h.copy_(gw.out, non_blocking=True)
         t1.record(stream)
         t1.synchronize()
@@ -383,7 +392,7 @@ def run_ours(args, w: wl.Workload):
     result = None
     if rank == 0:
         cpu = cpu_baseline(w, args.cpu_seconds) if not args.no_cpu_baseline else None
-        tokens_heads = float(np.sum(lens.astype(np.int64))) * w.num_q_heads
+        tokens_heads = float(np.sum(lens.astype(np.int64))) * w.num_q_heads * w.num_queries
         result = {
             "metric": METRIC,
             "value": round(value, 2),
@@ -401,7 +410,11 @@ def run_ours(args, w: wl.Workload):
                 "workload": w.name, "mode": w.mode, "B": w.num_seqs, "Hq": w.num_q_heads,
                 "Hkv": w.num_kv_heads, "D": w.head_dim, "page_size": w.page_size,
                 "seq_len": w.seq_len if w.seq_len else list(w.seq_len_range),
-                "io_dtype": w.io_dtype, "step": "quantize-write of 1 new token/seq + decode attention",
+                "io_dtype": w.io_dtype,
+                "step": "quantize-write of 1 new token/seq + decode attention" if w.num_queries == 1 else
+                        f"quantize-write of {w.num_queries} new tokens/seq + causal decode of "
+                        f"{w.num_queries} queries/seq",
+                "queries_per_seq": w.num_queries,
                 "l2": ("inputs larger than L2 (%.2f GB packed cache)" % (cache_bytes / 1e9)) if flush is None
                 else "L2 flushed (256 MiB write) before each timed step",
                 "decode_splits": gw.plan[0], "tokens_per_split": gw.plan[1],
@@ -461,8 +474,24 @@ def oracle_sample(w: wl.Workload, seconds: float, start: int = 0):
     import oracle
     G = w.group
     esz = 2 if w.io_dtype == "f16" else 4
-    q_all = wl.gen_q(w).astype(np.float32)
+    nq = w.num_queries
+    q_all = wl.gen_q(w, w.num_seqs * nq).astype(np.float32)
     done_bytes, spent, units, u = 0, 0.0, 0, start
+    while nq > 1:  # one unit = one (sequence, kv head) group: its G query heads, every query
+        b, kvh = (u // w.num_kv_heads) % w.num_seqs, u % w.num_kv_heads
+        pool, npg, n, ks, vs = _oracle_seq_pool(w, b)
+        qb = q_all[b * nq:(b + 1) * nq].reshape(1, nq, w.num_q_heads, w.head_dim)
+        rows = (np.arange(nq)[:, None] * w.num_q_heads + kvh * G + np.arange(G)[None, :]).reshape(-1)
+        t0 = time.perf_counter()
+        oracle.decode_multi(w.mode, pool, npg, w.page_size, w.num_kv_heads, w.head_dim, qb,
+                            np.arange(npg, dtype=np.int32)[None], np.array([n], np.int32),
+                            1.0 / math.sqrt(w.head_dim), ks, vs, rows=rows)
+        spent += time.perf_counter() - t0
+        done_bytes += int(n * bytes_per_token_head(w)) + 2 * nq * G * w.head_dim * esz
+        units += 1
+        u += 1
+        if spent >= seconds:
+            return done_bytes, spent, units, u
     while True:
         b, kvh = (u // w.num_kv_heads) % w.num_seqs, u % w.num_kv_heads
         pool, npg, n, ks, vs = _oracle_seq_pool(w, b)
@@ -484,8 +513,11 @@ def cpu_baseline(w: wl.Workload, seconds: float):
     oracle.build()
     nb, sec, units, _ = oracle_sample(w, seconds)
     return {"value": round(nb / sec / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{units} (sequence, kv head) groups of {w.name} decoded by the single-threaded C oracle "
-                      f"(each: all {w.group} query heads over the full sequence), {sec:.1f} s"}
+            "sample": (f"{units} (sequence, kv head) groups of {w.name} decoded by the single-threaded C oracle "
+                       f"(each: all {w.group} query heads over the full sequence), {sec:.1f} s")
+            if w.num_queries == 1 else
+            (f"{units} (sequence, kv head) groups of {w.name} decoded by the single-threaded C oracle (each: "
+             f"all {w.group} query heads, {w.num_queries} causal queries over the full sequence), {sec:.1f} s")}
 
 
 def run_reference(args, w: wl.Workload):
@@ -522,7 +554,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS) + sorted(VARIANTS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(wl.WORKLOADS) + sorted(VARIANTS) + sorted(SPEC_VARIANTS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -534,6 +567,10 @@ def main(argv=None):
     if args.workload in VARIANTS:
         base, mode = VARIANTS[args.workload]
         w = wl.WORKLOADS[base].with_mode(mode)
+    elif args.workload in SPEC_VARIANTS:
+        import dataclasses
+        base, nq = SPEC_VARIANTS[args.workload]
+        w = dataclasses.replace(wl.WORKLOADS[base], num_queries=nq, name=args.workload)
     else:
         w = wl.WORKLOADS[args.workload]
     if args.num_seqs is not None:

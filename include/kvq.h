@@ -202,6 +202,26 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
                                 void* out, int out_dtype, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/* Multi-query decode: num_queries queries per sequence, as in speculative
+ * decoding or a short prefill chunk, over the same packed pages ([P5] "K 与 V
+ * 的量化误差进入 attention 的位置不同": A = softmax(QK^T/sqrt(d) + M), O = AV,
+ * with M the causal mask).  q and out are [num_seqs][num_queries][num_q_heads]
+ * [head_dim]; query i of sequence b stands at position seq_len_b - num_queries
+ * + i and attends to tokens 0 .. seq_len_b - num_queries + i (none, output 0,
+ * when that is negative).  Each query row streams its causal prefix of the
+ * sequence's pages; the rows of one sequence run side by side, so the pages
+ * they share are mostly served from L2.  Other arguments and rules are those of
+ * kvq_decode_attention; num_seqs * num_queries <= 65535; not available for
+ * KVQ_KVARN_K4V2_G128 (KVQ_ERR_UNSUPPORTED).  Workspace:
+ * kvq_decode_multi_workspace_bytes. */
+kvq_status kvq_decode_multi_workspace_bytes(const kvq_cache* cache, int num_seqs, int num_queries,
+                                            int num_q_heads, int max_seq_len, size_t* bytes);
+kvq_status kvq_decode_attention_multi(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                                      int max_pages, const int32_t* seq_lens, int num_seqs, int num_queries,
+                                      int num_q_heads, int max_seq_len, int mode, float softmax_scale,
+                                      void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
 /* ---- KVarN open tiles ---------------------------------------------------
  * [P2] 注意事项: a KVarN tile is exactly one 128-token page, and the backend
  * keeps a small fixed decode workspace.  A sequence's last, incomplete tile is

@@ -354,17 +354,19 @@ def decode_kvarn_tail(pool: np.ndarray, num_pages: int, num_kv_heads: int, q: np
 
 def decode_multi(mode, pool: np.ndarray, num_pages: int, page_size: int, num_kv_heads: int, head_dim: int,
                  q: np.ndarray, block_table: np.ndarray, seq_lens: np.ndarray, softmax_scale: float,
-                 k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
+                 k_scale: float = 1.0, v_scale: float = 1.0,
+                 rows: Optional[Sequence[int]] = None) -> np.ndarray:
     """Several queries per sequence under the causal mask of A = softmax(QK^T/sqrt(d) + M) V:
     q [B][nq][Hq][D]; query i of sequence b stands at position seq_len_b - nq + i and
     sees tokens 0 .. seq_len_b - nq + i (none if that is negative).  Written as the
     plain decode of B * nq sequences, query (b, i) reading sequence b's pages up to
-    its own causal length; fp64 output [B][nq][Hq][D]."""
+    its own causal length; fp64 output [B][nq][Hq][D] (rows: flat (b*nq + i)*Hq + h
+    indices to compute, the others left 0)."""
     q = np.ascontiguousarray(q, dtype=np.float32)
     B, nq, Hq, D = q.shape
     lens = np.asarray(seq_lens, np.int64)
     rows_len = np.maximum(lens[:, None] - (nq - 1 - np.arange(nq))[None, :], 0).astype(np.int32).reshape(-1)
     bt = np.repeat(np.ascontiguousarray(block_table, dtype=np.int32), nq, axis=0)
     out = decode(mode, pool, num_pages, page_size, num_kv_heads, head_dim, q.reshape(B * nq, Hq, D), bt,
-                 rows_len, softmax_scale, k_scale, v_scale)
+                 rows_len, softmax_scale, k_scale, v_scale, rows=rows)
     return out.reshape(B, nq, Hq, D)

@@ -320,6 +320,62 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
   return KVQ_OK;
 }
 
+// ---- multi-query decode
+kvq_status kvq_decode_multi_workspace_bytes(const kvq_cache* cache, int num_seqs, int num_queries, int num_q_heads,
+                                            int max_seq_len, size_t* bytes) {
+  kvq_status s = check_cache(cache);
+  if (s) return s;
+  if (!bytes) return fail(KVQ_ERR_INVALID_ARG, "bytes is NULL");
+  if (num_seqs < 0 || num_queries < 1 || num_q_heads <= 0 || max_seq_len < 0)
+    return fail(KVQ_ERR_INVALID_ARG, "bad sizes (num_seqs %d, num_queries %d, num_q_heads %d, max_seq_len %d)",
+                num_seqs, num_queries, num_q_heads, max_seq_len);
+  *bytes = kvq::plan_decode(cache, num_seqs * num_queries, num_q_heads, max_seq_len).workspace_bytes;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention_multi(const kvq_cache* cache, const void* q, const int32_t* block_table,
+                                      int max_pages, const int32_t* seq_lens, int num_seqs, int num_queries,
+                                      int num_q_heads, int max_seq_len, int mode, float softmax_scale, void* out,
+                                      int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  kvq_status s = check_cache(cache);
+  if (s) return s;
+  const kvq_cache_config& c = cache->cfg;
+  if (mode != c.mode)
+    return fail(KVQ_ERR_MODE_MISMATCH, "decode mode %d but the cache holds mode %d", mode, c.mode);
+  if (c.mode == KVQ_KVARN_K4V2_G128)
+    return fail(KVQ_ERR_UNSUPPORTED, "multi-query decode is not available for kvarn_k4v2_g128");
+  if (num_seqs < 0 || max_pages < 0 || max_seq_len < 0 || num_queries < 1)
+    return fail(KVQ_ERR_INVALID_ARG, "negative size or num_queries < 1");
+  if ((long long)num_seqs * num_queries > 65535)
+    return fail(KVQ_ERR_UNSUPPORTED, "num_seqs * num_queries = %lld > 65535", (long long)num_seqs * num_queries);
+  if (num_q_heads <= 0 || num_q_heads % c.num_kv_heads != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                c.num_kv_heads);
+  if (num_q_heads / c.num_kv_heads > 8)
+    return fail(KVQ_ERR_UNSUPPORTED, "GQA group %d > 8", num_q_heads / c.num_kv_heads);
+  if ((long long)max_seq_len > (long long)max_pages * c.page_size)
+    return fail(KVQ_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
+  if (out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return fail(KVQ_ERR_UNSUPPORTED, "out_dtype %d", out_dtype);
+  if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f)
+    return fail(KVQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+  if (num_seqs == 0) return KVQ_OK;
+  if (!q || !block_table || !seq_lens || !out) return fail(KVQ_ERR_INVALID_ARG, "NULL q, table, lens or out");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return fail(KVQ_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  const kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs * num_queries, num_q_heads, max_seq_len);
+  if (p.workspace_bytes > 0) {
+    if (!workspace || workspace_bytes < p.workspace_bytes)
+      return fail(KVQ_ERR_CAPACITY, "workspace needs %zu bytes, got %zu", p.workspace_bytes,
+                  workspace ? workspace_bytes : 0);
+    if (!aligned(workspace, 16)) return fail(KVQ_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  }
+  cudaError_t e = kvq::launch_decode(cache, p, q, block_table, max_pages, seq_lens, num_seqs, num_q_heads,
+                                     max_seq_len, softmax_scale, out, out_dtype, workspace,
+                                     static_cast<cudaStream_t>(stream), nullptr, num_queries);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return KVQ_OK;
+}
+
 // ---- KVarN open tiles
 kvq_status kvq_kvarn_tail_bytes(const kvq_cache* cache, int num_seqs, size_t* bytes) {
   kvq_status s = check_cache(cache);

@@ -422,16 +422,19 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   // 1024-byte alignment of the ring (swizzle patterns are address based)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
+  // b: the query row -- query b % nq of sequence b / nq (nq = 1: the sequence)
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, tq = lane & 3;
+  const int seq = b / a.nq;
 
-  int n = a.seq_lens[b];
+  int n = a.seq_lens[seq];
   const int lim = min(a.max_seq_len, a.max_pages * kPage);
   if (n > lim || n < 0) {
     if (threadIdx.x == 0 && split == 0 && kvh == 0) set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_SEQ_LEN);
     n = n < 0 ? 0 : lim;
   }
+  n = max(n - (a.nq - 1 - b % a.nq), 0);  // causal: the tokens up to the query's own position
   const int t_begin = split * a.tokens_per_split;
   const int t_end = min(n, t_begin + a.tokens_per_split);
   if (t_begin >= t_end) {
@@ -459,7 +462,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   // the warp's page ids (an out-of-range id is flagged and its page skipped)
   int* ids = page_ids + warp * kIdsPerWarp;
   for (int k = lane; k < my_count; k += 32) {
-    int pid = __ldg(a.block_table + (long long)b * a.max_pages + p0 + warp + kWarps * k);
+    int pid = __ldg(a.block_table + (long long)seq * a.max_pages + p0 + warp + kWarps * k);
     if (pid < 0 || pid >= a.num_pages) {
       set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_PAGE_RANGE);
       pid = -1;
@@ -697,10 +700,11 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
 template <int D>
 __global__ void __launch_bounds__(D) combine_kernel(const __grid_constant__ DecodeArgs a) {
   __shared__ float wts[D], red[D / 32];
-  const int b = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, d = threadIdx.x;
-  int n = a.seq_lens[b];
+  const int b = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, d = threadIdx.x;  // b: query row
+  int n = a.seq_lens[b / a.nq];
   const int lim = min(a.max_seq_len, a.max_pages * kPage);
   n = n < 0 ? 0 : (n > lim ? lim : n);
+  n = max(n - (a.nq - 1 - b % a.nq), 0);
   const int ns = (n + a.tokens_per_split - 1) / a.tokens_per_split;
   const float r = merge_split_row<D>(a, ((long long)b * a.Hq + hq) * a.num_splits, ns, wts, red);
   const long long oi = ((long long)b * a.Hq + hq) * D + d;
@@ -842,16 +846,19 @@ DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int ma
 cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void* q, const int32_t* block_table,
                           int max_pages, const int32_t* seq_lens, int num_seqs, int num_q_heads, int max_seq_len,
                           float softmax_scale, void* out, int out_dtype, void* workspace, cudaStream_t stream,
-                          const void* kvarn_tail) {
+                          const void* kvarn_tail, int num_queries) {
   DecodeArgs a;
   a.pool = c->base;
   a.q = q;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.out = out;
+  a.nq = num_queries;
+  num_seqs *= num_queries;  // query rows: q, out and the split partials are [num_seqs * nq][Hq]..
   a.ws_o = static_cast<float*>(workspace);
-  a.ws_ml = (plan.num_splits > 1 || kvarn_tail) ? a.ws_o + (size_t)num_seqs * num_q_heads * plan.num_splits * c->cfg.head_dim
-                                : nullptr;
+  a.ws_ml = (plan.num_splits > 1 || kvarn_tail)
+                ? a.ws_o + (size_t)num_seqs * num_q_heads * plan.num_splits * c->cfg.head_dim
+                : nullptr;
   a.num_pages = c->cfg.num_pages;
   a.Hkv = c->cfg.num_kv_heads;
   a.Hq = num_q_heads;

@@ -215,6 +215,9 @@ struct DecodeArgs {
   // KVarN open tiles (kvq_kvarn_decode_attention): the tail buffer, K rows
   // [B][128][Hkv][D] then V rows, io dtype; null for whole-tile decode
   const uint8_t* tail;
+  // queries per sequence (multi-query decode under the causal mask); B counts
+  // query rows, B = sequences * nq
+  int nq;
 };
 
 // Split-KV merge of one (sequence, query head) row by a CTA of D threads,

@@ -43,6 +43,6 @@ DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int ma
 cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void* q, const int32_t* block_table,
                           int max_pages, const int32_t* seq_lens, int num_seqs, int num_q_heads,
                           int max_seq_len, float softmax_scale, void* out, int out_dtype, void* workspace,
-                          cudaStream_t stream, const void* kvarn_tail = nullptr);
+                          cudaStream_t stream, const void* kvarn_tail = nullptr, int num_queries = 1);
 
 }  // namespace kvq

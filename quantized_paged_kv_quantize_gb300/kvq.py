@@ -39,6 +39,7 @@ EXPORTED = [
     "kvq_cache_set_tensor_scales_from_amax", "kvq_cache_read_errors", "kvq_quantize_write",
     "kvq_decode_plan", "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_decode_attention_noalloc",
     "kvq_kvarn_tail_bytes", "kvq_kvarn_append", "kvq_kvarn_decode_workspace_bytes", "kvq_kvarn_decode_attention",
+    "kvq_decode_multi_workspace_bytes", "kvq_decode_attention_multi",
 ]
 
 
@@ -78,6 +79,9 @@ def _load():
         "kvq_decode_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, f32, vp, i32, vp, sz, vp]),
         "kvq_decode_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, f32, vp, i32, vp]),
         "kvq_kvarn_tail_bytes": (i32, [vp, i32, ctypes.POINTER(sz)]),
+        "kvq_decode_multi_workspace_bytes": (i32, [vp, i32, i32, i32, i32, ctypes.POINTER(sz)]),
+        "kvq_decode_attention_multi": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, vp, i32, vp, sz,
+                                             vp]),
         "kvq_kvarn_append": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, vp]),
         "kvq_kvarn_decode_workspace_bytes": (i32, [vp, i32, i32, i32, ctypes.POINTER(sz)]),
         "kvq_kvarn_decode_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, f32, vp, vp, i32, vp, sz, vp]),
@@ -260,6 +264,31 @@ def kvq_decode_attention_noalloc(cache: KVCache, q, block_table, seq_lens, out, 
     _check(_lib.kvq_decode_attention_noalloc(cache.handle, _ptr(q), _ptr(block_table), mp, _ptr(seq_lens), B,
                                              Hq, max_seq_len, cache.mode if mode is None else _mode(mode), sm,
                                              _ptr(out), od, _stream(stream)))
+
+
+# ---- multi-query decode
+def kvq_decode_multi_workspace_bytes(cache: KVCache, num_seqs: int, num_queries: int, num_q_heads: int,
+                                     max_seq_len: int) -> int:
+    ws = ctypes.c_size_t()
+    _check(_lib.kvq_decode_multi_workspace_bytes(cache.handle, num_seqs, num_queries, num_q_heads, max_seq_len,
+                                                 ctypes.byref(ws)))
+    return ws.value
+
+
+def kvq_decode_attention_multi(cache: KVCache, q, block_table, seq_lens, out, *, max_seq_len: int,
+                               workspace=None, softmax_scale: Optional[float] = None, mode=None,
+                               out_dtype=None, workspace_bytes: Optional[int] = None, stream=None):
+    """q, out [num_seqs][num_queries][Hq][D]: query i of sequence b attends causally
+    to tokens 0 .. seq_len_b - num_queries + i."""
+    B, nq, Hq = q.shape[0], q.shape[1], q.shape[2]
+    sm = softmax_scale if softmax_scale is not None else cache.cfg.head_dim ** -0.5
+    od = _dtype_code(out.dtype) if out_dtype is None else _dtype_code(out_dtype)
+    wb = workspace_bytes if workspace_bytes is not None else (
+        0 if workspace is None else workspace.numel() * workspace.element_size())
+    _check(_lib.kvq_decode_attention_multi(cache.handle, _ptr(q), _ptr(block_table), block_table.shape[1],
+                                           _ptr(seq_lens), B, nq, Hq, max_seq_len,
+                                           cache.mode if mode is None else _mode(mode), sm, _ptr(out), od,
+                                           _ptr(workspace), wb, _stream(stream)))
 
 
 # ---- KVarN open tiles

@@ -349,3 +349,51 @@ def test_decode_kvarn_single_split_and_partial_tile():
     out2, _ = gpu_decode(cache2, c2, lens=np.array([200, 0], np.int32), max_seq_len=256)
     assert K.kvq_cache_read_errors(cache2) & 0x4
     check_attention(out2, oracle_decode(c2, pool2, lens=np.array([128, 0], np.int32)))
+
+
+# ------------------------------------------------------------------ multi-query decode
+@pytest.mark.parametrize("nq,out_dtype", [(2, torch.float32), (4, torch.float16), (7, torch.float32)])
+@pytest.mark.parametrize("mode", MODES4)
+def test_decode_multi_query_parity(mode, nq, out_dtype):
+    """nq queries per sequence under the causal mask, against the oracle; the
+    last query row of each sequence equals the plain decode of that query."""
+    K = kvq()
+    c = make_case(small_workload(mode), [3, 16, 100, 1000, 2500], slack_pages=1)
+    pool = oracle_pool(c)
+    cache = gpu_cache(c)
+    _upload_oracle_pool(cache, pool, c)
+    B, Hq, D = len(c.lay.seq_lens), c.w.num_q_heads, c.w.head_dim
+    rng = np.random.default_rng(nq)
+    q = rng.standard_normal((B, nq, Hq, D)).astype(c.w.np_dtype)
+    msl = int(c.lay.seq_lens.max())
+    wsb = K.kvq_decode_multi_workspace_bytes(cache, B, nq, Hq, msl)
+    ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+    out = torch.full((B, nq, Hq, D), float("nan"), dtype=out_dtype, device="cuda")
+    K.kvq_decode_attention_multi(cache, _dev(q), _dev(c.lay.block_table), _dev(c.lay.seq_lens), out,
+                                 max_seq_len=msl, workspace=ws)
+    torch.cuda.synchronize()
+    ref = oracle.decode_multi(c.w.mode, pool, c.lay.num_pages, c.w.page_size, c.w.num_kv_heads, D,
+                              q.astype(np.float32), c.lay.block_table, c.lay.seq_lens, 1.0 / math.sqrt(D),
+                              c.k_scale, c.v_scale)
+    check_attention(out.reshape(B * nq, Hq, D), ref.reshape(B * nq, Hq, D))
+    assert (out[0, :max(nq - 3, 0)] == 0).all()          # sequence of 3 tokens: queries before it see nothing
+    one = torch.empty((B, Hq, D), dtype=out_dtype, device="cuda")
+    ws1 = torch.empty(max(K.kvq_decode_workspace_bytes(cache, B, Hq, msl) // 4, 1), dtype=torch.float32,
+                      device="cuda")
+    K.kvq_decode_attention(cache, _dev(np.ascontiguousarray(q[:, -1])), _dev(c.lay.block_table),
+                           _dev(c.lay.seq_lens), one, max_seq_len=msl, workspace=ws1)
+    torch.cuda.synchronize()
+    check_attention(one, ref[:, -1])
+    assert K.kvq_cache_read_errors(cache) == 0
+
+
+def test_decode_multi_query_rejects_kvarn():
+    K = kvq()
+    c = make_case(small_workload("kvarn_k4v2_g128"), [128])
+    cache = gpu_cache(c)
+    q = torch.zeros((1, 2, 16, 128), dtype=torch.float16, device="cuda")
+    out = torch.empty_like(q)
+    with pytest.raises(K.KVQError) as e:
+        K.kvq_decode_attention_multi(cache, q, _dev(c.lay.block_table), _dev(c.lay.seq_lens), out,
+                                     max_seq_len=128)
+    assert e.value.status == 2

@@ -65,6 +65,7 @@ class Workload:
     outlier_channels: int = 0         # number of (kv head, dim) channels scaled by channel_gain
     channels_per_head: bool = False   # if True, outlier_channels is per kv head
     channel_gain: float = 1.0
+    num_queries: int = 1              # queries per sequence per decode step (causal; >1: speculative decoding)
     description: str = ""
 
     @property
@@ -261,7 +262,7 @@ def decode_bytes(w: Workload, lens: np.ndarray, bytes_per_token_head: float, sca
     token, the per-tensor scales, q in and out."""
     esz = 2 if w.io_dtype == "f16" else 4
     kv = int(round(float(np.sum(lens.astype(np.int64))) * w.num_kv_heads * bytes_per_token_head))
-    return kv + scale_bytes + 2 * w.num_seqs * w.num_q_heads * w.head_dim * esz
+    return kv + scale_bytes + 2 * w.num_seqs * w.num_queries * w.num_q_heads * w.head_dim * esz
 
 
 def describe(w: Workload) -> dict:
