@@ -106,10 +106,14 @@ typedef struct kvq_cache kvq_cache;
  *   INT4 PTH       : K[P][D/2] | V[P/2][D] | K scale[P] f32 | V scale[P] f32
  *   KVarN (P=D=128): K[128][64] u4 | V[128][32] u2 |
  *                    K scale[D] zero[D] c[D] r[P] f32 | V scale[P] zero[P] r[P] c[D] f32
- * 4-bit codes (E2M1, or two's-complement int4): the even head_dim index in the
- * low nibble, except 4-bit V (NVFP4, INT4), whose byte [k][d] holds channel d
- * of tokens 2k (low nibble) and 2k+1 -- the pairing decode's tensor-core
- * fragments take, with no nibble shuffling.
+ * 4-bit codes: NVFP4 K (E2M1) the even head_dim index in the low nibble;
+ * NVFP4 V byte [k][d] holds channel d of tokens 2k (low nibble) and 2k+1 --
+ * the pairing decode's tensor-core fragments take, with no nibble shuffling.
+ * INT4 (two's complement) in 32-bit little-endian words, nibble k = bits
+ * 4k..4k+3: a K row word m holds channel 8m + 2k in nibble k < 4 and
+ * 8m + 2(k-4) + 1 in nibble k >= 4; a V pair row [k] word m holds channel
+ * 4m + k of token 2k' = 2k in nibble k < 4 and channel 4m + k - 4 of token
+ * 2k + 1 in nibble k >= 4 -- the orders one lop3 turns into f16 pairs.
  * 2-bit codes: element 4i+j in bits 2j..2j+1 of byte i.  The header holds, at byte 16 and
  * 20, the per-tensor K and V scales (FP8 per-tensor s; NVFP4 s_t), and at
  * byte 12 the device error word.  This is the same content as the in-page

@@ -417,6 +417,8 @@ void kvqo_hadamard_f64(double* x, int n) {
 /*   INT8/FP8 PTH   : K[P][D] | V[P][D] | K scale[P] f32 | V scale[P] f32       */
 /*   NVFP4, 4over6  : K[P][D/2] | V[P/2][D] | K s_b[P][D/16] | V s_b[P][D/16]   */
 /*   INT4 PTH       : K[P][D/2] | V[P/2][D] | K scale[P] f32 | V scale[P] f32   */
+/*     with its own nibble order inside each 32-bit word (see int4_k_nibble,    */
+/*     int4_v_nibble)                                                            */
 /*   KVarN (P=D=128): K[128][64] 4-bit | V[128][32] 2-bit |                      */
 /*                    K scale[D] zero[D] c[D] r[P] | V scale[P] zero[P] r[P] c[D] */
 /* 4-bit: even index in the low nibble (4-bit V of NVFP4 and INT4: byte [k][d] */
@@ -449,6 +451,24 @@ static uint8_t* block_at(uint8_t* pool, int mode, int P, int Hkv, int D, int64_t
 
 static void put_f32(uint8_t* p, float v) { memcpy(p, &v, 4); }
 static float get_f32(const uint8_t* p) { float v; memcpy(&v, p, 4); return v; }
+
+/* INT4 storage order.  Inside each 4-byte word of a K row (8 channels 8m ..
+ * 8m+7) nibble k (bits 4k .. 4k+3) holds channel 8m + 2k for k < 4 and
+ * 8m + 2(k-4) + 1 for k >= 4: even channels in the low half-word, odd ones in
+ * the high half-word.  Inside each 4-byte word of a V token-pair row (channels
+ * 4m .. 4m+3 of tokens 2j, 2j+1) nibble k holds channel 4m + k of token 2j for
+ * k < 4 and channel 4m + k - 4 of token 2j+1 for k >= 4.  These give the byte
+ * and the shift of one code. */
+static void int4_k_nibble(int d, int* byte, int* shift) {
+  int e = d % 8, k = (e & 1) ? 4 + e / 2 : e / 2;
+  *byte = 4 * (d / 8) + k / 2;
+  *shift = 4 * (k & 1);
+}
+static void int4_v_nibble(int t, int d, int* byte, int* shift) {
+  int k = 4 * (t & 1) + d % 4;
+  *byte = 4 * (d / 4) + k / 2;
+  *shift = 4 * (k & 1);
+}
 
 /* Token `off`'s value codes (packed two per byte, even channel low) into its
  * nibble of each byte of its token pair's row. */
@@ -557,8 +577,16 @@ int kvqo_write(int mode, uint8_t* pool, int num_pages, int P, int Hkv, int D, co
             uint8_t* dst = side ? packed : blk + (size_t)off * D / 2;
             if (D > 1024) return -1;
             if (mode == KVQO_INT4_PER_TOKEN_HEAD) {
-              kvqo_quant_row_int4_pth(x, D, dst, &s);
+              uint8_t* row = side ? blk + (size_t)P * D / 2 + (size_t)(off / 2) * D : blk + (size_t)off * D / 2;
+              int d, by, sh;
+              kvqo_quant_row_int4_pth(x, D, packed, &s);
               put_f32(blk + (size_t)P * D + (size_t)side * 4 * P + 4 * off, s);
+              for (d = 0; d < D; d++) {           /* the storage order above */
+                uint8_t code = (d & 1) ? (uint8_t)(packed[d / 2] >> 4) : (uint8_t)(packed[d / 2] & 15);
+                if (side) int4_v_nibble(off, d, &by, &sh); else int4_k_nibble(d, &by, &sh);
+                row[by] = (uint8_t)((row[by] & ~(15 << sh)) | (code << sh));
+              }
+              break;
             } else {
               uint8_t* bs = blk + (size_t)P * D + (size_t)side * P * D / 16 + (size_t)off * D / 16;
               if (mode == KVQO_NVFP4) kvqo_quant_row_nvfp4(x, D, side ? v_scale : k_scale, dst, bs);
@@ -601,11 +629,12 @@ int kvqo_dequant_row(int mode, const uint8_t* pool, int num_pages, int P, int Hk
       return 0;
     }
     case KVQO_INT4_PER_TOKEN_HEAD: {
-      const uint8_t* row = blk + (size_t)t * D / 2;                               /* K */
-      const uint8_t* pair = blk + (size_t)P * D / 2 + (size_t)(t / 2) * D;         /* V */
+      const uint8_t* row = side ? blk + (size_t)P * D / 2 + (size_t)(t / 2) * D : blk + (size_t)t * D / 2;
       double s = get_f32(blk + (size_t)P * D + (size_t)side * 4 * P + 4 * t);
       for (d = 0; d < D; d++) {
-        int nib = side ? (pair[d] >> (4 * (t & 1))) & 15 : ((d & 1) ? row[d / 2] >> 4 : row[d / 2] & 15);
+        int by, sh, nib;
+        if (side) int4_v_nibble(t, d, &by, &sh); else int4_k_nibble(d, &by, &sh);
+        nib = (row[by] >> sh) & 15;
         out[d] = s * (double)(nib >= 8 ? nib - 16 : nib);
       }
       return 0;

@@ -104,20 +104,27 @@ __device__ __forceinline__ int swz(int off) {
   return off ^ (((off >> 7) & MASK) << 4);
 }
 
-// Four bytes of two's-complement 4-bit pairs -> four exact f16x2 (byte i ->
-// out[i], low nibble -> low half).  The biased nibble b = n + 8 goes into an
-// f16 mantissa as 1024 + b (low half) and 1024 + 16 b (high half); one f16x2
-// fma maps them to n: (1024 + b) * 1 - 1032 and (1024 + 16 b) * 2^-4 - 72.
-__device__ __forceinline__ void s4x8_to_f16x2x4(uint32_t w, uint32_t* out) {
-  const uint32_t b = w ^ 0x88888888u;
-  const __half2 mul = __halves2half2(__ushort_as_half(0x3C00), __ushort_as_half(0x2C00));  // 1, 2^-4
-  const __half2 add = __halves2half2(__ushort_as_half(0xE408), __ushort_as_half(0xD480));  // -1032, -72
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t y = prmt(b, 0u, 0x4040u + 0x0101u * i);  // byte i in both halves
-    const uint32_t t = bitsel(y, 0x64006400u, 0x00F0000Fu);
-    out[i] = h2_as_u32(__hfma2(u32_as_h2(t), mul, add));
-  }
+// One INT4 storage word (eight two's-complement 4-bit codes) -> four exact
+// f16x2, out[i] = (nibble i, nibble i + 4): for a key word the channel pairs
+// (2i, 2i + 1), for a value word channel i of the even and of the odd token.
+// One lop3 per register: with two constant operands it maps each bit to 0, 1,
+// w or ~w (LUT 0x6A: per bit (K1, K2) = (0,0) -> 0, (0,1) -> 1, (1,0) -> w,
+// (1,1) -> ~w), so it selects two nibbles, flips their top bit (the code
+// biased by 8) and supplies f16 1024 (nibble at mantissa bits 0-3) or 64
+// (mantissa bits 4-7, step 1); one f16x2 subtraction of 1032 or 72 leaves
+// the signed code.
+__device__ __forceinline__ uint32_t lop3_sel(uint32_t w, uint32_t k1, uint32_t k2) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(w), "r"(k1), "r"(k2));
+  return r;
+}
+__device__ __forceinline__ void s4w_to_f16x2x4(uint32_t w, uint32_t* out) {
+  const __half2 c1032 = u32_as_h2(0x64086408u), c72 = u32_as_h2(0x54805480u);
+  const uint32_t w8 = w >> 8;
+  out[0] = h2_as_u32(__hsub2(u32_as_h2(lop3_sel(w, 0x000F000Fu, 0x64086408u)), c1032));
+  out[1] = h2_as_u32(__hsub2(u32_as_h2(lop3_sel(w, 0x00F000F0u, 0x54805480u)), c72));
+  out[2] = h2_as_u32(__hsub2(u32_as_h2(lop3_sel(w8, 0x000F000Fu, 0x64086408u)), c1032));
+  out[3] = h2_as_u32(__hsub2(u32_as_h2(lop3_sel(w8, 0x00F000F0u, 0x54805480u)), c72));
 }
 
 // int8 pair (bytes 0,1 or 2,3 of w) -> exact f16x2 via 1024 + (x + 128) - 1152.
@@ -203,8 +210,8 @@ __device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
         uint32_t fg[4], fh[4];
-        s4x8_to_f16x2x4(kg[p][w], fg);
-        s4x8_to_f16x2x4(kh8[p][w], fh);
+        s4w_to_f16x2x4(kg[p][w], fg);
+        s4w_to_f16x2x4(kh8[p][w], fh);
 #pragma unroll
         for (int hlf = 0; hlf < 2; ++hlf) {
           const int j = 2 * w + hlf;
@@ -282,9 +289,9 @@ __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq
   constexpr int MTILES = C::MTILES;
   const int r0 = 2 * tq, r1 = 2 * tq + 1, r2 = 2 * tq + 8, r3 = 2 * tq + 9;  // tokens
   if constexpr (MODE == KVQ_INT4_PER_TOKEN_HEAD) {
-    // Token-pair rows as for NVFP4 below; the per-token V scale is folded into
-    // P, and a token past seq_len has p = 0 with finite codes, so nothing is
-    // masked here.
+    // Token-pair rows (each word: 4 channels of the pair's two tokens); the
+    // per-token V scale is folded into P, and a token past seq_len has p = 0
+    // with finite codes, so nothing is masked here.
     constexpr int CPG = D / 8;
     constexpr int VW = CPG / 4;
     uint32_t W0[NP][VW], W2[NP][VW];
@@ -299,8 +306,8 @@ __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq
 #pragma unroll
       for (int w = 0; w < VW; ++w) {
         uint32_t f0[4], f2[4];  // byte e of the word: channel cgb + 4w + e
-        s4x8_to_f16x2x4(W0[p][w], f0);
-        s4x8_to_f16x2x4(W2[p][w], f2);
+        s4w_to_f16x2x4(W0[p][w], f0);
+        s4w_to_f16x2x4(W2[p][w], f2);
         uint32_t av[2][4];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {

@@ -137,10 +137,11 @@ struct QDiv {
     return w;
   }
   // N <= 8 signed 4-bit codes clamp(rint(x/s), -7, 7) of x[0..N), two's
-  // complement, packed two per byte with x[0] in the low nibble.  Same rint
-  // as int8x4; the fast path requires both ends inside [-7, 7] (bit patterns
-  // 0x4B400000 -7 .. +7), whose low nibble is then the code.
-  template <int N>
+  // complement.  Same rint as int8x4; the fast path requires both ends inside
+  // [-7, 7] (bit patterns 0x4B400000 -7 .. +7), whose low nibble is then the
+  // code.  KEY = false: x[e] in nibble e.  KEY = true, the key-word order of
+  // an 8-channel group: x[e] in nibble e/2 for even e, 4 + e/2 for odd e.
+  template <int N, bool KEY = false>
   __device__ __forceinline__ uint32_t int4x8(const float* x) const {
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
     uint32_t lo[N], bad = fast ? 0u : 1u;
@@ -159,7 +160,7 @@ struct QDiv {
     }
     uint32_t w = 0;
 #pragma unroll
-    for (int e = 0; e < N; ++e) w |= (lo[e] & 0xFu) << (4 * e);
+    for (int e = 0; e < N; ++e) w |= (lo[e] & 0xFu) << (4 * (KEY ? ((e & 1) ? 4 + e / 2 : e / 2) : e));
     return w;
   }
   // eight E2M1 codes (pairs packed low nibble first) of x[0..n)
@@ -308,9 +309,16 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
     for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
     amax = group_max<TPR>(amax);
     const float s = __fdiv_rn(fmaxf(amax, 1e-8f), 7.0f);
-    uint32_t w[1] = {QDiv(s).int4x8<VEC>(x)};
+    // a key word holds an 8-channel group, even channels in its low half-word:
+    // with 4 values per thread, two lanes fill one word (the odd lane's
+    // channels 4..7 sit one byte higher) and the even lane stores it
+    uint32_t w[1] = {QDiv(s).int4x8<VEC, true>(x)};
+    if constexpr (VEC == 4) {
+      if (j & 1) w[0] <<= 8;
+      w[0] |= __shfl_xor_sync(kFull, w[0], 1);
+    }
     if (active) {
-      store_bytes<VEC / 2>(blk + (size_t)off * D / 2 + j * VEC / 2, w);
+      if (VEC == 8 || (j & 1) == 0) store_bytes<4>(blk + (size_t)off * D / 2 + (j * VEC / 8) * 4, w);
       if (j == 0) *reinterpret_cast<float*>(blk + (size_t)a.P * D + 4 * off) = s;
     }
   }
@@ -394,6 +402,26 @@ __device__ __forceinline__ void pair_values_pass(const WriteArgs& a, int h, cons
     const int page = s >> a.log2P, off = s & (a.P - 1);
     uint8_t* dst = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes + (size_t)a.P * D / 2 +
                    (size_t)(off >> 1) * D + j * VEC;
+    if constexpr (MODE == KVQ_INT4_PER_TOKEN_HEAD) {
+      // INT4 pair-row word: 4 channels of the even token in the low half-word,
+      // the same channels of the odd token in the high half-word
+      if (!(s & 1) && next == s + 1) {
+        const uint2 both = make_uint2(prmt(wr[r], other, 0x5410u), prmt(wr[r], other, 0x7632u));
+        if constexpr (VEC == 8) *reinterpret_cast<uint2*>(dst) = both;
+        else *reinterpret_cast<uint32_t*>(dst) = both.x;
+      } else {
+        const int sh = 16 * (off & 1);
+        const uint32_t m = 0xFFFFu << sh;
+        unsigned int* wd = reinterpret_cast<unsigned int*>(dst);
+        atomicAnd(wd, ~m);
+        atomicOr(wd, (wr[r] & 0xFFFFu) << sh);
+        if constexpr (VEC == 8) {
+          atomicAnd(wd + 1, ~m);
+          atomicOr(wd + 1, (wr[r] >> 16) << sh);
+        }
+      }
+      continue;
+    }
     if (!(s & 1) && next == s + 1) {
       // even channels: my low nibbles | the successor's low nibbles << 4; odd
       // channels: my high nibbles >> 4 | the successor's high nibbles; then

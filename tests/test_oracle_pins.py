@@ -256,12 +256,33 @@ def test_per_token_head_scale_counts():
     assert oracle.block_bytes("fp8_per_tensor", P, D) // P * Hkv == 4096 // 2
 
 
+def _int4_words(codes_k, codes_e, codes_o):
+    """INT4 storage words written out from the layout text: a K row word m holds
+    channels 8m, 8m+2, 8m+4, 8m+6 in nibbles 0-3 and 8m+1, .., 8m+7 in nibbles
+    4-7; a V pair-row word m holds channels 4m..4m+3 of the even token in
+    nibbles 0-3 and of the odd token in nibbles 4-7."""
+    D = codes_k.size
+    kw = np.zeros(D // 8, np.uint32)
+    for m in range(D // 8):
+        for k in range(8):
+            ch = 8 * m + (2 * k if k < 4 else 2 * (k - 4) + 1)
+            kw[m] |= np.uint32(int(codes_k[ch]) << (4 * k))
+    vw = np.zeros(D // 4, np.uint32)
+    for m in range(D // 4):
+        for k in range(8):
+            src = codes_e if k < 4 else codes_o
+            vw[m] |= np.uint32(int(src[4 * m + k % 4]) << (4 * k))
+    return kw, vw
+
+
 @pytest.mark.parametrize("mode", ["nvfp4", "nvfp4_4over6", "int4_per_token_head"])
 def test_4bit_value_bytes_pair_tokens(mode):
-    """The pool's 4-bit value payload pairs tokens: byte [k][d] of a page holds
-    channel d of tokens 2k (low nibble) and 2k+1, each the code quant_row gives
-    for that token alone; keys and scales stay per token; the bytes do not
-    depend on the order the tokens are written in."""
+    """The pool's 4-bit value payload pairs tokens: a V row of D bytes holds
+    the codes of tokens 2k and 2k+1 (NVFP4: byte d holds channel d of token 2k
+    in the low nibble and of 2k+1 in the high one; INT4: the word order of the
+    layout text), each the code quant_row gives for that token alone; keys and
+    scales stay per token; the bytes do not depend on the order the tokens are
+    written in."""
     P, Hkv, D = 16, 1, 128
     rng = np.random.default_rng(5)
     k = rng.standard_normal((P, Hkv, D)).astype(np.float32)
@@ -278,16 +299,26 @@ def test_4bit_value_bytes_pair_tokens(mode):
     vpay, kbs = P * D // 2, P * D
     sw = 4 if mode == "int4_per_token_head" else D // 16     # scale bytes per token and side
     vbs = kbs + P * sw
+
+    def codes_of(q):
+        c = np.empty(D, np.uint8)
+        c[0::2], c[1::2] = q & 15, q >> 4
+        return c
     for t in range(P):
         qk, bk = oracle.quant_row(mode, k[t, 0], ks)
         qv, bv = oracle.quant_row(mode, v[t, 0], vs)
-        assert np.array_equal(blk[t * D // 2:(t + 1) * D // 2], qk)                 # K row t
         assert np.array_equal(blk[kbs + t * sw:kbs + (t + 1) * sw], bk)             # K scale(s)
         assert np.array_equal(blk[vbs + t * sw:vbs + (t + 1) * sw], bv)             # V scale(s)
-        codes = np.empty(D, np.uint8)
-        codes[0::2], codes[1::2] = qv & 15, qv >> 4
         pair = blk[vpay + (t // 2) * D:vpay + (t // 2 + 1) * D]
-        assert np.array_equal((pair >> (4 * (t & 1))) & 15, codes)                  # V nibbles of token t
+        if mode == "int4_per_token_head":
+            qv2, _ = oracle.quant_row(mode, v[t ^ 1, 0], vs)                   # the pair's other token
+            kw, vw = _int4_words(codes_of(qk), *((codes_of(qv), codes_of(qv2)) if t % 2 == 0
+                                                 else (codes_of(qv2), codes_of(qv))))
+            assert np.array_equal(blk[t * D // 2:(t + 1) * D // 2].view("<u4"), kw)        # K row t
+            assert np.array_equal(pair.view("<u4"), vw)                                    # V pair row
+        else:
+            assert np.array_equal(blk[t * D // 2:(t + 1) * D // 2], qk)                 # K row t
+            assert np.array_equal((pair >> (4 * (t & 1))) & 15, codes_of(qv))           # V nibbles of token t
 
 
 def test_nvfp4_two_block_worked_example():
