@@ -49,6 +49,9 @@ constexpr int kWarps = 4;
 #ifndef KVQ_B1_MINB
 #define KVQ_B1_MINB 4
 #endif
+#ifndef KVQ_PT_STAGES
+#define KVQ_PT_STAGES KVQ_B1_STAGES
+#endif
 // A warp's page ids for one split live in shared memory (at most this many
 // pages per warp, so at most kWarps * kIdsPerWarp pages per split).
 constexpr int kIdsPerWarp = 256;
@@ -72,7 +75,7 @@ struct Cfg {
   static constexpr int S_OFF = 2 * kPage * RW;        // scales region
   // SW128 for 128-byte rows, SW64 for 64-byte rows (XOR of address bits 7.. into 4..).
   static constexpr int SWZ_MASK = !TMA ? 0 : (RW == 128 ? 7 : 3);
-  static constexpr int STAGES = FOUR ? KVQ_FP4_STAGES : KVQ_B1_STAGES;
+  static constexpr int STAGES = FOUR ? KVQ_FP4_STAGES : MODE == KVQ_FP8_PER_TENSOR ? KVQ_PT_STAGES : KVQ_B1_STAGES;
   static constexpr int MINB = FOUR ? KVQ_FP4_MINB : KVQ_B1_MINB;
   // The running reference max may lag the true max by up to SLACK (log2 units)
   // before it is moved, so probabilities reach 2^SLACK; they are scaled by
