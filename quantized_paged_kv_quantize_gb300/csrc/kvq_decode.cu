@@ -437,6 +437,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, tq = lane & 3;
   const int seq = b / a.nq;
+  pdl_launch_dependents();
 
   int n = a.seq_lens[seq];
   const int lim = min(a.max_seq_len, a.max_pages * kPage);
@@ -711,6 +712,7 @@ template <int D>
 __global__ void __launch_bounds__(D) combine_kernel(const __grid_constant__ DecodeArgs a) {
   __shared__ float wts[D], red[D / 32];
   const int b = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, d = threadIdx.x;  // b: query row
+  pdl_wait_primary();  // the decode grid's partials are complete and visible
   int n = a.seq_lens[b / a.nq];
   const int lim = min(a.max_seq_len, a.max_pages * kPage);
   n = n < 0 ? 0 : (n > lim ? lim : n);
@@ -777,8 +779,8 @@ cudaError_t launch_mode(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s)
   kern<<<grid, kWarps * 32, smem, s>>>(a, c->tmap);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.num_splits == 1) return e;
-  combine_kernel<D><<<a.B * a.Hq, D, 0, s>>>(a);
-  return cudaGetLastError();
+  e = launch_dependent(combine_kernel<D>, dim3(a.B * a.Hq), dim3(D), s, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int D, bool QF32>

@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
   uint8_t* pool = const_cast<uint8_t*>(a.pool);
+  pdl_launch_dependents();
 
   int n = a.seq_lens[b];
   const int lim = min(a.max_seq_len, a.max_pages * kT);
@@ -495,6 +496,7 @@ __global__ void __launch_bounds__(kD) kvarn_combine_kernel(const __grid_constant
   __shared__ float v[kD], wts[kD], red[kD / 32], tsc[kT];
   const int b = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, d = threadIdx.x;
   const int lane = d & 31, warp = d >> 5;
+  pdl_wait_primary();  // the decode grid's partials are complete and visible
   int n = a.seq_lens[b];
   const int lim = min(a.max_seq_len, a.max_pages * kT);
   n = n < 0 ? 0 : (n > lim ? lim : n);
@@ -588,8 +590,8 @@ cudaError_t launch_kvarn_decode(const DecodeArgs& a, cudaStream_t s) {
   kvarn_decode_kernel<<<grid, kW * 32, kSmem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || (a.num_splits == 1 && a.tail == nullptr)) return e;
-  kvarn_combine_kernel<<<a.B * a.Hq, kD, 0, s>>>(a);
-  return cudaGetLastError();
+  e = launch_dependent(kvarn_combine_kernel, dim3(a.B * a.Hq), dim3(kD), s, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace kvq

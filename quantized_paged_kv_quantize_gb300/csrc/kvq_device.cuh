@@ -95,6 +95,31 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// A decode kernel lets its split-combine kernel be scheduled before it ends
+// (the combine's CTAs fill SMs during the decode's last wave); the combine
+// waits for the whole decode grid and its memory before reading the partials.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kern` as a programmatic dependent of the previous kernel on `s`.
+template <typename Arg>
+inline cudaError_t launch_dependent(void (*kern)(Arg), dim3 grid, dim3 block, cudaStream_t s, const Arg& arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, arg);
+}
+
 // ---------------------------------------------------------------- conversions
 // Two fp32 -> two E4M3 (round-to-nearest-even, saturate to +-448);
 // `hi` goes to the upper byte of the 16-bit result.
