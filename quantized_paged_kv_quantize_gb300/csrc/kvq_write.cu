@@ -90,18 +90,25 @@ __device__ __forceinline__ void store_bytes<8>(uint8_t* dst, const uint32_t* w) 
 }
 
 // Encoding of the IEEE quotient RN(x/s) without a division on the common path.
-// With r = RN(1/s), rlo = RN(r(1 - 2^-20)) and rhi = RN(r(1 + 2^-20)), the
-// products RN(x rlo) and RN(x rhi) enclose RN(x/s): their relative distance to
-// x/s is at least 16u - 3u (u = 2^-24) on each side, while RN(x/s) is within u
-// of it.  Every encoder used here (round-to-nearest-even onto a grid, with
-// saturation) is monotone, so when both ends encode to the same code, that is
-// the code of RN(x/s); when they differ the quotient is computed exactly.
-// Scales whose reciprocal is not a comfortable normal number always divide.
+// With r the hardware's approximate reciprocal of s (relative error below
+// 2^-21 = 8u, u = 2^-24), rlo = RN(r(1 - 2^-20)) and rhi = RN(r(1 + 2^-20)),
+// the products RN(x rlo) and RN(x rhi) enclose RN(x/s): their relative
+// distance to x/s is at least 16u - 8u - 2u on each side, while RN(x/s) is
+// within u of it.  Every encoder used here (round-to-nearest-even onto a
+// grid, with saturation) is monotone, so when both ends encode to the same
+// code, that is the code of RN(x/s); when they differ the quotient is computed
+// exactly.  Scales whose reciprocal is not a comfortable normal number always
+// divide.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 struct QDiv {
   float s, rlo, rhi;
   bool fast;
   __device__ __forceinline__ explicit QDiv(float s_) : s(s_) {
-    const float r = __frcp_rn(s_);
+    const float r = rcp_approx(s_);
     fast = r >= 0x1p-100f && r <= 0x1p100f;
     rlo = __fmul_rn(r, 1.0f - 0x1p-20f);
     rhi = __fmul_rn(r, 1.0f + 0x1p-20f);
@@ -228,12 +235,12 @@ __device__ __forceinline__ void nvfp4_codes(const float* x, float st, uint32_t& 
 #pragma unroll
   for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
   amax = group_max<TPB>(amax);
-  sb = f32x2_to_e4m3x2(0.0f, __fdiv_rn(amax, six_st)) & 0xFFu;
+  sb = QDiv(six_st).e4m3x2(0.0f, amax) & 0xFFu;  // E4M3(RN(amax / (6 s_t)))
   const float sbf = e4m3_to_f32(sb);
   const float den = __fmul_rn(st, sbf);
   w = sbf != 0.0f ? QDiv(den).e2m1x8<VEC>(x) : 0u;
   if constexpr (F46) {
-    const uint32_t sb4 = f32x2_to_e4m3x2(0.0f, __fdiv_rn(amax, __fmul_rn(4.0f, st))) & 0xFFu;
+    const uint32_t sb4 = QDiv(__fmul_rn(4.0f, st)).e4m3x2(0.0f, amax) & 0xFFu;
     const float sbf4 = e4m3_to_f32(sb4);
     const float den4 = __fmul_rn(st, sbf4);
     const uint32_t w4 = sbf4 != 0.0f ? QDiv(den4).e2m1x8<VEC>(x) : 0u;
