@@ -112,7 +112,10 @@ class GpuWorkload:
         self.cfg = kvq.make_config(self.lay.num_pages, w.page_size, w.num_kv_heads, w.head_dim, w.mode, tdt)
         self.pool = torch.zeros(kvq.kvq_cache_bytes(self.cfg), dtype=torch.uint8, device=device)
         self.cache = kvq.kvq_cache_alloc(self.cfg, self.pool)
-        ns, tps, wsb = kvq.kvq_decode_plan(self.cache, w.num_seqs * nq, w.num_q_heads, self.max_seq_len)
+        if nq > 1:
+            ns, tps, wsb = kvq.kvq_decode_multi_plan(self.cache, w.num_seqs, nq, w.num_q_heads, self.max_seq_len)
+        else:
+            ns, tps, wsb = kvq.kvq_decode_plan(self.cache, w.num_seqs, w.num_q_heads, self.max_seq_len)
         self.plan = (ns, tps, wsb)
         self.ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device=device)
         self.out = torch.empty(tuple(self.q.shape), dtype=tdt, device=device)

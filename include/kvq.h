@@ -212,12 +212,14 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
  * with M the causal mask).  q and out are [num_seqs][num_queries][num_q_heads]
  * [head_dim]; query i of sequence b stands at position seq_len_b - num_queries
  * + i and attends to tokens 0 .. seq_len_b - num_queries + i (none, output 0,
- * when that is negative).  Each query row streams its causal prefix of the
- * sequence's pages; the rows of one sequence run side by side, so the pages
- * they share are mostly served from L2.  Other arguments and rules are those of
+ * when that is negative).  Other arguments and rules are those of
  * kvq_decode_attention; num_seqs * num_queries <= 65535; not available for
- * KVQ_KVARN_K4V2_G128 (KVQ_ERR_UNSUPPORTED).  Workspace:
- * kvq_decode_multi_workspace_bytes. */
+ * KVQ_KVARN_K4V2_G128 (KVQ_ERR_UNSUPPORTED).  Each query is one row of the
+ * decode grid over its causal prefix; the rows of a sequence run side by side,
+ * so the pages they share are mostly served from L2.  Plan and workspace:
+ * kvq_decode_multi_plan / kvq_decode_multi_workspace_bytes. */
+kvq_status kvq_decode_multi_plan(const kvq_cache* cache, int num_seqs, int num_queries, int num_q_heads,
+                                 int max_seq_len, int* num_splits, int* tokens_per_split, size_t* workspace_bytes);
 kvq_status kvq_decode_multi_workspace_bytes(const kvq_cache* cache, int num_seqs, int num_queries,
                                             int num_q_heads, int max_seq_len, size_t* bytes);
 kvq_status kvq_decode_attention_multi(const kvq_cache* cache, const void* q, const int32_t* block_table,

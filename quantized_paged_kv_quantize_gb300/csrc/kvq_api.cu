@@ -321,16 +321,27 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
 }
 
 // ---- multi-query decode
-kvq_status kvq_decode_multi_workspace_bytes(const kvq_cache* cache, int num_seqs, int num_queries, int num_q_heads,
-                                            int max_seq_len, size_t* bytes) {
+kvq_status kvq_decode_multi_plan(const kvq_cache* cache, int num_seqs, int num_queries, int num_q_heads,
+                                 int max_seq_len, int* num_splits, int* tokens_per_split, size_t* workspace_bytes) {
   kvq_status s = check_cache(cache);
   if (s) return s;
-  if (!bytes) return fail(KVQ_ERR_INVALID_ARG, "bytes is NULL");
   if (num_seqs < 0 || num_queries < 1 || num_q_heads <= 0 || max_seq_len < 0)
     return fail(KVQ_ERR_INVALID_ARG, "bad sizes (num_seqs %d, num_queries %d, num_q_heads %d, max_seq_len %d)",
                 num_seqs, num_queries, num_q_heads, max_seq_len);
-  *bytes = kvq::plan_decode(cache, num_seqs * num_queries, num_q_heads, max_seq_len).workspace_bytes;
+  if (num_q_heads % cache->cfg.num_kv_heads != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                cache->cfg.num_kv_heads);
+  const kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs * num_queries, num_q_heads, max_seq_len);
+  if (num_splits) *num_splits = p.num_splits;
+  if (tokens_per_split) *tokens_per_split = p.tokens_per_split;
+  if (workspace_bytes) *workspace_bytes = p.workspace_bytes;
   return KVQ_OK;
+}
+
+kvq_status kvq_decode_multi_workspace_bytes(const kvq_cache* cache, int num_seqs, int num_queries, int num_q_heads,
+                                            int max_seq_len, size_t* bytes) {
+  if (!bytes) return fail(KVQ_ERR_INVALID_ARG, "bytes is NULL");
+  return kvq_decode_multi_plan(cache, num_seqs, num_queries, num_q_heads, max_seq_len, nullptr, nullptr, bytes);
 }
 
 kvq_status kvq_decode_attention_multi(const kvq_cache* cache, const void* q, const int32_t* block_table,

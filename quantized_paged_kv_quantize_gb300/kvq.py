@@ -39,7 +39,7 @@ EXPORTED = [
     "kvq_cache_set_tensor_scales_from_amax", "kvq_cache_read_errors", "kvq_quantize_write",
     "kvq_decode_plan", "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_decode_attention_noalloc",
     "kvq_kvarn_tail_bytes", "kvq_kvarn_append", "kvq_kvarn_decode_workspace_bytes", "kvq_kvarn_decode_attention",
-    "kvq_decode_multi_workspace_bytes", "kvq_decode_attention_multi",
+    "kvq_decode_multi_plan", "kvq_decode_multi_workspace_bytes", "kvq_decode_attention_multi",
 ]
 
 
@@ -79,6 +79,8 @@ def _load():
         "kvq_decode_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, f32, vp, i32, vp, sz, vp]),
         "kvq_decode_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, f32, vp, i32, vp]),
         "kvq_kvarn_tail_bytes": (i32, [vp, i32, ctypes.POINTER(sz)]),
+        "kvq_decode_multi_plan": (i32, [vp, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                        ctypes.POINTER(sz)]),
         "kvq_decode_multi_workspace_bytes": (i32, [vp, i32, i32, i32, i32, ctypes.POINTER(sz)]),
         "kvq_decode_attention_multi": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, vp, i32, vp, sz,
                                              vp]),
@@ -267,6 +269,13 @@ def kvq_decode_attention_noalloc(cache: KVCache, q, block_table, seq_lens, out, 
 
 
 # ---- multi-query decode
+def kvq_decode_multi_plan(cache: KVCache, num_seqs: int, num_queries: int, num_q_heads: int, max_seq_len: int):
+    ns, tps, ws = ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+    _check(_lib.kvq_decode_multi_plan(cache.handle, num_seqs, num_queries, num_q_heads, max_seq_len, ctypes.byref(ns),
+                                      ctypes.byref(tps), ctypes.byref(ws)))
+    return ns.value, tps.value, ws.value
+
+
 def kvq_decode_multi_workspace_bytes(cache: KVCache, num_seqs: int, num_queries: int, num_q_heads: int,
                                      max_seq_len: int) -> int:
     ws = ctypes.c_size_t()

@@ -397,3 +397,30 @@ def test_decode_multi_query_rejects_kvarn():
         K.kvq_decode_attention_multi(cache, q, _dev(c.lay.block_table), _dev(c.lay.seq_lens), out,
                                      max_seq_len=128)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("mode,nq,Hkv", [("nvfp4", 4, 2), ("nvfp4_4over6", 3, 2), ("int8_per_token_head", 4, 2),
+                                         ("nvfp4", 2, 8)])
+def test_decode_multi_query_one_split(mode, nq, Hkv):
+    """Short sequences (one KV split: outputs written by the decode kernel
+    itself), empty ones and ones shorter than the query count."""
+    K = kvq()
+    c = make_case(small_workload(mode, Hq=16, Hkv=Hkv), [0, 1, 3, 16, 40, 64], slack_pages=1)
+    pool = oracle_pool(c)
+    cache = gpu_cache(c)
+    _upload_oracle_pool(cache, pool, c)
+    B, Hq, D = len(c.lay.seq_lens), c.w.num_q_heads, c.w.head_dim
+    q = np.random.default_rng(3).standard_normal((B, nq, Hq, D)).astype(c.w.np_dtype)
+    msl = int(c.lay.seq_lens.max())
+    wsb = K.kvq_decode_multi_workspace_bytes(cache, B, nq, Hq, msl)
+    ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+    out = torch.full((B, nq, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+    K.kvq_decode_attention_multi(cache, _dev(q), _dev(c.lay.block_table), _dev(c.lay.seq_lens), out,
+                                 max_seq_len=msl, workspace=ws)
+    torch.cuda.synchronize()
+    ref = oracle.decode_multi(c.w.mode, pool, c.lay.num_pages, c.w.page_size, c.w.num_kv_heads, D,
+                              q.astype(np.float32), c.lay.block_table, c.lay.seq_lens, 1.0 / math.sqrt(D),
+                              c.k_scale, c.v_scale)
+    check_attention(out.reshape(B * nq, Hq, D), ref.reshape(B * nq, Hq, D))
+    assert (out[0] == 0).all()
+    assert K.kvq_cache_read_errors(cache) == 0
