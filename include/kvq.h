@@ -80,7 +80,8 @@ typedef enum { KVQ_F16 = 0, KVQ_F32 = 1 } kvq_dtype;
 /* Device error bits (kvq_cache_read_errors). */
 #define KVQ_DEVERR_SLOT_RANGE 0x1u   /* a write slot >= num_pages * page_size */
 #define KVQ_DEVERR_PAGE_RANGE 0x2u   /* a block_table entry outside [0, num_pages) */
-#define KVQ_DEVERR_PARTIAL_TILE 0x4u /* KVarN: a write or a sequence that is not whole tiles */
+#define KVQ_DEVERR_PARTIAL_TILE 0x4u /* KVarN: a write or a sequence that is not whole tiles, or an
+                                        append carrying rows of two tiles of one sequence */
 #define KVQ_DEVERR_SEQ_LEN 0x8u      /* a seq_len above max_seq_len or max_pages * page_size */
 #define KVQ_DEVERR_TIMEOUT 0x10u     /* a bounded wait on a copy ran out (work skipped) */
 #define KVQ_DEVERR_SEQ_ID 0x20u      /* kvq_kvarn_append: a seq_id outside [0, num_seqs) */
@@ -247,7 +248,9 @@ kvq_status kvq_kvarn_tail_bytes(const kvq_cache* cache, int num_seqs, size_t* by
  * whole-tile kvq_quantize_write would.  Within one call a sequence's tokens
  * must belong to one tile (a decode step appends one token per sequence; a
  * prefill writes its whole tiles with kvq_quantize_write and appends the rest);
- * otherwise the completed tile's rows may be overwritten first.  A negative
+ * a tile completed by a call that also carries rows of another tile of the
+ * same sequence is not written and sets KVQ_DEVERR_PARTIAL_TILE (its rows may
+ * already be overwritten in the tail).  A negative
  * slot skips the token; a slot past the pool (KVQ_DEVERR_SLOT_RANGE) or a
  * seq_id outside [0, num_seqs) (KVQ_DEVERR_SEQ_ID) skips it and flags it.
  * Cache mode must be KVQ_KVARN_K4V2_G128; `tail` is 16-byte aligned and at

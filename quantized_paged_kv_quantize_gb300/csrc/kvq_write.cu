@@ -633,6 +633,18 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
     if (slot < 0 || slot % kKvTile != kKvTile - 1 || slot / kKvTile >= a.num_pages || seq < 0 || seq >= a.num_seqs)
       return;
     page = slot / kKvTile;
+    // The call must not also carry rows of another tile of this sequence: the
+    // copy would have overwritten rows of this one.  Such a tile is not
+    // written, and the error is flagged.
+    int other = 0;
+    for (long long i = tid; i < a.num_tokens; i += kKvThreads) {
+      const int s2 = __ldg(a.slots + i);
+      other |= __ldg(a.seq_ids + i) == seq && s2 >= 0 && s2 / kKvTile != page;
+    }
+    if (__syncthreads_or(other)) {
+      if (tid == 0 && h == 0 && side == 0) set_error(a.pool, KVQ_DEVERR_PARTIAL_TILE);
+      return;
+    }
     const size_t side_bytes = (size_t)a.num_seqs * kKvTile * a.Hkv * D * sizeof(T);
     src = reinterpret_cast<const T*>(a.tail + side * side_bytes) + (size_t)seq * kKvTile * a.Hkv * D;
   } else {

@@ -186,3 +186,34 @@ def test_append_flags_bad_sequence_ids_and_slots():
         pool = torch.zeros(K.kvq_cache_bytes(cfg), dtype=torch.uint8, device="cuda")
         K.kvq_kvarn_tail_bytes(K.kvq_cache_alloc(cfg, pool), 2)
     assert e.value.status == 3
+
+
+def test_append_across_two_tiles_of_a_sequence_is_flagged():
+    """One call carrying rows 126, 127 of a sequence's tile and row 0 of its
+    next tile breaks the one-tile-per-call rule: the tile is not written (its
+    page keeps the fill bytes) and KVQ_DEVERR_PARTIAL_TILE is set; another
+    sequence completing its tile in the same call is written normally."""
+    K = kvq()
+    s = Seqs([126, 126], Hq=8, Hkv=2)
+    _fill(s)
+    assert K.kvq_cache_read_errors(s.cache) == 0
+    s.append([(1, 126), (1, 127)])                      # sequence 1: a clean completion
+    k0, v0 = s.kv[0]
+    items = [(0, 126), (0, 127), (0, 128)]              # sequence 0: crosses into its next tile
+    ks = np.stack([k0[t] for _, t in items])
+    vs = np.stack([v0[t] for _, t in items])
+    slots = np.array([s.slot(0, t) for _, t in items], np.int32)
+    K.kvq_kvarn_append(s.cache, _dev(ks), _dev(vs), _dev(slots), _dev(np.zeros(3, np.int32)), s.tail, 2)
+    assert K.kvq_cache_read_errors(s.cache) == 0x4
+    blk = oracle.block_bytes("kvarn_k4v2_g128", P, D)
+    page0 = int(s.lay.block_table[0, 0])
+    got = s.pool.cpu().numpy()
+    for h in range(2):
+        o0 = 256 + (page0 * 2 + h) * blk
+        assert (got[o0:o0 + blk] == 0xCD).all()        # sequence 0's tile was not written
+    s.lens = np.array([126, 128], np.int32)             # sequence 1's tile matches the oracle
+    page1 = int(s.lay.block_table[1, 0])
+    for h in range(2):
+        o1 = 256 + (page1 * 2 + h) * blk
+        assert np.array_equal(got[o1:o1 + blk], s.ref_pool[o1:o1 + blk])
+
