@@ -1,13 +1,17 @@
 // kvq_decode.cu -- paged decode attention over the packed quantized cache,
-// dequantization fused into the load path (modes 1-4), plus the split-KV
-// combine kernel.
+// dequantization fused into the load path, for the 16-token-page modes (FP8
+// per-tensor; INT8, FP8 and INT4 per-token-head; NVFP4, whose storage the
+// 4over6 variant shares), plus the split-KV combine kernel.  Several causal
+// queries per sequence run as one grid row each (query b % nq of sequence
+// b / nq); the combine is launched as a programmatic dependent of the decode.
 //
 // Sources (web pages, by title and section):
 //  "NVFP4 KV Cache：Blackwell 上的 4-bit 缓存量化": "K 与 V 的量化误差进入 attention 的位置不同"
 //     (A = softmax(QK^T/sqrt(d)), O = AV), "KV 的写入与读取路径" (unpack, apply block and tensor
 //     scales inside the attention tile load, no dequantized temporary), "GQA";
 //  "KV Cache 量化 · LLM Glossary": dequantize while loading inside the attention kernel;
-//  "KV 量化" (rustineverything.app), 写和读: read by block table, multiply by the descale.
+//  "KV 量化" (rustineverything.app), 写和读: read by block table, multiply by the descale;
+//     scale 和数据放在一起: the per-token-head modes, int4_per_token_head among them.
 //
 // Design (GB300): one CTA per (KV split, kv head, sequence), W warps; each
 // warp owns a ring of STAGES shared-memory buffers and streams whole

@@ -7,11 +7,15 @@
 // Sources (web pages, by title and section):
 //  "KV Cache 量化深度解析：Per-Tensor、Per-Token-Head 与 NVFP4", sec. 2.1-2.3;
 //  "KV Cache 量化 · LLM Glossary", first section (s = max|x|/127, q = clip(round(x/s)));
-//  "KV 量化" (rustineverything.app), 写和读 (divide by the scale, cast, store as uint8);
+//  "KV 量化" (rustineverything.app), 写和读 (divide by the scale, cast, store as uint8),
+//     scale 和数据放在一起 (int4_per_token_head: head_size/2 bytes plus an fp32 scale);
 //  "NVFP4 KV Cache：Blackwell 上的 4-bit 缓存量化", 双层缩放 (q = Q_E2M1(x/(s_t s_b))),
-//     KV 的写入与读取路径 (compute scales, round and clip to E2M1, pack two per byte);
+//     KV 的写入与读取路径 (compute scales, round and clip to E2M1, pack two per byte),
+//     用一组数直观看缩放的作用 (nvfp4_4over6: a max/6 or max/4 block scale by
+//     reconstruction error);
 //  "KVarN：华为推出的原生 vLLM KV-cache 量化后端...", 技术原理 (tile, Hadamard rotation,
-//     alternating std normalisation, asymmetric RTN) and 配置与部署 (k4v2, tile 128).
+//     alternating std normalisation, asymmetric RTN), 配置与部署 (k4v2, tile 128) and
+//     注意事项 (tile = page; the open tile's raw rows wait in a tail buffer).
 #include <cuda_fp16.h>
 
 #include "kvq_device.cuh"
