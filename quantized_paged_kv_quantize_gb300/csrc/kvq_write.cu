@@ -232,19 +232,20 @@ __device__ __forceinline__ float block_sse(const float* x, uint32_t w, float den
 // per byte, even channel in the low nibble (sb = 0 gives all-zero codes).
 // F46 (nvfp4_4over6): the block is also coded with the max/4 scale
 // E4M3(amax / (4 s_t)), and that coding is kept when its block_sse is smaller.
+// q6, q4: the quotient brackets of RN(6 s_t) and RN(4 s_t).
 template <int VEC, int TPB, bool F46>
-__device__ __forceinline__ void nvfp4_codes(const float* x, float st, uint32_t& w, uint32_t& sb) {
-  const float six_st = __fmul_rn(6.0f, st);
+__device__ __forceinline__ void nvfp4_codes(const float* x, float st, const QDiv& q6, const QDiv& q4, uint32_t& w,
+                                            uint32_t& sb) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
   amax = group_max<TPB>(amax);
-  sb = QDiv(six_st).e4m3x2(0.0f, amax) & 0xFFu;  // E4M3(RN(amax / (6 s_t)))
+  sb = q6.e4m3x2(0.0f, amax) & 0xFFu;  // E4M3(RN(amax / (6 s_t)))
   const float sbf = e4m3_to_f32(sb);
   const float den = __fmul_rn(st, sbf);
   w = sbf != 0.0f ? QDiv(den).e2m1x8<VEC>(x) : 0u;
   if constexpr (F46) {
-    const uint32_t sb4 = QDiv(__fmul_rn(4.0f, st)).e4m3x2(0.0f, amax) & 0xFFu;
+    const uint32_t sb4 = q4.e4m3x2(0.0f, amax) & 0xFFu;  // E4M3(RN(amax / (4 s_t)))
     const float sbf4 = e4m3_to_f32(sb4);
     const float den4 = __fmul_rn(st, sbf4);
     const uint32_t w4 = sbf4 != 0.0f ? QDiv(den4).e2m1x8<VEC>(x) : 0u;
@@ -265,11 +266,26 @@ __device__ __forceinline__ uint2 spread_codes(uint32_t w) {
   return make_uint2(prmt(even, odd, 0x5140u), prmt(even, odd, 0x7362u));
 }
 
+// The side's per-tensor scale (FP8 per-tensor s, NVFP4 s_t) and the quotient
+// brackets built from it, set up once per thread: the pool header does not
+// change during a write.
+struct TensorScale {
+  float st;
+  QDiv qs;  // FP8 per-tensor: x / s; NVFP4: amax / (6 s_t)
+  QDiv q4;  // NVFP4 4over6: amax / (4 s_t)
+  template <int MODE>
+  __device__ __forceinline__ static TensorScale make(const WriteArgs& a, int side) {
+    const float st = *reinterpret_cast<const float*>(a.pool + (side ? kHdrVScaleOffset : kHdrKScaleOffset));
+    return TensorScale{st, QDiv(MODE == KVQ_FP8_PER_TENSOR ? st : __fmul_rn(6.0f, st)), QDiv(__fmul_rn(4.0f, st))};
+  }
+};
+
 // Quantize one (token, kv head, side) row of D values, held by a group of TPR
 // threads with VEC values each (thread j: values j*VEC ..), and store it at
 // slot (skipped when slot < 0; flagged and skipped when out of range).
 template <int MODE, int D, int VEC, int TPR>
-__device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side, int slot, int j, const float* x) {
+__device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side, int slot, int j, const float* x,
+                                             const TensorScale& ts) {
   bool active = slot >= 0;
   const int page = slot >> a.log2P;
   const int off = slot & (a.P - 1);
@@ -280,7 +296,7 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
   uint8_t* blk = a.pool + kHeaderBytes + ((size_t)page * a.Hkv + h) * a.block_bytes;
 
   if constexpr (MODE == KVQ_FP8_PER_TENSOR) {
-    const QDiv q(*reinterpret_cast<const float*>(a.pool + (side ? kHdrVScaleOffset : kHdrKScaleOffset)));
+    const QDiv& q = ts.qs;
     uint32_t w[VEC / 4];
 #pragma unroll
     for (int i = 0; i < VEC; i += 4) w[i / 4] = q.e4m3x2(x[i + 1], x[i]) | (q.e4m3x2(x[i + 3], x[i + 2]) << 16);
@@ -308,8 +324,7 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
   } else if constexpr (MODE == KVQ_NVFP4 || MODE == KVQ_NVFP4_4OVER6) {  // keys; values: pair_values_pass
     constexpr int TPB = 16 / VEC;  // threads per 16-value block
     uint32_t w[1], sb;
-    nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, *reinterpret_cast<const float*>(a.pool + kHdrKScaleOffset),
-                                                   w[0], sb);
+    nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, ts.st, ts.qs, ts.q4, w[0], sb);
     if (active) {
       store_bytes<VEC / 2>(blk + (size_t)off * D / 2 + j * VEC / 2, w);
       if ((j % TPB) == 0) blk[(size_t)a.P * D + (size_t)off * D / 16 + (j * VEC) / 16] = static_cast<uint8_t>(sb);
@@ -348,14 +363,13 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
 // scale) are per token and stored directly.
 template <int MODE, int D, int VEC, int TPR, int NTOK, int R, typename T>
 __device__ __forceinline__ void pair_values_pass(const WriteArgs& a, int h, const int* slot, const uint4* raw,
-                                                 int j) {
+                                                 int j, const TensorScale& ts) {
   constexpr int TPB = 16 / VEC;
   constexpr int TOK = NTOK / R;
   constexpr bool kInWarp = TPR == 16;
   __shared__ uint32_t codes[kInWarp ? 1 : NTOK * TPR];
   __shared__ int vslot[kInWarp ? 1 : NTOK];
   const int g = threadIdx.x / TPR;
-  const float st = *reinterpret_cast<const float*>(a.pool + kHdrVScaleOffset);
   uint32_t wr[R];
   int sr[R];
 #pragma unroll
@@ -380,7 +394,7 @@ __device__ __forceinline__ void pair_values_pass(const WriteArgs& a, int h, cons
       if (active && j == 0) *reinterpret_cast<float*>(blk + (size_t)a.P * D + (size_t)4 * a.P + 4 * off) = sc;
     } else {
       uint32_t sb;
-      nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, st, wr[r], sb);
+      nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, ts.st, ts.qs, ts.q4, wr[r], sb);
       if (active && (j % TPB) == 0)
         blk[(size_t)a.P * D + (size_t)a.P * D / 16 + (size_t)off * D / 16 + (j * VEC) / 16] = static_cast<uint8_t>(sb);
     }
@@ -490,9 +504,10 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
     raw[r] = in ? __ldg(reinterpret_cast<const uint4*>(src + (token * a.Hkv + h) * D + j * VEC))
                 : make_uint4(0u, 0u, 0u, 0u);
   }
+  const TensorScale ts = TensorScale::make<MODE>(a, side);  // unused (and dropped) by the per-token-head modes
   if constexpr (kFourBit<MODE>) {
     if (side == 1) {
-      pair_values_pass<MODE, D, VEC, TPR, TOK * R, R, T>(a, h, slot, raw, j);
+      pair_values_pass<MODE, D, VEC, TPR, TOK * R, R, T>(a, h, slot, raw, j, ts);
       return;
     }
   }
@@ -500,7 +515,7 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
   for (int r = 0; r < R; ++r) {
     float x[VEC];
     widen16<T>(raw[r], x);
-    quantize_row<MODE, D, VEC, TPR>(a, h, side, slot[r], j, x);
+    quantize_row<MODE, D, VEC, TPR>(a, h, side, slot[r], j, x, ts);
   }
 }
 
