@@ -103,6 +103,23 @@ __device__ __forceinline__ void store_bytes<8>(uint8_t* dst, const uint32_t* w) 
 // code, that is the code of RN(x/s); when they differ the quotient is computed
 // exactly.  Scales whose reciprocal is not a comfortable normal number always
 // divide.
+// x / d for a constant divisor d, given rd = RN(1/d): q0 = RN(x rd), the
+// remainder r = x - q0 d (exact, one FMA), q = RN(q0 + r rd) -- Markstein's
+// correction step ("Computation of elementary functions on the IBM RISC
+// System/6000 processor", 1990).  For the divisors and inputs used here it
+// returns the IEEE quotient RN(x/d) for every input, checked exhaustively over
+// all fp32 values: d = 127, 448, 7 with x >= 1e-8 (scales of max(amax, 1e-8))
+// and d = 15, 3 with any finite x >= 0 (KVarN ranges, zero and subnormals
+// included); infinities and NaN take the IEEE division.
+__device__ __forceinline__ float div_const(float x, float d, float rd) {
+  if (!(x <= 0x1.fffffep127f)) return __fdiv_rn(x, d);  // inf and NaN keep IEEE semantics
+  const float q0 = __fmul_rn(x, rd);
+  const float r = __fmaf_rn(-q0, d, x);
+  return __fmaf_rn(r, rd, q0);
+}
+constexpr float kRcp127 = 0x1.020408p-7f, kRcp448 = 0x1.24924ap-9f, kRcp7 = 0x1.24924ap-3f;
+constexpr float kRcp15 = 0x1.111112p-4f, kRcp3 = 0x1.555556p-2f;
+
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -306,7 +323,8 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
 #pragma unroll
     for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
     amax = group_max<TPR>(amax);
-    const float s = __fdiv_rn(fmaxf(amax, 1e-8f), MODE == KVQ_INT8_PER_TOKEN_HEAD ? 127.0f : 448.0f);
+    const float s = MODE == KVQ_INT8_PER_TOKEN_HEAD ? div_const(fmaxf(amax, 1e-8f), 127.0f, kRcp127)
+                                                    : div_const(fmaxf(amax, 1e-8f), 448.0f, kRcp448);
     const QDiv q(s);
     uint32_t w[VEC / 4];
 #pragma unroll
@@ -334,7 +352,7 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
 #pragma unroll
     for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
     amax = group_max<TPR>(amax);
-    const float s = __fdiv_rn(fmaxf(amax, 1e-8f), 7.0f);
+    const float s = div_const(fmaxf(amax, 1e-8f), 7.0f, kRcp7);
     // a key word holds an 8-channel group, even channels in its low half-word:
     // with 4 values per thread, two lanes fill one word (the odd lane's
     // channels 4..7 sit one byte higher) and the even lane stores it
@@ -389,7 +407,7 @@ __device__ __forceinline__ void pair_values_pass(const WriteArgs& a, int h, cons
 #pragma unroll
       for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
       amax = group_max<TPR>(amax);
-      const float sc = __fdiv_rn(fmaxf(amax, 1e-8f), 7.0f);
+      const float sc = div_const(fmaxf(amax, 1e-8f), 7.0f, kRcp7);
       wr[r] = QDiv(sc).int4x8<VEC>(x);
       if (active && j == 0) *reinterpret_cast<float*>(blk + (size_t)a.P * D + (size_t)4 * a.P + 4 * off) = sc;
     } else {
@@ -828,7 +846,7 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
         mn = fminf(mn, sm.part[i * kKvYS + tid]);
         mx = fmaxf(mx, sm.part2[i * kKvYS + tid]);
       }
-      const float sc = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+      const float sc = div_const(__fsub_rn(mx, mn), 15.0f, kRcp15);
       sm.st0[tid] = sc;
       sm.st1[tid] = mn;
       meta[tid] = sc;
@@ -860,7 +878,7 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
     }
     float mn, mx;
     row_minmax(mn8, mx8, lane, mn, mx);
-    const float sc = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+    const float sc = div_const(__fsub_rn(mx, mn), 3.0f, kRcp3);
     float* meta = reinterpret_cast<float*>(blk + kKvTile * D / 2 + kKvTile * D / 4 + 4 * (3 * D + kKvTile));
     if ((lane & 1) == 0) {  // lanes 2k (+16) own token tl + 16 (4 b3 + 2 b2 + b1)
       const int t = tl + 16 * (((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1));
