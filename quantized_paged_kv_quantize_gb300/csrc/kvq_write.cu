@@ -93,16 +93,6 @@ __device__ __forceinline__ void store_bytes<8>(uint8_t* dst, const uint32_t* w) 
   *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
 }
 
-// Encoding of the IEEE quotient RN(x/s) without a division on the common path.
-// With r the hardware's approximate reciprocal of s (relative error below
-// 2^-21 = 8u, u = 2^-24), rlo = RN(r(1 - 2^-20)) and rhi = RN(r(1 + 2^-20)),
-// the products RN(x rlo) and RN(x rhi) enclose RN(x/s): their relative
-// distance to x/s is at least 16u - 8u - 2u on each side, while RN(x/s) is
-// within u of it.  Every encoder used here (round-to-nearest-even onto a
-// grid, with saturation) is monotone, so when both ends encode to the same
-// code, that is the code of RN(x/s); when they differ the quotient is computed
-// exactly.  Scales whose reciprocal is not a comfortable normal number always
-// divide.
 // x / d for a constant divisor d, given rd = RN(1/d): q0 = RN(x rd), the
 // remainder r = x - q0 d (exact, one FMA), q = RN(q0 + r rd) -- Markstein's
 // correction step ("Computation of elementary functions on the IBM RISC
@@ -120,6 +110,22 @@ __device__ __forceinline__ float div_const(float x, float d, float rd) {
 constexpr float kRcp127 = 0x1.020408p-7f, kRcp448 = 0x1.24924ap-9f, kRcp7 = 0x1.24924ap-3f;
 constexpr float kRcp15 = 0x1.111112p-4f, kRcp3 = 0x1.555556p-2f;
 
+// The reciprocals are RN(1/d): checked here against the compiler's own
+// correctly rounded constant division.
+static_assert(kRcp127 == 1.0f / 127.0f && kRcp448 == 1.0f / 448.0f && kRcp7 == 1.0f / 7.0f,
+              "reciprocal constants of the per-token-head scales");
+static_assert(kRcp15 == 1.0f / 15.0f && kRcp3 == 1.0f / 3.0f, "reciprocal constants of the RTN scales");
+
+// Encoding of the IEEE quotient RN(x/s) without a division on the common path.
+// With r the hardware's approximate reciprocal of s (relative error below
+// 2^-21 = 8u, u = 2^-24), rlo = RN(r(1 - 2^-20)) and rhi = RN(r(1 + 2^-20)),
+// the products RN(x rlo) and RN(x rhi) enclose RN(x/s): their relative
+// distance to x/s is at least 16u - 8u - 2u on each side, while RN(x/s) is
+// within u of it.  Every encoder used here (round-to-nearest-even onto a
+// grid, with saturation) is monotone, so when both ends encode to the same
+// code, that is the code of RN(x/s); when they differ the quotient is computed
+// exactly.  Scales whose reciprocal is not a comfortable normal number always
+// divide.
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -676,7 +682,7 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
     int other = 0;
     for (long long i = tid; i < a.num_tokens; i += kKvThreads) {
       const int s2 = __ldg(a.slots + i);
-      other |= __ldg(a.seq_ids + i) == seq && s2 >= 0 && s2 / kKvTile != page;
+      other |= __ldg(a.seq_ids + i) == seq && s2 >= 0 && s2 / kKvTile < a.num_pages && s2 / kKvTile != page;
     }
     if (__syncthreads_or(other)) {
       if (tid == 0 && h == 0 && side == 0) set_error(a.pool, KVQ_DEVERR_PARTIAL_TILE);

@@ -551,6 +551,91 @@ def test_kvarn_tile_rtn(is_value):
     assert rel < (0.15 if not is_value else 0.5)
 
 
+@pytest.mark.parametrize("side", [0, 1])
+def test_kvarn_pool_round_trip(side):
+    """The KVarN page layout and the oracle's dequantization of it.  Tiles are
+    written through the pool writer and every stored row is read back:
+    (1) each element equals r_t c_d (scale q + zero) built from the tile
+    quantizer's own outputs, with the key scale and zero per channel and the
+    value scale and zero per token ("KVarN…", 技术原理: keys per channel, values
+    per token), so a swap of the metadata fields, of their axes, or of the K
+    and V metadata fails; (2) against the input rotated by scipy's Hadamard
+    matrix (not the oracle's transform), every element stays within the RTN
+    bound r_t c_d scale / 2 (plus fp32 rounding of the rotation and of the
+    normalisation)."""
+    from scipy.linalg import hadamard
+    rng = np.random.default_rng(31 + side)
+    Hkv, P, D, num_pages, page = 2, 128, 128, 3, 2
+    k = rng.standard_normal((P, Hkv, D)).astype(np.float32)
+    v = (rng.standard_normal((P, Hkv, D)) * 0.5 + 0.2).astype(np.float32)
+    k[:, :, [5, 64]] *= 15
+    v[:, 1, [7, 100]] *= 15
+    pool = np.zeros(oracle.pool_bytes("kvarn_k4v2_g128", num_pages, P, Hkv, D), np.uint8)
+    slots = (page * P + np.arange(P)).astype(np.int32)
+    assert oracle.write("kvarn_k4v2_g128", pool, num_pages, P, Hkv, D, k, v, slots) == 0
+    H = hadamard(128).astype(np.float64) / math.sqrt(128)
+    steps = 3 if side else 15
+    for h in range(Hkv):
+        X = (v if side else k)[:, h]
+        codes, scale, zero, r, c = oracle.kvarn_tile(X, bool(side))
+        got = np.stack([oracle.dequant_row("kvarn_k4v2_g128", pool, num_pages, P, Hkv, D, 1.0, 1.0,
+                                           page * P + t, h, side) for t in range(P)])
+        sc = scale[:, None] if side else scale[None, :]
+        z = zero[:, None] if side else zero[None, :]
+        rc = r[:, None].astype(np.float64) * c[None, :]
+        want = rc * (sc.astype(np.float64) * codes + z)
+        assert np.array_equal(got, want)
+        assert codes.max() == steps and codes.min() == 0
+        Yrot = X.astype(np.float64) @ H                 # the rotated tile, fp64
+        bound = rc * sc / 2 * (1 + 1e-5) + 2e-5 * np.abs(Yrot) + 1e-6
+        assert np.all(np.abs(got - Yrot) <= bound)
+    # the other side's metadata was written too, and differs (K and V use their own)
+    other = np.stack([oracle.dequant_row("kvarn_k4v2_g128", pool, num_pages, P, Hkv, D, 1.0, 1.0,
+                                         page * P + t, 0, 1 - side) for t in range(P)])
+    Xo = (k if side else v)[:, 0].astype(np.float64) @ H
+    assert np.abs(other - Xo).max() < 0.5 * np.abs(Xo).max()
+
+
+@pytest.mark.parametrize("side", [0, 1])
+def test_kvarn_constant_tile_round_trips_exactly(side):
+    """A tile of one constant: the rotation leaves one non-zero channel, every
+    std step meets zero spread on one axis, and the asymmetric RTN codes it
+    with no error, so rotating the stored tile back gives the constant."""
+    from scipy.linalg import hadamard
+    Hkv, P, D = 1, 128, 128
+    x = np.full((P, Hkv, D), 0.8125, np.float32)
+    pool = np.zeros(oracle.pool_bytes("kvarn_k4v2_g128", 1, P, Hkv, D), np.uint8)
+    assert oracle.write("kvarn_k4v2_g128", pool, 1, P, Hkv, D, x, x, np.arange(P, dtype=np.int32)) == 0
+    H = hadamard(128).astype(np.float64) / math.sqrt(128)
+    got = np.stack([oracle.dequant_row("kvarn_k4v2_g128", pool, 1, P, Hkv, D, 1.0, 1.0, t, 0, side)
+                    for t in range(P)]) @ H
+    assert np.allclose(got, 0.8125, rtol=0, atol=1e-6)
+
+
+def test_nvfp4_tensor_scale_maps_the_tensor_max_to_the_top_of_both_grids():
+    """The NVFP4 global scale s_t = amax / (448 * 6) ("NVFP4 KV Cache…",
+    双层缩放 with the block max mapped to about 6, 用一组数直观看缩放的作用): the
+    block holding the tensor's largest magnitude gets the largest finite E4M3
+    block scale, 448 (byte 0x7E), its largest element gets E2M1 magnitude 6
+    (code 7, sign kept), and no block scale exceeds 448.  A divisor of 448 or 6
+    instead of 2688 fails all three."""
+    rng = np.random.default_rng(17)
+    for trial in range(300):
+        D, rows = 128, 4
+        x = (rng.standard_normal((rows, D)) * 10.0 ** rng.uniform(-4, 4)).astype(np.float32)
+        x[rng.integers(rows), rng.integers(D)] *= rng.uniform(1, 30)
+        st = oracle.nvfp4_tensor_scale(oracle.amax(x))
+        i, j = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+        for row in range(rows):
+            q, bs = oracle.quant_row("nvfp4", x[row], st)
+            assert (bs & 0x7F).max() <= 0x7E and not (bs & 0x80).any()
+            if row == i:
+                assert bs[j // 16] == 0x7E, (trial, hex(int(bs[j // 16])))
+                code = (q[j // 2] >> (4 * (j & 1))) & 15
+                assert code & 7 == 7 and (code >> 3) == (x[i, j] < 0)
+                assert abs(oracle.e2m1_decode(int(code)) * 448.0 * st - x[i, j]) <= 1e-6 * abs(x[i, j])
+
+
 # --------------------------------------------------------------------------- pool + attention
 def _fill(mode, w, lay, k, v, slots, ks=1.0, vs=1.0):
     pool = np.zeros(oracle.pool_bytes(mode, lay.num_pages, w.page_size, w.num_kv_heads, w.head_dim), np.uint8)
