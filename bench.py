@@ -1,17 +1,22 @@
 """Benchmark of the quantized paged KV-cache hot path on GB300.
 
-One step = one decode step of the workload: quantize-on-write of each
+One step = one decode step of a workload: quantize-on-write of each
 sequence's newest token into its page, then paged decode attention of every
 sequence over its whole packed history (the split-KV combine included).  The
 bulk fill of the cache (per-tensor scale calibration + quantize-write of every
 token) runs once before the timed steps and is timed on its own (``write``).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--suite all|none|NAME,NAME..] [--impl ours|reference]
 
-Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
-of the workload (the path has no data exchange; weak scaling).  Inputs are
-seeded synthetic tensors from workloads.py; the decode working set (the
-packed cache) is larger than L2 for the default workload, and for smaller ones
+Prints one JSON line (rank 0).  Its headline (``value``, ``roofline``,
+``e2e``, ...) is the ``--workload`` (default: the 32K-context NVFP4
+configuration); ``workloads`` holds the same decode / write / step
+measurements for every other configuration of the suite, each timed the same
+way, one after another, each freed before the next.  Under torchrun each rank
+runs its own replica (the path has no data exchange; weak scaling).  Inputs
+are seeded synthetic tensors from workloads.py; the decode working set (the
+packed cache) is larger than L2 for the large workloads, and for smaller ones
 L2 is flushed between timed steps.
 """
 from __future__ import annotations
@@ -45,6 +50,26 @@ VARIANTS = {
 }
 # speculative-decoding shape: 4 causal queries per sequence over the same pages
 SPEC_VARIANTS = {"nvfp4_b32_s32768:spec4": ("nvfp4_b32_s32768", 4)}
+# every configuration the default run measures, grouped so that the variants of
+# one base reuse its K/V inputs on the device
+SUITE = ["nvfp4_b32_s32768", "nvfp4_b32_s32768:4over6", "nvfp4_b32_s32768:spec4",
+         "pth_b64_u1k_32k", "pth_b64_u1k_32k:fp8", "pth_b64_u1k_32k:int4",
+         "fp8_pt_b16_s4096", "kvarn_b16_s16384", "int8_pth_tiny"]
+
+
+def workload_by_name(name: str) -> wl.Workload:
+    if name in VARIANTS:
+        base, mode = VARIANTS[name]
+        return wl.WORKLOADS[base].with_mode(mode)
+    if name in SPEC_VARIANTS:
+        import dataclasses
+        base, nq = SPEC_VARIANTS[name]
+        return dataclasses.replace(wl.WORKLOADS[base], num_queries=nq, name=name)
+    return wl.WORKLOADS[name]
+
+
+def base_of(name: str) -> str:
+    return name.split("[")[0].split(":")[0]
 
 
 def measured_peaks():
@@ -70,11 +95,60 @@ def write_bytes(w: wl.Workload, ntok: int) -> int:
     return int(ntok * w.num_kv_heads * (2 * w.head_dim * esz + bytes_per_token_head(w)) + 4 * ntok)
 
 
-# --------------------------------------------------------------------------- GPU side
-class GpuWorkload:
-    """The workload resident on one GPU: full K/V, the packed cache, q, tables."""
+def cache_pool_bytes(w: wl.Workload, lay: wl.PagedLayout) -> int:
+    """Bytes of the packed pool: the 256-byte header and one block of
+    page_size x (bytes per token and kv head) per (page, kv head)."""
+    return 256 + int(lay.num_pages * w.num_kv_heads * w.page_size * bytes_per_token_head(w))
 
-    def __init__(self, w: wl.Workload, device="cuda", keep_host: bool = False):
+
+def l2_policy(w: wl.Workload, lay: wl.PagedLayout) -> str:
+    cb = cache_pool_bytes(w, lay)
+    if cb >= 2 * L2_BYTES:
+        return "inputs larger than L2 (%.2f GB packed cache)" % (cb / 1e9)
+    return ("L2 flushed before each timed step (256 MiB written, then 256 MiB read so that no dirty "
+            "line is written back inside the timed region)")
+
+
+def config_of(w: wl.Workload, lay: wl.PagedLayout = None) -> dict:
+    """The workload's description, identical in both arms of the bench."""
+    lay = wl.paged_layout(w) if lay is None else lay
+    return {
+        "workload": w.name, "mode": w.mode, "B": w.num_seqs, "Hq": w.num_q_heads,
+        "Hkv": w.num_kv_heads, "D": w.head_dim, "page_size": w.page_size,
+        "seq_len": w.seq_len if w.seq_len else list(w.seq_len_range),
+        "io_dtype": w.io_dtype,
+        "step": "quantize-write of 1 new token/seq + decode attention" if w.num_queries == 1 else
+                f"quantize-write of {w.num_queries} new tokens/seq + causal decode of "
+                f"{w.num_queries} queries/seq",
+        "queries_per_seq": w.num_queries,
+        "l2": l2_policy(w, lay),
+    }
+
+
+# --------------------------------------------------------------------------- GPU side
+def _host_kv_chunks(w: wl.Workload, lens: np.ndarray, window: int = 16):
+    """(b, K_b, V_b) for every sequence in order, drawn on a pool of host
+    threads (numpy's generators release the GIL), at most `window` sequences
+    ahead of the consumer."""
+    from concurrent.futures import ThreadPoolExecutor
+    nthreads = max(1, min(16, os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=nthreads) as ex:
+        pending = {}
+        nxt = 0
+        for b in range(len(lens)):
+            while nxt < len(lens) and nxt < b + window:
+                pending[nxt] = ex.submit(wl.gen_kv_seq, w, nxt, int(lens[nxt]))
+                nxt += 1
+            k, v = pending.pop(b).result()
+            yield b, k, v
+
+
+class GpuWorkload:
+    """The workload resident on one GPU: full K/V, the packed cache, q, tables.
+    `kv` = (K, V) device tensors of another workload with the same inputs (a
+    mode variant of the same base) are reused instead of drawn again."""
+
+    def __init__(self, w: wl.Workload, device="cuda", keep_host: bool = False, kv=None):
         import torch
         from quantized_paged_kv_quantize_gb300 import kvq
         self.kvq = kvq
@@ -85,24 +159,27 @@ class GpuWorkload:
         N = self.lay.num_tokens
         tdt = torch.float16 if w.io_dtype == "f16" else torch.float32
         self.tdt = tdt
-        self.K = torch.empty((N, w.num_kv_heads, w.head_dim), dtype=tdt, device=device)
-        self.V = torch.empty_like(self.K)
         self.slots = torch.from_numpy(wl.slot_mapping(w, self.lay)).to(device)
         self.host = [] if keep_host else None
-        off = 0
-        pin_k = torch.empty((int(lens.max()), w.num_kv_heads, w.head_dim), dtype=tdt).pin_memory()
-        pin_v = torch.empty_like(pin_k)
-        for b in range(len(lens)):
-            k, v = wl.gen_kv_seq(w, b, int(lens[b]))
-            n = len(k)
-            pin_k[:n].copy_(torch.from_numpy(k))
-            pin_v[:n].copy_(torch.from_numpy(v))
-            self.K[off:off + n].copy_(pin_k[:n], non_blocking=True)
-            self.V[off:off + n].copy_(pin_v[:n], non_blocking=True)
-            torch.cuda.synchronize()
-            if keep_host:
-                self.host.append((k, v))
-            off += n
+        if kv is not None and not keep_host:
+            self.K, self.V = kv
+            assert tuple(self.K.shape) == (N, w.num_kv_heads, w.head_dim) and self.K.dtype == tdt
+        else:
+            self.K = torch.empty((N, w.num_kv_heads, w.head_dim), dtype=tdt, device=device)
+            self.V = torch.empty_like(self.K)
+            off = 0
+            pin_k = torch.empty((int(lens.max()), w.num_kv_heads, w.head_dim), dtype=tdt).pin_memory()
+            pin_v = torch.empty_like(pin_k)
+            for b, k, v in _host_kv_chunks(w, lens):
+                n = len(k)
+                pin_k[:n].copy_(torch.from_numpy(k))
+                pin_v[:n].copy_(torch.from_numpy(v))
+                self.K[off:off + n].copy_(pin_k[:n], non_blocking=True)
+                self.V[off:off + n].copy_(pin_v[:n], non_blocking=True)
+                torch.cuda.synchronize()
+                if keep_host:
+                    self.host.append((k, v))
+                off += n
         nq = w.num_queries
         q = wl.gen_q(w, w.num_seqs * nq)
         self.q = torch.from_numpy(q.reshape(w.num_seqs, nq, w.num_q_heads, w.head_dim) if nq > 1 else q).to(device)
@@ -111,6 +188,7 @@ class GpuWorkload:
         self.max_seq_len = int(lens.max())
         self.cfg = kvq.make_config(self.lay.num_pages, w.page_size, w.num_kv_heads, w.head_dim, w.mode, tdt)
         self.pool = torch.zeros(kvq.kvq_cache_bytes(self.cfg), dtype=torch.uint8, device=device)
+        assert self.pool.numel() == cache_pool_bytes(w, self.lay)
         self.cache = kvq.kvq_cache_alloc(self.cfg, self.pool)
         if nq > 1:
             ns, tps, wsb = kvq.kvq_decode_multi_plan(self.cache, w.num_seqs, nq, w.num_q_heads, self.max_seq_len)
@@ -275,22 +353,18 @@ def recorded_traffic(workload: str, kernel: str, kv_tokens: int):
     return None
 
 
-def run_ours(args, w: wl.Workload):
+def measure(gw: GpuWorkload, args, dev, ws: int, full: bool, sampler=None) -> dict:
+    """Bulk write, then W warm-up and K timed decode steps of one resident
+    workload (CUDA events on the launching stream; L2 flushed before every step
+    when the packed cache is under 2 x L2).  With `full`, also the end-to-end
+    pass through the C ABI with host buffers.  Times are the max over ranks."""
     import torch
-    import torch.distributed as dist
-    ws, rank, local = _dist()
-    if ws > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if ws > 1 else 0)
-    torch.cuda.set_device(dev)
-    gw = GpuWorkload(w, dev)
+    w = gw.w
+    stream = torch.cuda.current_stream(dev)
     lens = gw.lay.seq_lens
     dbytes = decode_bytes(w, lens)
     n_step_tok = int(gw.step_slots.numel())
-    sbytes = write_bytes(w, n_step_tok)
-    step_bytes = dbytes + sbytes
-    stream = torch.cuda.current_stream(dev)
+    step_bytes = dbytes + write_bytes(w, n_step_tok)
 
     # ---- bulk fill (timed once): a0 calibration, then quantize-write of every token
     torch.cuda.synchronize()
@@ -313,29 +387,26 @@ def run_ours(args, w: wl.Workload):
     fill_ms = min(fill_ms, f0.elapsed_time(f1) / reps)
     flags = gw.kvq.kvq_cache_read_errors(gw.cache)
     if flags:
-        raise RuntimeError(f"device error word after fill: {flags:#x}")
+        raise RuntimeError(f"{w.name}: device error word after fill: {flags:#x}")
     wbytes = write_bytes(w, gw.lay.num_tokens)
 
     flush = None
-    cache_bytes = gw.pool.numel()
-    if cache_bytes < 2 * L2_BYTES:
+    if gw.pool.numel() < 2 * L2_BYTES:
         flush = (torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev),
                  torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev))
-
-    def step():
-        gw.write_step()
-        gw.decode()
 
     for _ in range(args.warmup):
         if flush is not None:
             flush_l2(flush)
-        step()
+        gw.write_step()
+        gw.decode()
     torch.cuda.synchronize()
     if ws > 1:
+        import torch.distributed as dist
         dist.barrier()
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    sampler.start()
-    time.sleep(0.3)
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.3)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -349,20 +420,38 @@ def run_ours(args, w: wl.Workload):
         gw.decode()
         ends[i].record(stream)
     torch.cuda.synchronize()
-    clocks = sampler.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    dec_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
-    total_ms = float(np.sum(step_ms))
-    total_ms = reduce_max(total_ms, ws, dev)
-    if ws > 1:
-        dist.barrier()
+    clocks = sampler.stop() if sampler is not None else None
+    step_ms = [x.elapsed_time(y) for x, y in zip(starts, ends)]
+    dec_ms = [x.elapsed_time(y) for x, y in zip(mids, ends)]
+    total_ms = reduce_max(float(np.sum(step_ms)), ws, dev)
+    dec_total = reduce_max(float(np.sum(dec_ms)), ws, dev)
     ms_per_step = total_ms / args.steps
-    value = ws * step_bytes / (ms_per_step * 1e-3) / 1e9
-    dec_avg = float(np.mean(dec_ms))
+    dec_avg = dec_total / args.steps
     peak, peak_kind = measured_peaks()
     dec_gbs = dbytes / (dec_avg * 1e-3) / 1e9
     dec_kernel = "kvarn_decode_kernel" if w.mode == "kvarn_k4v2_g128" else "decode_kernel"
-    traffic = recorded_traffic(w.name.split("[")[0], dec_kernel, int(gw.lay.seq_lens.sum()))
+    traffic = recorded_traffic(w.name.split("[")[0], dec_kernel, int(lens.sum()))
+    tokens_heads = float(np.sum(lens.astype(np.int64))) * w.num_q_heads * w.num_queries
+    res = {
+        "config": config_of(w, gw.lay),
+        "step": {"ms": round(ms_per_step, 5), "gbs": round(ws * step_bytes / (ms_per_step * 1e-3) / 1e9, 2),
+                 "bytes": step_bytes},
+        "decode": {"gbs": round(dec_gbs, 2), "us": round(dec_avg * 1e3, 2),
+                   "frac_of_peak": round(dec_gbs / peak, 4), "algorithmic_bytes": dbytes,
+                   "tokens_heads_per_s": tokens_heads / (dec_avg * 1e-3),
+                   "splits": gw.plan[0], "tokens_per_split": gw.plan[1]},
+        "write": {"bulk_gbs": round(wbytes / (fill_ms * 1e-3) / 1e9, 2), "bulk_ms": round(fill_ms, 4),
+                  "bulk_bytes": wbytes, "tokens_heads_per_s": gw.lay.num_tokens * w.num_kv_heads / (fill_ms * 1e-3),
+                  "calibrate_ms": round(calib_ms, 4) if w.mode in TENSOR_SCALED else None},
+        "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(dec_gbs / peak, 4), "traffic": traffic,
+                     "kernel": dec_kernel, "peak_kind": peak_kind,
+                     "timed": dec_kernel + (" + its split combine" if gw.plan[0] > 1 else "")},
+        "gpu_launches": gw.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    if not full:
+        return res
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region)
     q_h = gw.q.cpu().pin_memory()
@@ -391,60 +480,82 @@ def run_ours(args, w: wl.Workload):
         if i >= args.warmup:
             e2e_ms.append(t0.elapsed_time(t1))
     e2e_tot = reduce_max(float(np.sum(e2e_ms)), ws, dev)
-    e2e_val = ws * step_bytes / (e2e_tot / args.steps * 1e-3) / 1e9
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, s_h))
-    d2h = out_h.numel() * out_h.element_size()
-
+    res["e2e"] = {"value": round(ws * step_bytes / (e2e_tot / args.steps * 1e-3) / 1e9, 2), "unit": "GB/s",
+                  "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, s_h)),
+                  "d2h_bytes_per_step": out_h.numel() * out_h.element_size()}
     flags = gw.kvq.kvq_cache_read_errors(gw.cache)
     if flags:
-        raise RuntimeError(f"device error word after the timed steps: {flags:#x}")
+        raise RuntimeError(f"{w.name}: device error word after the timed steps: {flags:#x}")
+    return res
+
+
+def suite_names(args) -> list:
+    if args.suite == "none":
+        return []
+    names = SUITE if args.suite == "all" else [n for n in args.suite.split(",") if n]
+    for n in names:
+        workload_by_name(n)  # unknown names fail here, before any GPU work
+    return [n for n in names if n != args.workload]
+
+
+def run_ours(args, w: wl.Workload):
+    import torch
+    import torch.distributed as dist
+    ws, rank, local = _dist()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    # the headline workload first: its line carries the contract keys
+    gw = GpuWorkload(w, dev)
+    head = measure(gw, args, dev, ws, full=True,
+                   sampler=ClockSampler(dev.index if dev.index is not None else 0))
+    kv = (base_of(w.name), gw.K, gw.V) if args.num_seqs is None else None
+    del gw
+    # then every other configuration of the suite, one at a time; mode variants
+    # of a base reuse its K/V on the device
+    others = {}
+    for name in suite_names(args):
+        wk = workload_by_name(name)
+        if kv is not None and kv[0] != base_of(name):
+            kv = None
+            torch.cuda.empty_cache()
+        g = GpuWorkload(wk, dev, kv=None if kv is None else kv[1:])
+        others[name] = measure(g, args, dev, ws, full=False)
+        kv = (base_of(name), g.K, g.V)
+        del g
+        torch.cuda.empty_cache()
+    del kv
+    torch.cuda.empty_cache()
 
     result = None
     if rank == 0:
         cpu = cpu_baseline(w, args.cpu_seconds) if not args.no_cpu_baseline else None
-        tokens_heads = float(np.sum(lens.astype(np.int64))) * w.num_q_heads * w.num_queries
         result = {
             "metric": METRIC,
-            "value": round(value, 2),
+            "value": head["step"]["gbs"],
             "unit": "GB/s",
             "n_gpus": ws,
             "steps": args.steps,
             "warmup": args.warmup,
-            "ms_per_step": round(ms_per_step, 5),
+            "ms_per_step": head["step"]["ms"],
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": "f16 x f16 -> f32 tensor-core math on dequantized codes (u8 storage)",
             "data": "synthetic",
-            "config": {
-                "workload": w.name, "mode": w.mode, "B": w.num_seqs, "Hq": w.num_q_heads,
-                "Hkv": w.num_kv_heads, "D": w.head_dim, "page_size": w.page_size,
-                "seq_len": w.seq_len if w.seq_len else list(w.seq_len_range),
-                "io_dtype": w.io_dtype,
-                "step": "quantize-write of 1 new token/seq + decode attention" if w.num_queries == 1 else
-                        f"quantize-write of {w.num_queries} new tokens/seq + causal decode of "
-                        f"{w.num_queries} queries/seq",
-                "queries_per_seq": w.num_queries,
-                "l2": ("inputs larger than L2 (%.2f GB packed cache)" % (cache_bytes / 1e9)) if flush is None
-                else "L2 flushed before each timed step (256 MiB written, then 256 MiB read so that no dirty "
-                     "line is written back inside the timed region)",
-                "decode_splits": gw.plan[0], "tokens_per_split": gw.plan[1],
-            },
-            "decode": {"gbs": round(dec_gbs, 2), "us": round(dec_avg * 1e3, 2),
-                       "frac_of_peak": round(dec_gbs / peak, 4), "algorithmic_bytes": dbytes,
-                       "tokens_heads_per_s": tokens_heads / (dec_avg * 1e-3)},
-            "write": {"bulk_gbs": round(wbytes / (fill_ms * 1e-3) / 1e9, 2), "bulk_ms": round(fill_ms, 4),
-                      "bulk_bytes": wbytes, "tokens_heads_per_s": gw.lay.num_tokens * w.num_kv_heads / (fill_ms * 1e-3),
-                      "calibrate_ms": round(calib_ms, 4) if w.mode in TENSOR_SCALED else None},
-            "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(dec_gbs / peak, 4), "traffic": traffic,
-                         "kernel": dec_kernel, "peak_kind": peak_kind,
-                         "timed": dec_kernel + (" + its split combine" if gw.plan[0] > 1 else "")},
-            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "gpu_launches": gw.launches_per_step() * args.steps,
-            "clocks": clocks,
+            "config": head["config"],
+            "decode": head["decode"],
+            "write": head["write"],
+            "roofline": head["roofline"],
+            "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"],
             "cpu_baseline": cpu,
+            "workloads": {n: {k: r[k] for k in ("config", "step", "decode", "write", "roofline", "gpu_launches")}
+                          for n, r in others.items()},
         }
     if ws > 1:
         dist.barrier()
@@ -551,8 +662,7 @@ def run_reference(args, w: wl.Workload):
         "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention from stored codes (oracle)",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": w.name, "mode": w.mode, "B": w.num_seqs, "Hq": w.num_q_heads,
-                   "Hkv": w.num_kv_heads, "D": w.head_dim, "page_size": w.page_size},
+        "config": config_of(w),
         "cpu_baseline": {"value": round(val, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step: one (sequence, kv head) group of {w.name} decoded by the "
                                    f"single-threaded C oracle"},
@@ -567,26 +677,23 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(wl.WORKLOADS) + sorted(VARIANTS) + sorted(SPEC_VARIANTS))
+    ap.add_argument("--suite", default="all",
+                    help="the other configurations measured after the headline one: 'all' (default), "
+                         "'none', or a comma-separated list of workload names")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None,
-                    help="shrink the batch (same shapes otherwise), e.g. to size an ncu capture")
+                    help="shrink the batch (same shapes otherwise), e.g. to size an ncu capture; "
+                         "implies --suite none")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.workload in VARIANTS:
-        base, mode = VARIANTS[args.workload]
-        w = wl.WORKLOADS[base].with_mode(mode)
-    elif args.workload in SPEC_VARIANTS:
-        import dataclasses
-        base, nq = SPEC_VARIANTS[args.workload]
-        w = dataclasses.replace(wl.WORKLOADS[base], num_queries=nq, name=args.workload)
-    else:
-        w = wl.WORKLOADS[args.workload]
+    w = workload_by_name(args.workload)
     if args.num_seqs is not None:
         import dataclasses
         w = dataclasses.replace(w, num_seqs=args.num_seqs, name=f"{w.name}[B={args.num_seqs}]")
+        args.suite = "none"
     res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if res is not None:
         print(json.dumps(res), flush=True)

@@ -65,6 +65,43 @@ kvq_status check_cache(const kvq_cache* c) {
   return KVQ_OK;
 }
 
+// Argument checks shared by every decode entry point (each checks the cache
+// mode itself first), in this order: sizes, the GQA group, max_seq_len against the block table, the
+// output dtype, the softmax scale, then (only when there is work) the device
+// pointers and their alignment.  `tail` is checked when `need_tail` is set
+// (KVarN open tiles).  Returns KVQ_OK with *empty set when num_seqs is 0.
+kvq_status check_decode_args(const kvq_cache* cache, const void* q, const int32_t* block_table, int max_pages,
+                             const int32_t* seq_lens, int num_seqs, int num_q_heads, int max_seq_len,
+                             float softmax_scale, const void* out, int out_dtype, bool need_tail,
+                             const void* tail, bool* empty) {
+  *empty = false;
+  kvq_status s = check_cache(cache);
+  if (s) return s;
+  const kvq_cache_config& c = cache->cfg;
+  if (num_seqs < 0 || max_pages < 0 || max_seq_len < 0) return fail(KVQ_ERR_INVALID_ARG, "negative size");
+  if (num_q_heads <= 0 || num_q_heads % c.num_kv_heads != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                c.num_kv_heads);
+  if (num_q_heads / c.num_kv_heads > 8)
+    return fail(KVQ_ERR_UNSUPPORTED, "GQA group %d > 8", num_q_heads / c.num_kv_heads);
+  if ((long long)max_seq_len > (long long)max_pages * c.page_size)
+    return fail(KVQ_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
+  if (out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return fail(KVQ_ERR_UNSUPPORTED, "out_dtype %d", out_dtype);
+  if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f)
+    return fail(KVQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+  if (num_seqs == 0) {
+    *empty = true;
+    return KVQ_OK;
+  }
+  if (!q || !block_table || !seq_lens || !out || (need_tail && !tail))
+    return fail(KVQ_ERR_INVALID_ARG, need_tail ? "NULL q, table, lens, tail or out" : "NULL q, table, lens or out");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      (need_tail && !aligned(tail, 16)))
+    return fail(KVQ_ERR_INVALID_ARG, need_tail ? "q, tail and out must be 16-byte aligned"
+                                               : "q and out must be 16-byte aligned");
+  return KVQ_OK;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -285,27 +322,12 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
                                 const int32_t* seq_lens, int num_seqs, int num_q_heads, int max_seq_len, int mode,
                                 float softmax_scale, void* out, int out_dtype, void* workspace,
                                 size_t workspace_bytes, void* stream) {
-  kvq_status s = check_cache(cache);
-  if (s) return s;
-  const kvq_cache_config& c = cache->cfg;
-  if (mode != c.mode)
-    return fail(KVQ_ERR_MODE_MISMATCH, "decode mode %d but the cache holds mode %d", mode, c.mode);
-  if (num_seqs < 0 || max_pages < 0 || max_seq_len < 0)
-    return fail(KVQ_ERR_INVALID_ARG, "negative size");
-  if (num_q_heads <= 0 || num_q_heads % c.num_kv_heads != 0)
-    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
-                c.num_kv_heads);
-  if (num_q_heads / c.num_kv_heads > 8)
-    return fail(KVQ_ERR_UNSUPPORTED, "GQA group %d > 8", num_q_heads / c.num_kv_heads);
-  if ((long long)max_seq_len > (long long)max_pages * c.page_size)
-    return fail(KVQ_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
-  if (out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return fail(KVQ_ERR_UNSUPPORTED, "out_dtype %d", out_dtype);
-  if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f)
-    return fail(KVQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
-  if (num_seqs == 0) return KVQ_OK;
-  if (!q || !block_table || !seq_lens || !out) return fail(KVQ_ERR_INVALID_ARG, "NULL q, table, lens or out");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
-    return fail(KVQ_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if (cache && mode != cache->cfg.mode)
+    return fail(KVQ_ERR_MODE_MISMATCH, "decode mode %d but the cache holds mode %d", mode, cache->cfg.mode);
+  bool empty = false;
+  kvq_status s = check_decode_args(cache, q, block_table, max_pages, seq_lens, num_seqs, num_q_heads, max_seq_len,
+                                   softmax_scale, out, out_dtype, false, nullptr, &empty);
+  if (s || empty) return s;
   kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs, num_q_heads, max_seq_len);
   if (p.workspace_bytes > 0) {
     if (!workspace) return fail(KVQ_ERR_CAPACITY, "workspace of %zu bytes required", p.workspace_bytes);
@@ -348,31 +370,17 @@ kvq_status kvq_decode_attention_multi(const kvq_cache* cache, const void* q, con
                                       int max_pages, const int32_t* seq_lens, int num_seqs, int num_queries,
                                       int num_q_heads, int max_seq_len, int mode, float softmax_scale, void* out,
                                       int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  kvq_status s = check_cache(cache);
-  if (s) return s;
-  const kvq_cache_config& c = cache->cfg;
-  if (mode != c.mode)
-    return fail(KVQ_ERR_MODE_MISMATCH, "decode mode %d but the cache holds mode %d", mode, c.mode);
-  if (c.mode == KVQ_KVARN_K4V2_G128)
+  if (cache && mode != cache->cfg.mode)
+    return fail(KVQ_ERR_MODE_MISMATCH, "decode mode %d but the cache holds mode %d", mode, cache->cfg.mode);
+  if (cache && cache->cfg.mode == KVQ_KVARN_K4V2_G128)
     return fail(KVQ_ERR_UNSUPPORTED, "multi-query decode is not available for kvarn_k4v2_g128");
-  if (num_seqs < 0 || max_pages < 0 || max_seq_len < 0 || num_queries < 1)
-    return fail(KVQ_ERR_INVALID_ARG, "negative size or num_queries < 1");
+  if (num_queries < 1) return fail(KVQ_ERR_INVALID_ARG, "num_queries < 1");
   if ((long long)num_seqs * num_queries > 65535)
     return fail(KVQ_ERR_UNSUPPORTED, "num_seqs * num_queries = %lld > 65535", (long long)num_seqs * num_queries);
-  if (num_q_heads <= 0 || num_q_heads % c.num_kv_heads != 0)
-    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
-                c.num_kv_heads);
-  if (num_q_heads / c.num_kv_heads > 8)
-    return fail(KVQ_ERR_UNSUPPORTED, "GQA group %d > 8", num_q_heads / c.num_kv_heads);
-  if ((long long)max_seq_len > (long long)max_pages * c.page_size)
-    return fail(KVQ_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
-  if (out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return fail(KVQ_ERR_UNSUPPORTED, "out_dtype %d", out_dtype);
-  if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f)
-    return fail(KVQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
-  if (num_seqs == 0) return KVQ_OK;
-  if (!q || !block_table || !seq_lens || !out) return fail(KVQ_ERR_INVALID_ARG, "NULL q, table, lens or out");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
-    return fail(KVQ_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  bool empty = false;
+  kvq_status s = check_decode_args(cache, q, block_table, max_pages, seq_lens, num_seqs, num_q_heads, max_seq_len,
+                                   softmax_scale, out, out_dtype, false, nullptr, &empty);
+  if (s || empty) return s;
   const kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs * num_queries, num_q_heads, max_seq_len);
   if (p.workspace_bytes > 0) {
     if (!workspace || workspace_bytes < p.workspace_bytes)
@@ -437,27 +445,13 @@ kvq_status kvq_kvarn_decode_attention(const kvq_cache* cache, const void* q, con
                                       int max_pages, const int32_t* seq_lens, int num_seqs, int num_q_heads,
                                       int max_seq_len, float softmax_scale, const void* tail, void* out,
                                       int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  kvq_status s = check_cache(cache);
-  if (s) return s;
+  if (cache && cache->cfg.mode != KVQ_KVARN_K4V2_G128)
+    return fail(KVQ_ERR_MODE_MISMATCH, "kvq_kvarn_decode_attention needs a KVarN cache (mode %d)", cache->cfg.mode);
+  bool empty = false;
+  kvq_status s = check_decode_args(cache, q, block_table, max_pages, seq_lens, num_seqs, num_q_heads, max_seq_len,
+                                   softmax_scale, out, out_dtype, true, tail, &empty);
+  if (s || empty) return s;
   const kvq_cache_config& c = cache->cfg;
-  if (c.mode != KVQ_KVARN_K4V2_G128)
-    return fail(KVQ_ERR_MODE_MISMATCH, "kvq_kvarn_decode_attention needs a KVarN cache (mode %d)", c.mode);
-  if (num_seqs < 0 || max_pages < 0 || max_seq_len < 0) return fail(KVQ_ERR_INVALID_ARG, "negative size");
-  if (num_q_heads <= 0 || num_q_heads % c.num_kv_heads != 0)
-    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
-                c.num_kv_heads);
-  if (num_q_heads / c.num_kv_heads > 8)
-    return fail(KVQ_ERR_UNSUPPORTED, "GQA group %d > 8", num_q_heads / c.num_kv_heads);
-  if ((long long)max_seq_len > (long long)max_pages * c.page_size)
-    return fail(KVQ_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
-  if (out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return fail(KVQ_ERR_UNSUPPORTED, "out_dtype %d", out_dtype);
-  if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f)
-    return fail(KVQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
-  if (num_seqs == 0) return KVQ_OK;
-  if (!q || !block_table || !seq_lens || !out || !tail)
-    return fail(KVQ_ERR_INVALID_ARG, "NULL q, table, lens, tail or out");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(tail, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
-    return fail(KVQ_ERR_INVALID_ARG, "q, tail and out must be 16-byte aligned");
   const kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs, num_q_heads, max_seq_len);
   const size_t need = (size_t)num_seqs * num_q_heads * p.num_splits * (c.head_dim + 2) * sizeof(float);
   if (!workspace || workspace_bytes < need)
@@ -515,26 +509,12 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_cache* cache, const
                                                    const int32_t* seq_lens, int num_seqs, int num_q_heads,
                                                    int max_seq_len, int mode, float softmax_scale, void* out,
                                                    int out_dtype, void* stream) {
-  kvq_status s = check_cache(cache);
-  if (s) return s;
-  const kvq_cache_config& c = cache->cfg;
-  if (mode != c.mode)
-    return fail(KVQ_ERR_MODE_MISMATCH, "decode mode %d but the cache holds mode %d", mode, c.mode);
-  if (num_seqs < 0 || max_pages < 0 || max_seq_len < 0) return fail(KVQ_ERR_INVALID_ARG, "negative size");
-  if (num_q_heads <= 0 || num_q_heads % c.num_kv_heads != 0)
-    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
-                c.num_kv_heads);
-  if (num_q_heads / c.num_kv_heads > 8)
-    return fail(KVQ_ERR_UNSUPPORTED, "GQA group %d > 8", num_q_heads / c.num_kv_heads);
-  if ((long long)max_seq_len > (long long)max_pages * c.page_size)
-    return fail(KVQ_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
-  if (out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return fail(KVQ_ERR_UNSUPPORTED, "out_dtype %d", out_dtype);
-  if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f)
-    return fail(KVQ_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
-  if (num_seqs == 0) return KVQ_OK;
-  if (!q || !block_table || !seq_lens || !out) return fail(KVQ_ERR_INVALID_ARG, "NULL q, table, lens or out");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
-    return fail(KVQ_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if (cache && mode != cache->cfg.mode)
+    return fail(KVQ_ERR_MODE_MISMATCH, "decode mode %d but the cache holds mode %d", mode, cache->cfg.mode);
+  bool empty = false;
+  kvq_status s = check_decode_args(cache, q, block_table, max_pages, seq_lens, num_seqs, num_q_heads, max_seq_len,
+                                   softmax_scale, out, out_dtype, false, nullptr, &empty);
+  if (s || empty) return s;
   kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs, num_q_heads, max_seq_len);
   if (p.workspace_bytes > (size_t)KVQ_NOALLOC_SCRATCH_BYTES)
     return fail(KVQ_ERR_CAPACITY,

@@ -28,6 +28,8 @@ def test_reference_arm_prints_one_contract_line():
     assert d["value"] > 0 and d["higher_is_better"] is True and d["steps"] == 3 and d["warmup"] == 3
     assert d["n_gpus"] == 1 and d["scaling"] == "weak" and d["vs_baseline"] is None
     assert d["config"]["workload"] == "int8_pth_tiny"
+    import workloads as wl
+    assert d["config"] == bench.config_of(wl.WORKLOADS["int8_pth_tiny"])   # the product arm's config, too
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
@@ -38,3 +40,16 @@ def test_product_arm_has_no_cpu_fallback():
     r = _run("--workload", "int8_pth_tiny", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", timeout=300)
     assert r.returncode != 0
     assert not any(l.startswith("{") for l in r.stdout.splitlines())
+
+
+def test_suite_names_resolve_and_cover_every_configuration():
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as wl
+    names = set(bench.SUITE)
+    assert set(wl.WORKLOADS) <= names and set(bench.VARIANTS) <= names and set(bench.SPEC_VARIANTS) <= names
+    for n in bench.SUITE:
+        w = bench.workload_by_name(n)
+        assert w.name == n and bench.base_of(n) in wl.WORKLOADS
+        lay = wl.paged_layout(w)
+        assert bench.config_of(w, lay)["workload"] == n

@@ -217,3 +217,29 @@ def test_append_across_two_tiles_of_a_sequence_is_flagged():
         o1 = 256 + (page1 * 2 + h) * blk
         assert np.array_equal(got[o1:o1 + blk], s.ref_pool[o1:o1 + blk])
 
+
+
+def test_append_completion_with_an_out_of_range_slot_alongside():
+    """A call that completes a sequence's tile and also carries a token of the
+    same sequence whose slot lies past the pool: that token is skipped and
+    flagged (KVQ_DEVERR_SLOT_RANGE) and overwrites nothing, so the tile is still
+    complete and is quantized (byte-identical to the oracle); no partial-tile
+    flag is raised."""
+    K = kvq()
+    s = Seqs([126], Hq=8, Hkv=2)
+    _fill(s)
+    assert K.kvq_cache_read_errors(s.cache) == 0
+    k0, v0 = s.kv[0]
+    ks = np.stack([k0[126], k0[127], k0[128]])
+    vs = np.stack([v0[126], v0[127], v0[128]])
+    slots = np.array([s.slot(0, 126), s.slot(0, 127), s.lay.num_pages * P + 5], np.int32)
+    K.kvq_kvarn_append(s.cache, _dev(ks), _dev(vs), _dev(slots), _dev(np.zeros(3, np.int32)), s.tail, 1)
+    assert K.kvq_cache_read_errors(s.cache) == 0x1
+    for t in (126, 127):
+        s.tail_np[0, 0, t], s.tail_np[1, 0, t] = k0[t], v0[t]
+    oracle.write("kvarn_k4v2_g128", s.ref_pool, s.lay.num_pages, P, s.w.num_kv_heads, D,
+                 s.tail_np[0, 0].astype(np.float32), s.tail_np[1, 0].astype(np.float32),
+                 np.array([s.slot(0, x) for x in range(P)], np.int32))
+    s.lens = np.array([128], np.int32)
+    s.check_pool_and_tail()
+    s.decode(s.lens)
