@@ -58,11 +58,11 @@ SUITE = ["nvfp4_b32_s32768", "nvfp4_b32_s32768:4over6", "nvfp4_b32_s32768:spec4"
 
 
 def workload_by_name(name: str) -> wl.Workload:
+    import dataclasses
     if name in VARIANTS:
         base, mode = VARIANTS[name]
-        return wl.WORKLOADS[base].with_mode(mode)
+        return dataclasses.replace(wl.WORKLOADS[base].with_mode(mode), name=name)
     if name in SPEC_VARIANTS:
-        import dataclasses
         base, nq = SPEC_VARIANTS[name]
         return dataclasses.replace(wl.WORKLOADS[base], num_queries=nq, name=name)
     return wl.WORKLOADS[name]
