@@ -82,7 +82,12 @@ def measured_peaks():
 
 
 def bytes_per_token_head(w: wl.Workload) -> float:
-    return BYTES_PER_TOKEN_HEAD[w.mode] * w.head_dim / 128.0
+    """Packed bytes of one token and kv head, K + V, payload and in-page scales
+    (BYTES_PER_TOKEN_HEAD holds them at head_dim 128)."""
+    D, P = w.head_dim, w.page_size
+    return {"fp8_per_tensor": 2 * D, "int8_per_token_head": 2 * D + 8, "fp8_per_token_head": 2 * D + 8,
+            "nvfp4": D + D / 8, "nvfp4_4over6": D + D / 8, "int4_per_token_head": D + 8,
+            "kvarn_k4v2_g128": (P * D * 3 / 4 + 4 * (3 * D + P) + 4 * (3 * P + D)) / P}[w.mode]
 
 
 def decode_bytes(w: wl.Workload, lens: np.ndarray) -> int:
@@ -522,10 +527,15 @@ def run_ours(args, w: wl.Workload):
         if kv is not None and kv[0] != base_of(name):
             kv = None
             torch.cuda.empty_cache()
-        g = GpuWorkload(wk, dev, kv=None if kv is None else kv[1:])
-        others[name] = measure(g, args, dev, ws, full=False)
-        kv = (base_of(name), g.K, g.V)
-        del g
+        try:
+            g = GpuWorkload(wk, dev, kv=None if kv is None else kv[1:])
+            others[name] = measure(g, args, dev, ws, full=False)
+            kv = (base_of(name), g.K, g.V)
+            del g
+        except Exception as e:  # reported in the line; the headline stands on its own
+            print(f"bench: {name} failed: {e!r}", file=sys.stderr, flush=True)
+            others[name] = {"error": repr(e)}
+            kv = None
         torch.cuda.empty_cache()
     del kv
     torch.cuda.empty_cache()
@@ -554,8 +564,8 @@ def run_ours(args, w: wl.Workload):
             "gpu_launches": head["gpu_launches"],
             "clocks": head["clocks"],
             "cpu_baseline": cpu,
-            "workloads": {n: {k: r[k] for k in ("config", "step", "decode", "write", "roofline", "gpu_launches")}
-                          for n, r in others.items()},
+            "workloads": {n: ({k: r[k] for k in ("config", "step", "decode", "write", "roofline", "gpu_launches")}
+                              if "error" not in r else r) for n, r in others.items()},
         }
     if ws > 1:
         dist.barrier()

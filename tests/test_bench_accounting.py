@@ -18,9 +18,25 @@ import workloads as wl  # noqa: E402
 
 
 @pytest.mark.parametrize("mode", sorted(bench.BYTES_PER_TOKEN_HEAD))
-def test_bytes_per_token_head_is_the_page_layout(mode):
+@pytest.mark.parametrize("D", [32, 128])
+def test_bytes_per_token_head_is_the_page_layout(mode, D):
     P = 128 if mode == "kvarn_k4v2_g128" else 16
-    assert bench.BYTES_PER_TOKEN_HEAD[mode] * P == oracle.block_bytes(mode, P, 128)
+    if P == 128 and D != 128:
+        pytest.skip("KVarN has head_dim 128 only")
+    w = dataclasses.replace(wl.WORKLOADS["pth_b64_u1k_32k"].with_mode(mode), head_dim=D, page_size=P)
+    assert bench.bytes_per_token_head(w) * P == oracle.block_bytes(mode, P, D)
+    if D == 128:
+        assert bench.BYTES_PER_TOKEN_HEAD[mode] * P == oracle.block_bytes(mode, P, 128)
+
+
+def test_tiny_config_bytes_are_the_pages_fake_quant_bytes():
+    """The [P3] experiment's shape (B=2, H=4, T=16, D=32): 8192 B of int8 K+V
+    and 1024 B of fp32 scales, plus q and out (fp32)."""
+    w = wl.WORKLOADS["int8_pth_tiny"]
+    lens = wl.seq_lens(w)
+    assert bench.decode_bytes(w, lens) == 8192 + 1024 + 2 * 2 * 4 * 32 * 4
+    lay = wl.paged_layout(w)
+    assert bench.cache_pool_bytes(w, lay) == oracle.pool_bytes(w.mode, lay.num_pages, 16, 4, 32)
 
 
 @pytest.mark.parametrize("nq", [1, 4])
