@@ -353,7 +353,7 @@ kvq_status kvq_decode_multi_plan(const kvq_cache* cache, int num_seqs, int num_q
   if (num_q_heads % cache->cfg.num_kv_heads != 0)
     return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
                 cache->cfg.num_kv_heads);
-  const kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs * num_queries, num_q_heads, max_seq_len);
+  const kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs, num_q_heads, max_seq_len, num_queries);
   if (num_splits) *num_splits = p.num_splits;
   if (tokens_per_split) *tokens_per_split = p.tokens_per_split;
   if (workspace_bytes) *workspace_bytes = p.workspace_bytes;
@@ -381,7 +381,7 @@ kvq_status kvq_decode_attention_multi(const kvq_cache* cache, const void* q, con
   kvq_status s = check_decode_args(cache, q, block_table, max_pages, seq_lens, num_seqs, num_q_heads, max_seq_len,
                                    softmax_scale, out, out_dtype, false, nullptr, &empty);
   if (s || empty) return s;
-  const kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs * num_queries, num_q_heads, max_seq_len);
+  const kvq::DecodePlan p = kvq::plan_decode(cache, num_seqs, num_q_heads, max_seq_len, num_queries);
   if (p.workspace_bytes > 0) {
     if (!workspace || workspace_bytes < p.workspace_bytes)
       return fail(KVQ_ERR_CAPACITY, "workspace needs %zu bytes, got %zu", p.workspace_bytes,

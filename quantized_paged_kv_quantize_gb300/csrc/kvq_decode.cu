@@ -804,58 +804,89 @@ cudaError_t launch_d(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s) {
 
 // Split plan.  Sequence lengths are known only on the device, so the plan
 // takes every sequence to be max_seq_len long.  One CTA per (split, kv head,
-// sequence), R of them resident per SM; pages per split pps = ceil(pages / s).
-//  Modes 1-4 (16-token pages, 1 to kIdsPerWarp per warp) stream at the memory
-//  system's pace: a plan with s splits is estimated at
+// sequence) -- per query row for the mma.sync kernel's multi-query decode --,
+// R of them resident per SM; pages per split pps = ceil(pages / s).
+//  mma.sync kernel (16-token pages, 1 to kIdsPerWarp per warp) streams at the
+//  memory system's pace: a plan with s splits is estimated at
 //      ceil(units * s / (R * SMs)) waves  x  (pps + kSplitCostPages).
+//  tcgen05 kernel (128-token tiles, all queries of a sequence in one CTA):
+//      ceil(units * s / (R * SMs)) waves  x  (tiles per split + kSplitCostUmma).
 //  KVarN (the CTA shares each 128-token tile, at most 64 per split) is bound
 //  by instruction issue, so a partial wave runs faster and what counts is the
 //  busiest SM: ceil(units * s / SMs) x (pps + kSplitCostTiles), with at least
 //  one full wave of CTAs (R per SM) to hide latency when there is work for it.
 // The overheads are a CTA's cost beyond its pages (start-up, pipeline fill,
-// merge, partial write) in page units, fitted to GB300 timings; the smallest
-// estimate wins, ties going to the split that divides the pages most evenly,
-// then to fewer splits.
+// merge, partial write) in page or tile units, fitted to GB300 timings; the
+// smallest estimate wins, ties going to the split that divides the pages most
+// evenly, then to fewer splits.
 constexpr long long kSplitCostPages = 16;
 constexpr long long kSplitCostTiles = 2;
+constexpr long long kSplitCostUmma = 1;
 
-DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int max_seq_len) {
+DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int max_seq_len, int num_queries) {
   DecodePlan p{1, c->cfg.page_size, 0};
   const int P = c->cfg.page_size;
   const long long pages = (max_seq_len + P - 1) / P;
   if (pages <= 0) return p;
-  const long long units = (long long)num_seqs * c->cfg.num_kv_heads;
-  const bool kvarn = c->cfg.mode == KVQ_KVARN_K4V2_G128;
-  const long long cap = kvarn ? 64 : (long long)kWarps * kIdsPerWarp;
-  const long long min_pages = kvarn ? 1 : kWarps;
-  long long min_splits = (pages + cap - 1) / cap;
-  const long long max_splits = (pages + min_pages - 1) / min_pages;
   const long long sms = num_sms();
-  const long long slots = (long long)(kvarn ? kvarn_resident_ctas() : resident_ctas_of(c)) * sms;
-  if (kvarn) {  // one full wave when the tiles allow it
-    long long full = (slots + units - 1) / units;
-    if (full > max_splits) full = max_splits;
-    if (full > min_splits) min_splits = full;
-  }
-  long long best = -1, best_ragged = 0, splits = min_splits;
-  const long long hi = max_splits < min_splits + 256 ? max_splits : min_splits + 256;
-  for (long long s = min_splits; s <= hi; ++s) {
-    const long long pps = (pages + s - 1) / s;
-    const long long cost = kvarn ? (units * s + sms - 1) / sms * (pps + kSplitCostTiles)
-                                 : (units * s + slots - 1) / slots * (pps + kSplitCostPages);
-    const long long ragged = s * pps - pages;  // ties: the evener split
-    if (best < 0 || cost < best || (cost == best && ragged < best_ragged)) {
-      best = cost;
-      best_ragged = ragged;
-      splits = s;
+  const bool kvarn = c->cfg.mode == KVQ_KVARN_K4V2_G128;
+  const bool umma = !kvarn && umma_decode_eligible(c, num_q_heads, num_queries);
+  const long long rows = (long long)num_seqs * num_queries;  // query rows: the partials' first index
+  long long splits = 1;
+  if (umma) {
+    const long long units = (long long)num_seqs * c->cfg.num_kv_heads;
+    const long long tiles = (pages + 7) / 8;
+    const long long cap_tiles = umma_max_pages_per_split() / 8;
+    const long long slots = (long long)umma_resident_ctas(c, num_q_heads, num_queries) * sms;
+    const long long min_s = (tiles + cap_tiles - 1) / cap_tiles;
+    const long long hi = tiles < min_s + 256 ? tiles : min_s + 256;
+    long long best = -1, best_ragged = 0;
+    splits = min_s;
+    for (long long s = min_s; s <= hi; ++s) {
+      const long long tps = (tiles + s - 1) / s;
+      const long long cost = (units * s + slots - 1) / slots * (tps + kSplitCostUmma);
+      const long long ragged = s * tps - tiles;
+      if (best < 0 || cost < best || (cost == best && ragged < best_ragged)) {
+        best = cost;
+        best_ragged = ragged;
+        splits = s;
+      }
     }
+    const long long tps = (tiles + splits - 1) / splits;
+    p.tokens_per_split = (int)(tps * 8 * P);
+  } else {
+    const long long units = rows * c->cfg.num_kv_heads;
+    const long long cap = kvarn ? 64 : (long long)kWarps * kIdsPerWarp;
+    const long long min_pages = kvarn ? 1 : kWarps;
+    long long min_splits = (pages + cap - 1) / cap;
+    const long long max_splits = (pages + min_pages - 1) / min_pages;
+    const long long slots = (long long)(kvarn ? kvarn_resident_ctas() : resident_ctas_of(c)) * sms;
+    if (kvarn) {  // one full wave when the tiles allow it
+      long long full = (slots + units - 1) / units;
+      if (full > max_splits) full = max_splits;
+      if (full > min_splits) min_splits = full;
+    }
+    long long best = -1, best_ragged = 0;
+    splits = min_splits;
+    const long long hi = max_splits < min_splits + 256 ? max_splits : min_splits + 256;
+    for (long long s = min_splits; s <= hi; ++s) {
+      const long long pps = (pages + s - 1) / s;
+      const long long cost = kvarn ? (units * s + sms - 1) / sms * (pps + kSplitCostTiles)
+                                   : (units * s + slots - 1) / slots * (pps + kSplitCostPages);
+      const long long ragged = s * pps - pages;  // ties: the evener split
+      if (best < 0 || cost < best || (cost == best && ragged < best_ragged)) {
+        best = cost;
+        best_ragged = ragged;
+        splits = s;
+      }
+    }
+    if (splits < 1) splits = 1;
+    const long long pps = (pages + splits - 1) / splits;
+    p.tokens_per_split = (int)(pps * P);
   }
-  if (splits < 1) splits = 1;
-  const long long pps = (pages + splits - 1) / splits;
-  p.tokens_per_split = (int)(pps * P);
   p.num_splits = (int)((max_seq_len + p.tokens_per_split - 1) / p.tokens_per_split);
   if (p.num_splits > 1)
-    p.workspace_bytes = (size_t)num_seqs * num_q_heads * p.num_splits * (c->cfg.head_dim + 2) * sizeof(float);
+    p.workspace_bytes = (size_t)rows * num_q_heads * p.num_splits * (c->cfg.head_dim + 2) * sizeof(float);
   return p;
 }
 
@@ -892,6 +923,13 @@ cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void
   a.rows_per_block = c->rows_per_block;
   if (num_seqs == 0) return cudaSuccess;
   if (c->cfg.mode == KVQ_KVARN_K4V2_G128) return launch_kvarn_decode(a, stream);
+  if (umma_decode_eligible(c, num_q_heads, num_queries)) {
+    cudaError_t e = launch_umma_decode(c, a, stream);
+    if (e != cudaSuccess || a.num_splits == 1) return e;
+    const int D = c->cfg.head_dim;
+    e = D == 128 ? launch_dependent(combine_kernel<128>, dim3(a.B * a.Hq), dim3(128), stream, a) : cudaErrorInvalidValue;
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   const bool qf32 = c->cfg.io_dtype == KVQ_F32;
   if (c->cfg.head_dim == 128)
     return qf32 ? launch_d<128, true>(c, a, stream) : launch_d<128, false>(c, a, stream);

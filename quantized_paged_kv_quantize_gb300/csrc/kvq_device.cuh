@@ -11,6 +11,8 @@
 
 #include "kvq.h"
 
+struct kvq_cache;
+
 namespace kvq {
 
 constexpr int kHeaderBytes = 256;
@@ -93,6 +95,108 @@ __device__ __forceinline__ void tma_g2s_2d(void* smem, const CUtensorMap* map, i
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05 (5th-generation tensor cores)
+// Tensor memory (TMEM): 128 lanes x 512 columns of 32 bits per SM; an address
+// is (lane << 16) | column.  Warp w of a CTA reaches lanes 32 (w % 4) .. + 31.
+// Allocation and release are warp-wide; the allocated base is written to
+// shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Order tcgen05 operations around a thread barrier (before: issuing side; after: waiting side).
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// One arrival on `bar` once every tcgen05.mma this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// Shared-memory matrix descriptor, no swizzle: 8-row x 16-byte core matrices,
+// `lbo` bytes between core matrices along K, `sbo` bytes between 8-row groups.
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+         (1ull << 46);
+}
+// Instruction descriptor of kind::f16: f16 A and B (both K-major), f32 accumulate, M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// D[tmem] (+)= A[tmem] * B[smem]; accumulate when acc != 0.  One thread issues.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 32 bits, N columns: thread i of the warp <-> lane (warp base + i), registers <-> columns.
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t* r);
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t* r);
+template <>
+__device__ __forceinline__ void tmem_st<4>(uint32_t t, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(t), "r"(r[0]), "r"(r[1]), "r"(r[2]),
+               "r"(r[3])
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st<8>(uint32_t t, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(t), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st<16>(uint32_t t, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(t),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st<32>(uint32_t t, const uint32_t* r) {
+  tmem_st<16>(t, r);
+  tmem_st<16>(t + 16, r + 16);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<4>(uint32_t t, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(t)
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t t, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(t)
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t t, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(t)
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t t, uint32_t* r) {
+  tmem_ld<16>(t, r);
+  tmem_ld<16>(t + 16, r + 16);
 }
 
 // ---------------------------------------------------------------- dependent launch
@@ -305,6 +409,14 @@ __device__ float merge_split_row(const DecodeArgs& a, long long base, int ns, fl
   }
   return lsum > 0.0f ? acc / lsum : 0.0f;
 }
+
+// tcgen05 decode of the 4-bit page modes at head_dim 128 (kvq_decode_umma.cu):
+// whether a cache and query shape take it, its resident CTAs per SM, the pages
+// one split may hold, and the launch (decode only; the caller adds the combine).
+bool umma_decode_eligible(const kvq_cache* c, int num_q_heads, int num_queries);
+int umma_resident_ctas(const kvq_cache* c, int num_q_heads, int num_queries);
+int umma_max_pages_per_split();
+cudaError_t launch_umma_decode(const kvq_cache* c, const DecodeArgs& a, cudaStream_t stream);
 
 // KVarN decode + combine (kvq_decode_kvarn.cu).
 cudaError_t launch_kvarn_decode(const DecodeArgs& a, cudaStream_t stream);

@@ -39,7 +39,8 @@ cudaError_t launch_amax(const void* x, int dtype, size_t n, float* out, cudaStre
 cudaError_t launch_scales_from_amax(uint8_t* pool, const float* amax_k, const float* amax_v, float div,
                                     cudaStream_t stream);
 
-DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int max_seq_len);
+// num_seqs counts sequences; each has num_queries query rows (multi-query decode).
+DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int max_seq_len, int num_queries = 1);
 cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void* q, const int32_t* block_table,
                           int max_pages, const int32_t* seq_lens, int num_seqs, int num_q_heads,
                           int max_seq_len, float softmax_scale, void* out, int out_dtype, void* workspace,
