@@ -34,6 +34,7 @@
 // per-tensor NVFP4 scales to the scores (K) and the output (V).
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "kvq_device.cuh"
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
     pages[k] = pid;
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full_bar[s], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&full_bar[s], kTilePages);  // one arrival per page
     mbar_init(&qk_bar, 1);
     mbar_init(&pv_bar, 1);
     mbar_fence_init();
@@ -206,26 +207,28 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
   const uint32_t tb = tmem_base_s;
   const uint32_t tAK = tb + kColAK, tAV = tb + kColAV, tS = tb + kColS, tO = tb + kColS + N;
 
-  // the tile's blocks into stage i % kStages (thread 0)
-  auto issue_tile = [&](int i) {
+  // page p of tile i into stage i % kStages, by one lane of warp p: one arrival
+  // with the page's bytes (none for a missing page) on the stage's barrier
+  auto issue_page = [&](int i, int p) {
     uint64_t* bar = &full_bar[i % kStages];
-    uint8_t* dst = stage + (i % kStages) * kStageBytes;
-    uint32_t bytes = 0;
-    for (int p = 0; p < kTilePages; ++p) {
-      const int k = i * kTilePages + p;
-      if (k < np && pages[k] >= 0) bytes += BLK;
-    }
-    mbar_arrive_expect_tx(bar, bytes);
-    for (int p = 0; p < kTilePages; ++p) {
-      const int k = i * kTilePages + p;
-      if (k < np && pages[k] >= 0) {
-        const long long r0 = (kHeaderBytes + ((long long)pages[k] * a.Hkv + kvh) * BLK) / 64;
-        tma_g2s_2d(dst + p * kPageSlot, &tmap, 0, (int)r0, bar);
-      }
+    const int k = i * kTilePages + p;
+    const int pid = k < np ? pages[k] : -1;
+    mbar_arrive_expect_tx(bar, pid >= 0 ? (uint32_t)BLK : 0u);
+    if (pid >= 0) {
+      const long long r0 = (kHeaderBytes + ((long long)pid * a.Hkv + kvh) * BLK) / 64;
+      tma_g2s_2d(stage + (i % kStages) * kStageBytes + p * kPageSlot, &tmap, 0, (int)r0, bar);
     }
   };
-  if (tid == 0)
-    for (int i = 0; i < min(kStages, ntiles); ++i) issue_tile(i);
+  if (elect_one())
+    for (int i = 0; i < min(kStages, ntiles); ++i) issue_page(i, warp);
+  __syncwarp();
+  // B operand descriptors at k-step 0; k-step j starts 2 j kCoreK bytes further (the
+  // start-address field holds bytes / 16 and never carries: shared addresses < 2^18)
+  const uint64_t dQ = umma_sdesc(smem_u32(qt), kCoreK, kGroup8);
+  const uint64_t dQlo = umma_sdesc(smem_u32(qt + (QF32 ? L::BOP : 0)), kCoreK, kGroup8);
+  const uint64_t dP = umma_sdesc(smem_u32(pt), kCoreK, kGroup8);
+  const uint64_t dPlo = umma_sdesc(smem_u32(pt + L::BOP), kCoreK, kGroup8);
+  constexpr uint64_t kStep = (2 * kCoreK) >> 4;
 
   float kfac = a.sm_log2, vfac = 1.0f;
   if constexpr (Md::FP4) {
@@ -238,6 +241,12 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
     m[k] = -1e30f;  // finite start: no inf - inf
     l[k] = 0.0f;
   }
+  // this thread's columns: real ones first (k < nreal), each with its query's
+  // causal end (query i sees the tokens before n - (nq - 1 - i))
+  const int nreal = (Nr - half + 1) / 2;
+  int climit[CPT];
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) climit[k] = k < nreal ? n - (nq - 1 - (2 * k + half) / G) : 0;
   uint32_t qk_phase = 0, pv_phase = 0;
   bool qk_pending = false, pv_pending = false, o_valid = false, timed_out = false;
 
@@ -283,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
     // valid tokens of each page of the tile (0 for a missing page)
     auto page_valid = [&](int p) -> int {
       const int k = i * kTilePages + p;
-      if (k >= np || pages[k] < 0) return 0;
-      return min(kPage, t_end - (p0 + k) * kPage);
+      const int nv = min(kPage, t_end - (p0 + k) * kPage);
+      return (k < np && pages[k] >= 0) ? nv : 0;
     };
     if constexpr (Md::FP4) {
       // V block-scale pairs of the tile: entry (block b, pair k) = f16x2 of the
@@ -306,18 +315,18 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       timed_out = true;
       break;
     }
-    if (tid == 0) {
+    if (warp == 0) {
       tc_fence_after();
+      if (elect_one()) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        umma_f16_ts(tS, tAK + 8 * j, umma_sdesc(smem_u32(qt) + j * 2 * kCoreK, kCoreK, kGroup8), IDESC, j > 0);
-      if constexpr (QF32) {
+        for (int j = 0; j < 8; ++j) umma_f16_ts(tS, tAK + 8 * j, dQ + j * kStep, IDESC, j > 0 ? 1u : 0u);
+        if constexpr (QF32) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          umma_f16_ts(tS, tAK + 8 * j, umma_sdesc(smem_u32(qt + L::BOP) + j * 2 * kCoreK, kCoreK, kGroup8), IDESC,
-                      1u);
+          for (int j = 0; j < 8; ++j) umma_f16_ts(tS, tAK + 8 * j, dQlo + j * kStep, IDESC, 1u);
+        }
+        tc_commit(&qk_bar);
       }
-      tc_commit(&qk_bar);
+      __syncwarp();
     }
     qk_pending = true;
 
@@ -375,11 +384,7 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       float f = kfac;
       if constexpr (!Md::FP4) f *= *reinterpret_cast<const float*>(st + p * kPageSlot + kSOff + 4 * (row & 15));
 #pragma unroll
-      for (int k = 0; k < CPT; ++k) {  // query i = r / G sees the tokens before n - (nq - 1 - i)
-        const int r = 2 * k + half;
-        const bool vis = tok_ok && r < Nr && pos < n - (nq - 1 - r / G);
-        sc[k] = vis ? __uint_as_float(sv[k]) * f : -INFINITY;
-      }
+      for (int k = 0; k < CPT; ++k) sc[k] = (tok_ok && pos < climit[k]) ? __uint_as_float(sv[k]) * f : -INFINITY;
     }
     bool exceed = false;
 #pragma unroll
@@ -422,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       const int kb = (row & 7) * 2 + (row >> 3) * kCoreK;
 #pragma unroll
       for (int k = 0; k < CPT; ++k) {
-        if (2 * k + half >= Nr) continue;
+        if (k >= nreal) break;
         const float p = ex2(sc[k] + ((float)PSHIFT - m[k]));  // ex2(-inf) = 0
         l[k] += p;
         float x = p;
@@ -438,21 +443,20 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
     fence_proxy_async_smem();  // P^T, written by the generic proxy, is read by the tensor core
     tc_fence_before();
     __syncthreads();           // A_V and P^T complete; this stage's bytes are consumed
-    if (tid == 0) {
+    if (warp == 0) {
       tc_fence_after();
+      if (elect_one()) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        umma_f16_ts(tO, tAV + 8 * j, umma_sdesc(smem_u32(pt) + j * 2 * kCoreK, kCoreK, kGroup8), IDESC,
-                    (o_valid || j > 0) ? 1u : 0u);
+        for (int j = 0; j < 8; ++j) umma_f16_ts(tO, tAV + 8 * j, dP + j * kStep, IDESC, (o_valid || j > 0) ? 1u : 0u);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        umma_f16_ts(tO, tAV + 8 * j, umma_sdesc(smem_u32(pt + L::BOP) + j * 2 * kCoreK, kCoreK, kGroup8), IDESC,
-                    1u);
-      tc_commit(&pv_bar);
-      if (i + kStages < ntiles) {
-        fence_proxy_async_smem();
-        issue_tile(i + kStages);
+        for (int j = 0; j < 8; ++j) umma_f16_ts(tO, tAV + 8 * j, dPlo + j * kStep, IDESC, 1u);
+        tc_commit(&pv_bar);
       }
+      __syncwarp();
+    }
+    if (i + kStages < ntiles) {  // refill this stage (every thread is done reading it): page `warp`
+      if (elect_one()) issue_page(i + kStages, warp);
+      __syncwarp();
     }
     pv_pending = true;
     o_valid = true;
@@ -513,6 +517,10 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
   if (warp == 0) tmem_dealloc(tb, kTmemCols);
 }
 
+// Resident CTAs per SM, from the per-SM limits (shared memory with its per-CTA
+// reserve, registers, threads) and the 512 tensor-memory columns; the
+// occupancy query answers 1 for this kernel on GB300 although two CTAs run
+// side by side (measured), so it is not used.
 template <int MODE, int NT, bool QF32>
 int resident() {
   static std::atomic<int> cached{0};
@@ -520,13 +528,23 @@ int resident() {
   if (r > 0) return r;
   auto kern = umma_decode_kernel<MODE, NT, QF32>;
   constexpr size_t smem = Smem<NT, QF32, Mode<MODE>::FP4>::dynamic();
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, kern, kThreads, smem) != cudaSuccess || r <= 0) {
+  cudaFuncAttributes fa;
+  int dev = 0, smem_sm = 0, reserve = 0, regs_sm = 0, thr_sm = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaFuncGetAttributes(&fa, kern) == cudaSuccess &&
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&reserve, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) == cudaSuccess) {
+    const long long per_cta = (long long)fa.sharedSizeBytes + (long long)smem + reserve;
+    r = 512 / kTmemCols;
+    r = (int)std::min<long long>(r, smem_sm / per_cta);
+    r = std::min(r, regs_sm / std::max(1, fa.numRegs * kThreads));
+    r = std::min(r, thr_sm / kThreads);
+  } else {
     (void)cudaGetLastError();
     r = 1;
   }
-  // every resident CTA holds kTmemCols of the SM's 512 tensor-memory columns
-  r = r < 512 / kTmemCols ? r : 512 / kTmemCols;
+  r = std::max(r, 1);
   cached.store(r, std::memory_order_relaxed);
   return r;
 }
@@ -560,7 +578,12 @@ int umma_column_tiles(int group, int num_queries) {
   return nr <= 16 ? 1 : nr <= 32 ? 2 : nr <= 64 ? 4 : 0;
 }
 
+// Several queries per sequence only: with one query the products have 8 real
+// columns, and the tile's conversion and synchronisation work outweigh the
+// MMAs it saves against the mma.sync kernel (measured on GB300: NVFP4 B = 32 x
+// 32K, 504 us here against 257 us; with 4 queries 730 us against 917 us).
 bool umma_decode_eligible(const kvq_cache* c, int num_q_heads, int num_queries) {
+  if (num_queries < 2) return false;
   const int m = c->cfg.mode;
   if (c->cfg.head_dim != kD || c->cfg.page_size != kPage || c->rows_per_block == 0) return false;
   if (m != KVQ_NVFP4 && m != KVQ_NVFP4_4OVER6 && m != KVQ_INT4_PER_TOKEN_HEAD) return false;

@@ -120,6 +120,15 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
+// One lane of the (converged) warp gets true: the tcgen05.mma issuer.  Issuing
+// from a warp-uniform branch keeps the operands in uniform registers; a
+// single-thread branch around the issue loop costs several times as many
+// cycles per MMA (measured on GB300).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred P1;\n\telect.sync _|P1, 0xffffffff;\n\tselp.b32 %0, 1, 0, P1;\n\t}" : "=r"(pred));
+  return pred != 0;
+}
 // Shared-memory matrix descriptor, no swizzle: 8-row x 16-byte core matrices,
 // `lbo` bytes between core matrices along K, `sbo` bytes between 8-row groups.
 __device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
