@@ -85,6 +85,8 @@ typedef enum { KVQ_F16 = 0, KVQ_F32 = 1 } kvq_dtype;
 #define KVQ_DEVERR_SEQ_LEN 0x8u      /* a seq_len above max_seq_len or max_pages * page_size */
 #define KVQ_DEVERR_TIMEOUT 0x10u     /* a bounded wait on a copy ran out (work skipped) */
 #define KVQ_DEVERR_SEQ_ID 0x20u      /* kvq_kvarn_append: a seq_id outside [0, num_seqs) */
+#define KVQ_DEVERR_BOUNDS 0x40u      /* debug build only: a store fell outside the buffer its
+                                        arguments describe (skipped); see kvq_debug_build */
 
 typedef struct {
   int32_t num_pages;    /* pages in the pool */
@@ -124,6 +126,21 @@ typedef struct kvq_cache kvq_cache;
 
 const char* kvq_last_error(void);
 int kvq_version(void); /* layout/ABI version, currently 1 */
+
+/* 1 when the library was built with -DKVQ_DEBUG=1, else 0.  In such a build
+ * every global store of every kernel first checks that its bytes lie inside
+ * the buffer its arguments describe (the pool, the tail buffer, the output,
+ * the workspace); a store that does not is skipped and KVQ_DEVERR_BOUNDS is
+ * set in the cache's error word.  It stands in for a memory checker: an
+ * indexing fault shows up as a flag instead of a corrupted neighbour.  A
+ * release build checks nothing and never sets KVQ_DEVERR_BOUNDS. */
+int kvq_debug_build(void);
+
+/* Debug builds only (KVQ_ERR_UNSUPPORTED otherwise): one kernel tries a store
+ * one byte past the end of the pool's header span, which lies inside the
+ * pool's memory, and so must set KVQ_DEVERR_BOUNDS and leave the byte as it
+ * was.  Lets a test see that the checks are live.  Enqueued on `stream`. */
+kvq_status kvq_debug_bounds_selftest(kvq_cache* cache, void* stream);
 
 /* Bytes of the pool for `cfg` (header included), and of one (page, kv head)
  * block.  No device work. */

@@ -133,6 +133,17 @@ const char* kvq_last_error(void) { return g_err; }
 
 int kvq_version(void) { return 1; }
 
+int kvq_debug_build(void) { return KVQ_DEBUG ? 1 : 0; }
+
+kvq_status kvq_debug_bounds_selftest(kvq_cache* cache, void* stream) {
+  kvq_status s = check_cache(cache);
+  if (s) return s;
+  if (!KVQ_DEBUG) return fail(KVQ_ERR_UNSUPPORTED, "a release build has no store checks (build with -DKVQ_DEBUG=1)");
+  cudaError_t e = kvq::launch_bounds_selftest(cache->base, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return KVQ_OK;
+}
+
 kvq_status kvq_cache_bytes(const kvq_cache_config* cfg, size_t* bytes) {
   kvq_status s = check_config(cfg);
   if (s) return s;

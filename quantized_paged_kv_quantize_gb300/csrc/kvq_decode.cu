@@ -456,8 +456,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
     if (a.num_splits == 1) {  // empty sequence: zero output rows
       for (int i = threadIdx.x; i < a.G * D; i += blockDim.x) {
         const long long o = ((long long)b * a.Hq + (long long)kvh * a.G + i / D) * D + i % D;
-        if (a.out_f32) static_cast<float*>(a.out)[o] = 0.0f;
-        else static_cast<__half*>(a.out)[o] = __float2half_rn(0.0f);
+        store_out(a, o, 0.0f);
       }
     }
     return;
@@ -698,14 +697,13 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
     if (a.num_splits == 1) {
       const float r = L > 0.0f ? O * vfac / L : 0.0f;
       const long long oi = ((long long)b * a.Hq + hq) * D + d;
-      if (a.out_f32) static_cast<float*>(a.out)[oi] = r;
-      else static_cast<__half*>(a.out)[oi] = __float2half_rn(r);
+      store_out(a, oi, r);
     } else {
       const long long pi = ((long long)b * a.Hq + hq) * a.num_splits + split;
-      a.ws_o[pi * D + d] = O * vfac;
+      store_ws(a, a.ws_o + (pi * D + d), O * vfac);
       if (d == 0) {
-        a.ws_ml[2 * pi] = M;
-        a.ws_ml[2 * pi + 1] = L;
+        store_ws(a, a.ws_ml + (2 * pi), M);
+        store_ws(a, a.ws_ml + (2 * pi + 1), L);
       }
     }
   }
@@ -724,8 +722,7 @@ __global__ void __launch_bounds__(D) combine_kernel(const __grid_constant__ Deco
   const int ns = (n + a.tokens_per_split - 1) / a.tokens_per_split;
   const float r = merge_split_row<D>(a, ((long long)b * a.Hq + hq) * a.num_splits, ns, wts, red);
   const long long oi = ((long long)b * a.Hq + hq) * D + d;
-  if (a.out_f32) static_cast<float*>(a.out)[oi] = r;
-  else static_cast<__half*>(a.out)[oi] = __float2half_rn(r);
+  store_out(a, oi, r);
 }
 
 template <int MODE, int D>
@@ -921,6 +918,16 @@ cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void
   a.block_bytes = c->block_bytes;
   a.tail = static_cast<const uint8_t*>(kvarn_tail);
   a.rows_per_block = c->rows_per_block;
+  {
+    uint8_t* o = static_cast<uint8_t*>(out);
+    const size_t oel = (size_t)num_seqs * num_q_heads * c->cfg.head_dim;  // num_seqs counts query rows here
+    a.out_span = Span{o, o + oel * (out_dtype == KVQ_F32 ? 4 : 2)};
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    const size_t wbytes = (plan.num_splits > 1 || kvarn_tail)
+                              ? (size_t)num_seqs * num_q_heads * plan.num_splits * (c->cfg.head_dim + 2) * sizeof(float)
+                              : 0;
+    a.ws_span = Span{w, w ? w + wbytes : nullptr};
+  }
   if (num_seqs == 0) return cudaSuccess;
   if (c->cfg.mode == KVQ_KVARN_K4V2_G128) return launch_kvarn_decode(a, stream);
   if (umma_decode_eligible(c, num_q_heads, num_queries)) {

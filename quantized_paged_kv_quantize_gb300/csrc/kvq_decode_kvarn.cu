@@ -142,8 +142,7 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
     if (direct) {
       for (int i = tid; i < a.G * kD; i += blockDim.x) {
         const long long o = ((long long)b * a.Hq + (long long)kvh * a.G + i / kD) * kD + i % kD;
-        if (a.out_f32) static_cast<float*>(a.out)[o] = 0.0f;
-        else static_cast<__half*>(a.out)[o] = __float2half_rn(0.0f);
+        store_out(a, o, 0.0f);
       }
     }
     return;
@@ -463,10 +462,10 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
       fin[idx] = L > 0.0f ? O / L : 0.0f;
     } else if (h < a.G) {
       const long long pi = ((long long)b * a.Hq + (long long)kvh * a.G + h) * a.num_splits + split;
-      a.ws_o[pi * kD + d] = O;
+      store_ws(a, a.ws_o + (pi * kD + d), O);
       if (d == 0) {
-        a.ws_ml[2 * pi] = M;
-        a.ws_ml[2 * pi + 1] = L;
+        store_ws(a, a.ws_ml + (2 * pi), M);
+        store_ws(a, a.ws_ml + (2 * pi + 1), L);
       }
     }
   }
@@ -480,8 +479,7 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
       const long long ob = ((long long)b * a.Hq + (long long)kvh * a.G + h) * kD + 4 * lane;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        if (a.out_f32) static_cast<float*>(a.out)[ob + i] = v[i];
-        else static_cast<__half*>(a.out)[ob + i] = __float2half_rn(v[i]);
+        store_out(a, ob + i, v[i]);
       }
     }
   }
@@ -561,8 +559,7 @@ __global__ void __launch_bounds__(kD) kvarn_combine_kernel(const __grid_constant
     r = Lt > 0.0f ? Ot / Lt : 0.0f;
   }
   const long long oi = ((long long)b * a.Hq + hq) * kD + d;
-  if (a.out_f32) static_cast<float*>(a.out)[oi] = r;
-  else static_cast<__half*>(a.out)[oi] = __float2half_rn(r);
+  store_out(a, oi, r);
 }
 
 }  // namespace

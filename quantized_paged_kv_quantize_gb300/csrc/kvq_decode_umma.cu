@@ -141,8 +141,7 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       for (int idx = tid; idx < Nr * kD; idx += kThreads) {
         const int r = idx / kD, d = idx % kD;
         const long long o = ((long long)(seq * nq + r / G) * a.Hq + (long long)kvh * G + r % G) * kD + d;
-        if (a.out_f32) static_cast<float*>(a.out)[o] = 0.0f;
-        else static_cast<__half*>(a.out)[o] = __float2half_rn(0.0f);
+        store_out(a, o, 0.0f);
       }
     }
     return;
@@ -499,14 +498,13 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
         const long long qrow = (long long)(seq * nq + r / G) * a.Hq + (long long)kvh * G + r % G;
         if (a.num_splits == 1) {
           const float res = Lc > 0.0f ? O / Lc : 0.0f;
-          if (a.out_f32) static_cast<float*>(a.out)[qrow * kD + d] = res;
-          else static_cast<__half*>(a.out)[qrow * kD + d] = __float2half_rn(res);
+          store_out(a, qrow * kD + d, res);
         } else {
           const long long pi = qrow * a.num_splits + split;
-          a.ws_o[pi * kD + d] = Lc > 0.0f ? O : 0.0f;
+          store_ws(a, a.ws_o + (pi * kD + d), Lc > 0.0f ? O : 0.0f);
           if (d == 0) {
-            a.ws_ml[2 * pi] = m[k];
-            a.ws_ml[2 * pi + 1] = Lc;
+            store_ws(a, a.ws_ml + (2 * pi), m[k]);
+            store_ws(a, a.ws_ml + (2 * pi + 1), Lc);
           }
         }
       }

@@ -36,6 +36,36 @@ __device__ __forceinline__ void set_error(uint8_t* pool, uint32_t bits) {
   atomicOr(reinterpret_cast<uint32_t*>(pool + kHdrErrOffset), bits);
 }
 
+// ---------------------------------------------------------------- debug-build store checks
+#ifndef KVQ_DEBUG
+#define KVQ_DEBUG 0
+#endif
+// [lo, hi): the bytes one buffer of a kernel's arguments spans.
+struct Span {
+  uint8_t* lo;
+  uint8_t* hi;
+};
+// In a debug build (-DKVQ_DEBUG=1) every global store checks that its bytes
+// lie in the span of its buffer; one that does not is skipped and
+// KVQ_DEVERR_BOUNDS is set in the pool's error word.  A release build checks
+// nothing.
+__device__ __forceinline__ bool in_span(const void* p, size_t bytes, const Span& s, const uint8_t* pool) {
+#if KVQ_DEBUG
+  const uint8_t* q = static_cast<const uint8_t*>(p);
+  if (q < s.lo || q + bytes > s.hi) {
+    set_error(const_cast<uint8_t*>(pool), KVQ_DEVERR_BOUNDS);
+    return false;
+  }
+#else
+  (void)p; (void)bytes; (void)s; (void)pool;
+#endif
+  return true;
+}
+template <typename T>
+__device__ __forceinline__ void st_chk(T* p, const T& v, const Span& s, const uint8_t* pool) {
+  if (in_span(p, sizeof(T), s, pool)) *p = v;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -356,7 +386,15 @@ struct DecodeArgs {
   // queries per sequence (multi-query decode under the causal mask); B counts
   // query rows, B = sequences * nq
   int nq;
+  // the output [B][Hq][D] and the split workspace, as spans (debug-build checks)
+  Span out_span, ws_span;
 };
+// Checked stores of one output element and of one split partial.
+__device__ __forceinline__ void store_out(const DecodeArgs& a, long long i, float v) {
+  if (a.out_f32) st_chk(static_cast<float*>(a.out) + i, v, a.out_span, a.pool);
+  else st_chk(static_cast<__half*>(a.out) + i, __float2half_rn(v), a.out_span, a.pool);
+}
+__device__ __forceinline__ void store_ws(const DecodeArgs& a, float* p, float v) { st_chk(p, v, a.ws_span, a.pool); }
 
 // Split-KV merge of one (sequence, query head) row by a CTA of D threads,
 // thread d owning channel d; base indexes the row's first split partial.

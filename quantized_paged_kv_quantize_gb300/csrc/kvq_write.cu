@@ -39,6 +39,8 @@ struct WriteArgs {
   const int32_t* seq_ids;
   uint8_t* tail;
   int num_seqs;
+  // the pool's blocks and the tail buffer, as spans (debug-build store checks)
+  Span pool_span, tail_span;
 };
 
 template <typename T>
@@ -80,6 +82,10 @@ __device__ __forceinline__ void widen16<float>(const uint4& u, float* f) {
 
 template <int N>
 __device__ __forceinline__ void store_bytes(uint8_t* dst, const uint32_t* w);
+template <int N>
+__device__ __forceinline__ void store_bytes_chk(uint8_t* dst, const uint32_t* w, const WriteArgs& a) {
+  if (in_span(dst, N, a.pool_span, a.pool)) store_bytes<N>(dst, w);
+}
 template <>
 __device__ __forceinline__ void store_bytes<2>(uint8_t* dst, const uint32_t* w) {
   *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w[0]);
@@ -323,7 +329,7 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
     uint32_t w[VEC / 4];
 #pragma unroll
     for (int i = 0; i < VEC; i += 4) w[i / 4] = q.e4m3x2(x[i + 1], x[i]) | (q.e4m3x2(x[i + 3], x[i + 2]) << 16);
-    if (active) store_bytes<VEC>(blk + (size_t)side * a.P * D + (size_t)off * D + j * VEC, w);
+    if (active) store_bytes_chk<VEC>(blk + (size_t)side * a.P * D + (size_t)off * D + j * VEC, w, a);
   } else if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD || MODE == KVQ_FP8_PER_TOKEN_HEAD) {
     float amax = 0.0f;
 #pragma unroll
@@ -342,16 +348,17 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
       }
     }
     if (active) {
-      store_bytes<VEC>(blk + (size_t)side * a.P * D + (size_t)off * D + j * VEC, w);
-      if (j == 0) *reinterpret_cast<float*>(blk + (size_t)2 * a.P * D + (size_t)side * 4 * a.P + 4 * off) = s;
+      store_bytes_chk<VEC>(blk + (size_t)side * a.P * D + (size_t)off * D + j * VEC, w, a);
+      if (j == 0) st_chk(reinterpret_cast<float*>(blk + (size_t)2 * a.P * D + (size_t)side * 4 * a.P + 4 * off), s, a.pool_span, a.pool);
     }
   } else if constexpr (MODE == KVQ_NVFP4 || MODE == KVQ_NVFP4_4OVER6) {  // keys; values: pair_values_pass
     constexpr int TPB = 16 / VEC;  // threads per 16-value block
     uint32_t w[1], sb;
     nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, ts.st, ts.qs, ts.q4, w[0], sb);
     if (active) {
-      store_bytes<VEC / 2>(blk + (size_t)off * D / 2 + j * VEC / 2, w);
-      if ((j % TPB) == 0) blk[(size_t)a.P * D + (size_t)off * D / 16 + (j * VEC) / 16] = static_cast<uint8_t>(sb);
+      store_bytes_chk<VEC / 2>(blk + (size_t)off * D / 2 + j * VEC / 2, w, a);
+      if ((j % TPB) == 0)
+        st_chk(blk + (size_t)a.P * D + (size_t)off * D / 16 + (j * VEC) / 16, static_cast<uint8_t>(sb), a.pool_span, a.pool);
     }
   } else if constexpr (MODE == KVQ_INT4_PER_TOKEN_HEAD) {  // keys; values: pair_values_pass
     float amax = 0.0f;
@@ -368,8 +375,8 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
       w[0] |= __shfl_xor_sync(kFull, w[0], 1);
     }
     if (active) {
-      if (VEC == 8 || (j & 1) == 0) store_bytes<4>(blk + (size_t)off * D / 2 + (j * VEC / 8) * 4, w);
-      if (j == 0) *reinterpret_cast<float*>(blk + (size_t)a.P * D + 4 * off) = s;
+      if (VEC == 8 || (j & 1) == 0) store_bytes_chk<4>(blk + (size_t)off * D / 2 + (j * VEC / 8) * 4, w, a);
+      if (j == 0) st_chk(reinterpret_cast<float*>(blk + (size_t)a.P * D + 4 * off), s, a.pool_span, a.pool);
     }
   }
 }
@@ -415,12 +422,14 @@ __device__ __forceinline__ void pair_values_pass(const WriteArgs& a, int h, cons
       amax = group_max<TPR>(amax);
       const float sc = div_const(fmaxf(amax, 1e-8f), 7.0f, kRcp7);
       wr[r] = QDiv(sc).int4x8<VEC>(x);
-      if (active && j == 0) *reinterpret_cast<float*>(blk + (size_t)a.P * D + (size_t)4 * a.P + 4 * off) = sc;
+      if (active && j == 0)
+        st_chk(reinterpret_cast<float*>(blk + (size_t)a.P * D + (size_t)4 * a.P + 4 * off), sc, a.pool_span, a.pool);
     } else {
       uint32_t sb;
       nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, ts.st, ts.qs, ts.q4, wr[r], sb);
       if (active && (j % TPB) == 0)
-        blk[(size_t)a.P * D + (size_t)a.P * D / 16 + (size_t)off * D / 16 + (j * VEC) / 16] = static_cast<uint8_t>(sb);
+        st_chk(blk + (size_t)a.P * D + (size_t)a.P * D / 16 + (size_t)off * D / 16 + (j * VEC) / 16, static_cast<uint8_t>(sb),
+               a.pool_span, a.pool);
     }
     sr[r] = active ? s : -1;
     if constexpr (!kInWarp) {
@@ -456,12 +465,13 @@ __device__ __forceinline__ void pair_values_pass(const WriteArgs& a, int h, cons
       // the same channels of the odd token in the high half-word
       if (!(s & 1) && next == s + 1) {
         const uint2 both = make_uint2(prmt(wr[r], other, 0x5410u), prmt(wr[r], other, 0x7632u));
-        if constexpr (VEC == 8) *reinterpret_cast<uint2*>(dst) = both;
-        else *reinterpret_cast<uint32_t*>(dst) = both.x;
+        if constexpr (VEC == 8) st_chk(reinterpret_cast<uint2*>(dst), both, a.pool_span, a.pool);
+        else st_chk(reinterpret_cast<uint32_t*>(dst), both.x, a.pool_span, a.pool);
       } else {
         const int sh = 16 * (off & 1);
         const uint32_t m = 0xFFFFu << sh;
         unsigned int* wd = reinterpret_cast<unsigned int*>(dst);
+        if (!in_span(wd, VEC == 8 ? 8 : 4, a.pool_span, a.pool)) continue;
         atomicAnd(wd, ~m);
         atomicOr(wd, (wr[r] & 0xFFFFu) << sh);
         if constexpr (VEC == 8) {
@@ -478,13 +488,14 @@ __device__ __forceinline__ void pair_values_pass(const WriteArgs& a, int h, cons
       const uint32_t ev = bitsel(wr[r], other << 4, 0x0F0F0F0Fu);
       const uint32_t od = bitsel(wr[r] >> 4, other, 0x0F0F0F0Fu);
       const uint2 both = make_uint2(prmt(ev, od, 0x5140u), prmt(ev, od, 0x7362u));
-      if constexpr (VEC == 8) *reinterpret_cast<uint2*>(dst) = both;
-      else *reinterpret_cast<uint32_t*>(dst) = both.x;
+      if constexpr (VEC == 8) st_chk(reinterpret_cast<uint2*>(dst), both, a.pool_span, a.pool);
+      else st_chk(reinterpret_cast<uint32_t*>(dst), both.x, a.pool_span, a.pool);
     } else {
       const uint2 mine = spread_codes(wr[r]);
       const int sh = 4 * (off & 1);
       const uint32_t m = 0x0F0F0F0Fu << sh;
       unsigned int* wd = reinterpret_cast<unsigned int*>(dst);
+      if (!in_span(wd, VEC == 8 ? 8 : 4, a.pool_span, a.pool)) continue;
       atomicAnd(wd, ~m);
       atomicOr(wd, mine.x << sh);
       if constexpr (VEC == 8) {
@@ -855,10 +866,10 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
       const float sc = div_const(__fsub_rn(mx, mn), 15.0f, kRcp15);
       sm.st0[tid] = sc;
       sm.st1[tid] = mn;
-      meta[tid] = sc;
-      meta[D + tid] = mn;
-      meta[2 * D + tid] = sm.fc[tid];
-      meta[3 * D + tid] = sm.fr[tid];
+      st_chk(meta + tid, sc, a.pool_span, a.pool);
+      st_chk(meta + D + tid, mn, a.pool_span, a.pool);
+      st_chk(meta + 2 * D + tid, sm.fc[tid], a.pool_span, a.pool);
+      st_chk(meta + 3 * D + tid, sm.fr[tid], a.pool_span, a.pool);
     }
     __syncthreads();
 #pragma unroll
@@ -888,8 +899,8 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
     float* meta = reinterpret_cast<float*>(blk + kKvTile * D / 2 + kKvTile * D / 4 + 4 * (3 * D + kKvTile));
     if ((lane & 1) == 0) {  // lanes 2k (+16) own token tl + 16 (4 b3 + 2 b2 + b1)
       const int t = tl + 16 * (((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1));
-      meta[t] = sc;
-      meta[kKvTile + t] = mn;
+      st_chk(meta + t, sc, a.pool_span, a.pool);
+      st_chk(meta + kKvTile + t, mn, a.pool_span, a.pool);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -901,8 +912,8 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
         codes[(tl + 16 * i) * kKvCS + dl + 16 * j] = static_cast<uint8_t>(rtn_code(__fsub_rn(y[i][j], mni), q, 3.0f));
     }
     if (tid < kKvTile) {
-      meta[2 * kKvTile + tid] = sm.fr[tid];
-      meta[3 * kKvTile + tid] = sm.fc[tid];
+      st_chk(meta + 2 * kKvTile + tid, sm.fr[tid], a.pool_span, a.pool);
+      st_chk(meta + 3 * kKvTile + tid, sm.fc[tid], a.pool_span, a.pool);
     }
   }
   __syncthreads();
@@ -921,7 +932,8 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
         const uint32_t x0 = in[2 * q] | (in[2 * q] >> 4), x1 = in[2 * q + 1] | (in[2 * q + 1] >> 4);
         out[q] = prmt(x0, x1, 0x6420u);  // bytes 0, 2 of each: (c0 | c1 << 4), (c2 | c3 << 4)
       }
-      *reinterpret_cast<uint4*>(pay + t * 64 + (c & 3) * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+      st_chk(reinterpret_cast<uint4*>(pay + t * 64 + (c & 3) * 16), make_uint4(out[0], out[1], out[2], out[3]), a.pool_span,
+             a.pool);
     }
   } else {  // [128][32]: element 4i + j in bits 2j..2j+1; 64 codes per chunk
     uint8_t* pay = blk + kKvTile * D / 2;
@@ -936,8 +948,18 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
       for (int e = 0; e < 4; ++e) b[e] = (in[e] | (in[e] >> 6) | (in[e] >> 12) | (in[e] >> 18)) & 0xFFu;
       out[q] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
     }
-    *reinterpret_cast<uint4*>(pay + t * 32 + (tid & 1) * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+    st_chk(reinterpret_cast<uint4*>(pay + t * 32 + (tid & 1) * 16), make_uint4(out[0], out[1], out[2], out[3]), a.pool_span,
+           a.pool);
   }
+}
+
+// ------------------------------------------------------------------ debug self-test
+// A store at pool byte 41 against the span [40, 41): outside it, so a debug
+// build skips it and flags KVQ_DEVERR_BOUNDS (byte 41 is inside the header,
+// unused, so even a missing check could not touch anything but that byte).
+__global__ void bounds_selftest_kernel(uint8_t* pool) {
+  const Span s{pool + 40, pool + 41};
+  st_chk(pool + 41, static_cast<uint8_t>(0x5A), s, pool);
 }
 
 // ------------------------------------------------------------------ scales
@@ -1033,7 +1055,7 @@ __global__ void __launch_bounds__(256) kvarn_tail_copy_kernel(WriteArgs a) {
                                                          (i * a.Hkv + h) * D) + c);
     uint4* dst = reinterpret_cast<uint4*>(a.tail + side * side_bytes +
                                           ((((size_t)seq * kKvTile + slot % kKvTile) * a.Hkv + h) * D) * sizeof(T));
-    dst[c] = v;
+    st_chk(dst + c, v, a.tail_span, a.pool);
   }
 }
 
@@ -1051,6 +1073,12 @@ cudaError_t launch_kvarn_tail(const WriteArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+// The span of the pool's (page, kv head) blocks: every store a write kernel makes.
+Span pool_blocks(const kvq_cache* c) {
+  uint8_t* lo = c->base + kHeaderBytes;
+  return Span{lo, lo + (size_t)c->cfg.num_pages * c->cfg.num_kv_heads * c->block_bytes};
+}
 
 cudaError_t launch_write(const kvq_cache* c, const void* k, const void* v, const int32_t* slots, int num_tokens,
                          cudaStream_t stream) {
@@ -1071,6 +1099,8 @@ cudaError_t launch_write(const kvq_cache* c, const void* k, const void* v, const
   a.seq_ids = nullptr;
   a.tail = nullptr;
   a.num_seqs = 0;
+  a.pool_span = pool_blocks(c);
+  a.tail_span = Span{nullptr, nullptr};
   if (mode == KVQ_KVARN_K4V2_G128)
     return f16 ? launch_kvarn<__half, false>(a, stream) : launch_kvarn<float, false>(a, stream);
   if (D == 128) return f16 ? launch_mode<__half, 128>(mode, a, stream) : launch_mode<float, 128>(mode, a, stream);
@@ -1095,7 +1125,15 @@ cudaError_t launch_kvarn_append(const kvq_cache* c, const void* k, const void* v
   a.seq_ids = seq_ids;
   a.tail = static_cast<uint8_t*>(tail);
   a.num_seqs = num_seqs;
+  a.pool_span = pool_blocks(c);
+  const size_t esz = c->cfg.io_dtype == KVQ_F16 ? 2 : 4;
+  a.tail_span = Span{a.tail, a.tail + (size_t)2 * num_seqs * 128 * a.Hkv * c->cfg.head_dim * esz};
   return c->cfg.io_dtype == KVQ_F16 ? launch_kvarn_tail<__half>(a, stream) : launch_kvarn_tail<float>(a, stream);
+}
+
+cudaError_t launch_bounds_selftest(uint8_t* pool, cudaStream_t stream) {
+  bounds_selftest_kernel<<<1, 1, 0, stream>>>(pool);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_amax(const void* x, int dtype, size_t n, float* out, cudaStream_t stream) {

@@ -40,6 +40,7 @@ EXPORTED = [
     "kvq_decode_plan", "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_decode_attention_noalloc",
     "kvq_kvarn_tail_bytes", "kvq_kvarn_append", "kvq_kvarn_decode_workspace_bytes", "kvq_kvarn_decode_attention",
     "kvq_decode_multi_plan", "kvq_decode_multi_workspace_bytes", "kvq_decode_attention_multi",
+    "kvq_debug_build", "kvq_debug_bounds_selftest",
 ]
 
 
@@ -64,6 +65,8 @@ def _load():
     sig = {
         "kvq_last_error": (ctypes.c_char_p, []),
         "kvq_version": (i32, []),
+        "kvq_debug_build": (i32, []),
+        "kvq_debug_bounds_selftest": (i32, [vp, vp]),
         "kvq_cache_bytes": (i32, [cfgp, ctypes.POINTER(sz)]),
         "kvq_cache_block_bytes": (i32, [cfgp, ctypes.POINTER(sz)]),
         "kvq_cache_alloc": (i32, [cfgp, vp, sz, ctypes.POINTER(vp)]),
@@ -142,6 +145,15 @@ def make_config(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int
 
 def kvq_version() -> int:
     return _lib.kvq_version()
+
+
+def kvq_debug_build() -> bool:
+    """True when libkvq was built with -DKVQ_DEBUG=1 (store checks in every kernel)."""
+    return bool(_lib.kvq_debug_build())
+
+
+def kvq_debug_bounds_selftest(cache: "KVCache", stream=None):
+    _check(_lib.kvq_debug_bounds_selftest(cache.handle, _stream(stream)))
 
 
 def kvq_cache_bytes(cfg: CacheConfig) -> int:

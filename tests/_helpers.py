@@ -16,6 +16,37 @@ MODE_NAMES = ["fp8_per_tensor", "int8_per_token_head", "fp8_per_token_head", "nv
               "nvfp4_4over6", "kvarn_k4v2_g128"]
 TENSOR_SCALED = {"fp8_per_tensor", "nvfp4", "nvfp4_4over6"}
 FILL = 0xCD  # untouched bytes of both pools
+GUARD = 4096        # canary bytes on each side of every device buffer a kernel writes
+GUARD_BYTE = 0xA5
+_guarded = []       # (raw tensor, payload bytes, name) of the buffers handed out since the last check
+
+
+def guarded(shape, dtype, fill=None, name="buffer") -> torch.Tensor:
+    """A CUDA tensor with GUARD canary bytes before and after it (the pool,
+    an output, a workspace, a tail buffer): a kernel store that strays past
+    its buffer changes a canary, which check_guards() reports after the test."""
+    shape = (shape,) if isinstance(shape, int) else tuple(shape)
+    esz = torch.empty((), dtype=dtype).element_size()
+    n = 1
+    for x in shape:
+        n *= int(x)
+    raw = torch.full((2 * GUARD + n * esz,), GUARD_BYTE, dtype=torch.uint8, device="cuda")
+    view = raw[GUARD:GUARD + n * esz].view(dtype).view(shape)
+    if fill is not None:
+        view.fill_(fill)
+    _guarded.append((raw, n * esz, name))
+    return view
+
+
+def check_guards():
+    """Every canary band still holds GUARD_BYTE (then forget the buffers)."""
+    bad = []
+    for raw, n, name in _guarded:
+        lo, hi = raw[:GUARD], raw[GUARD + n:]
+        if bool((lo != GUARD_BYTE).any()) or bool((hi != GUARD_BYTE).any()):
+            bad.append(name)
+    _guarded.clear()
+    assert not bad, f"canary bytes overwritten next to: {bad}"
 
 
 def kvq():
@@ -75,7 +106,7 @@ def config(c: Case):
 def gpu_cache(c: Case, fill: int = FILL):
     K = kvq()
     cfg = config(c)
-    pool = torch.full((K.kvq_cache_bytes(cfg),), fill, dtype=torch.uint8, device="cuda")
+    pool = guarded(K.kvq_cache_bytes(cfg), torch.uint8, fill=fill, name="pool")
     return K.kvq_cache_alloc(cfg, pool)
 
 
@@ -102,9 +133,9 @@ def gpu_decode(cache, c: Case, q_dev=None, out_dtype=torch.float32, max_seq_len=
     q_dev = torch.from_numpy(c.q).cuda() if q_dev is None else q_dev
     bt_dev = torch.from_numpy(c.lay.block_table if bt is None else bt).cuda()
     sl_dev = torch.from_numpy(c.lay.seq_lens if lens is None else np.asarray(lens, np.int32)).cuda()
-    out = torch.full((B, w.num_q_heads, w.head_dim), float("nan"), dtype=out_dtype, device="cuda")
+    out = guarded((B, w.num_q_heads, w.head_dim), out_dtype, fill=float("nan"), name="out")
     ns, tps, wsb = K.kvq_decode_plan(cache, B, w.num_q_heads, msl)
-    ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
+    ws = guarded(max(wsb // 4, 1), torch.float32, name="workspace")
     K.kvq_decode_attention(cache, q_dev, bt_dev, sl_dev, out, max_seq_len=msl, workspace=ws)
     torch.cuda.synchronize()
     return out, (ns, tps, wsb)

@@ -2,6 +2,8 @@ import importlib.util
 import os
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -21,3 +23,12 @@ def pytest_sessionstart(session):
     mod.build()
     import oracle
     oracle.build()
+
+
+@pytest.fixture(autouse=True)
+def _canaries():
+    """After every test, the canary bands around the device buffers it handed
+    to the kernels (tests/_helpers.guarded) must be intact."""
+    yield
+    if "_helpers" in sys.modules:
+        sys.modules["_helpers"].check_guards()

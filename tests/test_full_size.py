@@ -12,7 +12,7 @@ import torch
 import bench
 import oracle
 import workloads as wl
-from _helpers import check_attention
+from _helpers import check_attention, guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +42,7 @@ def test_full_size_sampled_parity(name, mode, sample):
         gw.write_step()
         gw.decode()
     out16 = gw.out.clone()
-    out32 = torch.empty(gw.out.shape, dtype=torch.float32, device="cuda")
+    out32 = guarded(tuple(gw.out.shape), torch.float32, name="out")
     gw.decode(out32)
     torch.cuda.synchronize()
     assert gw.kvq.kvq_cache_read_errors(gw.cache) == 0
@@ -96,7 +96,7 @@ def test_full_size_spec_decode_sampled_parity():
     for _ in range(3):
         gw.write_step()
         gw.decode()
-    out32 = torch.empty(gw.out.shape, dtype=torch.float32, device="cuda")
+    out32 = guarded(tuple(gw.out.shape), torch.float32, name="out")
     gw.decode(out32)
     torch.cuda.synchronize()
     assert gw.kvq.kvq_cache_read_errors(gw.cache) == 0

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import workloads as wl
-from _helpers import check_attention, kvq
+from _helpers import check_attention, guarded, kvq
 
 pytestmark = pytest.mark.gpu
 
@@ -40,10 +40,10 @@ class Seqs:
         K = kvq()
         tdt = torch.float16 if io == "f16" else torch.float32
         self.cfg = K.make_config(self.lay.num_pages, P, Hkv, D, "kvarn_k4v2_g128", tdt)
-        self.pool = torch.full((K.kvq_cache_bytes(self.cfg),), 0xCD, dtype=torch.uint8, device="cuda")
+        self.pool = guarded(K.kvq_cache_bytes(self.cfg), torch.uint8, fill=0xCD, name="pool")
         self.cache = K.kvq_cache_alloc(self.cfg, self.pool)
         B = len(lens)
-        self.tail = torch.zeros(K.kvq_kvarn_tail_bytes(self.cache, B), dtype=torch.uint8, device="cuda")
+        self.tail = guarded(K.kvq_kvarn_tail_bytes(self.cache, B), torch.uint8, fill=0, name="tail")
         self.ref_pool = np.full(oracle.pool_bytes("kvarn_k4v2_g128", self.lay.num_pages, P, Hkv, D), 0xCD, np.uint8)
         self.tail_np = np.zeros((2, B, P, Hkv, D), self.w.np_dtype)
 
@@ -90,9 +90,9 @@ class Seqs:
         K = kvq()
         B, Hq = len(lens), self.w.num_q_heads
         msl = int(max(lens)) if len(lens) else 0
-        ws = torch.empty(max(K.kvq_kvarn_decode_workspace_bytes(self.cache, B, Hq, msl) // 4, 1),
-                         dtype=torch.float32, device="cuda")
-        out = torch.full((B, Hq, D), float("nan"), dtype=out_dtype, device="cuda")
+        ws = guarded(max(K.kvq_kvarn_decode_workspace_bytes(self.cache, B, Hq, msl) // 4, 1), torch.float32,
+                     name="workspace")
+        out = guarded((B, Hq, D), out_dtype, fill=float("nan"), name="out")
         K.kvq_kvarn_decode_attention(self.cache, _dev(self.q), _dev(self.lay.block_table),
                                      _dev(np.asarray(lens, np.int32)), self.tail, out, max_seq_len=msl,
                                      workspace=ws)

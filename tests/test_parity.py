@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads as wl
-from _helpers import (FILL, TENSOR_SCALED, check_attention, gpu_cache, gpu_calibrate, gpu_decode, header_scales,
+from _helpers import (guarded, FILL, TENSOR_SCALED, check_attention, gpu_cache, gpu_calibrate, gpu_decode, header_scales,
                       kvq, make_case, oracle_decode, oracle_pool)
 
 pytestmark = pytest.mark.gpu
@@ -367,8 +367,8 @@ def test_decode_multi_query_parity(mode, nq, out_dtype):
     q = rng.standard_normal((B, nq, Hq, D)).astype(c.w.np_dtype)
     msl = int(c.lay.seq_lens.max())
     wsb = K.kvq_decode_multi_workspace_bytes(cache, B, nq, Hq, msl)
-    ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
-    out = torch.full((B, nq, Hq, D), float("nan"), dtype=out_dtype, device="cuda")
+    ws = guarded(max(wsb // 4, 1), torch.float32, name="workspace")
+    out = guarded((B, nq, Hq, D), out_dtype, fill=float("nan"), name="out")
     K.kvq_decode_attention_multi(cache, _dev(q), _dev(c.lay.block_table), _dev(c.lay.seq_lens), out,
                                  max_seq_len=msl, workspace=ws)
     torch.cuda.synchronize()
@@ -413,8 +413,8 @@ def test_decode_multi_query_one_split(mode, nq, Hkv):
     q = np.random.default_rng(3).standard_normal((B, nq, Hq, D)).astype(c.w.np_dtype)
     msl = int(c.lay.seq_lens.max())
     wsb = K.kvq_decode_multi_workspace_bytes(cache, B, nq, Hq, msl)
-    ws = torch.empty(max(wsb // 4, 1), dtype=torch.float32, device="cuda")
-    out = torch.full((B, nq, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+    ws = guarded(max(wsb // 4, 1), torch.float32, name="workspace")
+    out = guarded((B, nq, Hq, D), torch.float32, fill=float("nan"), name="out")
     K.kvq_decode_attention_multi(cache, _dev(q), _dev(c.lay.block_table), _dev(c.lay.seq_lens), out,
                                  max_seq_len=msl, workspace=ws)
     torch.cuda.synchronize()

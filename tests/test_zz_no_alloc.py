@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from _helpers import check_attention, kvq, make_case, gpu_cache, oracle_pool
+from _helpers import check_attention, guarded, kvq, make_case, gpu_cache, oracle_pool
 from test_parity import small_workload
 
 pytestmark = pytest.mark.gpu
@@ -41,13 +41,13 @@ def test_noalloc_matches_workspace_entry_point_twice(mode, D, io):
     ns, tps, wsb = K.kvq_decode_plan(cache, B, Hq, msl)
     assert ns > 1 and 0 < wsb <= K.NOALLOC_SCRATCH_BYTES   # the scratch is really used
     bt, sl = _dev(c.lay.block_table), _dev(c.lay.seq_lens)
-    ws = torch.empty(wsb // 4, dtype=torch.float32, device="cuda")
+    ws = guarded(wsb // 4, torch.float32, name="workspace")
     rng = np.random.default_rng(3)
     for call in range(2):   # the second call finds the first call's partials in the scratch
         q_np = (c.q.astype(np.float32) * (1.0 + 0.5 * call) + rng.standard_normal(c.q.shape) * 0.1).astype(c.q.dtype)
         q = _dev(q_np)
-        ref = torch.full((B, Hq, Dh), float("nan"), dtype=torch.float32, device="cuda")
-        out = torch.full_like(ref, float("nan"))
+        ref = guarded((B, Hq, Dh), torch.float32, fill=float("nan"), name="out (workspace entry point)")
+        out = guarded((B, Hq, Dh), torch.float32, fill=float("nan"), name="out (allocation-free entry point)")
         K.kvq_decode_attention(cache, q, bt, sl, ref, max_seq_len=msl, workspace=ws)
         K.kvq_decode_attention_noalloc(cache, q, bt, sl, out, max_seq_len=msl)
         torch.cuda.synchronize()
