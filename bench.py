@@ -394,6 +394,7 @@ def measure(gw: GpuWorkload, args, dev, ws: int, full: bool, sampler=None) -> di
     if flags:
         raise RuntimeError(f"{w.name}: device error word after fill: {flags:#x}")
     wbytes = write_bytes(w, gw.lay.num_tokens)
+    diag = tensor_diagnostics(gw)
 
     flush = None
     if gw.pool.numel() < 2 * L2_BYTES:
@@ -454,6 +455,7 @@ def measure(gw: GpuWorkload, args, dev, ws: int, full: bool, sampler=None) -> di
                      "timed": dec_kernel + (" + its split combine" if gw.plan[0] > 1 else "")},
         "gpu_launches": gw.launches_per_step() * args.steps,
         "clocks": clocks,
+        "diagnostics": diag,
     }
     if not full:
         return res
@@ -492,6 +494,31 @@ def measure(gw: GpuWorkload, args, dev, ws: int, full: bool, sampler=None) -> di
     if flags:
         raise RuntimeError(f"{w.name}: device error word after the timed steps: {flags:#x}")
     return res
+
+
+def tensor_diagnostics(gw: GpuWorkload) -> dict:
+    """Tensor-level error of the filled cache against its inputs (kvq_tensor_error_stats),
+    K and V apart: the ratios the NVFP4 page lists under 张量层, plus the worst head."""
+    import torch
+    K = gw.kvq
+    Hkv = gw.w.num_kv_heads
+    stats = torch.zeros((2, Hkv, K.ERROR_STATS_DOUBLES), dtype=torch.float64, device=gw.dev)
+    K.kvq_tensor_error_stats(gw.cache, gw.K, gw.V, gw.slots, stats)
+    st = stats.cpu().numpy()
+    out = {}
+    for side, name in enumerate(("K", "V")):
+        f = {k: st[side, :, i] for i, k in enumerate(K.ERROR_STATS_FIELDS)}
+        n, se, sr, sd, dot = (float(f[k].sum()) for k in ("count", "sum_sq_err", "sum_sq_ref", "sum_sq_deq", "dot"))
+        head_nmse = f["sum_sq_err"] / np.maximum(f["sum_sq_ref"], 1e-300)
+        hist = st[side, :, len(K.ERROR_STATS_FIELDS):].sum(axis=0)
+        out[name] = {
+            "mse": se / n, "nmse": se / sr, "cosine": dot / math.sqrt(sr * sd),
+            "max_abs_err": float(f["max_abs_err"].max()), "zero_ratio": float(f["zeros"].sum()) / n,
+            "saturation_ratio": float(f["saturated"].sum()) / n, "clipping_ratio": float(f["clipped"].sum()) / n,
+            "worst_head_nmse": float(head_nmse.max()), "worst_head": int(head_nmse.argmax()),
+            "scale_log2_hist": {str(b - 32): int(c) for b, c in enumerate(hist) if c},
+        }
+    return out
 
 
 def suite_names(args) -> list:
@@ -564,7 +591,9 @@ def run_ours(args, w: wl.Workload):
             "gpu_launches": head["gpu_launches"],
             "clocks": head["clocks"],
             "cpu_baseline": cpu,
-            "workloads": {n: ({k: r[k] for k in ("config", "step", "decode", "write", "roofline", "gpu_launches")}
+            "diagnostics": head["diagnostics"],
+            "workloads": {n: ({k: r[k] for k in ("config", "step", "decode", "write", "roofline", "gpu_launches",
+                                                 "diagnostics")}
                               if "error" not in r else r) for n, r in others.items()},
         }
     if ws > 1:

@@ -288,6 +288,36 @@ kvq_status kvq_kvarn_decode_attention(const kvq_cache* cache, const void* q, con
                                       int max_seq_len, float softmax_scale, const void* tail, void* out,
                                       int out_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- Tensor-level quantization error ([P5] "量化误差该怎样测", 张量层: MSE and
+ * normalised MSE, max absolute error, cosine similarity, zero ratio,
+ * clipping/saturation ratio, scale distribution, by head; K and V counted
+ * separately).  For each token i with slot_mapping[i] >= 0 and each kv head,
+ * the row the pool holds at that slot is dequantized and compared with the
+ * row k[i] (v[i]) it was written from (KVarN rows are rotated back to the
+ * input domain first).  dev_stats is a device array [2][num_kv_heads]
+ * (index side * num_kv_heads + head, side 0 = K), zeroed by the call and then
+ * accumulated; derived ratios are the caller's (e.g. NMSE = sum_sq_err /
+ * sum_sq_ref, cosine = dot / sqrt(sum_sq_ref * sum_sq_deq)).  A slot past the
+ * pool is skipped (KVQ_DEVERR_SLOT_RANGE).  Rows must have been written
+ * (KVarN: whole tiles).  Diagnostic, not on the decode path. */
+typedef struct {
+  double count;           /* values compared */
+  double sum_sq_err;      /* sum (x^ - x)^2 */
+  double sum_sq_ref;      /* sum x^2 */
+  double sum_sq_deq;      /* sum x^^2 */
+  double dot;             /* sum x x^ */
+  double max_abs_err;     /* max |x^ - x| */
+  double zeros;           /* x^ == 0 */
+  double saturated;       /* code at the largest magnitude of its grid (KVarN: the largest code) */
+  double clipped;         /* saturated and |x| beyond |x^| by more than half the grid's last step
+                             (INT8, INT4: s/2; E4M3: 16 s; NVFP4: one s_t s_b; KVarN: never) */
+  double scale_hist[64];  /* stored scales by floor(log2 s) + 32, clamped to [0, 63]: per-token-head
+                             and KVarN value scales once per row, NVFP4 block scales, KVarN key
+                             scales once per tile (at its row 0), the per-tensor scale once per row */
+} kvq_error_stats;
+kvq_status kvq_tensor_error_stats(const kvq_cache* cache, const void* k, const void* v, const int32_t* slot_mapping,
+                                  int num_tokens, kvq_error_stats* dev_stats, void* stream);
+
 /* Allocation-free variant of kvq_decode_attention.  (No counterpart on the
  * source pages: this is an interface for callers, not part of the method.)
  * It is for callers that cannot allocate device memory when they decode --

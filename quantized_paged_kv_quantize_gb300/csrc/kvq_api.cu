@@ -309,6 +309,21 @@ kvq_status kvq_quantize_write(kvq_cache* cache, const void* k, const void* v, co
   return KVQ_OK;
 }
 
+kvq_status kvq_tensor_error_stats(const kvq_cache* cache, const void* k, const void* v, const int32_t* slot_mapping,
+                                  int num_tokens, kvq_error_stats* dev_stats, void* stream) {
+  kvq_status s = check_cache(cache);
+  if (s) return s;
+  if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "num_tokens < 0");
+  if (!dev_stats || !aligned(dev_stats, 8)) return fail(KVQ_ERR_INVALID_ARG, "dev_stats must be a non-NULL, 8-byte aligned device array");
+  if (num_tokens > 0 && (!k || !v || !slot_mapping)) return fail(KVQ_ERR_INVALID_ARG, "NULL k, v or slot_mapping");
+  if (num_tokens > 0 && (!aligned(k, 4) || !aligned(v, 4) || !aligned(slot_mapping, 4)))
+    return fail(KVQ_ERR_INVALID_ARG, "k, v and slot_mapping must be 4-byte aligned");
+  cudaError_t e = kvq::launch_error_stats(cache, k, v, slot_mapping, num_tokens, dev_stats,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "error statistics launch");
+  return KVQ_OK;
+}
+
 kvq_status kvq_decode_plan(const kvq_cache* cache, int num_seqs, int num_q_heads, int max_seq_len, int* num_splits,
                            int* tokens_per_split, size_t* workspace_bytes) {
   kvq_status s = check_cache(cache);

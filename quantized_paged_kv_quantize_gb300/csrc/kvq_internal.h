@@ -38,6 +38,8 @@ cudaError_t launch_kvarn_append(const kvq_cache* c, const void* k, const void* v
 // Debug builds: one thread stores a byte just past a one-byte span inside the
 // pool header (byte 40); the check must skip it and set KVQ_DEVERR_BOUNDS.
 cudaError_t launch_bounds_selftest(uint8_t* pool, cudaStream_t stream);
+cudaError_t launch_error_stats(const kvq_cache* c, const void* k, const void* v, const int32_t* slots, int num_tokens,
+                               kvq_error_stats* out, cudaStream_t stream);
 cudaError_t launch_amax(const void* x, int dtype, size_t n, float* out, cudaStream_t stream);
 cudaError_t launch_scales_from_amax(uint8_t* pool, const float* amax_k, const float* amax_v, float div,
                                     cudaStream_t stream);

@@ -40,7 +40,7 @@ EXPORTED = [
     "kvq_decode_plan", "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_decode_attention_noalloc",
     "kvq_kvarn_tail_bytes", "kvq_kvarn_append", "kvq_kvarn_decode_workspace_bytes", "kvq_kvarn_decode_attention",
     "kvq_decode_multi_plan", "kvq_decode_multi_workspace_bytes", "kvq_decode_attention_multi",
-    "kvq_debug_build", "kvq_debug_bounds_selftest",
+    "kvq_debug_build", "kvq_debug_bounds_selftest", "kvq_tensor_error_stats",
 ]
 
 
@@ -67,6 +67,7 @@ def _load():
         "kvq_version": (i32, []),
         "kvq_debug_build": (i32, []),
         "kvq_debug_bounds_selftest": (i32, [vp, vp]),
+        "kvq_tensor_error_stats": (i32, [vp, vp, vp, vp, i32, vp, vp]),
         "kvq_cache_bytes": (i32, [cfgp, ctypes.POINTER(sz)]),
         "kvq_cache_block_bytes": (i32, [cfgp, ctypes.POINTER(sz)]),
         "kvq_cache_alloc": (i32, [cfgp, vp, sz, ctypes.POINTER(vp)]),
@@ -154,6 +155,21 @@ def kvq_debug_build() -> bool:
 
 def kvq_debug_bounds_selftest(cache: "KVCache", stream=None):
     _check(_lib.kvq_debug_bounds_selftest(cache.handle, _stream(stream)))
+
+
+# kvq_error_stats: nine fp64 sums and a 64-bin fp64 histogram per (side, kv head)
+ERROR_STATS_FIELDS = ["count", "sum_sq_err", "sum_sq_ref", "sum_sq_deq", "dot", "max_abs_err", "zeros", "saturated",
+                      "clipped"]
+ERROR_STATS_DOUBLES = len(ERROR_STATS_FIELDS) + 64
+
+
+def kvq_tensor_error_stats(cache: "KVCache", k, v, slot_mapping, stats: torch.Tensor, num_tokens: Optional[int] = None,
+                           stream=None):
+    """stats: float64 CUDA tensor [2, num_kv_heads, ERROR_STATS_DOUBLES], overwritten."""
+    n = k.shape[0] if num_tokens is None else num_tokens
+    assert stats.dtype == torch.float64 and stats.numel() >= 2 * cache.cfg.num_kv_heads * ERROR_STATS_DOUBLES
+    _check(_lib.kvq_tensor_error_stats(cache.handle, _ptr(k), _ptr(v), _ptr(slot_mapping), n, _ptr(stats),
+                                       _stream(stream)))
 
 
 def kvq_cache_bytes(cfg: CacheConfig) -> int:
