@@ -286,35 +286,93 @@ __device__ __forceinline__ void qk_pages(const uint8_t* const* st, int g, int tq
   }
 }
 
-// O^T += V^T P^T for NP staged pages (M-tiles interleaved across pages).  With
-// PARTIAL, rows (tokens) >= nvalid[p] are zeroed before use so that whatever
-// bytes an unwritten slot holds cannot reach the output.
-template <int MODE, int D, int NP, bool PARTIAL>
-__device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq, const int* nvalid,
-                                         const uint32_t (*bh)[2], const uint32_t (*bl)[2], float (*o)[4]) {
+// The V operands of a page pair, moved from the two stages into registers
+// before the stages are refilled.  w[row][p][k]: word k of the thread's row of
+// page p -- 4-bit modes: token-pair rows tq and tq + 4; one-byte modes: token
+// rows 2tq, 2tq + 1, 2tq + 8, 2tq + 9.  NVFP4 adds the block scales of the
+// thread's tokens as f16x2 pairs (tokens 2tq, 2tq + 1 and 2tq + 8, 2tq + 9).
+template <int MODE, int D>
+struct VRegs {
+  static constexpr int VW = D / 32;  // words per thread per row, both layouts
+  uint32_t w[Cfg<MODE, D>::FOUR ? 2 : 4][2][VW];
+  __half2 sc[2][MODE == KVQ_NVFP4 ? 2 : 1];
+};
+
+// Load both pages' V operands.  With PARTIAL, rows (tokens) >= nvalid[p] are
+// neutralised so that whatever bytes an unwritten slot (or a stage that holds
+// no page, nvalid = 0) holds cannot reach the output: one-byte codes are
+// zeroed, NVFP4 gets a zero block scale (E2M1 codes are all finite), and INT4
+// codes are finite anyway, their tokens entering with p = 0.
+template <int MODE, int D, bool PARTIAL>
+__device__ __forceinline__ void pv_load(const uint8_t* const* st, int g, int tq, const int* nvalid,
+                                        VRegs<MODE, D>& v) {
   using C = Cfg<MODE, D>;
-  constexpr int MTILES = C::MTILES;
+  constexpr int VW = VRegs<MODE, D>::VW;
   const int r0 = 2 * tq, r1 = 2 * tq + 1, r2 = 2 * tq + 8, r3 = 2 * tq + 9;  // tokens
-  if constexpr (MODE == KVQ_INT4_PER_TOKEN_HEAD) {
-    // Token-pair rows (each word: 4 channels of the pair's two tokens); the
-    // per-token V scale is folded into P, and a token past seq_len has p = 0
-    // with finite codes, so nothing is masked here.
-    constexpr int CPG = D / 8;
-    constexpr int VW = CPG / 4;
-    uint32_t W0[NP][VW], W2[NP][VW];
-    const int cgb = CPG * C::cgrp(g);
+  if constexpr (C::FOUR) {
+    // Token-pair rows: byte (k, d) holds channel d of tokens 2k (low nibble)
+    // and 2k + 1, so one pair conversion gives the A fragment's (token 2tq,
+    // 2tq + 1) f16x2 directly.  Lanes (g, tq) read pair rows tq and tq + 4,
+    // channels cgb .. cgb + D/8 - 1.
+    const int cgb = (D / 8) * C::cgrp(g);
 #pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + tq * D + cgb), W0[p]);
-      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + (tq + 4) * D + cgb), W2[p]);
+    for (int p = 0; p < 2; ++p) {
+      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + tq * D + cgb), v.w[0][p]);
+      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + (tq + 4) * D + cgb), v.w[1][p]);
     }
+    if constexpr (MODE == KVQ_NVFP4) {
+      const int vblk = cgb / 16;
+      constexpr int VS = C::S_OFF + kPage * (D / 16);  // V block scales [kPage][D/16]
 #pragma unroll
-    for (int p = 0; p < NP; ++p)
+      for (int p = 0; p < 2; ++p) {
+        uint32_t b0 = st[p][swz<C::SWZ_MASK>(VS + r0 * (D / 16) + vblk)];
+        uint32_t b1 = st[p][swz<C::SWZ_MASK>(VS + r1 * (D / 16) + vblk)];
+        uint32_t b2 = st[p][swz<C::SWZ_MASK>(VS + r2 * (D / 16) + vblk)];
+        uint32_t b3 = st[p][swz<C::SWZ_MASK>(VS + r3 * (D / 16) + vblk)];
+        if constexpr (PARTIAL) {
+          const int nv = nvalid[p];
+          if (r0 >= nv) b0 = 0;
+          if (r1 >= nv) b1 = 0;
+          if (r2 >= nv) b2 = 0;
+          if (r3 >= nv) b3 = 0;
+        }
+        v.sc[p][0] = u32_as_h2(e4m3x2_to_f16x2(b0 | (b1 << 8)));
+        v.sc[p][1] = u32_as_h2(e4m3x2_to_f16x2(b2 | (b3 << 8)));
+      }
+    }
+  } else {
+    const int cb = g * (D / 8);
+    const int rows[4] = {r0, r1, r2, r3};
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + rows[r] * C::RW + cb), v.w[r][p]);
+        if constexpr (PARTIAL) {
+#pragma unroll
+          for (int k = 0; k < VW; ++k)
+            if (rows[r] >= nvalid[p]) v.w[r][p][k] = 0;
+        }
+      }
+  }
+}
+
+// O^T += V^T P^T for the page pair in registers (M-tiles interleaved across
+// the two pages).  Tile t of the 4-bit layouts uses channel cgb + 2t in MMA
+// row g and cgb + 2t + 1 in row g + 8; the one-byte layout interleaves the
+// channels of each word with a byte permute.
+template <int MODE, int D>
+__device__ __forceinline__ void pv_mma(const VRegs<MODE, D>& v, const uint32_t (*bh)[2], const uint32_t (*bl)[2],
+                                       float (*o)[4]) {
+  constexpr int VW = VRegs<MODE, D>::VW;
+  if constexpr (MODE == KVQ_INT4_PER_TOKEN_HEAD) {
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
 #pragma unroll
       for (int w = 0; w < VW; ++w) {
         uint32_t f0[4], f2[4];  // byte e of the word: channel cgb + 4w + e
-        s4w_to_f16x2x4(W0[p][w], f0);
-        s4w_to_f16x2x4(W2[p][w], f2);
+        s4w_to_f16x2x4(v.w[0][p][w], f0);
+        s4w_to_f16x2x4(v.w[1][p][w], f2);
         uint32_t av[2][4];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -328,83 +386,33 @@ __device__ __forceinline__ void pv_pages(const uint8_t* const* st, int g, int tq
         for (int u = 0; u < 2; ++u) mma16816(o[2 * w + u], av[u], bl[p][0], bl[p][1]);
       }
   } else if constexpr (MODE == KVQ_NVFP4) {
-    // V payload: token-pair rows [kPage / 2][D] bytes, byte (k, d) holding
-    // channel d of tokens 2k (low nibble) and 2k + 1, so one E2M1 pair
-    // conversion gives the A fragment's (token 2tq, 2tq + 1) f16x2 directly.
-    // Lanes (g, tq) read pair rows tq and tq + 4, channels cgb .. cgb + D/8 - 1;
-    // tile t uses channel cgb + 2t in MMA row g and cgb + 2t + 1 in row g + 8.
-    constexpr int CPG = D / 8;       // channels (bytes) per lane per pair row
-    constexpr int VW = CPG / 4;      // words
-    uint32_t W0[NP][VW], W2[NP][VW];
-    __half2 sc01[NP], sc23[NP];
-    const int cgb = CPG * C::cgrp(g);
-    const int vblk = cgb / 16;
-    constexpr int VS = C::S_OFF + kPage * (D / 16);  // V block scales [kPage][D/16]
 #pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + tq * D + cgb), W0[p]);
-      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + (tq + 4) * D + cgb), W2[p]);
-      uint32_t b0 = st[p][swz<C::SWZ_MASK>(VS + r0 * (D / 16) + vblk)];
-      uint32_t b1 = st[p][swz<C::SWZ_MASK>(VS + r1 * (D / 16) + vblk)];
-      uint32_t b2 = st[p][swz<C::SWZ_MASK>(VS + r2 * (D / 16) + vblk)];
-      uint32_t b3 = st[p][swz<C::SWZ_MASK>(VS + r3 * (D / 16) + vblk)];
-      if constexpr (PARTIAL) {  // a zero scale zeroes the token: E2M1 codes are all finite
-        const int nv = nvalid[p];
-        if (r0 >= nv) b0 = 0;
-        if (r1 >= nv) b1 = 0;
-        if (r2 >= nv) b2 = 0;
-        if (r3 >= nv) b3 = 0;
-      }
-      sc01[p] = u32_as_h2(e4m3x2_to_f16x2(b0 | (b1 << 8)));
-      sc23[p] = u32_as_h2(e4m3x2_to_f16x2(b2 | (b3 << 8)));
-    }
-#pragma unroll
-    for (int p = 0; p < NP; ++p)
+    for (int p = 0; p < 2; ++p)
 #pragma unroll
       for (int w = 0; w < VW; ++w) {
         uint32_t f0[4], f2[4];  // byte e of the word: channel cgb + 4w + e
-        e2m1x8_to_f16x2x4(W0[p][w], f0);
-        e2m1x8_to_f16x2x4(W2[p][w], f2);
+        e2m1x8_to_f16x2x4(v.w[0][p][w], f0);
+        e2m1x8_to_f16x2x4(v.w[1][p][w], f2);
         // hi products of the word's two tiles first, then lo, so that a tile's
         // two MMAs are not issued back to back into the same accumulator
         uint32_t av[2][4];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          av[u][0] = h2_as_u32(__hmul2(u32_as_h2(f0[2 * u]), sc01[p]));
-          av[u][1] = h2_as_u32(__hmul2(u32_as_h2(f0[2 * u + 1]), sc01[p]));
-          av[u][2] = h2_as_u32(__hmul2(u32_as_h2(f2[2 * u]), sc23[p]));
-          av[u][3] = h2_as_u32(__hmul2(u32_as_h2(f2[2 * u + 1]), sc23[p]));
+          av[u][0] = h2_as_u32(__hmul2(u32_as_h2(f0[2 * u]), v.sc[p][0]));
+          av[u][1] = h2_as_u32(__hmul2(u32_as_h2(f0[2 * u + 1]), v.sc[p][0]));
+          av[u][2] = h2_as_u32(__hmul2(u32_as_h2(f2[2 * u]), v.sc[p][1]));
+          av[u][3] = h2_as_u32(__hmul2(u32_as_h2(f2[2 * u + 1]), v.sc[p][1]));
           mma16816(o[2 * w + u], av[u], bh[p][0], bh[p][1]);
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) mma16816(o[2 * w + u], av[u], bl[p][0], bl[p][1]);
       }
   } else {
-    constexpr int VW = D / 32;  // words per thread per row (D/8 one-byte channels)
-    uint32_t A0[NP][VW], A1[NP][VW], A2[NP][VW], A3[NP][VW];
-    const int cb = g * (D / 8);
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r0 * C::RW + cb), A0[p]);
-      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r1 * C::RW + cb), A1[p]);
-      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r2 * C::RW + cb), A2[p]);
-      lds<VW>(st[p] + swz<C::SWZ_MASK>(C::V_OFF + r3 * C::RW + cb), A3[p]);
-      if constexpr (PARTIAL) {
-        const int nv = nvalid[p];
-#pragma unroll
-        for (int w = 0; w < VW; ++w) {
-          if (r0 >= nv) A0[p][w] = 0;
-          if (r1 >= nv) A1[p][w] = 0;
-          if (r2 >= nv) A2[p][w] = 0;
-          if (r3 >= nv) A3[p][w] = 0;
-        }
-      }
-    }
 #pragma unroll
     for (int w = 0; w < VW; ++w)
 #pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        uint32_t a0 = A0[p][w], a1 = A1[p][w], a2 = A2[p][w], a3 = A3[p][w];
+      for (int p = 0; p < 2; ++p) {
+        uint32_t a0 = v.w[0][p][w], a1 = v.w[1][p][w], a2 = v.w[2][p][w], a3 = v.w[3][p][w];
         if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD) {  // bias once per word: x + 128
           a0 ^= 0x80808080u; a1 ^= 0x80808080u; a2 ^= 0x80808080u; a3 ^= 0x80808080u;
         }
@@ -578,6 +586,27 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
       fA0 *= sa[g]; fA8 *= sa[g + 8]; vA0 = sa[kPage + g]; vA8 = sa[kPage + g + 8];
       fB0 *= sb[g]; fB8 *= sb[g + 8]; vB0 = sb[kPage + g]; vB8 = sb[kPage + g + 8];
     }
+    // The V operands go to registers and both stages are refilled now, so the
+    // next pages are in flight during the softmax and the P V products (INT4:
+    // after them, measured faster there).
+    VRegs<MODE, D> vr;
+    if (full2) {
+      const int nv2[2] = {kPage, kPage};
+      pv_load<MODE, D, false>(stAB, g, tq, nv2, vr);
+    } else {
+      const int nvAB[2] = {nvA, nvB};
+      pv_load<MODE, D, true>(stAB, g, tq, nvAB, vr);
+    }
+    constexpr bool kEarlyRefill = MODE != KVQ_INT4_PER_TOKEN_HEAD;
+    auto refill = [&]() {
+      __syncwarp();
+      if (i + C::STAGES < my_count) {
+        if (lane == 0) fence_proxy_async_smem();
+        issue(i + C::STAGES);
+        if (i + 1 + C::STAGES < my_count) issue(i + 1 + C::STAGES);
+      }
+    };
+    if constexpr (kEarlyRefill) refill();
     float sA[4] = {cA[0] * fA0, cA[1] * fA0, cA[2] * fA8, cA[3] * fA8};
     float sB[4] = {cB[0] * fB0, cB[1] * fB0, cB[2] * fB8, cB[3] * fB8};
     if (nvA < kPage || nvB < kPage) {  // rare: a partial or missing page
@@ -634,20 +663,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
         bl[k >> 1][k & 1] = movmatrix_t(h2_as_u32(lo));
       }
     }
-    if (full2) {
-      const int nv2[2] = {kPage, kPage};
-      pv_pages<MODE, D, 2, false>(stAB, g, tq, nv2, bh, bl, o);
-    } else {
-      if (nvA > 0) pv_pages<MODE, D, 1, true>(stAB, g, tq, &nvA, bh, bl, o);
-      if (nvB > 0) pv_pages<MODE, D, 1, true>(stAB + 1, g, tq, &nvB, bh + 1, bl + 1, o);
-    }
-
-    __syncwarp();
-    if (i + C::STAGES < my_count) {
-      if (lane == 0) fence_proxy_async_smem();
-      issue(i + C::STAGES);
-      if (i + 1 + C::STAGES < my_count) issue(i + 1 + C::STAGES);
-    }
+    pv_mma<MODE, D>(vr, bh, bl, o);
+    if constexpr (!kEarlyRefill) refill();
   }
   if (timed_out && lane == 0) set_error(const_cast<uint8_t*>(a.pool), KVQ_DEVERR_TIMEOUT);
 
