@@ -75,11 +75,12 @@ struct Mode {
 template <int NT, bool QF32, bool FP4>
 struct Smem {
   static constexpr int N = 16 * NT;
-  static constexpr int BOP = (N / 8) * kGroup8;  // bytes of one B operand (N rows x 128, f16)
+  static constexpr int BOP = (N / 8) * kGroup8;  // bytes of one K-major B operand (N rows x 128, f16)
+  static constexpr int POP = N * kTileTok * 2;    // bytes of one MN-major P operand (128 token rows x N, f16)
   static constexpr int STAGE = 0;
   static constexpr int QT = STAGE + kStages * kStageBytes;
-  static constexpr int PT = QT + (QF32 ? 2 : 1) * BOP;  // P^T hi, then lo
-  static constexpr int VTAB = PT + 2 * BOP;             // NVFP4 V block-scale pairs [8 blocks][64 pairs]
+  static constexpr int PT = QT + (QF32 ? 2 : 1) * BOP;  // P hi, then lo
+  static constexpr int VTAB = PT + 2 * POP;             // NVFP4 V block-scale pairs [8 blocks][64 pairs]
   static constexpr int WRED = VTAB + (FP4 ? 8 * 64 * 4 : 0);
   static constexpr int PAGES = WRED + 4 * N * 4;
   static constexpr int BYTES = PAGES + kMaxPages * 4;
@@ -108,6 +109,8 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
   constexpr int PSHIFT = Md::pshift(QF32);
   constexpr float SLACK = (float)Md::slack(QF32);
   constexpr uint32_t IDESC = umma_idesc_f16(128, N);
+  constexpr uint32_t IDESC_PV = umma_idesc_f16_bmn(128, N);
+  constexpr int P_LBO = (N / 8) * 128;  // P: 8-token groups (K) after the N / 8 column groups (MN, 128 B apart)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage = sm + L::STAGE;
@@ -225,9 +228,13 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
   // start-address field holds bytes / 16 and never carries: shared addresses < 2^18)
   const uint64_t dQ = umma_sdesc(smem_u32(qt), kCoreK, kGroup8);
   const uint64_t dQlo = umma_sdesc(smem_u32(qt + (QF32 ? L::BOP : 0)), kCoreK, kGroup8);
-  const uint64_t dP = umma_sdesc(smem_u32(pt), kCoreK, kGroup8);
-  const uint64_t dPlo = umma_sdesc(smem_u32(pt + L::BOP), kCoreK, kGroup8);
+  // P (B operand of O^T = V^T P^T) is MN-major: element (token k, column c) at
+  // (c % 8) 2 + (k % 8) 16 + (c / 8) 128 + (k / 8) P_LBO, so each thread stores
+  // its token's columns as whole 16-byte rows; k-step j starts 2 j P_LBO further
+  const uint64_t dP = umma_sdesc(smem_u32(pt), P_LBO, 128);
+  const uint64_t dPlo = umma_sdesc(smem_u32(pt + L::POP), P_LBO, 128);
   constexpr uint64_t kStep = (2 * kCoreK) >> 4;
+  constexpr uint64_t kStepP = (2 * P_LBO) >> 4;
 
   float kfac = a.sm_log2, vfac = 1.0f;
   if constexpr (Md::FP4) {
@@ -246,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
   int climit[CPT];
 #pragma unroll
   for (int k = 0; k < CPT; ++k) climit[k] = k < nreal ? n - (nq - 1 - (2 * k + half) / G) : 0;
+  const int cmin = n - (nq - 1);  // the earliest query's end: tiles below it need no causal mask
   uint32_t qk_phase = 0, pv_phase = 0;
   bool qk_pending = false, pv_pending = false, o_valid = false, timed_out = false;
 
@@ -382,8 +390,13 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       const int pos = tok0 + row;
       float f = kfac;
       if constexpr (!Md::FP4) f *= *reinterpret_cast<const float*>(st + p * kPageSlot + kSOff + 4 * (row & 15));
+      if (tok0 + kTileTok <= cmin) {  // CTA-uniform: the whole tile precedes every query
 #pragma unroll
-      for (int k = 0; k < CPT; ++k) sc[k] = (tok_ok && pos < climit[k]) ? __uint_as_float(sv[k]) * f : -INFINITY;
+        for (int k = 0; k < CPT; ++k) sc[k] = (tok_ok && k < nreal) ? __uint_as_float(sv[k]) * f : -INFINITY;
+      } else {
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) sc[k] = (tok_ok && pos < climit[k]) ? __uint_as_float(sv[k]) * f : -INFINITY;
+      }
     }
     bool exceed = false;
 #pragma unroll
@@ -423,19 +436,29 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       float vs = 1.0f;
       if constexpr (!Md::FP4)
         vs = tok_ok ? *reinterpret_cast<const float*>(st + (row >> 4) * kPageSlot + kSOff + 64 + 4 * (row & 15)) : 0.0f;
-      const int kb = (row & 7) * 2 + (row >> 3) * kCoreK;
+      uint32_t ph[CPT / 2], pl[CPT / 2];  // f16 pairs of columns (2e, 2e + 1): hi, lo
 #pragma unroll
-      for (int k = 0; k < CPT; ++k) {
-        if (k >= nreal) break;
-        const float p = ex2(sc[k] + ((float)PSHIFT - m[k]));  // ex2(-inf) = 0
-        l[k] += p;
-        float x = p;
-        if constexpr (!Md::FP4) x *= vs;
-        const float h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-        const int c = CPT * half + k;
-        const int off = kb + (c & 7) * 16 + (c >> 3) * kGroup8;
-        *reinterpret_cast<__half*>(pt + off) = __float2half_rn(h);
-        *reinterpret_cast<__half*>(pt + L::BOP + off) = __float2half_rn(x - h);
+      for (int e = 0; e < CPT / 2; ++e) {
+        float x[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int k = 2 * e + u;
+          const float p = ex2(sc[k] + ((float)PSHIFT - m[k]));  // ex2(-inf) = 0: masked and padding columns
+          l[k] += p;
+          x[u] = p;
+          if constexpr (!Md::FP4) x[u] *= vs;
+        }
+        const float h0 = __uint_as_float(__float_as_uint(x[0]) & 0xFFFFE000u);
+        const float h1 = __uint_as_float(__float_as_uint(x[1]) & 0xFFFFE000u);
+        ph[e] = h2_as_u32(__floats2half2_rn(h0, h1));
+        pl[e] = h2_as_u32(__floats2half2_rn(x[0] - h0, x[1] - h1));
+      }
+      const int kb = (row & 7) * 16 + (row >> 3) * P_LBO + (CPT * half / 8) * 128;
+#pragma unroll
+      for (int q = 0; q < CPT / 8; ++q) {
+        *reinterpret_cast<uint4*>(pt + kb + 128 * q) = make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+        *reinterpret_cast<uint4*>(pt + L::POP + kb + 128 * q) =
+            make_uint4(pl[4 * q], pl[4 * q + 1], pl[4 * q + 2], pl[4 * q + 3]);
       }
     }
     tmem_wait_st();            // A_V (and a rescaled O) are in tensor memory
@@ -446,9 +469,10 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       tc_fence_after();
       if (elect_one()) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) umma_f16_ts(tO, tAV + 8 * j, dP + j * kStep, IDESC, (o_valid || j > 0) ? 1u : 0u);
+        for (int j = 0; j < 8; ++j)
+          umma_f16_ts(tO, tAV + 8 * j, dP + j * kStepP, IDESC_PV, (o_valid || j > 0) ? 1u : 0u);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) umma_f16_ts(tO, tAV + 8 * j, dPlo + j * kStep, IDESC, 1u);
+        for (int j = 0; j < 8; ++j) umma_f16_ts(tO, tAV + 8 * j, dPlo + j * kStepP, IDESC_PV, 1u);
         tc_commit(&pv_bar);
       }
       __syncwarp();
