@@ -79,8 +79,12 @@ struct Smem {
   static constexpr int POP = N * kTileTok * 2;    // bytes of one MN-major P operand (128 token rows x N, f16)
   static constexpr int STAGE = 0;
   static constexpr int QT = STAGE + kStages * kStageBytes;
-  static constexpr int PT = QT + (QF32 ? 2 : 1) * BOP;  // P hi, then lo
-  static constexpr int VTAB = PT + 2 * POP;             // NVFP4 V block-scale pairs [8 blocks][64 pairs]
+  static constexpr int PT = QT + (QF32 ? 2 : 1) * BOP;  // P hi, then lo (then the second buffer's)
+  // A V and P are double-buffered (tile i in buffer i % 2) where the second A V
+  // fits in the tensor-memory columns above O and two CTAs still fit an SM
+  static constexpr int SINGLE = PT + 2 * POP + (FP4 ? 8 * 64 * 4 : 0) + 4 * N * 4 + kMaxPages * 4 + 1024;
+  static constexpr bool DB = 128 + 2 * N + 64 <= kTmemCols && 2 * (SINGLE + 2 * POP + 1024) <= 228 * 1024;
+  static constexpr int VTAB = PT + (DB ? 4 : 2) * POP;  // NVFP4 V block-scale pairs [8 blocks][64 pairs]
   static constexpr int WRED = VTAB + (FP4 ? 8 * 64 * 4 : 0);
   static constexpr int PAGES = WRED + 4 * N * 4;
   static constexpr int BYTES = PAGES + kMaxPages * 4;
@@ -120,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
   float* wred = reinterpret_cast<float*>(sm + L::WRED);
   int* pages = reinterpret_cast<int*>(sm + L::PAGES);
   __shared__ uint64_t full_bar[kStages];
-  __shared__ uint64_t qk_bar, pv_bar;
+  __shared__ uint64_t qk_bar, pv_bar[2];  // A V of tile i commits on pv_bar[i % 2]
   __shared__ uint32_t tmem_base_s;
 
   const int split = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
@@ -164,7 +168,8 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&full_bar[s], kTilePages);  // one arrival per page
     mbar_init(&qk_bar, 1);
-    mbar_init(&pv_bar, 1);
+    mbar_init(&pv_bar[0], 1);
+    mbar_init(&pv_bar[1], 1);
     mbar_fence_init();
     prefetch_tmap(&tmap);
   }
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = tmem_base_s;
-  const uint32_t tAK = tb + kColAK, tAV = tb + kColAV, tS = tb + kColS, tO = tb + kColS + N;
+  const uint32_t tAK = tb + kColAK, tAV0 = tb + kColAV, tS = tb + kColS, tO = tb + kColS + N;
 
   // page p of tile i into stage i % kStages, by one lane of warp p: one arrival
   // with the page's bytes (none for a missing page) on the stage's barrier
@@ -231,8 +236,9 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
   // P (B operand of O^T = V^T P^T) is MN-major: element (token k, column c) at
   // (c % 8) 2 + (k % 8) 16 + (c / 8) 128 + (k / 8) P_LBO, so each thread stores
   // its token's columns as whole 16-byte rows; k-step j starts 2 j P_LBO further
+  // (the lo operand and the second buffer as start-address offsets in 16 B units)
   const uint64_t dP = umma_sdesc(smem_u32(pt), P_LBO, 128);
-  const uint64_t dPlo = umma_sdesc(smem_u32(pt + L::POP), P_LBO, 128);
+  constexpr uint64_t dPlo = L::POP >> 4;
   constexpr uint64_t kStep = (2 * kCoreK) >> 4;
   constexpr uint64_t kStepP = (2 * P_LBO) >> 4;
 
@@ -254,8 +260,11 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
 #pragma unroll
   for (int k = 0; k < CPT; ++k) climit[k] = k < nreal ? n - (nq - 1 - (2 * k + half) / G) : 0;
   const int cmin = n - (nq - 1);  // the earliest query's end: tiles below it need no causal mask
-  uint32_t qk_phase = 0, pv_phase = 0;
-  bool qk_pending = false, pv_pending = false, o_valid = false, timed_out = false;
+  uint32_t qk_phase = 0;
+  bool qk_pending = false, o_valid = false, timed_out = false;
+  int last_pv = -1;  // the last tile whose A V was issued
+  // A V of tile j has completed (and with it every earlier product)
+  auto wait_pv = [&](int j) -> bool { return mbar_wait_bounded(&pv_bar[j & 1], (j >> 1) & 1); };
 
   for (int i = 0; i < ntiles; ++i) {
     const int s = i % kStages;
@@ -339,11 +348,9 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
 
     // ---- V: channel `row`, tokens 64 half .. + 63, into lane `row` of A_V
     //      (once the previous tile's A V has released A_V and P^T)
-    if (pv_pending) {
-      ok = mbar_wait_bounded(&pv_bar, pv_phase) && ok;
-      pv_phase ^= 1;
-      pv_pending = false;
-    }
+    const int buf = L::DB ? (i & 1) : 0;
+    const uint32_t tAV = buf ? tb + kColS + 2 * N : tAV0;  // the second A V: columns above O
+    if (i - (L::DB ? 2 : 1) >= 0 && i - (L::DB ? 2 : 1) <= last_pv) ok = wait_pv(i - (L::DB ? 2 : 1)) && ok;
     {
       const int d = row;
       uint32_t f[32];
@@ -422,7 +429,11 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
         m[k] = mn;
         l[k] *= alpha[k];
       }
-      if (o_valid) {  // O^T columns of this half, channel `row` (the previous A V is complete)
+      if (o_valid) {  // O^T columns of this half, channel `row`, once every A V issued is complete
+        if (__syncthreads_or(!wait_pv(last_pv))) {
+          timed_out = true;
+          break;
+        }
         uint32_t ov[CPT];
         tmem_ld<CPT>(tO + lane_base + CPT * half, ov);
         tmem_wait_ld();
@@ -456,8 +467,9 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       const int kb = (row & 7) * 16 + (row >> 3) * P_LBO + (CPT * half / 8) * 128;
 #pragma unroll
       for (int q = 0; q < CPT / 8; ++q) {
-        *reinterpret_cast<uint4*>(pt + kb + 128 * q) = make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
-        *reinterpret_cast<uint4*>(pt + L::POP + kb + 128 * q) =
+        *reinterpret_cast<uint4*>(pt + buf * 2 * L::POP + kb + 128 * q) =
+            make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+        *reinterpret_cast<uint4*>(pt + (buf * 2 + 1) * L::POP + kb + 128 * q) =
             make_uint4(pl[4 * q], pl[4 * q + 1], pl[4 * q + 2], pl[4 * q + 3]);
       }
     }
@@ -468,12 +480,13 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
     if (warp == 0) {
       tc_fence_after();
       if (elect_one()) {
+        const uint64_t dPb = dP + (uint64_t)((buf * 2 * L::POP) >> 4);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          umma_f16_ts(tO, tAV + 8 * j, dP + j * kStepP, IDESC_PV, (o_valid || j > 0) ? 1u : 0u);
+          umma_f16_ts(tO, tAV + 8 * j, dPb + j * kStepP, IDESC_PV, (o_valid || j > 0) ? 1u : 0u);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) umma_f16_ts(tO, tAV + 8 * j, dPlo + j * kStepP, IDESC_PV, 1u);
-        tc_commit(&pv_bar);
+        for (int j = 0; j < 8; ++j) umma_f16_ts(tO, tAV + 8 * j, dPb + dPlo + j * kStepP, IDESC_PV, 1u);
+        tc_commit(&pv_bar[i & 1]);
       }
       __syncwarp();
     }
@@ -481,14 +494,14 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       if (elect_one()) issue_page(i + kStages, warp);
       __syncwarp();
     }
-    pv_pending = true;
+    last_pv = i;
     o_valid = true;
   }
 
   // outstanding products must complete before tensor memory is read or freed
   bool ok_end = true;
   if (qk_pending) ok_end = mbar_wait_bounded(&qk_bar, qk_phase) && ok_end;
-  if (pv_pending) ok_end = mbar_wait_bounded(&pv_bar, pv_phase) && ok_end;
+  if (last_pv >= 0) ok_end = wait_pv(last_pv) && ok_end;
   tc_fence_after();
   if (__syncthreads_or(!ok_end)) timed_out = true;
   if (timed_out) {
