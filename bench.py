@@ -49,12 +49,12 @@ VARIANTS = {
     "nvfp4_b32_s32768:4over6": ("nvfp4_b32_s32768", "nvfp4_4over6"),
 }
 # speculative-decoding shape: 4 causal queries per sequence over the same pages
-SPEC_VARIANTS = {"nvfp4_b32_s32768:spec4": ("nvfp4_b32_s32768", 4)}
+SPEC_VARIANTS = {"nvfp4_b32_s32768:spec4": ("nvfp4_b32_s32768", 4), "kvarn_b16_s16384:spec4": ("kvarn_b16_s16384", 4)}
 # every configuration the default run measures, grouped so that the variants of
 # one base reuse its K/V inputs on the device
 SUITE = ["nvfp4_b32_s32768", "nvfp4_b32_s32768:4over6", "nvfp4_b32_s32768:spec4",
          "pth_b64_u1k_32k", "pth_b64_u1k_32k:fp8", "pth_b64_u1k_32k:int4",
-         "fp8_pt_b16_s4096", "kvarn_b16_s16384", "int8_pth_tiny"]
+         "fp8_pt_b16_s4096", "kvarn_b16_s16384", "kvarn_b16_s16384:spec4", "int8_pth_tiny"]
 
 
 def workload_by_name(name: str) -> wl.Workload:

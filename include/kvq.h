@@ -231,11 +231,16 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, const int
  * [head_dim]; query i of sequence b stands at position seq_len_b - num_queries
  * + i and attends to tokens 0 .. seq_len_b - num_queries + i (none, output 0,
  * when that is negative).  Other arguments and rules are those of
- * kvq_decode_attention; num_seqs * num_queries <= 65535; not available for
- * KVQ_KVARN_K4V2_G128 (KVQ_ERR_UNSUPPORTED).  Each query is one row of the
- * decode grid over its causal prefix; the rows of a sequence run side by side,
- * so the pages they share are mostly served from L2.  Plan and workspace:
- * kvq_decode_multi_plan / kvq_decode_multi_workspace_bytes. */
+ * kvq_decode_attention; num_seqs * num_queries <= 65535.  KVQ_KVARN_K4V2_G128
+ * reads whole tiles only (every seq_len a multiple of 128, no open tile); a
+ * query's causal prefix may end inside the last tile, whose later tokens it
+ * does not see.  NVFP4 (and 4over6) and INT4 at head_dim 128 with
+ * group * num_queries <= 64 read each page once for all the sequence's
+ * queries (tensor-core columns = queries x heads); the other modes run each
+ * query as one row of the decode grid over its causal prefix, the rows of a
+ * sequence side by side so that the pages they share are mostly served from
+ * L2.  Plan and workspace: kvq_decode_multi_plan /
+ * kvq_decode_multi_workspace_bytes. */
 kvq_status kvq_decode_multi_plan(const kvq_cache* cache, int num_seqs, int num_queries, int num_q_heads,
                                  int max_seq_len, int* num_splits, int* tokens_per_split, size_t* workspace_bytes);
 kvq_status kvq_decode_multi_workspace_bytes(const kvq_cache* cache, int num_seqs, int num_queries,

@@ -398,8 +398,6 @@ kvq_status kvq_decode_attention_multi(const kvq_cache* cache, const void* q, con
                                       int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
   if (cache && mode != cache->cfg.mode)
     return fail(KVQ_ERR_MODE_MISMATCH, "decode mode %d but the cache holds mode %d", mode, cache->cfg.mode);
-  if (cache && cache->cfg.mode == KVQ_KVARN_K4V2_G128)
-    return fail(KVQ_ERR_UNSUPPORTED, "multi-query decode is not available for kvarn_k4v2_g128");
   if (num_queries < 1) return fail(KVQ_ERR_INVALID_ARG, "num_queries < 1");
   if ((long long)num_seqs * num_queries > 65535)
     return fail(KVQ_ERR_UNSUPPORTED, "num_seqs * num_queries = %lld > 65535", (long long)num_seqs * num_queries);

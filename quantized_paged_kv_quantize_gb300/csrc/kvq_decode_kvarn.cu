@@ -117,13 +117,15 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
   uint8_t* ring = smem_raw;
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw + (size_t)kS * kBlk);
 
+  // b: the query row -- query b % nq of sequence b / nq (nq = 1: the sequence)
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
+  const int seq = b / a.nq;
   uint8_t* pool = const_cast<uint8_t*>(a.pool);
   pdl_launch_dependents();
 
-  int n = a.seq_lens[b];
+  int n = a.seq_lens[seq];
   const int lim = min(a.max_seq_len, a.max_pages * kT);
   const bool first = tid == 0 && split == 0 && kvh == 0;
   if (n > lim || n < 0) {
@@ -134,6 +136,9 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
     if (first && a.tail == nullptr) set_error(pool, KVQ_DEVERR_PARTIAL_TILE);
     n -= n % kT;
   }
+  // causal: the tokens up to the query's own position (several queries per
+  // sequence come without a tail, so the last tile a query sees may end early)
+  n = max(n - (a.nq - 1 - b % a.nq), 0);
   // with a tail, every CTA leaves a partial result for the merge kernel
   const bool direct = a.num_splits == 1 && a.tail == nullptr;
   const int t_begin = split * a.tokens_per_split;
@@ -147,10 +152,10 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
     }
     return;
   }
-  const int tile0 = t_begin / kT, ntiles = (t_end - t_begin) / kT;
+  const int tile0 = t_begin / kT, ntiles = (t_end - t_begin + kT - 1) / kT;
 
   if (tid < ntiles) {
-    int pid = __ldg(a.block_table + (long long)b * a.max_pages + tile0 + tid);
+    int pid = __ldg(a.block_table + (long long)seq * a.max_pages + tile0 + tid);
     if (pid < 0 || pid >= a.num_pages) {
       set_error(pool, KVQ_DEVERR_PAGE_RANGE);
       pid = -1;
@@ -304,10 +309,17 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
       }
       const int ta = 16 * sa + g, tb = 16 * sb + g;
       const float kA0 = sh.kf[ta], kA8 = sh.kf[ta + 8], kB0 = sh.kf[tb], kB8 = sh.kf[tb + 8];
-      const float sA[4] = {fmaf(cA[0], 16.0f, be0) * kA0, fmaf(cA[1], 16.0f, be1) * kA0,
-                           fmaf(cA[2], 16.0f, be0) * kA8, fmaf(cA[3], 16.0f, be1) * kA8};
-      const float sB[4] = {fmaf(cB[0], 16.0f, be0) * kB0, fmaf(cB[1], 16.0f, be1) * kB0,
-                           fmaf(cB[2], 16.0f, be0) * kB8, fmaf(cB[3], 16.0f, be1) * kB8};
+      float sA[4] = {fmaf(cA[0], 16.0f, be0) * kA0, fmaf(cA[1], 16.0f, be1) * kA0,
+                     fmaf(cA[2], 16.0f, be0) * kA8, fmaf(cA[3], 16.0f, be1) * kA8};
+      float sB[4] = {fmaf(cB[0], 16.0f, be0) * kB0, fmaf(cB[1], 16.0f, be1) * kB0,
+                     fmaf(cB[2], 16.0f, be0) * kB8, fmaf(cB[3], 16.0f, be1) * kB8};
+      const int nv = t_end - (t_begin + i * kT);  // tokens of this tile the query sees
+      if (nv < kT) {
+        if (ta >= nv) sA[0] = sA[1] = -INFINITY;
+        if (ta + 8 >= nv) sA[2] = sA[3] = -INFINITY;
+        if (tb >= nv) sB[0] = sB[1] = -INFINITY;
+        if (tb + 8 >= nv) sB[2] = sB[3] = -INFINITY;
+      }
       float bm0 = fmaxf(fmaxf(sA[0], sA[2]), fmaxf(sB[0], sB[2]));
       float bm1 = fmaxf(fmaxf(sA[1], sA[3]), fmaxf(sB[1], sB[3]));
 #pragma unroll
@@ -495,11 +507,12 @@ __global__ void __launch_bounds__(kD) kvarn_combine_kernel(const __grid_constant
   const int b = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, d = threadIdx.x;
   const int lane = d & 31, warp = d >> 5;
   pdl_wait_primary();  // the decode grid's partials are complete and visible
-  int n = a.seq_lens[b];
+  int n = a.seq_lens[b / a.nq];  // b: the query row
   const int lim = min(a.max_seq_len, a.max_pages * kT);
   n = n < 0 ? 0 : (n > lim ? lim : n);
-  const int nt = a.tail ? n % kT : 0;  // tail rows
+  const int nt = a.tail ? n % kT : 0;  // tail rows (one query per sequence)
   n -= n % kT;
+  n = max(n - (a.nq - 1 - b % a.nq), 0);  // causal: as the decode kernel
   const int ns = (n + a.tokens_per_split - 1) / a.tokens_per_split;
   float M = -INFINITY, L = 0.0f;
   const float r0 = merge_split_row<kD>(a, ((long long)b * a.Hq + hq) * a.num_splits, ns, wts, red,

@@ -387,16 +387,40 @@ def test_decode_multi_query_parity(mode, nq, out_dtype):
     assert K.kvq_cache_read_errors(cache) == 0
 
 
-def test_decode_multi_query_rejects_kvarn():
+@pytest.mark.parametrize("nq,Hq,io,out_dtype", [(2, 16, "f16", torch.float32), (5, 16, "f16", torch.float16),
+                                                (3, 8, "f32", torch.float32)])
+def test_decode_multi_query_kvarn_parity(nq, Hq, io, out_dtype):
+    """KVarN, nq causal queries per sequence over whole tiles: the earlier
+    queries' prefixes end inside the last tile (tokens 124..127 of a 128-token
+    sequence with nq = 5), across split boundaries (2048 tokens), and the last
+    query row equals the plain decode of that query."""
     K = kvq()
-    c = make_case(small_workload("kvarn_k4v2_g128"), [128])
+    c = make_case(small_workload("kvarn_k4v2_g128", Hq=Hq, io=io), [128, 256, 0, 2048, 640], slack_pages=1)
+    pool = oracle_pool(c)
     cache = gpu_cache(c)
-    q = torch.zeros((1, 2, 16, 128), dtype=torch.float16, device="cuda")
-    out = torch.empty_like(q)
-    with pytest.raises(K.KVQError) as e:
-        K.kvq_decode_attention_multi(cache, q, _dev(c.lay.block_table), _dev(c.lay.seq_lens), out,
-                                     max_seq_len=128)
-    assert e.value.status == 2
+    _upload_oracle_pool(cache, pool, c)
+    B, D = len(c.lay.seq_lens), c.w.head_dim
+    q = np.random.default_rng(nq).standard_normal((B, nq, Hq, D)).astype(c.w.np_dtype)
+    msl = int(c.lay.seq_lens.max())
+    ns, _, wsb = K.kvq_decode_multi_plan(cache, B, nq, Hq, msl)
+    assert ns > 1
+    ws = guarded(max(wsb // 4, 1), torch.float32, name="workspace")
+    out = guarded((B, nq, Hq, D), out_dtype, fill=float("nan"), name="out")
+    K.kvq_decode_attention_multi(cache, _dev(q), _dev(c.lay.block_table), _dev(c.lay.seq_lens), out,
+                                 max_seq_len=msl, workspace=ws)
+    torch.cuda.synchronize()
+    ref = oracle.decode_multi(c.w.mode, pool, c.lay.num_pages, c.w.page_size, c.w.num_kv_heads, D,
+                              q.astype(np.float32), c.lay.block_table, c.lay.seq_lens, 1.0 / math.sqrt(D))
+    check_attention(out.reshape(B * nq, Hq, D), ref.reshape(B * nq, Hq, D))
+    assert (out[2] == 0).all()                            # the empty sequence
+    assert K.kvq_cache_read_errors(cache) == 0
+    one = torch.empty((B, Hq, D), dtype=out_dtype, device="cuda")
+    ws1 = torch.empty(max(K.kvq_decode_workspace_bytes(cache, B, Hq, msl) // 4, 1), dtype=torch.float32,
+                      device="cuda")
+    K.kvq_decode_attention(cache, _dev(np.ascontiguousarray(q[:, -1])), _dev(c.lay.block_table),
+                           _dev(c.lay.seq_lens), one, max_seq_len=msl, workspace=ws1)
+    torch.cuda.synchronize()
+    check_attention(one, ref[:, -1])
 
 
 @pytest.mark.parametrize("mode,nq,Hkv", [("nvfp4", 4, 2), ("nvfp4_4over6", 3, 2), ("int8_per_token_head", 4, 2),
