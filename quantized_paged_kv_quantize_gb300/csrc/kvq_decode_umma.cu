@@ -54,7 +54,7 @@ constexpr int kStageBytes = kTilePages * kPageSlot;  // 20 KB
 constexpr int kMaxPages = 1024;                      // pages per split (ids kept in shared memory)
 constexpr int kCoreK = 144;                          // bytes between core matrices along K in a B operand
 constexpr int kGroup8 = 16 * kCoreK;                 // bytes of one 8-row group of a B operand (K = 128)
-constexpr int kTmemCols = 256;                       // A_K 64 | A_V 64 | S N | O N  (N <= 64)
+constexpr int kTmemCols = 256;                       // A_K 64 | A_V 64 | S N | O N or 2N (| A_V)
 constexpr int kColAK = 0, kColAV = 64, kColS = 128;
 // Block layout inside a page block (bytes; 4-bit modes, D = 128, P = 16)
 constexpr int kVOff = kPage * kD / 2;  // V payload (token-pair rows of 128 bytes)
@@ -76,14 +76,19 @@ template <int NT, bool QF32, bool FP4>
 struct Smem {
   static constexpr int N = 16 * NT;
   static constexpr int BOP = (N / 8) * kGroup8;  // bytes of one K-major B operand (N rows x 128, f16)
-  static constexpr int POP = N * kTileTok * 2;    // bytes of one MN-major P operand (128 token rows x N, f16)
+  static constexpr int POP = N * kTileTok * 2;    // bytes of P hi (128 token rows x N, f16); P lo the same
+  // P hi and lo as one B operand of 2N columns (one MMA per k-step of A V, hi
+  // products in O's first N columns, lo in the next N) where tensor memory allows
+  static constexpr bool FUSE = 128 + 3 * N <= kTmemCols;
+  static constexpr int PC = FUSE ? 2 * N : N;  // columns of a P operand
+  static constexpr int OC = FUSE ? 2 * N : N;  // columns of O
   static constexpr int STAGE = 0;
   static constexpr int QT = STAGE + kStages * kStageBytes;
   static constexpr int PT = QT + (QF32 ? 2 : 1) * BOP;  // P hi, then lo (then the second buffer's)
   // A V and P are double-buffered (tile i in buffer i % 2) where the second A V
   // fits in the tensor-memory columns above O and two CTAs still fit an SM
   static constexpr int SINGLE = PT + 2 * POP + (FP4 ? 8 * 64 * 4 : 0) + 4 * N * 4 + kMaxPages * 4 + 1024;
-  static constexpr bool DB = 128 + 2 * N + 64 <= kTmemCols && 2 * (SINGLE + 2 * POP + 1024) <= 228 * 1024;
+  static constexpr bool DB = 128 + N + OC + 64 <= kTmemCols && 2 * (SINGLE + 2 * POP + 1024) <= 228 * 1024;
   static constexpr int VTAB = PT + (DB ? 4 : 2) * POP;  // NVFP4 V block-scale pairs [8 blocks][64 pairs]
   static constexpr int WRED = VTAB + (FP4 ? 8 * 64 * 4 : 0);
   static constexpr int PAGES = WRED + 4 * N * 4;
@@ -113,8 +118,9 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
   constexpr int PSHIFT = Md::pshift(QF32);
   constexpr float SLACK = (float)Md::slack(QF32);
   constexpr uint32_t IDESC = umma_idesc_f16(128, N);
-  constexpr uint32_t IDESC_PV = umma_idesc_f16_bmn(128, N);
-  constexpr int P_LBO = (N / 8) * 128;  // P: 8-token groups (K) after the N / 8 column groups (MN, 128 B apart)
+  constexpr uint32_t IDESC_PV = umma_idesc_f16_bmn(128, L::PC);
+  constexpr int P_LBO = (L::PC / 8) * 128;  // P: 8-token groups (K) after the column groups (MN, 128 B apart)
+  constexpr int P_LO = L::FUSE ? (N / 8) * 128 : L::POP;  // P lo: columns N.. of the operand, or its own
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage = sm + L::STAGE;
@@ -349,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
     // ---- V: channel `row`, tokens 64 half .. + 63, into lane `row` of A_V
     //      (once the previous tile's A V has released A_V and P^T)
     const int buf = L::DB ? (i & 1) : 0;
-    const uint32_t tAV = buf ? tb + kColS + 2 * N : tAV0;  // the second A V: columns above O
+    const uint32_t tAV = buf ? tb + kColS + N + L::OC : tAV0;  // the second A V: columns above O
     if (i - (L::DB ? 2 : 1) >= 0 && i - (L::DB ? 2 : 1) <= last_pv) ok = wait_pv(i - (L::DB ? 2 : 1)) && ok;
     {
       const int d = row;
@@ -434,12 +440,15 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
           timed_out = true;
           break;
         }
-        uint32_t ov[CPT];
-        tmem_ld<CPT>(tO + lane_base + CPT * half, ov);
-        tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha[k]);
-        tmem_st<CPT>(tO + lane_base + CPT * half, ov);
+        for (int part = 0; part < (L::FUSE ? 2 : 1); ++part) {  // hi products, then lo
+          uint32_t ov[CPT];
+          tmem_ld<CPT>(tO + part * N + lane_base + CPT * half, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < CPT; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha[k]);
+          tmem_st<CPT>(tO + part * N + lane_base + CPT * half, ov);
+        }
       }
     }
     // ---- P = 2^(s - m + PSHIFT) into P^T (hi, lo), token `row` = K index
@@ -469,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       for (int q = 0; q < CPT / 8; ++q) {
         *reinterpret_cast<uint4*>(pt + buf * 2 * L::POP + kb + 128 * q) =
             make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
-        *reinterpret_cast<uint4*>(pt + (buf * 2 + 1) * L::POP + kb + 128 * q) =
+        *reinterpret_cast<uint4*>(pt + buf * 2 * L::POP + P_LO + kb + 128 * q) =
             make_uint4(pl[4 * q], pl[4 * q + 1], pl[4 * q + 2], pl[4 * q + 3]);
       }
     }
@@ -484,8 +493,10 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           umma_f16_ts(tO, tAV + 8 * j, dPb + j * kStepP, IDESC_PV, (o_valid || j > 0) ? 1u : 0u);
+        if constexpr (!L::FUSE) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) umma_f16_ts(tO, tAV + 8 * j, dPb + dPlo + j * kStepP, IDESC_PV, 1u);
+          for (int j = 0; j < 8; ++j) umma_f16_ts(tO, tAV + 8 * j, dPb + dPlo + j * kStepP, IDESC_PV, 1u);
+        }
         tc_commit(&pv_bar[i & 1]);
       }
       __syncwarp();
@@ -525,6 +536,13 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
       uint32_t ov[CPT];
       tmem_ld<CPT>(tO + lane_base + CPT * half, ov);
       tmem_wait_ld();
+      if constexpr (L::FUSE) {  // O = the hi products + the lo products
+        uint32_t ol[CPT];
+        tmem_ld<CPT>(tO + N + lane_base + CPT * half, ol);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) + __uint_as_float(ol[k]));
+      }
       const int d = row;
 #pragma unroll
       for (int k = 0; k < CPT; ++k) {
