@@ -327,7 +327,20 @@ CSRC = os.path.join(ROOT, "quantized_paged_kv_quantize_gb300", "csrc")
 KERNEL_SOURCES = {
     "decode_kernel": ["kvq_decode.cu", "kvq_device.cuh", "kvq_internal.h", "../_build.py"],
     "kvarn_decode_kernel": ["kvq_decode_kvarn.cu", "kvq_device.cuh", "kvq_internal.h", "../_build.py"],
+    "umma_decode_kernel": ["kvq_decode_umma.cu", "kvq_device.cuh", "kvq_internal.h", "../_build.py"],
 }
+
+
+def decode_kernel_of(w: wl.Workload) -> str:
+    """The decode kernel the library runs for the workload: the KVarN kernel, the
+    tcgen05 kernel (4-bit modes at head_dim 128 with several queries per sequence
+    and at most 64 query rows x heads per kv head), else the mma.sync kernel."""
+    if w.mode == "kvarn_k4v2_g128":
+        return "kvarn_decode_kernel"
+    if (w.mode in ("nvfp4", "nvfp4_4over6", "int4_per_token_head") and w.head_dim == 128 and w.page_size == 16
+            and w.num_queries >= 2 and w.group * w.num_queries <= 64):
+        return "umma_decode_kernel"
+    return "decode_kernel"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
@@ -435,7 +448,7 @@ def measure(gw: GpuWorkload, args, dev, ws: int, full: bool, sampler=None) -> di
     dec_avg = dec_total / args.steps
     peak, peak_kind = measured_peaks()
     dec_gbs = dbytes / (dec_avg * 1e-3) / 1e9
-    dec_kernel = "kvarn_decode_kernel" if w.mode == "kvarn_k4v2_g128" else "decode_kernel"
+    dec_kernel = decode_kernel_of(w)
     traffic = recorded_traffic(w.name.split("[")[0], dec_kernel, int(lens.sum()))
     tokens_heads = float(np.sum(lens.astype(np.int64))) * w.num_q_heads * w.num_queries
     res = {

@@ -53,3 +53,16 @@ def test_suite_names_resolve_and_cover_every_configuration():
         assert w.name == n and bench.base_of(n) in wl.WORKLOADS
         lay = wl.paged_layout(w)
         assert bench.config_of(w, lay)["workload"] == n
+
+
+def test_decode_kernel_named_per_workload():
+    """The roofline names the kernel that runs: tcgen05 for the 4-bit modes with
+    several queries, the KVarN kernel for KVarN (one or several queries), else
+    the mma.sync kernel."""
+    import bench
+    assert bench.decode_kernel_of(bench.workload_by_name("nvfp4_b32_s32768")) == "decode_kernel"
+    assert bench.decode_kernel_of(bench.workload_by_name("nvfp4_b32_s32768:spec4")) == "umma_decode_kernel"
+    assert bench.decode_kernel_of(bench.workload_by_name("kvarn_b16_s16384:spec4")) == "kvarn_decode_kernel"
+    assert bench.decode_kernel_of(bench.workload_by_name("pth_b64_u1k_32k:int4")) == "decode_kernel"
+    for k in ("decode_kernel", "kvarn_decode_kernel", "umma_decode_kernel"):
+        assert len(bench.kernel_sources_hash(k)) == 16
