@@ -509,16 +509,23 @@ def measure(gw: GpuWorkload, args, dev, ws: int, full: bool, sampler=None) -> di
     return res
 
 
+DIAG_TOKENS = 65536  # tokens the tensor-level diagnostics cover (whole KVarN tiles: a multiple of 128)
+
+
 def tensor_diagnostics(gw: GpuWorkload) -> dict:
     """Tensor-level error of the filled cache against its inputs (kvq_tensor_error_stats),
-    K and V apart: the ratios the NVFP4 page lists under 张量层, plus the worst head."""
+    K and V apart: the ratios the NVFP4 page lists under 张量层, plus the worst head.
+    The first DIAG_TOKENS tokens (every one for smaller caches): the statistics are
+    fp64 sums, slow on this GPU's fp64 units, and a sample of that size fixes them
+    to a few digits."""
     import torch
     K = gw.kvq
     Hkv = gw.w.num_kv_heads
+    n = min(int(gw.K.shape[0]), DIAG_TOKENS)
     stats = torch.zeros((2, Hkv, K.ERROR_STATS_DOUBLES), dtype=torch.float64, device=gw.dev)
-    K.kvq_tensor_error_stats(gw.cache, gw.K, gw.V, gw.slots, stats)
+    K.kvq_tensor_error_stats(gw.cache, gw.K[:n], gw.V[:n], gw.slots[:n], stats)
     st = stats.cpu().numpy()
-    out = {}
+    out = {"tokens": n}
     for side, name in enumerate(("K", "V")):
         f = {k: st[side, :, i] for i, k in enumerate(K.ERROR_STATS_FIELDS)}
         n, se, sr, sd, dot = (float(f[k].sum()) for k in ("count", "sum_sq_err", "sum_sq_ref", "sum_sq_deq", "dot"))
