@@ -41,6 +41,9 @@ struct WriteArgs {
   int num_seqs;
   // the pool's blocks and the tail buffer, as spans (debug-build store checks)
   Span pool_span, tail_span;
+  // -0.0f, as a value the compiler cannot see: the addend that turns a packed
+  // fused multiply-add into an exactly rounded product (see mul2z)
+  float neg_zero = -0.0f;
 };
 
 template <typename T>
@@ -667,6 +670,72 @@ __device__ __forceinline__ uint32_t rtn_code(float x, const QDiv& q, float steps
   return static_cast<uint32_t>(__float2int_rn(qv));
 }
 
+// Packed fp32 pairs (f32x2): each lane is rounded on its own, exactly as the
+// scalar __fadd_rn / __fmul_rn, so a pair op is two of the specification's
+// operations in one instruction.  Written as PTX with the explicit .rn
+// modifier, which keeps the compiler from contracting a product and a sum
+// into one fused multiply-add (the packed intrinsics were contracted).
+__device__ __forceinline__ unsigned long long f2_bits(float2 a) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ float2 bits_f2(unsigned long long r) {
+  float2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+// The code generator fuses a packed product into a packed sum that consumes it
+// (explicit .rn and -fmad=false notwithstanding; measured on GB300: 18% of
+// (a b) + c pairs differed from the two rounded steps).  A product that feeds
+// a sum is therefore written as fma(a, b, -0): a b + (-0) rounded once is the
+// rounded product, for every a b (a zero keeps its sign), and a fused
+// multiply-add has nothing left to fuse with.  z = (-0, -0) must come from a
+// kernel argument so that the addend is not folded away.
+__device__ __forceinline__ float2 mul2z(float2 a, float2 b, float2 z) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(z)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
+// tree8 of two interleaved lines at once (component-wise).
+__device__ __forceinline__ float2 tree8x2(const float2* v) {
+  const float2 a0 = add2(v[0], v[4]), a1 = add2(v[1], v[5]);
+  const float2 a2 = add2(v[2], v[6]), a3 = add2(v[3], v[7]);
+  return add2(add2(a0, a2), add2(a1, a3));
+}
+// rtn_code of two values with their own divisors: the two products and the
+// two magic-number additions are packed; the checks are per value.
+__device__ __forceinline__ uint32_t rtn_finish(float x, const QDiv& q, float steps, uint32_t lo, uint32_t hi) {
+  if (q.s == 0.0f) return 0u;
+  if (q.fast && lo == hi && lo - 0x4B400000u <= static_cast<uint32_t>(steps)) return lo & 0xFFu;
+  const float qv = fminf(fmaxf(rintf(__fdiv_rn(x, q.s)), 0.0f), steps);
+  return static_cast<uint32_t>(__float2int_rn(qv));
+}
+__device__ __forceinline__ void rtn_code2(float2 x, const QDiv& qa, const QDiv& qb, float steps, float2 z, uint32_t& ca,
+                                          uint32_t& cb) {
+  const float2 magic = dup2(12582912.0f);  // 1.5 * 2^23, as in rtn_code
+  const float2 lo = add2(mul2z(x, make_float2(qa.rlo, qb.rlo), z), magic);
+  const float2 hi = add2(mul2z(x, make_float2(qa.rhi, qb.rhi), z), magic);
+  ca = rtn_finish(x.x, qa, steps, __float_as_uint(lo.x), __float_as_uint(hi.x));
+  cb = rtn_finish(x.y, qb, steps, __float_as_uint(lo.y), __float_as_uint(hi.y));
+}
+
 // TAIL = false: tile blockIdx.x is batch rows 128 x .. 128 x + 127 of k / v.
 // TAIL = true (kvq_kvarn_append): CTA blockIdx.x looks at batch token x; when
 // that token filled the last row of its tile (slot % 128 == 127), the tile is
@@ -732,41 +801,58 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
     sm.fc[tid] = 1.0f;  // channel factors c_d
   }
 
-  // ---- 1. Walsh-Hadamard along channels
+  // ---- 1. Walsh-Hadamard along channels.  Adjacent channels travel as f32x2
+  //      pairs from stage h = 2 on (stage 1 mixes the two halves of a pair).
   {
-    float v[64];
+    float2 v2[32];  // channels 2m, 2m + 1 of this thread's half token
+    {
+      float v[64];
 #pragma unroll
-    for (int k = 0; k < NRAW; ++k) widen16<T>(raw[k], v + k * (16 / (int)sizeof(T)));
+      for (int k = 0; k < NRAW; ++k) widen16<T>(raw[k], v + k * (16 / (int)sizeof(T)));
 #pragma unroll
-    for (int hh = 1; hh <= 32; hh <<= 1)
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {  // the 32 butterflies (j, j + hh) of this stage
-        const int j = (k / hh) * 2 * hh + k % hh;
-        const float x = v[j], y = v[j + hh];
-        v[j] = __fadd_rn(x, y);
-        v[j + hh] = __fsub_rn(x, y);
-      }
-    const float c = __int_as_float(0x3DB504F3);
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      const float p = __shfl_xor_sync(kFull, v[j], 1);  // the other half of the token
-      v[j] = __fmul_rn(half ? __fsub_rn(p, v[j]) : __fadd_rn(v[j], p), c);
+      for (int m = 0; m < 32; ++m) v2[m] = make_float2(__fadd_rn(v[2 * m], v[2 * m + 1]), __fsub_rn(v[2 * m], v[2 * m + 1]));
     }
+#pragma unroll
+    for (int hp = 1; hp <= 16; hp <<= 1)  // stage h = 2 hp: the butterflies of pairs m and m + hp
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int m = (k / hp) * 2 * hp + k % hp;
+        const float2 x = v2[m], y = v2[m + hp];
+        v2[m] = add2(x, y);
+        v2[m + hp] = sub2(x, y);
+      }
+    // stage h = 64 between the two halves' lanes, then the fp32 1/sqrt(128):
+    // the upper half takes p - v as (-v) + p, the same rounding
+    const float2 sg = dup2(half ? -1.0f : 1.0f), c2 = dup2(__int_as_float(0x3DB504F3));
     float* dst = sm.Y + t * kKvYS + 64 * half;
 #pragma unroll
-    for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    for (int m = 0; m < 32; m += 2) {
+      float2 r[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float2 pv = make_float2(__shfl_xor_sync(kFull, v2[m + u].x, 1), __shfl_xor_sync(kFull, v2[m + u].y, 1));
+        r[u] = mul2(add2(mul2(v2[m + u], sg), pv), c2);
+      }
+      *reinterpret_cast<float4*>(dst + 2 * m) = make_float4(r[0].x, r[0].y, r[1].x, r[1].y);
+    }
   }
   __syncthreads();
 
-  // ---- 2. eight alternating std normalisation steps, tokens first
+  // ---- 2. eight alternating std normalisation steps, tokens first.  The
+  //      thread's eight tokens travel as f32x2 pairs (tokens tl + 32 i2 and
+  //      tl + 32 i2 + 16): per-token work is component-wise, and the per-channel
+  //      tree over the eight tokens takes its levels 64 and 32 on the pairs and
+  //      its level 16 inside each pair.
   const int dl = lane & 15, tl = (lane >> 4) | (warp << 1);
   // the lane that finishes token tl + 16 rr's sums (lanes 2k and 2k+1 agree)
   const int rr = ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-  float y[8][8];
+  const float2 nz = dup2(a.neg_zero);
+  float2 y[4][8];  // y[i2][j] = (token tl + 32 i2, token tl + 32 i2 + 16), channel dl + 16 j
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i2 = 0; i2 < 4; ++i2)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) y[i][j] = sm.Y[(tl + 16 * i) * kKvYS + dl + 16 * j];
+    for (int j = 0; j < 8; ++j)
+      y[i2][j] = make_float2(sm.Y[(tl + 32 * i2) * kKvYS + dl + 16 * j], sm.Y[(tl + 32 * i2 + 16) * kKvYS + dl + 16 * j]);
   // Steps alternate tokens, channels, ...; written as four (token, channel)
   // pairs so that no branch joins the two forms of the loop body.
 #pragma unroll kKvPairUnroll
@@ -774,18 +860,25 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
     {  // per token: sums over channels
       float p[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) p[i] = tree8(y[i]);
+      for (int i2 = 0; i2 < 4; ++i2) {
+        const float2 sum = tree8x2(y[i2]);
+        p[2 * i2] = sum.x;
+        p[2 * i2 + 1] = sum.y;
+      }
       const float mine = __fmul_rn(row_tree(p, lane), 0.0078125f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float mean = __shfl_sync(kFull, mine, row_owner(lane, i));
-        float d2[8];
+      for (int i2 = 0; i2 < 4; ++i2) {
+        const float2 mean = make_float2(__shfl_sync(kFull, mine, row_owner(lane, 2 * i2)),
+                                        __shfl_sync(kFull, mine, row_owner(lane, 2 * i2 + 1)));
+        float2 d2[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float dv = __fsub_rn(y[i][j], mean);
-          d2[j] = __fmul_rn(dv, dv);
+          const float2 dv = sub2(y[i2][j], mean);
+          d2[j] = mul2z(dv, dv, nz);
         }
-        p[i] = tree8(d2);
+        const float2 sum = tree8x2(d2);
+        p[2 * i2] = sum.x;
+        p[2 * i2 + 1] = sum.y;
       }
       float sd = __fsqrt_rn(__fmul_rn(row_tree(p, lane), 0.0078125f));
       float inv = __frcp_rn(sd);
@@ -795,32 +888,37 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
       }
       if ((lane & 1) == 0) sm.fr[tl + 16 * rr] = __fmul_rn(sm.fr[tl + 16 * rr], sd);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float iv = __shfl_sync(kFull, inv, row_owner(lane, i));
+      for (int i2 = 0; i2 < 4; ++i2) {
+        const float2 iv = make_float2(__shfl_sync(kFull, inv, row_owner(lane, 2 * i2)),
+                                      __shfl_sync(kFull, inv, row_owner(lane, 2 * i2 + 1)));
 #pragma unroll
-        for (int j = 0; j < 8; ++j) y[i][j] = __fmul_rn(y[i][j], iv);
+        for (int j = 0; j < 8; ++j) y[i2][j] = mul2z(y[i2][j], iv, nz);
       }
     }
-    {  // per channel: sums over tokens
-      float col[8];
+    {  // per channel: sums over tokens; tree8 over tokens i = 2 i2 + e:
+       // (v0 + v4, v1 + v5), (v2 + v6, v3 + v7), then their sums, then within
+      auto col8 = [](const float2* c) -> float {  // c[i2] = (v[2 i2], v[2 i2 + 1])
+        const float2 s = add2(add2(c[0], c[2]), add2(c[1], c[3]));
+        return __fadd_rn(s.x, s.y);
+      };
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) col[i] = y[i][j];
-        sm.part[tl * kKvYS + dl + 16 * j] = tree8(col);
+        const float2 col[4] = {y[0][j], y[1][j], y[2][j], y[3][j]};
+        sm.part[tl * kKvYS + dl + 16 * j] = col8(col);
       }
       __syncthreads();
       if (tid < D) sm.st0[tid] = __fmul_rn(col_tree(sm.part, tid), 0.0078125f);
       __syncthreads();
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float mean = sm.st0[dl + 16 * j];
+        const float2 mean = dup2(sm.st0[dl + 16 * j]);
+        float2 col[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float dv = __fsub_rn(y[i][j], mean);
-          col[i] = __fmul_rn(dv, dv);
+        for (int i2 = 0; i2 < 4; ++i2) {
+          const float2 dv = sub2(y[i2][j], mean);
+          col[i2] = mul2z(dv, dv, nz);
         }
-        sm.part[tl * kKvYS + dl + 16 * j] = tree8(col);
+        sm.part[tl * kKvYS + dl + 16 * j] = col8(col);
       }
       __syncthreads();
       if (tid < D) {
@@ -832,9 +930,9 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
       __syncthreads();
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float iv = sm.st1[dl + 16 * j];
+        const float2 iv = dup2(sm.st1[dl + 16 * j]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) y[i][j] = __fmul_rn(y[i][j], iv);
+        for (int i2 = 0; i2 < 4; ++i2) y[i2][j] = mul2z(y[i2][j], iv, nz);
       }
     }
   }
@@ -845,11 +943,11 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
   if (side == 0) {  // keys: per channel over the tile's tokens, 4 bits
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      float mn = y[0][j], mx = y[0][j];
+      float mn = fminf(y[0][j].x, y[0][j].y), mx = fmaxf(y[0][j].x, y[0][j].y);
 #pragma unroll
-      for (int i = 1; i < 8; ++i) {
-        mn = fminf(mn, y[i][j]);
-        mx = fmaxf(mx, y[i][j]);
+      for (int i2 = 1; i2 < 4; ++i2) {
+        mn = fminf(mn, fminf(y[i2][j].x, y[i2][j].y));
+        mx = fmaxf(mx, fmaxf(y[i2][j].x, y[i2][j].y));
       }
       sm.part[tl * kKvYS + dl + 16 * j] = mn;
       sm.part2[tl * kKvYS + dl + 16 * j] = mx;
@@ -875,23 +973,30 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int d = dl + 16 * j;
-      const float mn = sm.st1[d];
+      const float2 mn = dup2(sm.st1[d]);
       const QDiv q(sm.st0[d]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        codes[(tl + 16 * i) * kKvCS + d] = static_cast<uint8_t>(rtn_code(__fsub_rn(y[i][j], mn), q, 15.0f));
+      for (int i2 = 0; i2 < 4; ++i2) {
+        uint32_t c0, c1;
+        rtn_code2(sub2(y[i2][j], mn), q, q, 15.0f, nz, c0, c1);
+        codes[(tl + 32 * i2) * kKvCS + d] = static_cast<uint8_t>(c0);
+        codes[(tl + 32 * i2 + 16) * kKvCS + d] = static_cast<uint8_t>(c1);
+      }
     }
   } else {  // values: per token over the channels, 2 bits
     float mn8[8], mx8[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      mn8[i] = y[i][0];
-      mx8[i] = y[i][0];
+    for (int i2 = 0; i2 < 4; ++i2) {
+      float a0 = y[i2][0].x, a1 = y[i2][0].x, b0 = y[i2][0].y, b1 = y[i2][0].y;
 #pragma unroll
       for (int j = 1; j < 8; ++j) {
-        mn8[i] = fminf(mn8[i], y[i][j]);
-        mx8[i] = fmaxf(mx8[i], y[i][j]);
+        a0 = fminf(a0, y[i2][j].x);
+        a1 = fmaxf(a1, y[i2][j].x);
+        b0 = fminf(b0, y[i2][j].y);
+        b1 = fmaxf(b1, y[i2][j].y);
       }
+      mn8[2 * i2] = a0; mx8[2 * i2] = a1;
+      mn8[2 * i2 + 1] = b0; mx8[2 * i2 + 1] = b1;
     }
     float mn, mx;
     row_minmax(mn8, mx8, lane, mn, mx);
@@ -903,13 +1008,17 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
       st_chk(meta + kKvTile + t, mn, a.pool_span, a.pool);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int src = row_owner(lane, i);
-      const float mni = __shfl_sync(kFull, mn, src);
-      const QDiv q(__shfl_sync(kFull, sc, src));
+    for (int i2 = 0; i2 < 4; ++i2) {
+      const int sa = row_owner(lane, 2 * i2), sb = row_owner(lane, 2 * i2 + 1);
+      const float2 mni = make_float2(__shfl_sync(kFull, mn, sa), __shfl_sync(kFull, mn, sb));
+      const QDiv qa(__shfl_sync(kFull, sc, sa)), qb(__shfl_sync(kFull, sc, sb));
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        codes[(tl + 16 * i) * kKvCS + dl + 16 * j] = static_cast<uint8_t>(rtn_code(__fsub_rn(y[i][j], mni), q, 3.0f));
+      for (int j = 0; j < 8; ++j) {
+        uint32_t c0, c1;
+        rtn_code2(sub2(y[i2][j], mni), qa, qb, 3.0f, nz, c0, c1);
+        codes[(tl + 32 * i2) * kKvCS + dl + 16 * j] = static_cast<uint8_t>(c0);
+        codes[(tl + 32 * i2 + 16) * kKvCS + dl + 16 * j] = static_cast<uint8_t>(c1);
+      }
     }
     if (tid < kKvTile) {
       st_chk(meta + 2 * kKvTile + tid, sm.fr[tid], a.pool_span, a.pool);
