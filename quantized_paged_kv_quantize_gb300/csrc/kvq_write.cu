@@ -587,6 +587,7 @@ struct KvSmem {
   float part2[16 * kKvYS];      // per-channel maxima [t_lo][d]
   float st0[kKvTile], st1[kKvTile];  // per-line statistics
   float fr[kKvTile], fc[kKvTile];    // final factors r_t, c_d
+  float tm[kKvTile], ti[kKvTile];    // per-token mean, 1/std of the token steps, [tl][i]: token tl + 16 i
 };
 constexpr size_t kKvSmem = sizeof(KvSmem);
 #ifndef KVQ_KVARN_PAIR_UNROLL
@@ -865,11 +866,17 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
         p[2 * i2] = sum.x;
         p[2 * i2 + 1] = sum.y;
       }
+      // each lane's finished token goes to shared memory; the warp's sixteen
+      // tokens are its own, so a warp barrier orders the exchange
       const float mine = __fmul_rn(row_tree(p, lane), 0.0078125f);
+      if ((lane & 1) == 0) sm.tm[tl * 8 + rr] = mine;
+      __syncwarp();
+      float m8[8];
+      *reinterpret_cast<float4*>(m8) = *reinterpret_cast<const float4*>(sm.tm + tl * 8);
+      *reinterpret_cast<float4*>(m8 + 4) = *reinterpret_cast<const float4*>(sm.tm + tl * 8 + 4);
 #pragma unroll
       for (int i2 = 0; i2 < 4; ++i2) {
-        const float2 mean = make_float2(__shfl_sync(kFull, mine, row_owner(lane, 2 * i2)),
-                                        __shfl_sync(kFull, mine, row_owner(lane, 2 * i2 + 1)));
+        const float2 mean = make_float2(m8[2 * i2], m8[2 * i2 + 1]);
         float2 d2[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -886,11 +893,17 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
         sd = 1.0f;
         inv = 1.0f;
       }
-      if ((lane & 1) == 0) sm.fr[tl + 16 * rr] = __fmul_rn(sm.fr[tl + 16 * rr], sd);
+      if ((lane & 1) == 0) {
+        sm.fr[tl + 16 * rr] = __fmul_rn(sm.fr[tl + 16 * rr], sd);
+        sm.ti[tl * 8 + rr] = inv;
+      }
+      __syncwarp();
+      float i8[8];
+      *reinterpret_cast<float4*>(i8) = *reinterpret_cast<const float4*>(sm.ti + tl * 8);
+      *reinterpret_cast<float4*>(i8 + 4) = *reinterpret_cast<const float4*>(sm.ti + tl * 8 + 4);
 #pragma unroll
       for (int i2 = 0; i2 < 4; ++i2) {
-        const float2 iv = make_float2(__shfl_sync(kFull, inv, row_owner(lane, 2 * i2)),
-                                      __shfl_sync(kFull, inv, row_owner(lane, 2 * i2 + 1)));
+        const float2 iv = make_float2(i8[2 * i2], i8[2 * i2 + 1]);
 #pragma unroll
         for (int j = 0; j < 8; ++j) y[i2][j] = mul2z(y[i2][j], iv, nz);
       }
