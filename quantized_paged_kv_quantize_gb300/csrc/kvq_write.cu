@@ -125,6 +125,50 @@ static_assert(kRcp127 == 1.0f / 127.0f && kRcp448 == 1.0f / 448.0f && kRcp7 == 1
               "reciprocal constants of the per-token-head scales");
 static_assert(kRcp15 == 1.0f / 15.0f && kRcp3 == 1.0f / 3.0f, "reciprocal constants of the RTN scales");
 
+// Packed fp32 pairs (f32x2): each lane is rounded on its own, exactly as the
+// scalar __fadd_rn / __fmul_rn, so a pair op is two of the specification's
+// operations in one instruction.  Written as PTX with the explicit .rn
+// modifier, which keeps the compiler from contracting a product and a sum
+// into one fused multiply-add (the packed intrinsics were contracted).
+__device__ __forceinline__ unsigned long long f2_bits(float2 a) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ float2 bits_f2(unsigned long long r) {
+  float2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+// The code generator fuses a packed product into a packed sum that consumes it
+// (explicit .rn and -fmad=false notwithstanding; measured on GB300: 18% of
+// (a b) + c pairs differed from the two rounded steps).  A product that feeds
+// a sum is therefore written as fma(a, b, -0): a b + (-0) rounded once is the
+// rounded product, for every a b (a zero keeps its sign), and a fused
+// multiply-add has nothing left to fuse with.  z = (-0, -0) must come from a
+// kernel argument so that the addend is not folded away.
+__device__ __forceinline__ float2 mul2z(float2 a, float2 b, float2 z) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(z)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
+
 // Encoding of the IEEE quotient RN(x/s) without a division on the common path.
 // With r the hardware's approximate reciprocal of s (relative error below
 // 2^-21 = 8u, u = 2^-24), rlo = RN(r(1 - 2^-20)) and rhi = RN(r(1 + 2^-20)),
@@ -161,14 +205,18 @@ struct QDiv {
   // the low mantissa bits, whose low byte is the two's-complement code.  The
   // fast path also requires both ends inside [-127, 127] (bit patterns
   // 0x4B400000 -127 .. +127), so neither the clamp nor a NaN can reach it.
-  __device__ __forceinline__ uint32_t int8x4(const float* x) const {
-    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  // (The products and the additions run as packed pairs; z = (-0, -0), see mul2z.)
+  __device__ __forceinline__ uint32_t int8x4(const float* x, float2 z) const {
+    const float2 magic = dup2(12582912.0f);  // 1.5 * 2^23
     uint32_t lo[4], bad = fast ? 0u : 1u;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      lo[e] = __float_as_uint(__fadd_rn(__fmul_rn(x[e], rlo), kMagic));
-      const uint32_t hi = __float_as_uint(__fadd_rn(__fmul_rn(x[e], rhi), kMagic));
-      bad |= (lo[e] ^ hi) | static_cast<uint32_t>(lo[e] - 0x4B3FFF81u > 254u);
+    for (int e = 0; e < 4; e += 2) {
+      const float2 x2 = make_float2(x[e], x[e + 1]);
+      const float2 l2 = add2(mul2z(x2, dup2(rlo), z), magic), h2 = add2(mul2z(x2, dup2(rhi), z), magic);
+      lo[e] = __float_as_uint(l2.x);
+      lo[e + 1] = __float_as_uint(l2.y);
+      bad |= (lo[e] ^ __float_as_uint(h2.x)) | static_cast<uint32_t>(lo[e] - 0x4B3FFF81u > 254u);
+      bad |= (lo[e + 1] ^ __float_as_uint(h2.y)) | static_cast<uint32_t>(lo[e + 1] - 0x4B3FFF81u > 254u);
     }
     if (bad == 0) return prmt(prmt(lo[0], lo[1], 0x0040u), prmt(lo[2], lo[3], 0x0040u), 0x5410u);
     uint32_t w = 0;
@@ -185,14 +233,18 @@ struct QDiv {
   // code.  KEY = false: x[e] in nibble e.  KEY = true, the key-word order of
   // an 8-channel group: x[e] in nibble e/2 for even e, 4 + e/2 for odd e.
   template <int N, bool KEY = false>
-  __device__ __forceinline__ uint32_t int4x8(const float* x) const {
-    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  __device__ __forceinline__ uint32_t int4x8(const float* x, float2 z) const {
+    static_assert(N % 2 == 0, "pairs");
+    const float2 magic = dup2(12582912.0f);  // 1.5 * 2^23
     uint32_t lo[N], bad = fast ? 0u : 1u;
 #pragma unroll
-    for (int e = 0; e < N; ++e) {
-      lo[e] = __float_as_uint(__fadd_rn(__fmul_rn(x[e], rlo), kMagic));
-      const uint32_t hi = __float_as_uint(__fadd_rn(__fmul_rn(x[e], rhi), kMagic));
-      bad |= (lo[e] ^ hi) | static_cast<uint32_t>(lo[e] - 0x4B3FFFF9u > 14u);
+    for (int e = 0; e < N; e += 2) {
+      const float2 x2 = make_float2(x[e], x[e + 1]);
+      const float2 l2 = add2(mul2z(x2, dup2(rlo), z), magic), h2 = add2(mul2z(x2, dup2(rhi), z), magic);
+      lo[e] = __float_as_uint(l2.x);
+      lo[e + 1] = __float_as_uint(l2.y);
+      bad |= (lo[e] ^ __float_as_uint(h2.x)) | static_cast<uint32_t>(lo[e] - 0x4B3FFFF9u > 14u);
+      bad |= (lo[e + 1] ^ __float_as_uint(h2.y)) | static_cast<uint32_t>(lo[e + 1] - 0x4B3FFFF9u > 14u);
     }
     if (bad != 0) {
 #pragma unroll
@@ -237,23 +289,30 @@ __device__ __forceinline__ float group_max(float v) {
 // for its VEC consecutive values, then across the TPB lanes of the block
 // (xor 1, 2: each level adds two neighbouring subtrees, and fp32 addition is
 // commutative, so every lane holds the same total).
+// Packed: values i and i + VEC/2 share a pair, so the neighbour levels of the
+// tree are pair additions and the last one adds the pair's two halves.
 template <int VEC, int TPB>
-__device__ __forceinline__ float block_sse(const float* x, uint32_t w, float den) {
+__device__ __forceinline__ float block_sse(const float* x, uint32_t w, float den, float2 z) {
+  constexpr int H = VEC / 2;
   uint32_t h[4];
   e2m1x8_to_f16x2x4(w, h);
-  float e[VEC];
+  float val[VEC];
 #pragma unroll
   for (int i = 0; i < VEC; ++i) {
     const __half2 p = u32_as_h2(h[i / 2]);
-    const float val = (i & 1) ? __high2float(p) : __low2float(p);
-    const float d = __fsub_rn(x[i], __fmul_rn(val, den));
-    e[i] = __fmul_rn(d, d);
+    val[i] = (i & 1) ? __high2float(p) : __low2float(p);
+  }
+  float2 e[H];  // (error^2 of value k, of value k + H)
+#pragma unroll
+  for (int k = 0; k < H; ++k) {
+    const float2 d = sub2(make_float2(x[k], x[k + H]), mul2z(make_float2(val[k], val[k + H]), dup2(den), z));
+    e[k] = mul2z(d, d, z);
   }
 #pragma unroll
-  for (int st = 1; st < VEC; st <<= 1)
+  for (int st = 1; st < H; st <<= 1)
 #pragma unroll
-    for (int i = 0; i < VEC; i += 2 * st) e[i] = __fadd_rn(e[i], e[i + st]);
-  float t = e[0];
+    for (int k = 0; k < H; k += 2 * st) e[k] = add2(e[k], e[k + st]);
+  float t = __fadd_rn(e[0].x, e[0].y);
 #pragma unroll
   for (int o = 1; o < TPB; o <<= 1) t = __fadd_rn(t, __shfl_xor_sync(kFull, t, o));
   return t;
@@ -266,8 +325,8 @@ __device__ __forceinline__ float block_sse(const float* x, uint32_t w, float den
 // E4M3(amax / (4 s_t)), and that coding is kept when its block_sse is smaller.
 // q6, q4: the quotient brackets of RN(6 s_t) and RN(4 s_t).
 template <int VEC, int TPB, bool F46>
-__device__ __forceinline__ void nvfp4_codes(const float* x, float st, const QDiv& q6, const QDiv& q4, uint32_t& w,
-                                            uint32_t& sb) {
+__device__ __forceinline__ void nvfp4_codes(const float* x, float st, const QDiv& q6, const QDiv& q4, float2 z,
+                                            uint32_t& w, uint32_t& sb) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
@@ -281,7 +340,7 @@ __device__ __forceinline__ void nvfp4_codes(const float* x, float st, const QDiv
     const float sbf4 = e4m3_to_f32(sb4);
     const float den4 = __fmul_rn(st, sbf4);
     const uint32_t w4 = sbf4 != 0.0f ? QDiv(den4).e2m1x8<VEC>(x) : 0u;
-    if (block_sse<VEC, TPB>(x, w4, den4) < block_sse<VEC, TPB>(x, w, den)) {
+    if (block_sse<VEC, TPB>(x, w4, den4, z) < block_sse<VEC, TPB>(x, w, den, z)) {
       w = w4;
       sb = sb4;
     }
@@ -345,7 +404,7 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
 #pragma unroll
     for (int i = 0; i < VEC; i += 4) {
       if constexpr (MODE == KVQ_INT8_PER_TOKEN_HEAD) {
-        w[i / 4] = q.int8x4(x + i);
+        w[i / 4] = q.int8x4(x + i, dup2(a.neg_zero));
       } else {
         w[i / 4] = q.e4m3x2(x[i + 1], x[i]) | (q.e4m3x2(x[i + 3], x[i + 2]) << 16);
       }
@@ -357,7 +416,7 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
   } else if constexpr (MODE == KVQ_NVFP4 || MODE == KVQ_NVFP4_4OVER6) {  // keys; values: pair_values_pass
     constexpr int TPB = 16 / VEC;  // threads per 16-value block
     uint32_t w[1], sb;
-    nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, ts.st, ts.qs, ts.q4, w[0], sb);
+    nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, ts.st, ts.qs, ts.q4, dup2(a.neg_zero), w[0], sb);
     if (active) {
       store_bytes_chk<VEC / 2>(blk + (size_t)off * D / 2 + j * VEC / 2, w, a);
       if ((j % TPB) == 0)
@@ -372,7 +431,7 @@ __device__ __forceinline__ void quantize_row(const WriteArgs& a, int h, int side
     // a key word holds an 8-channel group, even channels in its low half-word:
     // with 4 values per thread, two lanes fill one word (the odd lane's
     // channels 4..7 sit one byte higher) and the even lane stores it
-    uint32_t w[1] = {QDiv(s).int4x8<VEC, true>(x)};
+    uint32_t w[1] = {QDiv(s).int4x8<VEC, true>(x, dup2(a.neg_zero))};
     if constexpr (VEC == 4) {
       if (j & 1) w[0] <<= 8;
       w[0] |= __shfl_xor_sync(kFull, w[0], 1);
@@ -424,12 +483,12 @@ __device__ __forceinline__ void pair_values_pass(const WriteArgs& a, int h, cons
       for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(x[i]));
       amax = group_max<TPR>(amax);
       const float sc = div_const(fmaxf(amax, 1e-8f), 7.0f, kRcp7);
-      wr[r] = QDiv(sc).int4x8<VEC>(x);
+      wr[r] = QDiv(sc).int4x8<VEC>(x, dup2(a.neg_zero));
       if (active && j == 0)
         st_chk(reinterpret_cast<float*>(blk + (size_t)a.P * D + (size_t)4 * a.P + 4 * off), sc, a.pool_span, a.pool);
     } else {
       uint32_t sb;
-      nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, ts.st, ts.qs, ts.q4, wr[r], sb);
+      nvfp4_codes<VEC, TPB, MODE == KVQ_NVFP4_4OVER6>(x, ts.st, ts.qs, ts.q4, dup2(a.neg_zero), wr[r], sb);
       if (active && (j % TPB) == 0)
         st_chk(blk + (size_t)a.P * D + (size_t)a.P * D / 16 + (size_t)off * D / 16 + (j * VEC) / 16, static_cast<uint8_t>(sb),
                a.pool_span, a.pool);
@@ -671,49 +730,6 @@ __device__ __forceinline__ uint32_t rtn_code(float x, const QDiv& q, float steps
   return static_cast<uint32_t>(__float2int_rn(qv));
 }
 
-// Packed fp32 pairs (f32x2): each lane is rounded on its own, exactly as the
-// scalar __fadd_rn / __fmul_rn, so a pair op is two of the specification's
-// operations in one instruction.  Written as PTX with the explicit .rn
-// modifier, which keeps the compiler from contracting a product and a sum
-// into one fused multiply-add (the packed intrinsics were contracted).
-__device__ __forceinline__ unsigned long long f2_bits(float2 a) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
-  return r;
-}
-__device__ __forceinline__ float2 bits_f2(unsigned long long r) {
-  float2 a;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
-  return a;
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  unsigned long long r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(r);
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  unsigned long long r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(r);
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  unsigned long long r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(r);
-}
-// The code generator fuses a packed product into a packed sum that consumes it
-// (explicit .rn and -fmad=false notwithstanding; measured on GB300: 18% of
-// (a b) + c pairs differed from the two rounded steps).  A product that feeds
-// a sum is therefore written as fma(a, b, -0): a b + (-0) rounded once is the
-// rounded product, for every a b (a zero keeps its sign), and a fused
-// multiply-add has nothing left to fuse with.  z = (-0, -0) must come from a
-// kernel argument so that the addend is not folded away.
-__device__ __forceinline__ float2 mul2z(float2 a, float2 b, float2 z) {
-  unsigned long long r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(z)));
-  return bits_f2(r);
-}
-__device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 // tree8 of two interleaved lines at once (component-wise).
 __device__ __forceinline__ float2 tree8x2(const float2* v) {
   const float2 a0 = add2(v[0], v[4]), a1 = add2(v[1], v[5]);
