@@ -414,7 +414,47 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
     bool exceed = false;
 #pragma unroll
     for (int k = 0; k < CPT; ++k) exceed |= sc[k] > m[k] + SLACK;
-    if (__syncthreads_or(exceed || !ok)) {  // rare: a reference max moves (always on the first tile)
+    // ---- P = 2^(s - m + PSHIFT) into P^T (hi, lo), token `row` = K index, with
+    //      the current reference maxima; pk keeps each column's p for l
+    float vs = 1.0f;
+    if constexpr (!Md::FP4)
+      vs = tok_ok ? *reinterpret_cast<const float*>(st + (row >> 4) * kPageSlot + kSOff + 64 + 4 * (row & 15)) : 0.0f;
+    float pk[CPT];
+    auto write_p = [&]() {
+      uint32_t ph[CPT / 2], pl[CPT / 2];  // f16 pairs of columns (2e, 2e + 1): hi, lo
+#pragma unroll
+      for (int e = 0; e < CPT / 2; ++e) {
+        float x[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int k = 2 * e + u;
+          pk[k] = ex2(sc[k] + ((float)PSHIFT - m[k]));  // ex2(-inf) = 0: masked and padding columns
+          x[u] = pk[k];
+          if constexpr (!Md::FP4) x[u] *= vs;
+        }
+        const float h0 = __uint_as_float(__float_as_uint(x[0]) & 0xFFFFE000u);
+        const float h1 = __uint_as_float(__float_as_uint(x[1]) & 0xFFFFE000u);
+        ph[e] = h2_as_u32(__floats2half2_rn(h0, h1));
+        pl[e] = h2_as_u32(__floats2half2_rn(x[0] - h0, x[1] - h1));
+      }
+      const int kb = (row & 7) * 16 + (row >> 3) * P_LBO + (CPT * half / 8) * 128;
+#pragma unroll
+      for (int q = 0; q < CPT / 8; ++q) {
+        *reinterpret_cast<uint4*>(pt + buf * 2 * L::POP + kb + 128 * q) =
+            make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+        *reinterpret_cast<uint4*>(pt + buf * 2 * L::POP + P_LO + kb + 128 * q) =
+            make_uint4(pl[4 * q], pl[4 * q + 1], pl[4 * q + 2], pl[4 * q + 3]);
+      }
+      tmem_wait_st();            // A_V (and a rescaled O) are in tensor memory
+      fence_proxy_async_smem();  // P^T, written by the generic proxy, is read by the tensor core
+      tc_fence_before();
+    };
+    write_p();
+    // One barrier completes A_V and P^T and the stage's reads, and votes on
+    // the maxima: where a score passed its reference max by more than SLACK
+    // (rare; always on the first tile) the maxima move, O and l are rescaled
+    // and P is written again.
+    if (__syncthreads_or(exceed || !ok)) {
       if (__syncthreads_or(!ok)) {
         timed_out = true;
         break;
@@ -450,42 +490,11 @@ __global__ void __launch_bounds__(kThreads, 2) umma_decode_kernel(const __grid_c
           tmem_st<CPT>(tO + part * N + lane_base + CPT * half, ov);
         }
       }
+      write_p();
+      __syncthreads();  // P^T with the new maxima (and the rescaled O) complete
     }
-    // ---- P = 2^(s - m + PSHIFT) into P^T (hi, lo), token `row` = K index
-    {
-      float vs = 1.0f;
-      if constexpr (!Md::FP4)
-        vs = tok_ok ? *reinterpret_cast<const float*>(st + (row >> 4) * kPageSlot + kSOff + 64 + 4 * (row & 15)) : 0.0f;
-      uint32_t ph[CPT / 2], pl[CPT / 2];  // f16 pairs of columns (2e, 2e + 1): hi, lo
 #pragma unroll
-      for (int e = 0; e < CPT / 2; ++e) {
-        float x[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int k = 2 * e + u;
-          const float p = ex2(sc[k] + ((float)PSHIFT - m[k]));  // ex2(-inf) = 0: masked and padding columns
-          l[k] += p;
-          x[u] = p;
-          if constexpr (!Md::FP4) x[u] *= vs;
-        }
-        const float h0 = __uint_as_float(__float_as_uint(x[0]) & 0xFFFFE000u);
-        const float h1 = __uint_as_float(__float_as_uint(x[1]) & 0xFFFFE000u);
-        ph[e] = h2_as_u32(__floats2half2_rn(h0, h1));
-        pl[e] = h2_as_u32(__floats2half2_rn(x[0] - h0, x[1] - h1));
-      }
-      const int kb = (row & 7) * 16 + (row >> 3) * P_LBO + (CPT * half / 8) * 128;
-#pragma unroll
-      for (int q = 0; q < CPT / 8; ++q) {
-        *reinterpret_cast<uint4*>(pt + buf * 2 * L::POP + kb + 128 * q) =
-            make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
-        *reinterpret_cast<uint4*>(pt + buf * 2 * L::POP + P_LO + kb + 128 * q) =
-            make_uint4(pl[4 * q], pl[4 * q + 1], pl[4 * q + 2], pl[4 * q + 3]);
-      }
-    }
-    tmem_wait_st();            // A_V (and a rescaled O) are in tensor memory
-    fence_proxy_async_smem();  // P^T, written by the generic proxy, is read by the tensor core
-    tc_fence_before();
-    __syncthreads();           // A_V and P^T complete; this stage's bytes are consumed
+    for (int k = 0; k < CPT; ++k) l[k] += pk[k];
     if (warp == 0) {
       tc_fence_after();
       if (elect_one()) {
