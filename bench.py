@@ -509,7 +509,7 @@ def measure(gw: GpuWorkload, args, dev, ws: int, full: bool, sampler=None) -> di
     return res
 
 
-DIAG_TOKENS = 65536  # tokens the tensor-level diagnostics cover (whole KVarN tiles: a multiple of 128)
+DIAG_TOKENS = 16384  # tokens the tensor-level diagnostics cover (whole KVarN tiles: a multiple of 128)
 
 
 def tensor_diagnostics(gw: GpuWorkload) -> dict:
