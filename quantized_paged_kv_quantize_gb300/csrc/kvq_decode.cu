@@ -607,18 +607,21 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
       }
     };
     if constexpr (kEarlyRefill) refill();
-    float sA[4] = {cA[0] * fA0, cA[1] * fA0, cA[2] * fA8, cA[3] * fA8};
-    float sB[4] = {cB[0] * fB0, cB[1] * fB0, cB[2] * fB8, cB[3] * fB8};
+    // (heads 2tq, 2tq + 1 of a token travel as packed f32x2 pairs)
+    float2 sA[2] = {__fmul2_rn(make_float2(cA[0], cA[1]), make_float2(fA0, fA0)),
+                    __fmul2_rn(make_float2(cA[2], cA[3]), make_float2(fA8, fA8))};  // tokens g, g + 8
+    float2 sB[2] = {__fmul2_rn(make_float2(cB[0], cB[1]), make_float2(fB0, fB0)),
+                    __fmul2_rn(make_float2(cB[2], cB[3]), make_float2(fB8, fB8))};
     if (nvA < kPage || nvB < kPage) {  // rare: a partial or missing page
-      if (g >= nvA) { sA[0] = sA[1] = -INFINITY; vA0 = 0.f; }
-      if (g + 8 >= nvA) { sA[2] = sA[3] = -INFINITY; vA8 = 0.f; }
-      if (g >= nvB) { sB[0] = sB[1] = -INFINITY; vB0 = 0.f; }
-      if (g + 8 >= nvB) { sB[2] = sB[3] = -INFINITY; vB8 = 0.f; }
+      if (g >= nvA) { sA[0] = make_float2(-INFINITY, -INFINITY); vA0 = 0.f; }
+      if (g + 8 >= nvA) { sA[1] = make_float2(-INFINITY, -INFINITY); vA8 = 0.f; }
+      if (g >= nvB) { sB[0] = make_float2(-INFINITY, -INFINITY); vB0 = 0.f; }
+      if (g + 8 >= nvB) { sB[1] = make_float2(-INFINITY, -INFINITY); vB8 = 0.f; }
     }
     // Lazy reference max: move it (and rescale) only when some score exceeds it
     // by more than SLACK -- rare once the first pages are seen.
-    float bm0 = fmaxf(fmaxf(sA[0], sA[2]), fmaxf(sB[0], sB[2]));  // this thread's max, heads 2tq, 2tq+1
-    float bm1 = fmaxf(fmaxf(sA[1], sA[3]), fmaxf(sB[1], sB[3]));
+    float bm0 = fmaxf(fmaxf(sA[0].x, sA[1].x), fmaxf(sB[0].x, sB[1].x));  // this thread's max, heads 2tq, 2tq+1
+    float bm1 = fmaxf(fmaxf(sA[0].y, sA[1].y), fmaxf(sB[0].y, sB[1].y));
     if (__any_sync(kFull, (bm0 > m0 + SLACK) | (bm1 > m1 + SLACK))) {
 #pragma unroll
       for (int x = 4; x <= 16; x <<= 1) {
@@ -637,28 +640,39 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
         o[t][1] *= al1; o[t][3] *= al1;
       }
     }
-    const float e0 = (float)PSHIFT - m0, e1 = (float)PSHIFT - m1;
-    const float pA0 = ex2(sA[0] + e0), pA1 = ex2(sA[1] + e1), pA2 = ex2(sA[2] + e0), pA3 = ex2(sA[3] + e1);
-    const float pB0 = ex2(sB[0] + e0), pB1 = ex2(sB[1] + e1), pB2 = ex2(sB[2] + e0), pB3 = ex2(sB[3] + e1);
-    l0 += (pA0 + pA2) + (pB0 + pB2);
-    l1 += (pA1 + pA3) + (pB1 + pB3);
+    const float2 e01 = make_float2((float)PSHIFT - m0, (float)PSHIFT - m1);
+    float2 pA[2], pB[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float2 ua = __fadd2_rn(sA[r], e01), ub = __fadd2_rn(sB[r], e01);
+      pA[r] = make_float2(ex2(ua.x), ex2(ua.y));
+      pB[r] = make_float2(ex2(ub.x), ex2(ub.y));
+    }
+    {
+      const float2 lsum = __fadd2_rn(__fadd2_rn(pA[0], pA[1]), __fadd2_rn(pB[0], pB[1]));
+      l0 += lsum.x;
+      l1 += lsum.y;
+    }
     // P^T as the B operand: f16 hi + lo, each 8x8 block transposed in registers
     uint32_t bh[2][2], bl[2][2];
     {
-      float x[8] = {pA0, pA1, pA2, pA3, pB0, pB1, pB2, pB3};
+      float2 x[4] = {pA[0], pA[1], pB[0], pB[1]};  // (heads 2tq, 2tq + 1) of tokens g, g + 8 of A, then B
       if constexpr (kPerToken) {
-        x[0] *= vA0; x[1] *= vA0; x[2] *= vA8; x[3] *= vA8;
-        x[4] *= vB0; x[5] *= vB0; x[6] *= vB8; x[7] *= vB8;
+        x[0] = __fmul2_rn(x[0], make_float2(vA0, vA0));
+        x[1] = __fmul2_rn(x[1], make_float2(vA8, vA8));
+        x[2] = __fmul2_rn(x[2], make_float2(vB0, vB0));
+        x[3] = __fmul2_rn(x[3], make_float2(vB8, vB8));
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         // hi = x cut to 10 mantissa bits (exact in f16 over P's range; below
         // 2^-14 the f16 conversion rounds it, an error under 2^-24), lo = the
         // exact remainder rounded to f16: together ~22 bits of x
-        const float h0 = __uint_as_float(__float_as_uint(x[2 * k]) & 0xFFFFE000u);
-        const float h1 = __uint_as_float(__float_as_uint(x[2 * k + 1]) & 0xFFFFE000u);
-        const __half2 h = __floats2half2_rn(h0, h1);
-        const __half2 lo = __floats2half2_rn(x[2 * k] - h0, x[2 * k + 1] - h1);
+        const float2 hh = make_float2(__uint_as_float(__float_as_uint(x[k].x) & 0xFFFFE000u),
+                                      __uint_as_float(__float_as_uint(x[k].y) & 0xFFFFE000u));
+        const __half2 h = __floats2half2_rn(hh.x, hh.y);
+        const float2 rem = __fadd2_rn(x[k], make_float2(-hh.x, -hh.y));
+        const __half2 lo = __floats2half2_rn(rem.x, rem.y);
         bh[k >> 1][k & 1] = movmatrix_t(h2_as_u32(h));
         bl[k >> 1][k & 1] = movmatrix_t(h2_as_u32(lo));
       }
