@@ -309,19 +309,22 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
       }
       const int ta = 16 * sa + g, tb = 16 * sb + g;
       const float kA0 = sh.kf[ta], kA8 = sh.kf[ta + 8], kB0 = sh.kf[tb], kB8 = sh.kf[tb + 8];
-      float sA[4] = {fmaf(cA[0], 16.0f, be0) * kA0, fmaf(cA[1], 16.0f, be1) * kA0,
-                     fmaf(cA[2], 16.0f, be0) * kA8, fmaf(cA[3], 16.0f, be1) * kA8};
-      float sB[4] = {fmaf(cB[0], 16.0f, be0) * kB0, fmaf(cB[1], 16.0f, be1) * kB0,
-                     fmaf(cB[2], 16.0f, be0) * kB8, fmaf(cB[3], 16.0f, be1) * kB8};
+      // (heads 2tq, 2tq + 1 of a token travel as packed f32x2 pairs)
+      const float2 be = make_float2(be0, be1), c16 = make_float2(16.0f, 16.0f);
+      float2 sA[2] = {__fmul2_rn(__ffma2_rn(make_float2(cA[0], cA[1]), c16, be), make_float2(kA0, kA0)),
+                      __fmul2_rn(__ffma2_rn(make_float2(cA[2], cA[3]), c16, be), make_float2(kA8, kA8))};
+      float2 sB[2] = {__fmul2_rn(__ffma2_rn(make_float2(cB[0], cB[1]), c16, be), make_float2(kB0, kB0)),
+                      __fmul2_rn(__ffma2_rn(make_float2(cB[2], cB[3]), c16, be), make_float2(kB8, kB8))};
       const int nv = t_end - (t_begin + i * kT);  // tokens of this tile the query sees
       if (nv < kT) {
-        if (ta >= nv) sA[0] = sA[1] = -INFINITY;
-        if (ta + 8 >= nv) sA[2] = sA[3] = -INFINITY;
-        if (tb >= nv) sB[0] = sB[1] = -INFINITY;
-        if (tb + 8 >= nv) sB[2] = sB[3] = -INFINITY;
+        const float2 ninf = make_float2(-INFINITY, -INFINITY);
+        if (ta >= nv) sA[0] = ninf;
+        if (ta + 8 >= nv) sA[1] = ninf;
+        if (tb >= nv) sB[0] = ninf;
+        if (tb + 8 >= nv) sB[1] = ninf;
       }
-      float bm0 = fmaxf(fmaxf(sA[0], sA[2]), fmaxf(sB[0], sB[2]));
-      float bm1 = fmaxf(fmaxf(sA[1], sA[3]), fmaxf(sB[1], sB[3]));
+      float bm0 = fmaxf(fmaxf(sA[0].x, sA[1].x), fmaxf(sB[0].x, sB[1].x));
+      float bm1 = fmaxf(fmaxf(sA[0].y, sA[1].y), fmaxf(sB[0].y, sB[1].y));
 #pragma unroll
       for (int x = 4; x <= 16; x <<= 1) {
         bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, x));
@@ -333,42 +336,53 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
       m0 = n0;
       m1 = n1;
       if (!__all_sync(kFull, al0 == 1.0f && al1 == 1.0f)) {
+        const float2 al = make_float2(al0, al1);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-          o[t][0] *= al0; o[t][2] *= al0;
-          o[t][1] *= al1; o[t][3] *= al1;
+          const float2 a01 = __fmul2_rn(make_float2(o[t][0], o[t][1]), al);
+          const float2 a23 = __fmul2_rn(make_float2(o[t][2], o[t][3]), al);
+          o[t][0] = a01.x; o[t][1] = a01.y; o[t][2] = a23.x; o[t][3] = a23.y;
         }
       }
-      const float e0 = (float)kPShift - z0, e1 = (float)kPShift - z1;
-      const float pA0 = ex2(sA[0] + e0), pA1 = ex2(sA[1] + e1), pA2 = ex2(sA[2] + e0), pA3 = ex2(sA[3] + e1);
-      const float pB0 = ex2(sB[0] + e0), pB1 = ex2(sB[1] + e1), pB2 = ex2(sB[2] + e0), pB3 = ex2(sB[3] + e1);
-      l0 = l0 * al0 + ((pA0 + pA2) + (pB0 + pB2));
-      l1 = l1 * al1 + ((pA1 + pA3) + (pB1 + pB3));
+      const float2 e01 = make_float2((float)kPShift - z0, (float)kPShift - z1);
+      float2 pA[2], pB[2];  // (heads 2tq, 2tq + 1) of tokens ta, ta + 8 and tb, tb + 8
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float2 ua = __fadd2_rn(sA[r], e01), ub = __fadd2_rn(sB[r], e01);
+        pA[r] = make_float2(ex2(ua.x), ex2(ua.y));
+        pB[r] = make_float2(ex2(ub.x), ex2(ub.y));
+      }
+      {
+        const float2 lsum = __fadd2_rn(__fadd2_rn(pA[0], pA[1]), __fadd2_rn(pB[0], pB[1]));
+        l0 = l0 * al0 + lsum.x;
+        l1 = l1 * al1 + lsum.y;
+      }
       // value-side bias: sum_t p'_t r_t zero_t over this warp's 32 tokens
       const float zA0 = sh.vz[ta], zA8 = sh.vz[ta + 8], zB0 = sh.vz[tb], zB8 = sh.vz[tb + 8];
-      float bv0 = (pA0 * zA0 + pA2 * zA8) + (pB0 * zB0 + pB2 * zB8);
-      float bv1 = (pA1 * zA0 + pA3 * zA8) + (pB1 * zB0 + pB3 * zB8);
+      float2 bv = __fadd2_rn(__ffma2_rn(pA[0], make_float2(zA0, zA0), __fmul2_rn(pA[1], make_float2(zA8, zA8))),
+                             __ffma2_rn(pB[0], make_float2(zB0, zB0), __fmul2_rn(pB[1], make_float2(zB8, zB8))));
       uint32_t bh[4], bl[4];
       {
         const float fA0 = sh.vf[ta] * vnorm, fA8 = sh.vf[ta + 8] * vnorm;
         const float fB0 = sh.vf[tb] * vnorm, fB8 = sh.vf[tb + 8] * vnorm;
-        const float x[8] = {pA0 * fA0, pA1 * fA0, pA2 * fA8, pA3 * fA8, pB0 * fB0, pB1 * fB0, pB2 * fB8, pB3 * fB8};
-        float u0 = 0.0f, u1 = 0.0f;  // sum of the f16 values the tensor core sees, per head
+        const float2 x[4] = {__fmul2_rn(pA[0], make_float2(fA0, fA0)), __fmul2_rn(pA[1], make_float2(fA8, fA8)),
+                             __fmul2_rn(pB[0], make_float2(fB0, fB0)), __fmul2_rn(pB[1], make_float2(fB8, fB8))};
+        float2 u = make_float2(0.0f, 0.0f);  // sum of the f16 values the tensor core sees, per head
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const __half2 h = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
+          const __half2 h = __floats2half2_rn(x[k].x, x[k].y);
           const float2 f = __half22float2(h);
-          const __half2 lo = __floats2half2_rn(x[2 * k] - f.x, x[2 * k + 1] - f.y);
+          const float2 rem = __fadd2_rn(x[k], make_float2(-f.x, -f.y));
+          const __half2 lo = __floats2half2_rn(rem.x, rem.y);
           const float2 fl = __half22float2(lo);
-          u0 += f.x + fl.x;
-          u1 += f.y + fl.y;
+          u = __fadd2_rn(u, __fadd2_rn(f, fl));
           bh[k] = movmatrix_t(h2_as_u32(h));
           bl[k] = movmatrix_t(h2_as_u32(lo));
         }
         // value codes enter as (1 + code/4): take out vback * sum of the probabilities used
-        bv0 = fmaf(-vback, u0, bv0);
-        bv1 = fmaf(-vback, u1, bv1);
+        bv = __ffma2_rn(make_float2(-vback, -vback), u, bv);
       }
+      float bv0 = bv.x, bv1 = bv.y;
 #pragma unroll
       for (int x = 4; x <= 16; x <<= 1) {
         bv0 += __shfl_xor_sync(kFull, bv0, x);
@@ -410,12 +424,14 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
         lds<4>(reinterpret_cast<const uint8_t*>(vm + 3 * kT + 16 * g + 4), reinterpret_cast<uint32_t*>(cv + 4));
         lds<4>(reinterpret_cast<const uint8_t*>(vm + 3 * kT + 16 * g + 8), reinterpret_cast<uint32_t*>(cv + 8));
         lds<4>(reinterpret_cast<const uint8_t*>(vm + 3 * kT + 16 * g + 12), reinterpret_cast<uint32_t*>(cv + 12));
+        const float2 vb = make_float2(vback, vback), bvv = make_float2(bv0, bv1);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-          o[t][0] = fmaf(cv[2 * t], fmaf(ot[t][0], vback, bv0), o[t][0]);
-          o[t][1] = fmaf(cv[2 * t], fmaf(ot[t][1], vback, bv1), o[t][1]);
-          o[t][2] = fmaf(cv[2 * t + 1], fmaf(ot[t][2], vback, bv0), o[t][2]);
-          o[t][3] = fmaf(cv[2 * t + 1], fmaf(ot[t][3], vback, bv1), o[t][3]);
+          const float2 a01 = __ffma2_rn(make_float2(cv[2 * t], cv[2 * t]), __ffma2_rn(make_float2(ot[t][0], ot[t][1]), vb, bvv),
+                                        make_float2(o[t][0], o[t][1]));
+          const float2 a23 = __ffma2_rn(make_float2(cv[2 * t + 1], cv[2 * t + 1]),
+                                        __ffma2_rn(make_float2(ot[t][2], ot[t][3]), vb, bvv), make_float2(o[t][2], o[t][3]));
+          o[t][0] = a01.x; o[t][1] = a01.y; o[t][2] = a23.x; o[t][3] = a23.y;
         }
       }
     }
