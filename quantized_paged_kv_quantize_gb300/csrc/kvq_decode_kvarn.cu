@@ -247,28 +247,38 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
       // ---- fold, part 2: warp w folds heads w and w + 4, lane = entry 4 j + tq
       {
         const float4 cs4 = sh.cs[lane], cz4 = sh.cz[lane];
-        const float csv[4] = {cs4.x, cs4.y, cs4.z, cs4.w}, czv[4] = {cz4.x, cz4.y, cz4.z, cz4.w};
+        const float2 csp[2] = {make_float2(cs4.x, cs4.y), make_float2(cs4.z, cs4.w)};
+        const float2 czp[2] = {make_float2(cz4.x, cz4.y), make_float2(cz4.z, cz4.w)};
+        float bph[2];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int h = warp + kW * hh;
-          __half hi[4], lo[4];
-          float bp = 0.0f;
+          uint32_t hw[2], lw[2];
+          float2 bpp = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float qt = qv[hh][i] * csv[i];
-            hi[i] = __float2half_rn(qt);
-            lo[i] = __float2half_rn(qt - __half2float(hi[i]));
+          for (int ip = 0; ip < 2; ++ip) {  // entries 2 ip, 2 ip + 1 as a packed pair
+            const float2 q2 = make_float2(qv[hh][2 * ip], qv[hh][2 * ip + 1]);
+            const float2 qt = __fmul2_rn(q2, csp[ip]);
+            const __half2 hi = __floats2half2_rn(qt.x, qt.y);
+            const float2 fh = __half22float2(hi);
+            const float2 rem = __fadd2_rn(qt, make_float2(-fh.x, -fh.y));
+            const __half2 lo = __floats2half2_rn(rem.x, rem.y);
+            const float2 fl = __half22float2(lo);
             // the tensor core sees (1 + code/16): take out 16 * the folded query it used
-            bp += qv[hh][i] * czv[i] - 16.0f * (__half2float(hi[i]) + __half2float(lo[i]));
+            bpp = __fadd2_rn(bpp, __ffma2_rn(q2, czp[ip], __fmul2_rn(make_float2(-16.0f, -16.0f), __fadd2_rn(fh, fl))));
+            hw[ip] = h2_as_u32(hi);
+            lw[ip] = h2_as_u32(lo);
           }
-          uint4 e;
-          e.x = h2_as_u32(__halves2half2(hi[0], hi[1]));
-          e.y = h2_as_u32(__halves2half2(hi[2], hi[3]));
-          e.z = h2_as_u32(__halves2half2(lo[0], lo[1]));
-          e.w = h2_as_u32(__halves2half2(lo[2], lo[3]));
-          sh.frag[fj][(4 * h + ftq) ^ (4 * fj)] = e;
-          bp = warp_sum(bp);
-          if (lane == 0) sh.beta[h] = bp;
+          sh.frag[fj][(4 * h + ftq) ^ (4 * fj)] = make_uint4(hw[0], hw[1], lw[0], lw[1]);
+          bph[hh] = bpp.x + bpp.y;
+        }
+        float2 bp = make_float2(bph[0], bph[1]);  // heads warp, warp + kW: one packed warp sum
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+          bp = __fadd2_rn(bp, make_float2(__shfl_xor_sync(kFull, bp.x, o), __shfl_xor_sync(kFull, bp.y, o)));
+        if (lane == 0) {
+          sh.beta[warp] = bp.x;
+          sh.beta[warp + kW] = bp.y;
         }
       }
       __syncthreads();
