@@ -244,7 +244,15 @@ class GpuWorkload:
                                           max_seq_len=self.max_seq_len, workspace=self.ws)
 
     def launches_per_step(self) -> int:
-        return 1 + 1 + (1 if self.plan[0] > 1 else 0)
+        # write + decode, + the split combine when the split partials go through
+        # memory (the plan then asks for workspace; splits merged inside a
+        # thread-block cluster need none and launch no combine)
+        return 1 + 1 + (1 if self.plan[2] > 0 else 0)
+
+    def split_merge(self) -> str:
+        if self.plan[0] <= 1:
+            return ""
+        return " + its split combine" if self.plan[2] > 0 else " (splits merged in a thread-block cluster)"
 
 
 class ClockSampler:
@@ -465,7 +473,7 @@ def measure(gw: GpuWorkload, args, dev, ws: int, full: bool, sampler=None) -> di
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
                      "kernel": dec_kernel, "peak_kind": peak_kind,
-                     "timed": dec_kernel + (" + its split combine" if gw.plan[0] > 1 else "")},
+                     "timed": dec_kernel + gw.split_merge()},
         "gpu_launches": gw.launches_per_step() * args.steps,
         "clocks": clocks,
         "diagnostics": diag,

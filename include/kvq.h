@@ -196,8 +196,11 @@ kvq_status kvq_quantize_write(kvq_cache* cache, const void* k, const void* v,
 
 /* Decode plan: how many KV splits per (sequence, kv head), the tokens per
  * split, and the workspace bytes kvq_decode_attention needs for these sizes
- * (0 when a single split suffices).  max_seq_len is a host-side upper bound
- * of every seq_len. */
+ * (0 when a single split suffices, and 0 when the splits of each query row
+ * merge on chip: 2 to 8 splits of the one-query kernel whose CTAs are all
+ * resident at once run as one thread-block cluster per row, so that no split
+ * partial goes through memory and no combine kernel is launched).
+ * max_seq_len is a host-side upper bound of every seq_len. */
 kvq_status kvq_decode_plan(const kvq_cache* cache, int num_seqs, int num_q_heads, int max_seq_len,
                            int* num_splits, int* tokens_per_split, size_t* workspace_bytes);
 kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int num_seqs, int num_q_heads,

@@ -431,6 +431,61 @@ __device__ __forceinline__ void pv_mma(const VRegs<MODE, D>& v, const uint32_t (
   }
 }
 
+// Dynamic shared memory of a decode CTA: the warps' stage rings, reused at the
+// end by the merge of the warps ([W][8][D] outputs, then [W][8] m and l) and,
+// right after that region, by the CTA's own partial for a merge across a
+// thread-block cluster ([8] m, [8] l, [8][D] outputs).
+template <int D>
+constexpr size_t warp_merge_bytes() { return (size_t)kWarps * 8 * (D + 2) * sizeof(float); }
+template <int D>
+constexpr size_t cluster_part_bytes() { return (size_t)8 * (D + 2) * sizeof(float); }
+template <int MODE, int D>
+constexpr size_t decode_smem() {
+  using C = Cfg<MODE, D>;
+  constexpr size_t ring = (size_t)kWarps * C::STAGES * C::STAGE;
+  constexpr size_t merge = warp_merge_bytes<D>() + cluster_part_bytes<D>();
+  return (ring > merge ? ring : merge) + 1024;  // + the 1024-byte alignment of the ring
+}
+
+// Merge of a query row's splits inside their thread-block cluster (one CTA per
+// split, ranks in split order).  Each CTA has left (m_h, l_h, o_h) for the G
+// heads of its split in `part` ([8] m, [8] l, [8][D] o); CTA r then takes
+// every cluster-size-th element (h, d) from r * blockDim on:
+// M = max_s m_s, w_s = 2^(m_s - M), out = sum_s o_s w_s / sum_s l_s w_s (0 for
+// a row without tokens).  The second barrier keeps every CTA's shared memory
+// alive until its peers have read it.
+template <int D>
+__device__ void merge_in_cluster(const DecodeArgs& a, int b, int kvh, const float* part) {
+  cluster_barrier();
+  const int r = cluster_rank(), ns = cluster_size();
+  const float* pm = part;
+  const float* pl = part + 8;
+  const float* po = part + 16;
+  for (int idx = r * blockDim.x + threadIdx.x; idx < a.G * D; idx += ns * blockDim.x) {
+    const int h = idx / D, d = idx % D;
+    float ms[8];
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      ms[s] = s < ns ? ld_cluster_f32(pm + h, s) : -INFINITY;
+      M = fmaxf(M, ms[s]);
+    }
+    float L = 0.0f, O = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        if (s < ns) {
+          const float w = exp2f(ms[s] - M);
+          L += ld_cluster_f32(pl + h, s) * w;
+          O += ld_cluster_f32(po + h * D + d, s) * w;
+        }
+      }
+    }
+    store_out(a, ((long long)b * a.Hq + (long long)kvh * a.G + h) * D + d, L > 0.0f ? O / L : 0.0f);
+  }
+  cluster_barrier();
+}
+
 template <int MODE, int D, bool QF32>
 __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel(const __grid_constant__ DecodeArgs a,
                                                                const __grid_constant__ CUtensorMap tmap) {
@@ -460,12 +515,16 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
   n = max(n - (a.nq - 1 - b % a.nq), 0);  // causal: the tokens up to the query's own position
   const int t_begin = split * a.tokens_per_split;
   const int t_end = min(n, t_begin + a.tokens_per_split);
+  float* cpart = reinterpret_cast<float*>(smem + warp_merge_bytes<D>());  // merge across the cluster
   if (t_begin >= t_end) {
     if (a.num_splits == 1) {  // empty sequence: zero output rows
       for (int i = threadIdx.x; i < a.G * D; i += blockDim.x) {
         const long long o = ((long long)b * a.Hq + (long long)kvh * a.G + i / D) * D + i % D;
         store_out(a, o, 0.0f);
       }
+    } else if (a.cluster) {  // an empty split still takes part in its cluster's merge
+      for (int i = threadIdx.x; i < 8 * (D + 2); i += blockDim.x) cpart[i] = i < 8 ? -INFINITY : 0.0f;
+      merge_in_cluster<D>(a, b, kvh, cpart);
     }
     return;
   }
@@ -729,6 +788,12 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
       const float r = L > 0.0f ? O * vfac / L : 0.0f;
       const long long oi = ((long long)b * a.Hq + hq) * D + d;
       store_out(a, oi, r);
+    } else if (a.cluster) {
+      cpart[16 + h * D + d] = O * vfac;
+      if (d == 0) {
+        cpart[h] = M;
+        cpart[8 + h] = L;
+      }
     } else {
       const long long pi = ((long long)b * a.Hq + hq) * a.num_splits + split;
       store_ws(a, a.ws_o + (pi * D + d), O * vfac);
@@ -738,6 +803,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
       }
     }
   }
+  if (a.cluster) merge_in_cluster<D>(a, b, kvh, cpart);
 }
 
 // Merge the splits of each (sequence, query head).
@@ -754,14 +820,6 @@ __global__ void __launch_bounds__(D) combine_kernel(const __grid_constant__ Deco
   const float r = merge_split_row<D>(a, ((long long)b * a.Hq + hq) * a.num_splits, ns, wts, red);
   const long long oi = ((long long)b * a.Hq + hq) * D + d;
   store_out(a, oi, r);
-}
-
-template <int MODE, int D>
-constexpr size_t decode_smem() {  // dynamic shared memory: the stage rings, reused by the merge
-  using C = Cfg<MODE, D>;
-  constexpr size_t ring = (size_t)kWarps * C::STAGES * C::STAGE;
-  constexpr size_t merge = (size_t)kWarps * 8 * (D + 2) * sizeof(float);
-  return (ring > merge ? ring : merge) + 1024;
 }
 
 // Resident CTAs per SM of one decode kernel instance (occupancy query, cached;
@@ -808,6 +866,22 @@ cudaError_t launch_mode(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s)
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_splits, a.Hkv, a.B);
+  if (a.cluster) {  // the splits of a row: one cluster along x, merged on chip
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.num_splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, c->tmap);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   kern<<<grid, kWarps * 32, smem, s>>>(a, c->tmap);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.num_splits == 1) return e;
@@ -850,6 +924,7 @@ cudaError_t launch_d(const kvq_cache* c, const DecodeArgs& a, cudaStream_t s) {
 constexpr long long kSplitCostPages = 16;
 constexpr long long kSplitCostTiles = 2;
 constexpr long long kSplitCostUmma = 1;
+constexpr int kMaxClusterSplits = 8;  // portable thread-block cluster size
 
 DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int max_seq_len, int num_queries) {
   DecodePlan p{1, c->cfg.page_size, 0};
@@ -861,6 +936,7 @@ DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int ma
   const bool umma = !kvarn && umma_decode_eligible(c, num_q_heads, num_queries);
   const long long rows = (long long)num_seqs * num_queries;  // query rows: the partials' first index
   long long splits = 1;
+  long long mma_slots = 0;  // mma.sync kernel: resident CTAs on the whole GPU
   if (umma) {
     const long long units = (long long)num_seqs * c->cfg.num_kv_heads;
     const long long tiles = (pages + 7) / 8;
@@ -889,6 +965,7 @@ DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int ma
     long long min_splits = (pages + cap - 1) / cap;
     const long long max_splits = (pages + min_pages - 1) / min_pages;
     const long long slots = (long long)(kvarn ? kvarn_resident_ctas() : resident_ctas_of(c)) * sms;
+    if (!kvarn) mma_slots = slots;
     if (kvarn) {  // one full wave when the tiles allow it
       long long full = (slots + units - 1) / units;
       if (full > max_splits) full = max_splits;
@@ -913,7 +990,12 @@ DecodePlan plan_decode(const kvq_cache* c, int num_seqs, int num_q_heads, int ma
     p.tokens_per_split = (int)(pps * P);
   }
   p.num_splits = (int)((max_seq_len + p.tokens_per_split - 1) / p.tokens_per_split);
-  if (p.num_splits > 1)
+  // mma.sync kernel, 2 to 8 splits, every CTA resident at once: the splits of
+  // a query row run as one thread-block cluster and merge on chip, so neither
+  // the partials' round trip through memory nor a combine launch remains
+  p.cluster_merge = mma_slots > 0 && p.num_splits >= 2 && p.num_splits <= kMaxClusterSplits &&
+                    rows * c->cfg.num_kv_heads * p.num_splits <= mma_slots;
+  if (p.num_splits > 1 && !p.cluster_merge)
     p.workspace_bytes = (size_t)rows * num_q_heads * p.num_splits * (c->cfg.head_dim + 2) * sizeof(float);
   return p;
 }
@@ -929,9 +1011,11 @@ cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void
   a.seq_lens = seq_lens;
   a.out = out;
   a.nq = num_queries;
+  a.cluster = plan.cluster_merge ? 1 : 0;
   num_seqs *= num_queries;  // query rows: q, out and the split partials are [num_seqs * nq][Hq]..
   a.ws_o = static_cast<float*>(workspace);
-  a.ws_ml = (plan.num_splits > 1 || kvarn_tail)
+  const bool partials = (plan.num_splits > 1 && !plan.cluster_merge) || kvarn_tail;  // split partials in memory
+  a.ws_ml = partials
                 ? a.ws_o + (size_t)num_seqs * num_q_heads * plan.num_splits * c->cfg.head_dim
                 : nullptr;
   a.num_pages = c->cfg.num_pages;
@@ -954,7 +1038,7 @@ cudaError_t launch_decode(const kvq_cache* c, const DecodePlan& plan, const void
     const size_t oel = (size_t)num_seqs * num_q_heads * c->cfg.head_dim;  // num_seqs counts query rows here
     a.out_span = Span{o, o + oel * (out_dtype == KVQ_F32 ? 4 : 2)};
     uint8_t* w = static_cast<uint8_t*>(workspace);
-    const size_t wbytes = (plan.num_splits > 1 || kvarn_tail)
+    const size_t wbytes = partials
                               ? (size_t)num_seqs * num_q_heads * plan.num_splits * (c->cfg.head_dim + 2) * sizeof(float)
                               : 0;
     a.ws_span = Span{w, w ? w + wbytes : nullptr};

@@ -70,6 +70,34 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---------------------------------------------------------------- clusters
+// This CTA's rank in its thread-block cluster and the cluster's CTA count.
+__device__ __forceinline__ int cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return (int)r;
+}
+__device__ __forceinline__ int cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return (int)r;
+}
+// Every thread of every CTA of the cluster: shared-memory writes made before
+// the barrier are visible to the cluster's CTAs after it (release / acquire).
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Load the float at the address `p` has in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_cluster_f32(const float* p, int rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -389,6 +417,9 @@ struct DecodeArgs {
   // queries per sequence (multi-query decode under the causal mask); B counts
   // query rows, B = sequences * nq
   int nq;
+  // 1: the num_splits CTAs of a query row form one thread-block cluster and
+  // merge their partials through distributed shared memory (no workspace)
+  int cluster;
   // the output [B][Hq][D] and the split workspace, as spans (debug-build checks)
   Span out_span, ws_span;
 };

@@ -26,6 +26,9 @@ struct DecodePlan {
   int num_splits;        // KV splits per (sequence, kv head)
   int tokens_per_split;  // multiple of the page size
   size_t workspace_bytes;
+  // the splits of each query row run as one thread-block cluster and merge
+  // through distributed shared memory (no combine kernel, workspace unused)
+  bool cluster_merge = false;
 };
 
 int num_sms();

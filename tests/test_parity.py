@@ -260,6 +260,28 @@ def test_decode_parity(mode, D, io, Hq, Hkv, out_dtype):
     assert kvq().kvq_cache_read_errors(cache) == 0
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+@pytest.mark.parametrize("nseq", [40, 76])
+@pytest.mark.parametrize("mode", MODES4)
+def test_decode_cluster_merge_parity(mode, nseq, out_dtype):
+    """Enough sequences that 2 to 8 splits fill one wave of CTAs: the splits
+    of each row then run as one thread-block cluster and merge on chip, and
+    the plan asks for no workspace (40 sequences: 7 splits, 76: 4 splits at 4
+    CTAs per SM).  Ragged lengths leave the later splits of short rows empty;
+    a zero-length row gives zeros."""
+    rng = np.random.default_rng(nseq)
+    lens = [int(x) for x in rng.integers(1, 2501, size=nseq - 3)] + [0, 2500, 16]
+    c = make_case(small_workload(mode), lens, slack_pages=2)
+    pool = oracle_pool(c)
+    cache = gpu_cache(c)
+    _upload_oracle_pool(cache, pool, c)
+    out, plan = gpu_decode(cache, c, out_dtype=out_dtype)
+    assert 2 <= plan[0] <= 8 and plan[2] == 0, f"plan {plan}: the case should merge its splits in a cluster"
+    check_attention(out, oracle_decode(c, pool))
+    assert (out[nseq - 3] == 0).all()
+    assert kvq().kvq_cache_read_errors(cache) == 0
+
+
 @pytest.mark.parametrize("mode", MODES4)
 def test_decode_empty_and_single_token(mode):
     c = make_case(small_workload(mode), [0, 1, 16, 0, 2], slack_pages=1)
