@@ -639,6 +639,12 @@ __global__ void __launch_bounds__(256) write_rows_kernel(WriteArgs a) {
 constexpr int kKvTile = 128;
 constexpr int kKvThreads = 256;
 constexpr int kKvYS = 144;  // floats per staged token row (banks: +16 per row)
+// Staged position of channel d in token row t: its 4-channel chunk index is
+// XORed with (d's bit 6, t's bit 1), so that the rotation's 16-byte stores
+// (8 threads: 4 rows x 2 halves, one chunk each) hit 8 distinct bank groups,
+// while the normalisation's loads (16 channels of row 2k, 16 of row 2k + 1)
+// still fill the 32 banks once.
+__device__ __forceinline__ int kv_ypos(int t, int d) { return d ^ ((d >> 4) & 4) ^ ((t << 2) & 8); }
 constexpr int kKvCS = 144;  // bytes per staged code row
 struct KvSmem {
   float Y[kKvTile * kKvYS];     // rotated tile; later the code bytes
@@ -841,7 +847,7 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
     // stage h = 64 between the two halves' lanes, then the fp32 1/sqrt(128):
     // the upper half takes p - v as (-v) + p, the same rounding
     const float2 sg = dup2(half ? -1.0f : 1.0f), c2 = dup2(__int_as_float(0x3DB504F3));
-    float* dst = sm.Y + t * kKvYS + 64 * half;
+    float* dst = sm.Y + t * kKvYS;
 #pragma unroll
     for (int m = 0; m < 32; m += 2) {
       float2 r[2];
@@ -850,7 +856,7 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
         const float2 pv = make_float2(__shfl_xor_sync(kFull, v2[m + u].x, 1), __shfl_xor_sync(kFull, v2[m + u].y, 1));
         r[u] = mul2(add2(mul2(v2[m + u], sg), pv), c2);
       }
-      *reinterpret_cast<float4*>(dst + 2 * m) = make_float4(r[0].x, r[0].y, r[1].x, r[1].y);
+      *reinterpret_cast<float4*>(dst + kv_ypos(t, 64 * half + 2 * m)) = make_float4(r[0].x, r[0].y, r[1].x, r[1].y);
     }
   }
   __syncthreads();
@@ -869,7 +875,8 @@ __global__ void __launch_bounds__(kKvThreads, 2) kvarn_write_kernel(WriteArgs a)
   for (int i2 = 0; i2 < 4; ++i2)
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      y[i2][j] = make_float2(sm.Y[(tl + 32 * i2) * kKvYS + dl + 16 * j], sm.Y[(tl + 32 * i2 + 16) * kKvYS + dl + 16 * j]);
+      y[i2][j] = make_float2(sm.Y[(tl + 32 * i2) * kKvYS + kv_ypos(tl, dl + 16 * j)],
+                             sm.Y[(tl + 32 * i2 + 16) * kKvYS + kv_ypos(tl, dl + 16 * j)]);
   // Steps alternate tokens, channels, ...; written as four (token, channel)
   // pairs so that no branch joins the two forms of the loop body.
 #pragma unroll kKvPairUnroll
