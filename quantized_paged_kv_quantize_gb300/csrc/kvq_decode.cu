@@ -757,15 +757,17 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
     red_l[warp * 8 + 2 * tq] = l0;
     red_l[warp * 8 + 2 * tq + 1] = l1;
   }
+  // staged column of (row h, channel d): bank-swizzled at D = 128
+  auto col = [](int h, int d) { return D == 128 ? merge_col128(h, d) : d; };
   {
     float* ow = red_o + warp * 8 * D;
     const int d0 = C::cgrp(g) * (D / 8);
 #pragma unroll
     for (int t = 0; t < MTILES; ++t) {
-      ow[(2 * tq) * D + d0 + 2 * t] = o[t][0];
-      ow[(2 * tq + 1) * D + d0 + 2 * t] = o[t][1];
-      ow[(2 * tq) * D + d0 + 2 * t + 1] = o[t][2];
-      ow[(2 * tq + 1) * D + d0 + 2 * t + 1] = o[t][3];
+      ow[(2 * tq) * D + col(2 * tq, d0 + 2 * t)] = o[t][0];
+      ow[(2 * tq + 1) * D + col(2 * tq + 1, d0 + 2 * t)] = o[t][1];
+      ow[(2 * tq) * D + col(2 * tq, d0 + 2 * t + 1)] = o[t][2];
+      ow[(2 * tq + 1) * D + col(2 * tq + 1, d0 + 2 * t + 1)] = o[t][3];
     }
   }
   __syncthreads();
@@ -780,7 +782,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<MODE, D>::MINB) decode_kernel
       for (int w = 0; w < kWarps; ++w) {
         const float e = exp2f(red_m[w * 8 + h] - M);
         L += red_l[w * 8 + h] * e;
-        O += red_o[(w * 8 + h) * D + d] * e;
+        O += red_o[(w * 8 + h) * D + col(h, d)] * e;
       }
     }
     const int hq = kvh * a.G + h;

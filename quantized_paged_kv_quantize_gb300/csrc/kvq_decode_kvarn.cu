@@ -474,11 +474,11 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
     float* ow = red_o + warp * 8 * kD;
     const int d0 = 16 * g;
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      ow[(2 * tq) * kD + d0 + 2 * t] = o[t][0];
-      ow[(2 * tq + 1) * kD + d0 + 2 * t] = o[t][1];
-      ow[(2 * tq) * kD + d0 + 2 * t + 1] = o[t][2];
-      ow[(2 * tq + 1) * kD + d0 + 2 * t + 1] = o[t][3];
+    for (int t = 0; t < 8; ++t) {  // bank-swizzled columns
+      ow[(2 * tq) * kD + merge_col128(2 * tq, d0 + 2 * t)] = o[t][0];
+      ow[(2 * tq + 1) * kD + merge_col128(2 * tq + 1, d0 + 2 * t)] = o[t][1];
+      ow[(2 * tq) * kD + merge_col128(2 * tq, d0 + 2 * t + 1)] = o[t][2];
+      ow[(2 * tq + 1) * kD + merge_col128(2 * tq + 1, d0 + 2 * t + 1)] = o[t][3];
     }
   }
   __syncthreads();
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kW * 32) kvarn_decode_kernel(const __grid_cons
       for (int w = 0; w < kW; ++w) {
         const float e = ex2(red_m[w * 8 + h] - M);
         L += red_l[w * 8 + h] * e;
-        O += red_o[(w * 8 + h) * kD + d] * e;
+        O += red_o[(w * 8 + h) * kD + merge_col128(h, d)] * e;
       }
     }
     if (direct) {

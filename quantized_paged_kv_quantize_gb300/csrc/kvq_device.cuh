@@ -395,6 +395,14 @@ __device__ __forceinline__ float warp_max_xor(float v, int first, int last) {
   return v;
 }
 
+// Column of (head row h, channel d) in a [8][128] block where the warps of a
+// decode CTA stage their m16n8 accumulators for the merge: the writing lanes
+// hold rows 2 tq, 2 tq + 1 and channels 16 g' + 2 t, + 1 (g' a permutation of
+// g), so XOR-ing channel bits 0..3 with (bits 5..6 of d, bits 1..2 of h) sends
+// the 32 lanes of each store to 32 different banks (unswizzled: 16-way), and a
+// row's 32 consecutive channels, read back, still fill the 32 banks once.
+__device__ __forceinline__ int merge_col128(int h, int d) { return d ^ (((d >> 5) & 3) | ((h >> 1) << 2)); }
+
 // Arguments of the decode kernels (passed by value as a __grid_constant__).
 struct DecodeArgs {
   const uint8_t* pool;
