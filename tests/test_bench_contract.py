@@ -66,3 +66,17 @@ def test_decode_kernel_named_per_workload():
     assert bench.decode_kernel_of(bench.workload_by_name("pth_b64_u1k_32k:int4")) == "decode_kernel"
     for k in ("decode_kernel", "kvarn_decode_kernel", "umma_decode_kernel"):
         assert len(bench.kernel_sources_hash(k)) == 16
+
+
+def test_launch_count_follows_the_plan():
+    """A decode step launches the write and the decode, plus the split combine
+    only when the plan asks for workspace (splits merged inside a thread-block
+    cluster need none and launch no combine)."""
+    import types
+    import bench
+    cases = [((1, 4096, 0), 2, ""), ((7, 4688, 1 << 20), 3, " + its split combine"),
+             ((4, 1024, 0), 2, " (splits merged in a thread-block cluster)")]
+    for plan, launches, label in cases:
+        gw = types.SimpleNamespace(plan=plan)
+        assert bench.GpuWorkload.launches_per_step(gw) == launches
+        assert bench.GpuWorkload.split_merge(gw) == label
